@@ -1,0 +1,235 @@
+"""fp64 CPU oracle for paged (block-sparse row) KV-cache attention.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / reference leg are the only callers.  The
+product package never imports this module, and this module never imports the
+product package: it takes plain host arrays (numpy, or torch CPU tensors) and
+shares no code, header or table with the CUDA path.
+
+The arithmetic lives in ``pkv_oracle.c`` (plain C, fp64, OpenMP over
+(query row, head) pairs); this file compiles it with gcc and marshals
+arguments through ctypes.  Every function follows the FlashInfer pages:
+
+* ``gather``        -- page-table gather ("FlashInfer" guide, section 2
+                       "Page-Level Attention").
+* ``attention``     -- softmax(scale * Q K^T) V over the gathered keys, with the
+                       logit soft-cap transform (fdeinterviews summary,
+                       "Customizable attention") and the end-aligned causal
+                       mask of ``causal=True`` prefill ("The Interface").
+* ``merge_states``  -- log-sum-exp composition of attention states (guide,
+                       section 3, "Cascade Attention" / "FlashDecoding").
+* ``cascade``       -- shared-prefix attention computed once for the whole
+                       row block, per-request suffix attention, then a merge
+                       (guide section 3, "Cascade Attention"; fdeinterviews
+                       "One format", composable formats).
+
+Parity pins: see tests/test_oracle_pins.py.  Every function here is pinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libpkv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F16, BF16 = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP, no fast-math).  Returns the .so path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            u16p = ctypes.POINTER(ctypes.c_uint16)
+            f64p = ctypes.POINTER(ctypes.c_double)
+            lib.pkv_oracle_attention.restype = ctypes.c_int
+            lib.pkv_oracle_attention.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                u16p, ctypes.c_int64, i32p, u16p, ctypes.c_int64, i32p, i32p, i32p,
+                ctypes.c_int, ctypes.c_double, ctypes.c_double, i64p, ctypes.c_int64,
+                f64p, f64p, ctypes.c_int]
+            lib.pkv_oracle_gather.restype = ctypes.c_int
+            lib.pkv_oracle_gather.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                u16p, ctypes.c_int64, i32p, i32p, i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                f64p, ctypes.c_int64]
+            lib.pkv_oracle_merge_states.restype = None
+            lib.pkv_oracle_merge_states.argtypes = [
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, f64p, f64p, f64p, f64p]
+            lib.pkv_oracle_decode16.restype = None
+            lib.pkv_oracle_decode16.argtypes = [u16p, f64p, ctypes.c_int64, ctypes.c_int]
+            lib.pkv_oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _u16(x) -> np.ndarray:
+    """Raw 16-bit storage of an fp16/bf16 array (torch CPU tensor or numpy)."""
+    if hasattr(x, "detach"):  # torch tensor, viewed as raw bits without importing torch here
+        x = x.detach().contiguous().view(dtype=_torch_int16()).numpy()
+    a = np.ascontiguousarray(x)
+    if a.dtype == np.float16:
+        a = a.view(np.uint16)
+    if a.dtype.itemsize != 2:
+        raise TypeError(f"expected a 16-bit storage array, got {a.dtype}")
+    return a.view(np.uint16)
+
+
+def _torch_int16():
+    import torch  # only for viewing the caller's tensors as raw bits
+    return torch.int16
+
+
+def _dtype_code(x, dtype: Optional[str]) -> int:
+    if dtype is not None:
+        return {"f16": F16, "fp16": F16, "float16": F16, "bf16": BF16, "bfloat16": BF16}[dtype]
+    name = str(getattr(x, "dtype", ""))
+    if "bfloat16" in name:
+        return BF16
+    if "float16" in name:
+        return F16
+    raise TypeError(f"cannot tell fp16 from bf16 for {name!r}; pass dtype=")
+
+
+def _i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def num_threads() -> int:
+    return int(_load().pkv_oracle_num_threads())
+
+
+def decode16(x, dtype: Optional[str] = None) -> np.ndarray:
+    """Exact fp64 values of 16-bit storage (the decoding every oracle routine uses)."""
+    code = _dtype_code(x, dtype)
+    a = _u16(x)
+    out = np.empty(a.shape, dtype=np.float64)
+    _load().pkv_oracle_decode16(_ptr(a, ctypes.c_uint16), _ptr(out, ctypes.c_double), a.size, code)
+    return out
+
+
+def gather(kv_data, kv_indptr, kv_indices, kv_last_page_len, b: int, kv_sel: int, kvh: int,
+           dtype: Optional[str] = None) -> np.ndarray:
+    """Request b's K (kv_sel=0) or V (kv_sel=1) rows for kv head ``kvh``: [kv_len, head_dim]."""
+    code = _dtype_code(kv_data, dtype)
+    kv = _u16(kv_data)
+    num_pages, _, hkv, page_size, d = kv.shape
+    indptr, indices, last = _i32(kv_indptr), _i32(kv_indices), _i32(kv_last_page_len)
+    batch = indptr.size - 1
+    n_pages = int(indptr[b + 1] - indptr[b]) if 0 <= b < batch else 0
+    out = np.empty((max(n_pages * page_size, 1), d), dtype=np.float64)
+    n = _load().pkv_oracle_gather(batch, hkv, d, page_size, code, _ptr(kv, ctypes.c_uint16),
+                                  num_pages, _ptr(indptr, ctypes.c_int32),
+                                  _ptr(indices, ctypes.c_int32), _ptr(last, ctypes.c_int32),
+                                  b, kv_sel, kvh, _ptr(out, ctypes.c_double), out.shape[0])
+    if n < 0:
+        raise ValueError(f"oracle gather rejected the page table (status {n})")
+    return out[:n]
+
+
+def attention(q, kv_data, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, *,
+              sm_scale: float, causal: bool = False, logits_cap: float = 0.0,
+              rows: Optional[Sequence[int]] = None, threads: int = 0,
+              dtype: Optional[str] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """fp64 attention over the paged KV cache.
+
+    q [total_q, Hq, d], kv_data [num_pages, 2, Hkv, page_size, d] (16-bit storage).
+    Returns (o [n, Hq, d], lse [n, Hq]) for the listed global rows (all rows when
+    ``rows`` is None); lse is the natural log-sum-exp of the (capped) logits.
+    """
+    code = _dtype_code(q, dtype)
+    qa, kv = _u16(q), _u16(kv_data)
+    total_q, hq, d = qa.shape
+    num_pages, two, hkv, page_size, d2 = kv.shape
+    if two != 2 or d2 != d:
+        raise ValueError("kv_data must be [num_pages, 2, num_kv_heads, page_size, head_dim]")
+    qo, indptr, indices, last = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(kv_last_page_len)
+    batch = indptr.size - 1
+    if rows is None:
+        row_arr = None
+        n = total_q
+    else:
+        row_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = row_arr.size
+    o = np.empty((n, hq, d), dtype=np.float64)
+    lse = np.empty((n, hq), dtype=np.float64)
+    st = _load().pkv_oracle_attention(
+        batch, hq, hkv, d, page_size, code, _ptr(qa, ctypes.c_uint16), total_q,
+        _ptr(qo, ctypes.c_int32), _ptr(kv, ctypes.c_uint16), num_pages,
+        _ptr(indptr, ctypes.c_int32), _ptr(indices, ctypes.c_int32), _ptr(last, ctypes.c_int32),
+        int(bool(causal)), float(sm_scale), float(logits_cap),
+        None if row_arr is None else _ptr(row_arr, ctypes.c_int64), n,
+        _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double), int(threads))
+    if st != 0:
+        raise ValueError(f"oracle rejected the inputs (status {st})")
+    return o, lse
+
+
+def attention_of(batch, rows=None, threads: int = 0):
+    """``attention`` on a workload object with the fields of a paged batch."""
+    return attention(batch.q, batch.kv_data, batch.qo_indptr, batch.kv_indptr, batch.kv_indices,
+                     batch.kv_last_page_len, sm_scale=batch.sm_scale, causal=batch.causal,
+                     logits_cap=batch.logits_cap, rows=rows, threads=threads)
+
+
+def merge_states(os_, lses) -> Tuple[np.ndarray, np.ndarray]:
+    """Merge states (o_i [..., d], lse_i [...]) over disjoint key sets (fp64)."""
+    o = np.ascontiguousarray(np.stack([np.asarray(x, dtype=np.float64) for x in os_]))
+    lse = np.ascontiguousarray(np.stack([np.asarray(x, dtype=np.float64) for x in lses]))
+    k = o.shape[0]
+    d = o.shape[-1]
+    lead = o.shape[1:-1]
+    if lse.shape[1:] != lead:
+        raise ValueError("lse shapes must match o without its last axis")
+    n = int(np.prod(lead)) if lead else 1
+    o2 = o.reshape(k, n, d)
+    l2 = lse.reshape(k, n)
+    out = np.empty((n, d), dtype=np.float64)
+    lout = np.empty((n,), dtype=np.float64)
+    _load().pkv_oracle_merge_states(k, n, d, _ptr(o2, ctypes.c_double), _ptr(l2, ctypes.c_double),
+                                    _ptr(out, ctypes.c_double), _ptr(lout, ctypes.c_double))
+    return out.reshape(*lead, d), lout.reshape(lead)
+
+
+def cascade(prefix_batch, suffix_batch, threads: int = 0):
+    """Cascade (shared-prefix) attention: prefix row block + per-request suffix, merged.
+
+    ``prefix_batch`` holds every request's query as one row block against the
+    shared prefix pages; ``suffix_batch`` holds each request against its own pages.
+    Both view the same pool.  Returns (o, lse) per request row.
+    """
+    o_p, l_p = attention_of(prefix_batch, threads=threads)
+    o_s, l_s = attention_of(suffix_batch, threads=threads)
+    return merge_states([o_p, o_s], [l_p, l_s])
