@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of paged (block-sparse) KV-cache attention on one or more GB300s.
+
+One step = one pass of the decode hot path over one batch of the
+Llama-3-8B-shaped decode workload (batch 64, 32 q / 8 kv heads, head_dim 128,
+page 16, bf16, kv_len ~ U[512, 4096], randomly permuted page pool): the host
+plan (validation + equal-chunk split) with its copy to the device, the
+split-KV decode kernel and the log-sum-exp merge kernel, all through the C ABI.
+Inputs are resident in HBM; the KV read per step (~0.63 GB) is larger than L2,
+so no flush is needed between steps.
+
+The JSON line also carries the prefill (ragged causal, tensor cores), skewed
+long-context decode and cascade measurements under "secondary".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no
+collective on the data path); rank 0 prints the line.  --impl reference times
+the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV GB/s & % of HBM peak; prefill TFLOP/s & % of tensor peak"
+WORKLOAD = "llama3_8b_decode"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="own", choices=["own", "reference"])
+    p.add_argument("--no-secondary", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_bsr_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(profile_name: str, src_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("source_hash", "dram_bytes_per_launch",
+                                                        "scale_to_bench_launch")):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_hash") != src_hash or "dram_bytes_per_launch" not in vals:
+        return None
+    return float(vals["dram_bytes_per_launch"]) * float(vals.get("scale_to_bench_launch", "1"))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not win and self.samples:  # a short window: take the samples nearest to it
+            mid = 0.5 * (t0 + t1)
+            win = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The fp64 CPU oracle, as it stands, on the host cores: each step one bounded
+    sample (a run of requests of the same workload, cycling through the batch)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from paged_kv_cache_bsr_gb300 import workloads as W
+    oracle.build()
+    b = W.llama3_decode(seed=1001)
+    per_req = [n * 2 * b.num_kv_heads * b.head_dim * 2 for n in b.kv_lens]
+    # Size one step so the whole run takes about two minutes at the oracle's speed.
+    t = time.time()
+    oracle.attention_of(b, rows=list(range(8)))
+    rate = sum(per_req[:8]) / max(time.time() - t, 1e-6)  # bytes / s
+    budget = 120.0 / max(args.steps + args.warmup, 1)
+    n_req = max(1, min(b.batch, int(budget * rate / (sum(per_req) / b.batch))))
+    cursor = [0]
+
+    def step():
+        rows = [(cursor[0] + i) % b.batch for i in range(n_req)]
+        cursor[0] = (cursor[0] + n_req) % b.batch
+        oracle.attention_of(b, rows=rows)
+        return sum(per_req[r] for r in rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    nbytes = sum(step() for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "batch": b.batch, "num_qo_heads": 32,
+                                        "num_kv_heads": 8, "head_dim": 128, "page_size": 16,
+                                        "kv_len": "U[512,4096]"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": f"{n_req} of {b.batch} requests per step, cycling"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- own arm
+def cpu_baseline(b, seconds=10.0):
+    """The oracle as it stands on the host cores over the whole batch, repeated ~10 s."""
+    import oracle
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention_of(b)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(b.kv_bytes() * reps / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"the full {WORKLOAD} batch (64 requests), {reps} passes, {dt:.1f} s"}
+
+
+def time_steps(fn, steps, warmup, stream, kernel_events=None, sync_each=False):
+    """Device time of `steps` calls of fn on `stream` (CUDA events), after `warmup` calls."""
+    import torch
+    for _ in range(warmup):
+        fn(None)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)] \
+        if kernel_events else None
+    start.record(stream)
+    for k in range(steps):
+        fn(pairs[k] if pairs else None)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(stop)
+    kern = None
+    if pairs:
+        kern = sum(a.elapsed_time(b) for a, b in pairs) / steps
+    return total, kern
+
+
+def decode_measure(b, steps, warmup, peaks, profile_name=None):
+    """Step time and main-kernel time of plan + decode + merge on one workload."""
+    import torch
+    from paged_kv_cache_bsr_gb300 import runner, api
+    db = runner.DeviceBatch.from_host(b)
+    plan = runner.make_plan(b, api.PLAN_DECODE)
+    o = torch.empty_like(db.q)
+    lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.q.device)
+    stream = torch.cuda.current_stream()
+
+    def step(ev):
+        if ev is not None:
+            plan.set_timing_events(*ev)
+        runner.plan_batch(plan, b)
+        plan.run(db.q, db.kv_data, db.kv_indices, db.kv_indptr, db.kv_last_page_len, o, lse)
+
+    total_ms, kern_ms = time_steps(step, steps, warmup, stream, kernel_events=True)
+    plan.set_timing_events(None, None)
+    assert plan.device_error() == 0
+    nbytes = b.kv_bytes()
+    ms = total_ms / steps
+    res = {"ms_per_step": ms, "kernel_ms": kern_ms, "bytes": nbytes, "value": nbytes / (ms * 1e-3) / 1e9,
+           "info": plan.info()}
+    traffic = recorded_traffic(profile_name, source_hash("decode.cu")) if profile_name else None
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    res["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                       "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                       "peak_source": peaks["source"], "kernel": "decode_kernel"}
+    del db, o, lse
+    return res
+
+
+def decode_e2e(b, steps):
+    """The same metric through the C ABI with HOST buffers: every step copies q,
+    the KV pool and the index arrays from pinned memory, plans, runs, and reads
+    o and lse back."""
+    import torch
+    from paged_kv_cache_bsr_gb300 import runner, api
+    dev = torch.device("cuda")
+    pin = lambda t: t.contiguous().pin_memory()
+    hq, hkv, hip, hix, hl = pin(b.q), pin(b.kv_data), pin(b.kv_indptr), pin(b.kv_indices), pin(b.kv_last_page_len)
+    q = torch.empty_like(hq, device=dev)
+    kv = torch.empty_like(hkv, device=dev)
+    ip, ix, last = (torch.empty_like(t, device=dev) for t in (hip, hix, hl))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    ho = torch.empty_like(o, device="cpu").pin_memory()
+    hlse = torch.empty_like(lse, device="cpu").pin_memory()
+    plan = runner.make_plan(b, api.PLAN_DECODE)
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hkv, hip, hix, hl))
+    d2h = ho.numel() * ho.element_size() + hlse.numel() * hlse.element_size()
+
+    def step(_):
+        for d, h in ((q, hq), (kv, hkv), (ip, hip), (ix, hix), (last, hl)):
+            d.copy_(h, non_blocking=True)
+        plan.plan(hip, hl, b.num_pages, kv_indices_h=hix)
+        plan.run(q, kv, ix, ip, last, o, lse)
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    total_ms, _ = time_steps(step, steps, 3, stream)
+    ms = total_ms / steps
+    del q, kv, o
+    return {"value": round(b.kv_bytes() / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+
+
+def prefill_measure(peaks, steps=20, warmup=3):
+    import torch
+    from paged_kv_cache_bsr_gb300 import runner, api, workloads as W
+    b = W.ragged_prefill(seed=1003)
+    try:
+        plan = runner.make_plan(b, api.PLAN_PREFILL)
+    except api.PkvError as e:
+        return {"unavailable": str(e)}
+    db = runner.DeviceBatch.from_host(b)
+    o = torch.empty_like(db.q)
+    lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.q.device)
+
+    def step(ev):
+        if ev is not None:
+            plan.set_timing_events(*ev)
+        runner.plan_batch(plan, b)
+        plan.run(db.q, db.kv_data, db.kv_indices, db.kv_indptr, db.kv_last_page_len, o, lse,
+                 qo_indptr=db.qo_indptr)
+
+    total_ms, kern_ms = time_steps(step, steps, warmup, torch.cuda.current_stream(), kernel_events=True)
+    plan.set_timing_events(None, None)
+    pairs = 0
+    for qo, kv in zip(b.qo_lens, b.kv_lens):
+        pre = kv - qo
+        pairs += qo * pre + qo * (qo + 1) // 2
+    flops = pairs * b.num_qo_heads * 4 * b.head_dim
+    ms = total_ms / steps
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    traffic = recorded_traffic("prefill_kernel_ragged_causal_prefill.txt", source_hash("prefill.cu"))
+    return {"workload": "ragged_causal_prefill", "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "kernel_ms": round(kern_ms, 4), "flops": flops,
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
+                         "peak_source": peaks["source"], "kernel": "prefill_kernel"}}
+
+
+def cascade_measure(steps=50, warmup=5):
+    import torch
+    from paged_kv_cache_bsr_gb300 import runner, api, workloads as W
+    cb = W.cascade_decode(seed=1004)
+    try:
+        pplan = runner.make_plan(cb.prefix, api.PLAN_PREFILL)
+    except api.PkvError as e:
+        return {"unavailable": str(e)}
+    splan = runner.make_plan(cb.suffix, api.PLAN_DECODE)
+    fplan = runner.make_plan(cb.full, api.PLAN_DECODE)
+    kv = cb.full.kv_data.cuda()
+    dp = runner.DeviceBatch.from_host(cb.prefix, kv_data=kv)
+    ds = runner.DeviceBatch.from_host(cb.suffix, kv_data=kv)
+    df = runner.DeviceBatch.from_host(cb.full, kv_data=kv)
+    s = torch.cuda.current_stream()
+
+    def casc(_):
+        runner.plan_batch(pplan, cb.prefix)
+        runner.plan_batch(splan, cb.suffix)
+        runner.cascade(dp, ds, pplan, splan)
+
+    def full(_):
+        runner.plan_batch(fplan, cb.full)
+        runner.decode(df, fplan)
+
+    c_ms, _ = time_steps(casc, steps, warmup, s)
+    f_ms, _ = time_steps(full, steps, warmup, s)
+    c_ms, f_ms = c_ms / steps, f_ms / steps
+    return {"workload": "cascade_softcap_decode", "cascade_us": round(c_ms * 1e3, 2),
+            "non_cascade_us": round(f_ms * 1e3, 2), "speedup": round(f_ms / c_ms, 3),
+            "non_cascade_kv_GBps": round(cb.full.kv_bytes() / (f_ms * 1e-3) / 1e9, 1)}
+
+
+def run_own(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from paged_kv_cache_bsr_gb300 import build, api, workloads as W
+    build.build()
+    api.load()
+    peaks = measured_peaks()
+    b = W.llama3_decode(seed=1001 + rank)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    res = decode_measure(b, args.steps, args.warmup, peaks, "decode_kernel_llama3_8b_decode.txt")
+    t_wall1 = time.time()
+    ms = res["ms_per_step"]
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        nb = torch.tensor([res["bytes"]], dtype=torch.float64, device="cuda")
+        dist.all_reduce(nb, op=dist.ReduceOp.SUM)
+        total_bytes = float(nb.item())
+        dist.barrier()
+    else:
+        total_bytes = res["bytes"]
+    clk = clocks.summary(t_wall0, t_wall1)
+    if rank != 0:
+        clocks.stop()
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    value = total_bytes / (ms * 1e-3) / 1e9
+    info = res["info"]
+    secondary = {}
+    e2e = None
+    if world == 1:
+        e2e = decode_e2e(b, args.e2e_steps)
+        if not args.no_secondary:
+            sk = W.skewed_decode(seed=1002)
+            r3 = decode_measure(sk, max(20, args.steps // 10), 5, peaks)
+            secondary["skewed_decode"] = {"value": round(r3["value"], 1), "unit": "GB/s",
+                                          "ms_per_step": round(r3["ms_per_step"], 4),
+                                          "roofline": r3["roofline"], "slots": r3["info"].num_slots}
+            del sk
+            ident = W.llama3_decode(seed=1001, identity_pages=True)
+            r_id = decode_measure(ident, max(20, args.steps // 10), 5, peaks)
+            secondary["page_permutation_overhead"] = {
+                "identity_pages_ms": round(r_id["ms_per_step"], 4), "permuted_pages_ms": round(ms, 4),
+                "overhead_pct": round((ms / r_id["ms_per_step"] - 1) * 100, 2)}
+            del ident
+            secondary["prefill"] = prefill_measure(peaks)
+            secondary["cascade"] = cascade_measure()
+    clocks.stop()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": b.batch, "num_qo_heads": 32, "num_kv_heads": 8, "head_dim": 128,
+                   "page_size": 16, "kv_len": "U[512,4096]", "kv_bytes_per_step": b.kv_bytes(),
+                   "l2": "inputs larger than L2 (KV read per step > 129 MB), no flush",
+                   "step": "plan_run + decode kernel + merge kernel", "workers": info.workers,
+                   "active_workers": info.active_workers, "split_sequences": info.num_merge},
+        "hbm_frac_of_step": round(value / world / peaks["hbm_gbs"], 4),
+        "roofline": res["roofline"],
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(b)
+    if secondary:
+        line["secondary"] = secondary
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_own(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,251 @@
+/*
+ * pkv_bsr.h -- C ABI of a GB300 (sm_103a) library for attention over a KV
+ * cache stored as a block-sparse row (BSR) matrix of pages.
+ *
+ * The method is the one the FlashInfer pages describe:
+ *  - "FlashInfer" guide (infra.bea.ai), section 2 "Page-Level Attention":
+ *    each request owns a page table; token t of request b lives in page
+ *    kv_indices[kv_indptr[b] + t / page_size] at slot t % page_size, and the
+ *    last page holds kv_last_page_len[b] valid slots.
+ *  - Same guide, "The Interface": batch_prefill (causal) and batch_decode
+ *    take (q, kv_data, kv_indices, kv_indptr, kv_last_page_len).
+ *  - Same guide, section 3 "FlashDecoding" and "Cascade Attention": split-KV
+ *    partial states and their log-sum-exp merge (merge_state).
+ *  - fdeinterviews summary, "Load balancing that survives CUDA graphs": a CPU
+ *    plan splits long KV sequences into equal chunks across the SMs and
+ *    records where partial results go; fixed-grid kernels then run (and can be
+ *    captured in a CUDA graph) and merge the partials.
+ *  - greptalks summary, "Runtime Scheduler": the plan / run split.
+ *
+ * Conventions for every entry point
+ *  - All tensors are dense, row-major, caller-owned device memory unless a
+ *    parameter says "host".  The library never allocates device memory and
+ *    never frees caller memory.  Pointers must be 16-byte aligned.
+ *  - Layouts:
+ *      q, o        [total_q, num_qo_heads, head_dim]  fp16 or bf16 (same dtype)
+ *      lse         [total_q, num_qo_heads]            fp32, natural log
+ *      kv_data     [num_pages, 2, num_kv_heads, page_size, head_dim]
+ *                  K at index 0, V at index 1 of the second axis.
+ *      qo_indptr   [batch + 1] int32, rows of request b: qo_indptr[b] .. qo_indptr[b+1]-1
+ *      kv_indptr   [batch + 1] int32, CSR row pointer over kv_indices
+ *      kv_indices  [kv_indptr[batch]] int32, physical page ids in [0, num_pages)
+ *      kv_last_page_len [batch] int32 in [1, page_size]; ignored for a request
+ *                  without pages, whose output is o = 0, lse = -inf
+ *  - Query head h reads kv head h / (num_qo_heads / num_kv_heads).
+ *  - logits = sm_scale * q.k; when logits_cap > 0 they become
+ *    logits_cap * tanh(logits / logits_cap) before the softmax; lse is the
+ *    natural log-sum-exp of the final logits.
+ *  - Causal prefill: row i of a request with qo_len rows and kv_len keys sees
+ *    keys j <= i + kv_len - qo_len.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Run calls
+ *    enqueue work and return; they never synchronise the host.
+ *  - Errors are returned as pkv_status; nothing is thrown and nothing is
+ *    printed.  A failed call enqueues no kernel.
+ */
+#ifndef PKV_BSR_H
+#define PKV_BSR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misaligned pointer, wrong plan kind */
+    PKV_ERR_BAD_INDEX = -2,    /* malformed indptr, page id out of range, bad last_page_len */
+    PKV_ERR_UNSUPPORTED = -3,  /* head_dim / group size / dtype / page size not built */
+    PKV_ERR_WORKSPACE = -4,    /* a workspace is too small, or the batch exceeds the plan limits */
+    PKV_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed */
+    PKV_ERR_DEVICE_CHECK = -6  /* a kernel recorded an error word (see pkv_get_device_error) */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
+
+typedef enum { PKV_PLAN_DECODE = 0, PKV_PLAN_PREFILL = 1 } pkv_plan_kind;
+
+/* Problem description shared by plan and run calls. */
+typedef struct {
+    int num_qo_heads;   /* Hq, a multiple of num_kv_heads */
+    int num_kv_heads;   /* Hkv */
+    int head_dim;       /* d: 64 or 128 */
+    int page_size;      /* P: 1..16, or a multiple of 16 */
+    int dtype;          /* pkv_dtype of q, kv_data and o: PKV_F16 or PKV_BF16 */
+    float sm_scale;     /* usually 1/sqrt(head_dim) */
+    float logits_cap;   /* <= 0: off */
+    int causal;         /* prefill: end-aligned causal mask; ignored by decode */
+} pkv_params;
+
+/* Upper bounds a plan is sized for (fixed for the plan's lifetime, so that a
+ * captured CUDA graph can be replayed after re-planning a different batch). */
+typedef struct {
+    int max_batch;          /* requests per call */
+    int64_t max_total_q;    /* query rows per call (decode: = max_batch) */
+    int64_t max_kv_pages;   /* entries of kv_indices per call */
+} pkv_limits;
+
+/* Opaque host-side plan object (inspector of the inspector-executor pair). */
+typedef struct pkv_plan pkv_plan;
+
+/* Human-readable name of a status code (static storage). */
+const char* pkv_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int pkv_version(void);
+
+/*
+ * Create a plan for `kind` on CUDA device `device`.  Validates params and
+ * limits, queries the device's SM count, and fixes the worker grid.
+ * Allocates only host memory (freed by pkv_plan_destroy).
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+pkv_status pkv_plan_create(pkv_plan** out, int kind, const pkv_params* params,
+                           const pkv_limits* limits, int device);
+
+pkv_status pkv_plan_destroy(pkv_plan* plan);
+
+/*
+ * Create a plan for a device with `num_sms` SMs without any CUDA call, so that
+ * the plan's decisions can be inspected on a machine without a GPU.  Such a
+ * plan computes tables (pkv_plan_compute) but cannot run (PKV_ERR_INVALID_ARG).
+ */
+pkv_status pkv_plan_create_host(pkv_plan** out, int kind, const pkv_params* params,
+                                const pkv_limits* limits, int num_sms);
+
+/*
+ * Bytes of caller-provided memory the plan needs:
+ *  - dev_bytes: device workspace (plan tables, fp32 partial states, error word);
+ *  - host_bytes: pinned host staging buffer for the plan tables.
+ * Both depend only on params and limits.
+ */
+pkv_status pkv_plan_workspace_bytes(const pkv_plan* plan, size_t* dev_bytes, size_t* host_bytes);
+
+/*
+ * The plan step (fdeinterviews "Load balancing"; greptalks "Runtime
+ * Scheduler").  Reads HOST copies of the index arrays, validates them
+ * (monotone indptr, page ids in [0, num_pages), last_page_len in range,
+ * sizes within the limits), splits the KV work into equal chunks over the
+ * fixed worker grid, records where every partial state goes, and enqueues one
+ * host-to-device copy of the tables (from `host_ws`, which must be pinned) into
+ * `dev_ws` on `stream`.  Clears the device error word.
+ *  - qo_indptr_h: host [batch+1]; NULL for decode (one row per request).
+ *  - kv_indices_h: host, may be NULL to skip the page-id range check.
+ *  - num_pages: rows of kv_data's first axis (the pool size).
+ * A later plan_run on the same plan first waits for the previous copy out of
+ * host_ws to finish.  Run calls must be enqueued after this call on the same
+ * stream (or ordered after it).
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_BAD_INDEX, PKV_ERR_WORKSPACE, PKV_ERR_CUDA.
+ */
+pkv_status pkv_plan_run(pkv_plan* plan, int batch, const int32_t* qo_indptr_h,
+                        const int32_t* kv_indptr_h, const int32_t* kv_indices_h,
+                        const int32_t* kv_last_page_len_h, int64_t num_pages, void* dev_ws,
+                        size_t dev_ws_bytes, void* host_ws, size_t host_ws_bytes, void* stream);
+
+/*
+ * The host half of pkv_plan_run: validate the host index arrays and write
+ * the plan tables into `host_ws` (ordinary or pinned host memory), with no
+ * CUDA call.  pkv_plan_run is this step followed by one asynchronous copy.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_BAD_INDEX, PKV_ERR_WORKSPACE.
+ */
+pkv_status pkv_plan_compute(pkv_plan* plan, int batch, const int32_t* qo_indptr_h,
+                            const int32_t* kv_indptr_h, const int32_t* kv_indices_h,
+                            const int32_t* kv_last_page_len_h, int64_t num_pages, void* host_ws,
+                            size_t host_ws_bytes);
+
+/* Summary of the fixed grid and of the last computed plan. */
+typedef struct {
+    int grid_ctas;       /* CTAs of the main kernel's fixed grid */
+    int workers;         /* workers of the grid (decode: warps; prefill: CTAs) */
+    int active_workers;  /* workers the last plan gave work to */
+    int num_work;        /* work entries (decode segments / prefill tiles) */
+    int num_merge;       /* split sequences whose partial states get merged */
+    int num_slots;       /* partial-state slots used */
+    int64_t max_cost;    /* largest per-worker cost (decode: pages; prefill: KV blocks) */
+    int64_t total_cost;  /* sum of the per-worker costs */
+} pkv_plan_info;
+
+pkv_status pkv_plan_get_info(const pkv_plan* plan, pkv_plan_info* info);
+
+/*
+ * Copy the last computed work list, 8 int32 per entry, in worker order:
+ *   decode:  {worker, b, kv_head, page_begin, n_pages, last_rows, slot, 0}
+ *   prefill: {worker, b, kv_head, q_pos0, n_pos, kv_begin, kv_end, slot}
+ * (slot = -1: the entry writes the final output itself).
+ * *rows_written receives the number of entries (also when capacity is short,
+ * in which case nothing is copied and PKV_ERR_WORKSPACE is returned).
+ */
+pkv_status pkv_plan_get_work(const pkv_plan* plan, int32_t* out, int64_t capacity,
+                             int64_t* rows_written);
+
+/*
+ * Profiling hook.  While set, every run call on this plan records `start` on
+ * its stream just before the main kernel (decode or prefill) and `stop` just
+ * after it, before the merge kernel, so the caller can time the main kernel
+ * alone with cudaEventElapsedTime.  The events (cudaEvent_t) stay the
+ * caller's; pass NULL for both to clear.
+ * Errors: PKV_ERR_INVALID_ARG.
+ */
+pkv_status pkv_plan_set_timing_events(pkv_plan* plan, void* start, void* stop);
+
+/*
+ * Batch decode over the paged KV cache ("The Interface", step 3; guide
+ * section 3 "FlashDecoding"): one query row per request, all query heads.
+ * q and o: [batch, Hq, d]; lse: [batch, Hq] fp32 (may be NULL).
+ * kv_indptr_d and kv_last_page_len_d must hold the values the plan saw; the
+ * kernels read page ids from kv_indices_d and check kv_indptr_d against the
+ * plan (a mismatch sets the device error word and skips the work).
+ * Long sequences are split into chunks whose fp32 partial states go to dev_ws
+ * and are merged by log-sum-exp in a second fixed-grid kernel.  Graph-capturable.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const void* kv_data,
+                                  const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
+                                  const int32_t* kv_last_page_len_d, void* o, float* lse,
+                                  void* dev_ws, void* stream);
+
+/*
+ * Batch prefill over the paged KV cache ("The Interface", step 2), ragged
+ * query rows given by qo_indptr_d, causal per params->causal, computed with
+ * tcgen05 tensor-core MMAs (bf16 and fp16) and fp32 TMEM accumulators.
+ * q and o: [total_q, Hq, d]; lse: [total_q, Hq] fp32 (may be NULL).
+ * With causal = 0 and one request whose rows are many requests' queries, this
+ * is the shared-prefix half of cascade attention.  Graph-capturable as long as
+ * kv_data and num_pages stay the same.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
+                                   const void* kv_data, const int32_t* kv_indices_d,
+                                   const int32_t* kv_indptr_d, const int32_t* kv_last_page_len_d,
+                                   void* o, float* lse, void* dev_ws, void* stream);
+
+/*
+ * merge_state (guide section 3, "Cascade Attention": the two partial results
+ * are combined with the online-softmax correction).  For each of n_rows *
+ * num_heads rows with states (o_a, lse_a) and (o_b, lse_b) over disjoint key
+ * sets:  m = max(lse_a, lse_b); w_x = exp(lse_x - m);
+ *        o = (w_a o_a + w_b o_b) / (w_a + w_b); lse = m + ln(w_a + w_b).
+ * Both lse = -inf gives o = 0, lse = -inf; a state with lse = -inf adds nothing.
+ * o_* : [n_rows, num_heads, head_dim] of `dtype` (PKV_F16, PKV_BF16 or PKV_F32;
+ * inputs and output share it); lse_*: [n_rows, num_heads] fp32.  o_out and
+ * lse_out may alias o_a and lse_a.  lse_out may be NULL.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
+                           void* o_out, float* lse_out, int64_t n_rows, int num_heads, int head_dim,
+                           int dtype, void* stream);
+
+/*
+ * Read (and, with clear != 0, reset) the device error word a plan's kernels
+ * write when a check fails (page id out of range, indptr mismatch, a bounded
+ * wait that ran out).  Synchronises `stream`.  *code = 0 means no error.
+ */
+pkv_status pkv_get_device_error(const pkv_plan* plan, void* dev_ws, int* code, int clear,
+                                void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_BSR_H */

@@ -1,0 +1,217 @@
+// api.cu -- the extern "C" run entry points declared in include/pkv_bsr.h.
+//
+// Each call checks its arguments on the host, fills the kernel argument block
+// from the plan's fixed tables, and enqueues fixed-grid kernels on the
+// caller's stream.  Nothing here allocates, synchronises (except
+// pkv_get_device_error) or depends on the batch contents, which live in the
+// device workspace; so a sequence of run calls can be captured in a CUDA graph
+// and replayed after plan_run has written a new plan into the same workspace.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <mutex>
+#include <vector>
+
+#include "pkv_bsr.h"
+#include "pkv_device.cuh"
+#include "pkv_launch.h"
+#include "pkv_plan.h"
+
+namespace pkv {
+
+cudaError_t ensure_smem_limit_ptr(const void* kern, int bytes) {
+  struct Entry {
+    const void* kern;
+    int dev;
+    int bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& x : done)
+    if (x.kern == kern && x.dev == dev && x.bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.push_back({kern, dev, bytes});
+  return e;
+}
+
+}  // namespace pkv
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+pkv_status check_device(const pkv_plan* plan) {
+  if (plan->device < 0) return PKV_ERR_INVALID_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return cur == plan->device ? PKV_OK : PKV_ERR_INVALID_ARG;
+}
+
+template <typename Args>
+void fill_tables(Args& a, const pkv_plan* plan, void* dev_ws) {
+  auto* base = static_cast<uint8_t*>(dev_ws);
+  a.hdr = reinterpret_cast<const pkv::PlanHeader*>(base + plan->L.header);
+  a.worker_ptr = reinterpret_cast<const int32_t*>(base + plan->L.worker_ptr);
+  a.part_o = reinterpret_cast<float*>(base + plan->L.part_o);
+  a.part_lse = reinterpret_cast<float*>(base + plan->L.part_lse);
+  a.err = reinterpret_cast<int32_t*>(base + plan->L.header + offsetof(pkv::PlanHeader, error));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_BAD_INDEX: return "bad index array";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_WORKSPACE: return "workspace too small or limits exceeded";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_DEVICE_CHECK: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+int pkv_version(void) { return 100; }
+
+pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const void* kv_data,
+                                  const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
+                                  const int32_t* kv_last_page_len_d, void* o, float* lse, void* dev_ws,
+                                  void* stream) {
+  if (!plan || plan->kind != PKV_PLAN_DECODE || !plan->planned) return PKV_ERR_INVALID_ARG;
+  if (!q || !kv_data || !kv_indices_d || !kv_indptr_d || !kv_last_page_len_d || !o || !dev_ws)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_data, 16) || !aligned(o, 16) || !aligned(dev_ws, 256) ||
+      !aligned(kv_indices_d, 4) || !aligned(kv_indptr_d, 4) || (lse && !aligned(lse, 4)))
+    return PKV_ERR_INVALID_ARG;
+  pkv_status st = check_device(plan);
+  if (st != PKV_OK) return st;
+  const pkv_params& p = plan->p;
+  const bool cap = p.logits_cap > 0.f;
+  pkv::DecodeArgs a{};
+  fill_tables(a, plan, dev_ws);
+  auto* base = static_cast<uint8_t*>(dev_ws);
+  a.segs = reinterpret_cast<const pkv::DecodeSeg*>(base + plan->L.segs);
+  a.merge = reinterpret_cast<const pkv::MergeItem*>(base + plan->L.merge);
+  a.q = q;
+  a.kv = kv_data;
+  a.kv_indices = kv_indices_d;
+  a.kv_indptr = kv_indptr_d;
+  a.o = o;
+  a.lse = lse;
+  a.num_qo_heads = p.num_qo_heads;
+  a.num_kv_heads = p.num_kv_heads;
+  a.page_size = p.page_size;
+  a.q_scale = cap ? p.sm_scale : p.sm_scale * pkv::kLog2e;
+  a.cap = cap ? p.logits_cap : 0.f;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (plan->time_start) cudaEventRecord(plan->time_start, s);
+  cudaError_t e = pkv::launch_decode(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, s);
+  if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
+  if (e == cudaSuccess) e = pkv::launch_decode_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
+                                   const void* kv_data, const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
+                                   const int32_t* kv_last_page_len_d, void* o, float* lse, void* dev_ws,
+                                   void* stream) {
+  if (!plan || plan->kind != PKV_PLAN_PREFILL || !plan->planned) return PKV_ERR_INVALID_ARG;
+  if (!q || !qo_indptr_d || !kv_data || !kv_indices_d || !kv_indptr_d || !kv_last_page_len_d || !o || !dev_ws)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_data, 16) || !aligned(o, 16) || !aligned(dev_ws, 256) ||
+      !aligned(kv_indices_d, 4) || (lse && !aligned(lse, 4)))
+    return PKV_ERR_INVALID_ARG;
+  pkv_status st = check_device(plan);
+  if (st != PKV_OK) return st;
+  const pkv_params& p = plan->p;
+  pkv::PrefillArgs a{};
+  fill_tables(a, plan, dev_ws);
+  auto* base = static_cast<uint8_t*>(dev_ws);
+  a.tiles = reinterpret_cast<const pkv::PrefillTile*>(base + plan->L.segs);
+  a.merge = reinterpret_cast<const pkv::PrefillMerge*>(base + plan->L.merge);
+  a.q = q;
+  a.kv = kv_data;
+  a.kv_indices = kv_indices_d;
+  a.o = o;
+  a.lse = lse;
+  a.num_qo_heads = p.num_qo_heads;
+  a.num_kv_heads = p.num_kv_heads;
+  a.page_size = p.page_size;
+  a.causal = p.causal;
+  const bool cap = p.logits_cap > 0.f;
+  a.sm_scale = p.sm_scale;
+  a.cap = cap ? p.logits_cap : 0.f;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (plan->time_start) cudaEventRecord(plan->time_start, s);
+  cudaError_t e = pkv::launch_prefill(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas,
+                                      plan->total_q, plan->num_pages, s);
+  if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
+  if (e == cudaSuccess)
+    e = pkv::launch_prefill_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o_out,
+                           float* lse_out, int64_t n_rows, int num_heads, int head_dim, int dtype, void* stream) {
+  if (n_rows < 0 || num_heads <= 0 || head_dim <= 0) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F16 && dtype != PKV_BF16 && dtype != PKV_F32) return PKV_ERR_UNSUPPORTED;
+  if (n_rows == 0) return PKV_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o_out) return PKV_ERR_INVALID_ARG;
+  if (!aligned(o_a, 16) || !aligned(o_b, 16) || !aligned(o_out, 16) || !aligned(lse_a, 4) ||
+      !aligned(lse_b, 4) || (lse_out && !aligned(lse_out, 4)))
+    return PKV_ERR_INVALID_ARG;
+  cudaError_t e = pkv::launch_merge_state(o_a, lse_a, o_b, lse_b, o_out, lse_out, n_rows * num_heads, head_dim,
+                                          dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_plan_set_timing_events(pkv_plan* plan, void* start, void* stop) {
+  if (!plan || (!start) != (!stop)) return PKV_ERR_INVALID_ARG;
+  plan->time_start = static_cast<cudaEvent_t>(start);
+  plan->time_stop = static_cast<cudaEvent_t>(stop);
+  return PKV_OK;
+}
+
+pkv_status pkv_get_device_error(const pkv_plan* plan, void* dev_ws, int* code, int clear, void* stream) {
+  if (!plan || !dev_ws || !code) return PKV_ERR_INVALID_ARG;
+  auto s = static_cast<cudaStream_t>(stream);
+  auto* word = static_cast<uint8_t*>(dev_ws) + plan->L.header + offsetof(pkv::PlanHeader, error);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  *code = v;
+  if (clear && v) {
+    if (cudaMemsetAsync(word, 0, sizeof(int32_t), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

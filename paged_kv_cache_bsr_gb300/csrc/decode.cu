@@ -1,0 +1,483 @@
+// decode.cu -- batch decode over a paged KV cache, split-KV capable.
+//
+// Method (FlashInfer pages): the kernel follows each request's page table to
+// gather K/V from non-contiguous pages ("FlashInfer" guide, section 2
+// "Page-Level Attention"), computes one query token's attention for all query
+// heads of one kv head at once (greptalks summary, "Head Group Packing"), and,
+// when the host plan split a long sequence into chunks, writes each chunk's
+// partial output with its log-sum-exp so a merge can combine them (guide,
+// section 3 "FlashDecoding"; fdeinterviews, "Load balancing").
+//
+// GB300 design.  Decode reads every K/V byte once, so it is HBM-bound
+// (about half a flop per byte at a group of 4).  One CTA per SM holds
+// kDecodeWarps independent workers (warps).  Each warp owns a ring of page
+// tiles in shared memory (32 KB) that its lane 0 fills with TMA bulk copies
+// (cp.async.bulk, completion on an mbarrier): one copy for the tile's K rows
+// and one for its V rows, each a contiguous 16-row x head_dim block of a page.
+// The copies run ahead of the compute by the depth of the ring, so every SM
+// keeps up to 192 KB of reads in flight.  A warp works through the list of
+// (request, kv head, page range) segments the plan gave it, back to back, so
+// the ring never drains between segments.
+//
+// Inside a tile, LPT lanes share one token (each holding D/LPT dims as
+// 16-byte chunks, interleaved so a quarter-warp reads 128 contiguous bytes),
+// 32/LPT tokens go per step, scores are summed with xor-shuffles inside the
+// token group, and the online softmax keeps (max, sum, o) per head in
+// registers, with max and o rescaled only when a tile raises the max.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "pkv_device.cuh"
+#include "pkv_launch.h"
+#include "pkv_bsr.h"
+
+namespace pkv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int D, typename T>
+struct DecodeShape {
+  static constexpr int kTileBytes = kDecodeTileRows * D * 2;  // K (or V) rows of one tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStages = kDecodeWarpSmem / kStageBytes;
+  static_assert(kStages >= 2, "ring too shallow");
+};
+
+struct SegInfo {
+  int b, kvh, idx_begin, n_pages, last_rows, page_begin, slot;
+};
+
+__device__ __forceinline__ SegInfo load_seg(const DecodeSeg* segs, int i, int lane) {
+  const int v = lane < 8 ? reinterpret_cast<const int32_t*>(segs + i)[lane] : 0;
+  SegInfo s;
+  s.b = __shfl_sync(kFull, v, 0);
+  s.kvh = __shfl_sync(kFull, v, 1);
+  s.idx_begin = __shfl_sync(kFull, v, 2);
+  s.n_pages = __shfl_sync(kFull, v, 3);
+  s.last_rows = __shfl_sync(kFull, v, 4);
+  s.page_begin = __shfl_sync(kFull, v, 5);
+  s.slot = __shfl_sync(kFull, v, 6);
+  return s;
+}
+
+// The copy side of a warp's ring: walks the same (segment, page, 16-row chunk)
+// sequence as the compute side, S tiles ahead of it.  Page ids come from a
+// 32-entry window of kv_indices held one per lane.
+struct Producer {
+  int seg, seg_end;
+  int page, chunk;
+  int idx_begin, n_pages, last_rows, kvh;
+  int win_base, win;
+  int issued;
+};
+
+template <int D, typename T>
+__device__ __forceinline__ void producer_enter(Producer& p, const DecodeArgs& a, int lane) {
+  const SegInfo s = load_seg(a.segs, p.seg, lane);
+  p.idx_begin = s.idx_begin;
+  p.n_pages = s.n_pages;
+  p.last_rows = s.last_rows;
+  p.kvh = s.kvh;
+  p.page = 0;
+  p.chunk = 0;
+  p.win_base = 0;
+  p.win = lane < p.n_pages ? __ldg(a.kv_indices + p.idx_begin + lane) : 0;
+}
+
+// Issue the next tile of the warp's stream into its stage; false when done.
+template <int D, typename T>
+__device__ __forceinline__ bool producer_issue(Producer& p, const DecodeArgs& a, uint8_t* ring,
+                                               uint32_t bar0, int lane, int64_t num_pages,
+                                               uint64_t policy) {
+  using Shape = DecodeShape<D, T>;
+  while (p.seg < p.seg_end) {
+    if (p.page < p.n_pages) {
+      if (p.page - p.win_base >= 32) {
+        p.win_base = p.page;
+        p.win = (p.page + lane < p.n_pages) ? __ldg(a.kv_indices + p.idx_begin + p.page + lane) : 0;
+      }
+      int page_id = __shfl_sync(kFull, p.win, p.page - p.win_base);
+      const int P = a.page_size;
+      const int rows_in_page = (p.page == p.n_pages - 1) ? p.last_rows : P;
+      const int r0 = p.chunk * kDecodeTileRows;
+      const int rows = min(kDecodeTileRows, rows_in_page - r0);
+      if (page_id < 0 || page_id >= num_pages) {
+        if (lane == 0) atomicOr(a.err, kErrPageIndex);
+        page_id = 0;
+      }
+      const int stage = p.issued % Shape::kStages;
+      if (lane == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(rows) * D * sizeof(T);
+        const T* kv = static_cast<const T*>(a.kv);
+        const int64_t head_rows = static_cast<int64_t>(P) * D;  // elements of one (page, K|V, head)
+        const T* k_src = kv + ((static_cast<int64_t>(page_id) * 2 + 0) * a.num_kv_heads + p.kvh) * head_rows +
+                         static_cast<int64_t>(r0) * D;
+        const T* v_src = k_src + static_cast<int64_t>(a.num_kv_heads) * head_rows;
+        const uint32_t dst = smem_addr(ring + stage * Shape::kStageBytes);
+        const uint32_t bar = bar0 + 8 * stage;
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_copy_g2s_hint(dst, k_src, bytes, bar, policy);
+        bulk_copy_g2s_hint(dst + Shape::kTileBytes, v_src, bytes, bar, policy);
+      }
+      ++p.issued;
+      ++p.chunk;
+      if (p.chunk * kDecodeTileRows >= rows_in_page) {
+        p.chunk = 0;
+        ++p.page;
+      }
+      return true;
+    }
+    ++p.seg;
+    if (p.seg < p.seg_end) producer_enter<D, T>(p, a, lane);
+  }
+  return false;
+}
+
+template <int D, int G, int LPT, typename T, bool CAP>
+__global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
+  using Shape = DecodeShape<D, T>;
+  constexpr int S = Shape::kStages;
+  constexpr int VEC = D / LPT;     // dims per lane
+  constexpr int CH = VEC / 8;      // 16-byte chunks per lane per row
+  constexpr int TPS = 32 / LPT;    // tokens per step
+  constexpr int STEPS = kDecodeTileRows / TPS;
+  static_assert(CH >= 1 && VEC % 8 == 0, "lane slice must be whole 16-byte chunks");
+  static_assert(kDecodeTileRows % TPS == 0, "steps must tile the 16 rows");
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kDecodeWarps][S];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % LPT;   // dim slice of this lane
+  const int grp = lane / LPT;   // token slot of this lane within a step
+  uint8_t* ring = smem + warp * kDecodeWarpSmem;
+  const uint32_t bar0 = smem_addr(&bars[warp][0]);
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(bar0 + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const int worker = blockIdx.x * kDecodeWarps + warp;
+  const PlanHeader* hdr = a.hdr;
+  if (worker >= hdr->num_workers) return;
+  const int64_t num_pages = hdr->num_pages;
+  const int seg_begin = a.worker_ptr[worker];
+  const int seg_end = a.worker_ptr[worker + 1];
+  if (seg_begin >= seg_end) return;
+  const uint64_t policy = l2_policy_evict_first();
+
+  Producer prod;
+  prod.seg = seg_begin;
+  prod.seg_end = seg_end;
+  prod.issued = 0;
+  producer_enter<D, T>(prod, a, lane);
+  for (int s = 0; s < S; ++s)
+    if (!producer_issue<D, T>(prod, a, ring, bar0, lane, num_pages, policy)) break;
+
+  int consumed = 0;
+  bool ok = true;
+  const T* q_all = static_cast<const T*>(a.q);
+
+  for (int si = seg_begin; si < seg_end && ok; ++si) {
+    const SegInfo sg = load_seg(a.segs, si, lane);
+    const int hq0 = sg.kvh * G;
+    int indptr_seen = 0;
+    if (lane == 0) indptr_seen = __ldg(a.kv_indptr + sg.b);
+
+    // Query rows of the head group, pre-scaled (log2 domain without a cap).
+    float qf[G][VEC];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const T* qrow = q_all + (static_cast<int64_t>(sg.b) * a.num_qo_heads + hq0 + g) * D;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        float f[8];
+        to_float8<T>(ld_nc_v4(qrow + (sub + c * LPT) * 8), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qf[g][c * 8 + e] = f[e] * a.q_scale;
+      }
+    }
+    float m[G], l[G], acc[G][VEC];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) acc[g][v] = 0.f;
+    }
+
+    for (int pg = 0; pg < sg.n_pages && ok; ++pg) {
+      const int rows_in_page = (pg == sg.n_pages - 1) ? sg.last_rows : a.page_size;
+      for (int r0 = 0; r0 < rows_in_page; r0 += kDecodeTileRows) {
+        const int rows = min(kDecodeTileRows, rows_in_page - r0);
+        const int stage = consumed % S;
+        if (!mbar_wait(bar0 + 8 * stage, (consumed / S) & 1, a.err)) {
+          ok = false;
+          break;
+        }
+        const T* ks = reinterpret_cast<const T*>(ring + stage * Shape::kStageBytes);
+        const T* vs = ks + kDecodeTileRows * D;
+
+        float sc[STEPS][G];
+#pragma unroll
+        for (int st = 0; st < STEPS; ++st) {
+          const int tok = st * TPS + grp;
+          float part[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) part[g] = 0.f;
+          if (tok < rows) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+              float kf[8];
+              to_float8<T>(*reinterpret_cast<const uint4*>(ks + tok * D + (sub + c * LPT) * 8), kf);
+#pragma unroll
+              for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) part[g] = fmaf(qf[g][c * 8 + e], kf[e], part[g]);
+            }
+          }
+#pragma unroll
+          for (int o = LPT / 2; o >= 1; o >>= 1)
+#pragma unroll
+            for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(kFull, part[g], o);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float x = part[g];
+            if constexpr (CAP) x = a.cap * tanhf(x / a.cap) * kLog2e;
+            sc[st][g] = tok < rows ? x : -INFINITY;
+          }
+        }
+        // Tile max per head over all tokens of the tile; rescale only when it grows.
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float mx = sc[0][g];
+#pragma unroll
+          for (int st = 1; st < STEPS; ++st) mx = fmaxf(mx, sc[st][g]);
+          mx = warp_max(mx, 16, LPT);
+          if (mx > m[g]) {
+            const float alpha = fast_exp2(m[g] - mx);
+            l[g] *= alpha;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc[g][v] *= alpha;
+            m[g] = mx;
+          }
+        }
+#pragma unroll
+        for (int st = 0; st < STEPS; ++st) {
+          const int tok = st * TPS + grp;
+          if (tok < rows) {
+            float p[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              p[g] = fast_exp2(sc[st][g] - m[g]);
+              l[g] += p[g];
+            }
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+              float vf[8];
+              to_float8<T>(*reinterpret_cast<const uint4*>(vs + tok * D + (sub + c * LPT) * 8), vf);
+#pragma unroll
+              for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[g][c * 8 + e] = fmaf(p[g], vf[e], acc[g][c * 8 + e]);
+            }
+          }
+        }
+        ++consumed;
+        __syncwarp();
+        producer_issue<D, T>(prod, a, ring, bar0, lane, num_pages, policy);
+      }
+    }
+    if (!ok) break;
+
+    // Combine the token groups: every lane ends with the full sums of its dims.
+#pragma unroll
+    for (int o = LPT; o < 32; o <<= 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        l[g] += __shfl_xor_sync(kFull, l[g], o);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[g][v] += __shfl_xor_sync(kFull, acc[g][v], o);
+      }
+
+    if (lane == 0 && indptr_seen != sg.idx_begin - sg.page_begin) atomicOr(a.err, kErrIndptrMismatch);
+
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (g % TPS != grp) continue;
+      const bool empty = sg.n_pages == 0;
+      const float inv = empty ? 0.f : 1.f / l[g];
+      const float lse_v = empty ? -INFINITY : (m[g] + log2f(l[g])) * kLn2;
+      if (sg.slot < 0) {
+        T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(sg.b) * a.num_qo_heads + hq0 + g) * D;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = acc[g][c * 8 + e] * inv;
+          *reinterpret_cast<uint4*>(orow + (sub + c * LPT) * 8) = from_float8<T>(f);
+        }
+        if (sub == 0 && a.lse) a.lse[static_cast<int64_t>(sg.b) * a.num_qo_heads + hq0 + g] = lse_v;
+      } else {
+        float* prow = a.part_o + (static_cast<int64_t>(sg.slot) * G + g) * D;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          float4* dst = reinterpret_cast<float4*>(prow + (sub + c * LPT) * 8);
+          dst[0] = make_float4(acc[g][c * 8 + 0] * inv, acc[g][c * 8 + 1] * inv,
+                               acc[g][c * 8 + 2] * inv, acc[g][c * 8 + 3] * inv);
+          dst[1] = make_float4(acc[g][c * 8 + 4] * inv, acc[g][c * 8 + 5] * inv,
+                               acc[g][c * 8 + 6] * inv, acc[g][c * 8 + 7] * inv);
+        }
+        if (sub == 0) a.part_lse[static_cast<int64_t>(sg.slot) * G + g] = lse_v;
+      }
+    }
+  }
+
+  if (!ok) {
+    // A wait ran out: let this warp's copies still in flight land before the
+    // CTA's shared memory is released, each wait again bounded.
+    for (int t = consumed + 1; t < prod.issued; ++t)
+      if (!mbar_wait(bar0 + 8 * (t % S), (t / S) & 1, a.err)) break;
+  }
+}
+
+// n-way merge of the partial states of split (request, kv head) sequences:
+// one CTA per (item, head of the group); warps take slots, lanes take dims.
+template <int D, int G, typename T>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
+  constexpr int NW = kMergeThreads / 32;
+  constexpr int PER = D / 32;  // dims per lane
+  __shared__ float s_acc[NW][D];
+  __shared__ float s_w[NW];
+  __shared__ float s_max[NW];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pairs = a.hdr->num_merge * G;
+  for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x) {
+    const MergeItem it = a.merge[pair / G];
+    const int g = pair % G;
+    float mx = -INFINITY;
+    for (int i = threadIdx.x; i < it.n_slots; i += kMergeThreads)
+      mx = fmaxf(mx, a.part_lse[static_cast<int64_t>(it.slot_begin + i) * G + g]);
+    mx = warp_max(mx);
+    if (lane == 0) s_max[warp] = mx;
+    __syncthreads();
+    mx = s_max[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) mx = fmaxf(mx, s_max[w]);
+    float acc[PER];
+#pragma unroll
+    for (int v = 0; v < PER; ++v) acc[v] = 0.f;
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+      for (int i = warp; i < it.n_slots; i += NW) {
+        const int64_t slot = it.slot_begin + i;
+        const float w = fast_exp2((a.part_lse[slot * G + g] - mx) * kLog2e);
+        const float* src = a.part_o + (slot * G + g) * D + lane * PER;
+        float v4[PER];
+        if constexpr (PER == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(src);
+          v4[0] = t.x; v4[1] = t.y; v4[2] = t.z; v4[3] = t.w;
+        } else {
+#pragma unroll
+          for (int v = 0; v < PER; ++v) v4[v] = src[v];
+        }
+#pragma unroll
+        for (int v = 0; v < PER; ++v) acc[v] = fmaf(w, v4[v], acc[v]);
+        wsum += w;
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < PER; ++v) s_acc[warp][lane * PER + v] = acc[v];
+    if (lane == 0) s_w[warp] = wsum;
+    __syncthreads();
+    if (warp == 0) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) tot += s_w[w];
+      const int hq = it.kvh * G + g;
+      T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(it.b) * a.num_qo_heads + hq) * D;
+      const float inv = tot > 0.f ? 1.f / tot : 0.f;
+#pragma unroll
+      for (int v = 0; v < PER; ++v) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) s += s_acc[w][lane * PER + v];
+        orow[lane * PER + v] = from_float<T>(s * inv);
+      }
+      if (lane == 0 && a.lse)
+        a.lse[static_cast<int64_t>(it.b) * a.num_qo_heads + hq] =
+            tot > 0.f ? mx + logf(tot) : -INFINITY;
+    }
+    __syncthreads();
+  }
+}
+
+template <int D, int G, int LPT, typename T>
+cudaError_t launch_decode_t(const DecodeArgs& a, bool cap, int grid, cudaStream_t stream) {
+  const int smem = kDecodeWarps * kDecodeWarpSmem;
+  auto kern = cap ? decode_kernel<D, G, LPT, T, true> : decode_kernel<D, G, LPT, T, false>;
+  cudaError_t e = ensure_smem_limit(kern, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kDecodeWarps * 32, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_decode(const DecodeArgs& a, int D, int G, bool cap, int grid, cudaStream_t s) {
+  if (D == 128) {
+    switch (G) {
+      case 1: return launch_decode_t<128, 1, 8, T>(a, cap, grid, s);
+      case 2: return launch_decode_t<128, 2, 8, T>(a, cap, grid, s);
+      case 4: return launch_decode_t<128, 4, 8, T>(a, cap, grid, s);
+      case 8: return launch_decode_t<128, 8, 16, T>(a, cap, grid, s);
+    }
+  } else if (D == 64) {
+    switch (G) {
+      case 1: return launch_decode_t<64, 1, 8, T>(a, cap, grid, s);
+      case 2: return launch_decode_t<64, 2, 8, T>(a, cap, grid, s);
+      case 4: return launch_decode_t<64, 4, 8, T>(a, cap, grid, s);
+      case 8: return launch_decode_t<64, 8, 8, T>(a, cap, grid, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t dispatch_merge(const DecodeArgs& a, int D, int G, int grid, cudaStream_t s) {
+#define PKV_MERGE_CASE(DD, GG)                                            \
+  if (D == DD && G == GG) {                                               \
+    decode_merge_kernel<DD, GG, T><<<grid, kMergeThreads, 0, s>>>(a);     \
+    return cudaGetLastError();                                            \
+  }
+  PKV_MERGE_CASE(128, 1) PKV_MERGE_CASE(128, 2) PKV_MERGE_CASE(128, 4) PKV_MERGE_CASE(128, 8)
+  PKV_MERGE_CASE(64, 1) PKV_MERGE_CASE(64, 2) PKV_MERGE_CASE(64, 4) PKV_MERGE_CASE(64, 8)
+#undef PKV_MERGE_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool decode_supported(int head_dim, int group, int dtype) {
+  return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4 || group == 8) &&
+         (dtype == PKV_F16 || dtype == PKV_BF16);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, int head_dim, int group, int dtype, bool cap, int grid,
+                          cudaStream_t stream) {
+  if (dtype == PKV_BF16) return dispatch_decode<__nv_bfloat16>(a, head_dim, group, cap, grid, stream);
+  if (dtype == PKV_F16) return dispatch_decode<__half>(a, head_dim, group, cap, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_merge(const DecodeArgs& a, int head_dim, int group, int dtype, int grid,
+                                cudaStream_t stream) {
+  if (dtype == PKV_BF16) return dispatch_merge<__nv_bfloat16>(a, head_dim, group, grid, stream);
+  if (dtype == PKV_F16) return dispatch_merge<__half>(a, head_dim, group, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

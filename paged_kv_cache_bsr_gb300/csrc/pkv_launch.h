@@ -1,0 +1,98 @@
+// pkv_launch.h -- host-side launch interface between the C ABI layer and the
+// kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// Arguments of the decode and decode-merge kernels.
+struct DecodeArgs {
+  const void* q;               // [batch, Hq, D]
+  const void* kv;              // [num_pages, 2, Hkv, P, D]
+  const int32_t* kv_indices;   // page table (BSR column indices)
+  const int32_t* kv_indptr;    // checked against the plan
+  void* o;                     // [batch, Hq, D]
+  float* lse;                  // [batch, Hq] or nullptr
+  const PlanHeader* hdr;       // plan tables in the device workspace
+  const int32_t* worker_ptr;
+  const DecodeSeg* segs;
+  const MergeItem* merge;
+  float* part_o;               // [slots, G, D]
+  float* part_lse;             // [slots, G]
+  int32_t* err;                // &hdr->error
+  int num_qo_heads;
+  int num_kv_heads;
+  int page_size;
+  float q_scale;               // multiplies q: sm_scale * log2(e) without a cap, sm_scale with one
+  float cap;                   // logits cap (> 0 only in the capped instantiation)
+};
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device): the
+// first launch on a device does it, so later launches (e.g. inside CUDA-graph
+// capture) make no attribute call.
+cudaError_t ensure_smem_limit_ptr(const void* kern, int bytes);
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kern, int bytes) {
+  return ensure_smem_limit_ptr(reinterpret_cast<const void*>(kern), bytes);
+}
+
+// Warps per decode CTA; each warp streams its own pages (one CTA per SM).
+constexpr int kDecodeWarps = 6;
+// Shared memory each decode warp uses for its ring of page tiles.
+constexpr int kDecodeWarpSmem = 32 * 1024;
+constexpr int kDecodeTileRows = 16;
+constexpr int kMergeThreads = 256;
+
+// Launch the decode kernel for (head_dim, group, dtype, cap); returns
+// cudaErrorInvalidValue for a combination that was not built.
+cudaError_t launch_decode(const DecodeArgs& a, int head_dim, int group, int dtype, bool cap,
+                          int grid, cudaStream_t stream);
+// Launch the n-way merge of split decode sequences (fixed grid).
+cudaError_t launch_decode_merge(const DecodeArgs& a, int head_dim, int group, int dtype, int grid,
+                                cudaStream_t stream);
+// Elementwise two-state merge_state.
+cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* o_b,
+                               const float* lse_b, void* o_out, float* lse_out, int64_t rows,
+                               int head_dim, int dtype, cudaStream_t stream);
+
+bool decode_supported(int head_dim, int group, int dtype);
+
+// Prefill work tile: kPrefillRows packed query rows x kPrefillKeys keys.
+constexpr int kPrefillRows = 128;
+constexpr int kPrefillKeys = 128;
+
+bool prefill_supported(int head_dim, int group, int dtype, int page_size);
+
+// Arguments of the prefill and prefill-merge kernels (tensor maps for q and
+// kv_data are built at launch and passed separately).
+struct PrefillArgs {
+  const void* q;               // [total_q, Hq, D]
+  const void* kv;              // [num_pages, 2, Hkv, P, D]
+  const int32_t* kv_indices;
+  void* o;                     // [total_q, Hq, D]
+  float* lse;                  // [total_q, Hq] or nullptr
+  const PlanHeader* hdr;
+  const int32_t* worker_ptr;
+  const PrefillTile* tiles;
+  const PrefillMerge* merge;
+  float* part_o;               // [slots, kPrefillRows, D]
+  float* part_lse;             // [slots, kPrefillRows]
+  int32_t* err;
+  int num_qo_heads;
+  int num_kv_heads;
+  int page_size;
+  int causal;
+  float sm_scale;
+  float cap;                   // > 0 only in the capped instantiation
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dtype, bool cap, int grid,
+                           int64_t total_q, int64_t num_pages, cudaStream_t stream);
+cudaError_t launch_prefill_merge(const PrefillArgs& a, int head_dim, int group, int dtype, int grid,
+                                 cudaStream_t stream);
+
+}  // namespace pkv

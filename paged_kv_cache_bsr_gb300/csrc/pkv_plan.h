@@ -1,0 +1,48 @@
+// pkv_plan.h -- the host plan object behind the opaque pkv_plan handle.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "pkv_bsr.h"
+#include "pkv_internal.h"
+
+struct pkv_plan {
+  int kind = 0;
+  pkv_params p{};
+  pkv_limits lim{};
+  int device = -1;          // -1: host-only plan (pkv_plan_create_host)
+  int num_sms = 0;
+  int group = 1;
+  // Fixed grid and table capacities (depend on params and limits only).
+  int grid_ctas = 0;
+  int workers = 0;
+  int max_work = 0;
+  int max_merge = 0;
+  int max_slots = 0;
+  int rows_per_slot = 0;
+  int merge_grid = 0;
+  pkv::WorkspaceLayout L{};
+  size_t host_bytes = 0;
+  // Last computed plan.
+  bool planned = false;
+  int batch = 0;
+  int64_t num_pages = 0;
+  int64_t total_q = 0;
+  int active_workers = 0;
+  int num_work = 0;
+  int num_merge = 0;
+  int num_slots = 0;
+  int64_t max_cost = 0;
+  int64_t total_cost = 0;
+  size_t used_bytes = 0;
+  std::vector<int32_t> work_rows;  // 8 int32 per work entry, for pkv_plan_get_work
+  // The copy of the tables out of the pinned buffer.
+  cudaEvent_t copy_done = nullptr;
+  bool copy_pending = false;
+  // Caller events recorded around the main kernel (pkv_plan_set_timing_events).
+  cudaEvent_t time_start = nullptr;
+  cudaEvent_t time_stop = nullptr;
+};

@@ -1,0 +1,517 @@
+// plan.cpp -- the host-side plan (the "inspector" of an inspector-executor pair).
+//
+// fdeinterviews summary, "Load balancing that survives CUDA graphs": each
+// step a CPU-side plan splits long KV sequences into equal chunks across the
+// GPU's processors and records where partial results go; fixed-grid kernels
+// then run.  greptalks summary, "Runtime Scheduler": a cost model decides the
+// schedule deterministically from the sequence lengths alone.
+//
+// Decode: the work is the sequence of (request, kv head) page lists laid end
+// to end.  With W workers (warps of the fixed grid) every worker takes one
+// contiguous run of ceil(total_pages / W) pages of that sequence, so all
+// workers stream the same number of pages whatever the length mix.  A page
+// list cut by a run boundary becomes several partial states, each with its own
+// slot, and one merge record.
+//
+// Prefill: the work is one tile per (request, kv head, block of query
+// positions); its cost is the number of 128-key blocks it must visit (after
+// the causal limit).  A tile costing more than total/CTAs is cut into key
+// chunks with partial slots; tiles are then assigned longest-first to the
+// least-loaded CTA.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <functional>
+#include <new>
+#include <queue>
+#include <utility>
+#include <vector>
+
+#include "pkv_bsr.h"
+#include "pkv_internal.h"
+#include "pkv_launch.h"
+#include "pkv_plan.h"
+
+using pkv::DecodeSeg;
+using pkv::MergeItem;
+using pkv::PlanHeader;
+using pkv::PrefillMerge;
+using pkv::PrefillTile;
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool is_pow2_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+pkv_status check_params(int kind, const pkv_params* p, const pkv_limits* lim) {
+  if (!p || !lim) return PKV_ERR_INVALID_ARG;
+  if (kind != PKV_PLAN_DECODE && kind != PKV_PLAN_PREFILL) return PKV_ERR_INVALID_ARG;
+  if (p->num_qo_heads <= 0 || p->num_kv_heads <= 0 || p->num_qo_heads % p->num_kv_heads)
+    return PKV_ERR_INVALID_ARG;
+  if (p->page_size <= 0 || (p->page_size > 16 && p->page_size % 16)) return PKV_ERR_UNSUPPORTED;
+  if (!(p->sm_scale > 0.f)) return PKV_ERR_INVALID_ARG;
+  if (lim->max_batch < 0 || lim->max_total_q < 0 || lim->max_kv_pages < 0) return PKV_ERR_INVALID_ARG;
+  if (lim->max_kv_pages > INT32_MAX || lim->max_total_q > INT32_MAX) return PKV_ERR_INVALID_ARG;
+  const int g = p->num_qo_heads / p->num_kv_heads;
+  if (p->dtype != PKV_F16 && p->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (kind == PKV_PLAN_DECODE && !pkv::decode_supported(p->head_dim, g, p->dtype)) return PKV_ERR_UNSUPPORTED;
+  if (kind == PKV_PLAN_PREFILL && !pkv::prefill_supported(p->head_dim, g, p->dtype, p->page_size))
+    return PKV_ERR_UNSUPPORTED;
+  if (!is_pow2_group(g)) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+void set_layout(pkv_plan* pl) {
+  pkv::WorkspaceLayout& L = pl->L;
+  const bool dec = pl->kind == PKV_PLAN_DECODE;
+  const size_t work_bytes = dec ? sizeof(DecodeSeg) : sizeof(PrefillTile);
+  const size_t merge_bytes = dec ? sizeof(MergeItem) : sizeof(PrefillMerge);
+  L.header = 0;
+  L.worker_ptr = align_up(sizeof(PlanHeader), 256);
+  L.merge = align_up(L.worker_ptr + sizeof(int32_t) * (pl->workers + 1), 256);
+  L.segs = align_up(L.merge + merge_bytes * std::max(pl->max_merge, 1), 256);
+  L.tables_end = align_up(L.segs + work_bytes * std::max(pl->max_work, 1), 256);
+  L.part_o = L.tables_end;
+  L.part_lse = align_up(L.part_o + sizeof(float) * (size_t)pl->max_slots * pl->rows_per_slot * pl->p.head_dim, 256);
+  L.total = align_up(L.part_lse + sizeof(float) * (size_t)pl->max_slots * pl->rows_per_slot, 256);
+}
+
+pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const pkv_limits* limits,
+                     int device, int num_sms) {
+  if (!out) return PKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  pkv_status st = check_params(kind, params, limits);
+  if (st != PKV_OK) return st;
+  if (num_sms <= 0) return PKV_ERR_INVALID_ARG;
+  pkv_plan* pl = new (std::nothrow) pkv_plan();
+  if (!pl) return PKV_ERR_INVALID_ARG;
+  pl->kind = kind;
+  pl->p = *params;
+  pl->lim = *limits;
+  pl->device = device;
+  pl->num_sms = num_sms;
+  pl->group = params->num_qo_heads / params->num_kv_heads;
+  const int64_t hkv = params->num_kv_heads;
+  if (kind == PKV_PLAN_DECODE) {
+    pl->grid_ctas = num_sms;
+    pl->workers = num_sms * pkv::kDecodeWarps;
+    // Each worker's run cuts at most two page lists, and every list adds at
+    // most one uncut entry; see the decode branch of compute_decode.
+    pl->max_work = static_cast<int>(pl->workers + (int64_t)limits->max_batch * hkv + 1);
+    pl->max_merge = static_cast<int>(std::min<int64_t>((int64_t)limits->max_batch * hkv, pl->workers) + 1);
+    pl->max_slots = 2 * pl->workers;
+    pl->rows_per_slot = pl->group;
+    pl->merge_grid = num_sms * 2;
+  } else {
+    const int mp = pkv::kPrefillRows / pl->group;  // query positions per tile
+    pl->grid_ctas = num_sms;
+    pl->workers = num_sms;
+    const int64_t tiles = (ceil_div(limits->max_total_q, mp) + limits->max_batch) * hkv;
+    // Splitting only touches tiles costing more than total / CTAs (fewer than
+    // CTAs of them), and adds at most CTAs chunks in total.
+    pl->max_work = static_cast<int>(tiles + 2 * (int64_t)num_sms + 1);
+    pl->max_merge = num_sms + 1;
+    pl->max_slots = 2 * num_sms + 2;
+    pl->rows_per_slot = pkv::kPrefillRows;
+    pl->merge_grid = num_sms * 4;
+  }
+  set_layout(pl);
+  pl->host_bytes = pl->L.tables_end;
+  *out = pl;
+  return PKV_OK;
+}
+
+// Common validation of the host index arrays.
+pkv_status validate(const pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                    const int32_t* kv_indices, const int32_t* kv_last, int64_t num_pages) {
+  if (batch < 0 || !kv_indptr || (batch > 0 && !kv_last)) return PKV_ERR_INVALID_ARG;
+  if (batch > pl->lim.max_batch) return PKV_ERR_WORKSPACE;
+  if (pl->kind == PKV_PLAN_PREFILL && !qo_indptr) return PKV_ERR_INVALID_ARG;
+  if (num_pages < 0 || num_pages > INT32_MAX) return PKV_ERR_INVALID_ARG;
+  if (kv_indptr[0] != 0) return PKV_ERR_BAD_INDEX;
+  for (int b = 0; b < batch; ++b) {
+    const int32_t n = kv_indptr[b + 1] - kv_indptr[b];
+    if (n < 0) return PKV_ERR_BAD_INDEX;
+    if (n > 0 && (kv_last[b] < 1 || kv_last[b] > pl->p.page_size)) return PKV_ERR_BAD_INDEX;
+  }
+  const int64_t nnz = kv_indptr[batch];
+  if (nnz > pl->lim.max_kv_pages) return PKV_ERR_WORKSPACE;
+  if (nnz > 0 && num_pages == 0) return PKV_ERR_BAD_INDEX;
+  if (kv_indices)
+    for (int64_t j = 0; j < nnz; ++j)
+      if (kv_indices[j] < 0 || kv_indices[j] >= num_pages) return PKV_ERR_BAD_INDEX;
+  if (qo_indptr) {
+    if (qo_indptr[0] != 0) return PKV_ERR_BAD_INDEX;
+    for (int b = 0; b < batch; ++b)
+      if (qo_indptr[b + 1] < qo_indptr[b]) return PKV_ERR_BAD_INDEX;
+    if (qo_indptr[batch] > pl->lim.max_total_q) return PKV_ERR_WORKSPACE;
+  } else if (batch > pl->lim.max_total_q) {
+    return PKV_ERR_WORKSPACE;
+  }
+  return PKV_OK;
+}
+
+int64_t kv_len_of(const int32_t* kv_indptr, const int32_t* kv_last, int b, int P) {
+  const int64_t n = kv_indptr[b + 1] - kv_indptr[b];
+  return n > 0 ? (n - 1) * P + kv_last[b] : 0;
+}
+
+pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, const int32_t* kv_last,
+                          uint8_t* host) {
+  const int P = pl->p.page_size;
+  const int hkv = pl->p.num_kv_heads;
+  const int W = pl->workers;
+  const int64_t pages_per_chunk = ceil_div(P, pkv::kDecodeTileRows);
+  const int64_t min_run = std::max<int64_t>(1, 8 / pages_per_chunk);  // keep runs >= 8 tiles
+  int64_t total = 0;
+  for (int b = 0; b < batch; ++b) total += (int64_t)(kv_indptr[b + 1] - kv_indptr[b]) * hkv;
+  const int64_t run = total > 0 ? std::max<int64_t>(ceil_div(total, W), min_run) : 1;
+  const int active = total > 0 ? static_cast<int>(ceil_div(total, run)) : (batch > 0 ? 1 : 0);
+
+  auto* hdr = reinterpret_cast<PlanHeader*>(host + pl->L.header);
+  auto* wptr = reinterpret_cast<int32_t*>(host + pl->L.worker_ptr);
+  auto* merge = reinterpret_cast<MergeItem*>(host + pl->L.merge);
+  auto* segs = reinterpret_cast<DecodeSeg*>(host + pl->L.segs);
+
+  int n_seg = 0, n_merge = 0, n_slot = 0;
+  int cur_worker = 0;
+  wptr[0] = 0;
+  auto emit = [&](int worker, const DecodeSeg& s) {
+    while (cur_worker < worker) wptr[++cur_worker] = n_seg;
+    segs[n_seg++] = s;
+  };
+  int64_t x = 0;  // offset of the current page list in the concatenated sequence
+  for (int b = 0; b < batch; ++b) {
+    const int32_t n = kv_indptr[b + 1] - kv_indptr[b];
+    for (int h = 0; h < hkv; ++h) {
+      DecodeSeg s{};
+      s.b = b;
+      s.kvh = h;
+      if (n == 0) {
+        const int w = static_cast<int>(std::min<int64_t>(x / run, active - 1));
+        s.idx_begin = kv_indptr[b];
+        s.n_pages = 0;
+        s.last_rows = 0;
+        s.page_begin = 0;
+        s.slot = -1;
+        emit(w, s);
+        continue;
+      }
+      const int w0 = static_cast<int>(x / run);
+      const int w1 = static_cast<int>((x + n - 1) / run);
+      if (w0 == w1) {
+        s.idx_begin = kv_indptr[b];
+        s.n_pages = n;
+        s.last_rows = kv_last[b];
+        s.page_begin = 0;
+        s.slot = -1;
+        emit(w0, s);
+      } else {
+        MergeItem m{b, h, n_slot, w1 - w0 + 1};
+        merge[n_merge++] = m;
+        for (int w = w0; w <= w1; ++w) {
+          const int64_t lo = std::max<int64_t>(x, (int64_t)w * run) - x;
+          const int64_t hi = std::min<int64_t>(x + n, (int64_t)(w + 1) * run) - x;
+          s.idx_begin = kv_indptr[b] + static_cast<int32_t>(lo);
+          s.n_pages = static_cast<int32_t>(hi - lo);
+          s.last_rows = hi == n ? kv_last[b] : P;
+          s.page_begin = static_cast<int32_t>(lo);
+          s.slot = n_slot++;
+          emit(w, s);
+        }
+      }
+      x += n;
+    }
+  }
+  while (cur_worker < active) wptr[++cur_worker] = n_seg;
+  if (n_seg > pl->max_work || n_slot > pl->max_slots || n_merge > pl->max_merge) return PKV_ERR_WORKSPACE;
+
+  std::memset(hdr, 0, sizeof(PlanHeader));
+  hdr->kind = PKV_PLAN_DECODE;
+  hdr->batch = batch;
+  hdr->num_workers = active;
+  hdr->num_segments = n_seg;
+  hdr->num_merge = n_merge;
+  hdr->num_slots = n_slot;
+
+  pl->active_workers = active;
+  pl->num_work = n_seg;
+  pl->num_merge = n_merge;
+  pl->num_slots = n_slot;
+  pl->total_cost = total;
+  pl->max_cost = 0;
+  pl->work_rows.assign((size_t)n_seg * 8, 0);
+  for (int w = 0; w < active; ++w) {
+    int64_t cost = 0;
+    for (int i = wptr[w]; i < wptr[w + 1]; ++i) {
+      const DecodeSeg& s = segs[i];
+      int32_t* r = &pl->work_rows[(size_t)i * 8];
+      r[0] = w; r[1] = s.b; r[2] = s.kvh; r[3] = s.page_begin; r[4] = s.n_pages;
+      r[5] = s.last_rows; r[6] = s.slot; r[7] = 0;
+      cost += s.n_pages;
+    }
+    pl->max_cost = std::max(pl->max_cost, cost);
+  }
+  pl->used_bytes = pl->L.segs + sizeof(DecodeSeg) * (size_t)n_seg;
+  return PKV_OK;
+}
+
+pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                           const int32_t* kv_last, uint8_t* host) {
+  const int P = pl->p.page_size;
+  const int hkv = pl->p.num_kv_heads;
+  const int G = pl->group;
+  const int mp = pkv::kPrefillRows / G;
+  const int BN = pkv::kPrefillKeys;
+  const int C = pl->workers;
+
+  struct Item {
+    PrefillTile t;
+    int64_t cost;
+  };
+  std::vector<Item> items;
+  std::vector<PrefillMerge> merges;
+  struct Tile {
+    int b, kvh, pos0, npos, qo, kv, kv_end;
+  };
+  std::vector<Tile> tiles;
+  int64_t total = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int qo = qo_indptr[b + 1] - qo_indptr[b];
+    const int kv = static_cast<int>(kv_len_of(kv_indptr, kv_last, b, P));
+    for (int h = 0; h < hkv; ++h)
+      for (int pos0 = 0; pos0 < qo; pos0 += mp) {
+        const int npos = std::min(mp, qo - pos0);
+        int kv_end = kv;
+        if (pl->p.causal) kv_end = std::max(0, std::min(kv, pos0 + npos + kv - qo));
+        tiles.push_back({b, h, pos0, npos, qo, kv, kv_end});
+        total += std::max<int64_t>(1, ceil_div(kv_end, BN));
+      }
+  }
+  const int64_t chunk = std::max<int64_t>(ceil_div(total, std::max(C, 1)), 2);
+  int n_slot = 0;
+  for (const Tile& t : tiles) {
+    PrefillTile pt{};
+    pt.b = t.b;
+    pt.kvh = t.kvh;
+    pt.q_row0 = qo_indptr[t.b] + t.pos0;
+    pt.q_pos0 = t.pos0;
+    pt.n_pos = t.npos;
+    pt.qo_len = t.qo;
+    pt.kv_len = t.kv;
+    pt.idx_base = kv_indptr[t.b];
+    pt.last_rows = kv_last[t.b];
+    const int64_t nb = ceil_div(t.kv_end, BN);
+    if (nb <= chunk) {
+      pt.kv_begin = 0;
+      pt.kv_end = t.kv_end;
+      pt.slot = -1;
+      items.push_back({pt, std::max<int64_t>(nb, 1) + 1});
+    } else {
+      const int64_t parts = ceil_div(nb, chunk);
+      PrefillMerge m{};
+      m.b = t.b;
+      m.kvh = t.kvh;
+      m.q_row0 = pt.q_row0;
+      m.n_pos = t.npos;
+      m.slot_begin = n_slot;
+      m.n_slots = static_cast<int32_t>(parts);
+      merges.push_back(m);
+      for (int64_t i = 0; i < parts; ++i) {
+        const int64_t blo = i * nb / parts, bhi = (i + 1) * nb / parts;
+        pt.kv_begin = static_cast<int32_t>(blo * BN);
+        pt.kv_end = static_cast<int32_t>(std::min<int64_t>(bhi * BN, t.kv_end));
+        pt.slot = n_slot++;
+        items.push_back({pt, (bhi - blo) + 1});
+      }
+    }
+  }
+  if ((int64_t)items.size() > pl->max_work || n_slot > pl->max_slots || (int)merges.size() > pl->max_merge)
+    return PKV_ERR_WORKSPACE;
+
+  // Longest processing time first onto the least-loaded CTA.
+  std::vector<int> order(items.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = static_cast<int>(i);
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return items[a].cost > items[b].cost; });
+  const int ctas = static_cast<int>(std::min<int64_t>(C, (int64_t)items.size()));
+  std::vector<std::vector<int>> per(ctas);
+  std::vector<int64_t> load(ctas, 0);
+  using Slot = std::pair<int64_t, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < ctas; ++c) heap.push({0, c});
+  for (int i : order) {
+    Slot s = heap.top();
+    heap.pop();
+    per[s.second].push_back(i);
+    s.first += items[i].cost;
+    load[s.second] = s.first;
+    heap.push(s);
+  }
+
+  auto* hdr = reinterpret_cast<PlanHeader*>(host + pl->L.header);
+  auto* wptr = reinterpret_cast<int32_t*>(host + pl->L.worker_ptr);
+  auto* mrec = reinterpret_cast<PrefillMerge*>(host + pl->L.merge);
+  auto* work = reinterpret_cast<PrefillTile*>(host + pl->L.segs);
+  int n = 0;
+  pl->work_rows.assign(items.size() * 8, 0);
+  pl->max_cost = 0;
+  for (int c = 0; c < ctas; ++c) {
+    wptr[c] = n;
+    for (int i : per[c]) {
+      work[n] = items[i].t;
+      int32_t* r = &pl->work_rows[(size_t)n * 8];
+      const PrefillTile& t = items[i].t;
+      r[0] = c; r[1] = t.b; r[2] = t.kvh; r[3] = t.q_pos0; r[4] = t.n_pos;
+      r[5] = t.kv_begin; r[6] = t.kv_end; r[7] = t.slot;
+      ++n;
+    }
+    pl->max_cost = std::max(pl->max_cost, load[c]);
+  }
+  wptr[ctas] = n;
+  for (size_t i = 0; i < merges.size(); ++i) mrec[i] = merges[i];
+
+  std::memset(hdr, 0, sizeof(PlanHeader));
+  hdr->kind = PKV_PLAN_PREFILL;
+  hdr->batch = batch;
+  hdr->num_workers = ctas;
+  hdr->num_segments = n;
+  hdr->num_merge = static_cast<int32_t>(merges.size());
+  hdr->num_slots = n_slot;
+
+  pl->active_workers = ctas;
+  pl->num_work = n;
+  pl->num_merge = static_cast<int>(merges.size());
+  pl->num_slots = n_slot;
+  int64_t tot = 0;
+  for (int64_t v : load) tot += v;
+  pl->total_cost = tot;
+  pl->used_bytes = pl->L.segs + sizeof(PrefillTile) * (size_t)n;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_plan_create(pkv_plan** out, int kind, const pkv_params* params, const pkv_limits* limits,
+                           int device) {
+  if (!out) return PKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  pkv_status st = make_plan(out, kind, params, limits, device, sms);
+  if (st != PKV_OK) return st;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(device);
+  cudaError_t e = cudaEventCreateWithFlags(&(*out)->copy_done, cudaEventDisableTiming);
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    delete *out;
+    *out = nullptr;
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_plan_create_host(pkv_plan** out, int kind, const pkv_params* params, const pkv_limits* limits,
+                                int num_sms) {
+  return make_plan(out, kind, params, limits, -1, num_sms);
+}
+
+pkv_status pkv_plan_destroy(pkv_plan* plan) {
+  if (!plan) return PKV_ERR_INVALID_ARG;
+  if (plan->copy_done) {
+    if (plan->copy_pending) cudaEventSynchronize(plan->copy_done);
+    cudaEventDestroy(plan->copy_done);
+  }
+  delete plan;
+  return PKV_OK;
+}
+
+pkv_status pkv_plan_workspace_bytes(const pkv_plan* plan, size_t* dev_bytes, size_t* host_bytes) {
+  if (!plan) return PKV_ERR_INVALID_ARG;
+  if (dev_bytes) *dev_bytes = plan->L.total;
+  if (host_bytes) *host_bytes = plan->host_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_plan_compute(pkv_plan* plan, int batch, const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
+                            const int32_t* kv_indices_h, const int32_t* kv_last_page_len_h, int64_t num_pages,
+                            void* host_ws, size_t host_ws_bytes) {
+  if (!plan || !host_ws) return PKV_ERR_INVALID_ARG;
+  if (host_ws_bytes < plan->host_bytes) return PKV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(host_ws) % 64) return PKV_ERR_INVALID_ARG;
+  pkv_status st = validate(plan, batch, qo_indptr_h, kv_indptr_h, kv_indices_h, kv_last_page_len_h, num_pages);
+  if (st != PKV_OK) return st;
+  if (plan->copy_pending) {
+    cudaEventSynchronize(plan->copy_done);
+    plan->copy_pending = false;
+  }
+  auto* host = static_cast<uint8_t*>(host_ws);
+  if (plan->kind == PKV_PLAN_DECODE) {
+    st = compute_decode(plan, batch, kv_indptr_h, kv_last_page_len_h, host);
+  } else {
+    st = compute_prefill(plan, batch, qo_indptr_h, kv_indptr_h, kv_last_page_len_h, host);
+  }
+  if (st != PKV_OK) return st;
+  reinterpret_cast<PlanHeader*>(host + plan->L.header)->num_pages = num_pages;
+  plan->batch = batch;
+  plan->num_pages = num_pages;
+  plan->total_q = plan->kind == PKV_PLAN_DECODE ? batch : (batch > 0 ? qo_indptr_h[batch] : 0);
+  plan->planned = true;
+  return PKV_OK;
+}
+
+pkv_status pkv_plan_run(pkv_plan* plan, int batch, const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
+                        const int32_t* kv_indices_h, const int32_t* kv_last_page_len_h, int64_t num_pages,
+                        void* dev_ws, size_t dev_ws_bytes, void* host_ws, size_t host_ws_bytes, void* stream) {
+  if (!plan || !dev_ws) return PKV_ERR_INVALID_ARG;
+  if (plan->device < 0) return PKV_ERR_INVALID_ARG;
+  if (dev_ws_bytes < plan->L.total) return PKV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(dev_ws) % 256) return PKV_ERR_INVALID_ARG;
+  pkv_status st = pkv_plan_compute(plan, batch, qo_indptr_h, kv_indptr_h, kv_indices_h, kv_last_page_len_h,
+                                   num_pages, host_ws, host_ws_bytes);
+  if (st != PKV_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dev_ws, host_ws, plan->used_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaEventRecord(plan->copy_done, s) != cudaSuccess) {
+    cudaGetLastError();
+    plan->planned = false;
+    return PKV_ERR_CUDA;
+  }
+  plan->copy_pending = true;
+  return PKV_OK;
+}
+
+pkv_status pkv_plan_get_info(const pkv_plan* plan, pkv_plan_info* info) {
+  if (!plan || !info) return PKV_ERR_INVALID_ARG;
+  info->grid_ctas = plan->grid_ctas;
+  info->workers = plan->workers;
+  info->active_workers = plan->active_workers;
+  info->num_work = plan->num_work;
+  info->num_merge = plan->num_merge;
+  info->num_slots = plan->num_slots;
+  info->max_cost = plan->max_cost;
+  info->total_cost = plan->total_cost;
+  return PKV_OK;
+}
+
+pkv_status pkv_plan_get_work(const pkv_plan* plan, int32_t* out, int64_t capacity, int64_t* rows_written) {
+  if (!plan) return PKV_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(plan->work_rows.size() / 8);
+  if (rows_written) *rows_written = rows;
+  if (!out) return rows == 0 ? PKV_OK : PKV_ERR_INVALID_ARG;
+  if (capacity < rows) return PKV_ERR_WORKSPACE;
+  std::memcpy(out, plan->work_rows.data(), plan->work_rows.size() * sizeof(int32_t));
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,216 @@
+"""CPU tests of the C ABI: exported symbols, argument validation, and the host
+plan's decisions (every page covered once, equal chunks, slot and merge maps).
+
+The plan is created with pkv_plan_create_host (no CUDA call), so these run
+without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from paged_kv_cache_bsr_gb300 import api, workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_bsr_gb300 import build
+    build.build()
+    return api.load()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 14
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert set(api.EXPORTS) <= set(declared)
+
+
+def test_status_strings(lib):
+    for st in range(-6, 1):
+        assert api.status_string(st) not in ("", "unknown status")
+    assert api.status_string(-99) == "unknown status"
+
+
+# --------------------------------------------------------------------------- helpers
+def host_plan(b, kind, num_sms=152, **lim):
+    params = api.make_params(b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.dtype, b.sm_scale,
+                             b.logits_cap, b.causal)
+    limits = api.Limits(lim.get("max_batch", max(b.batch, 1)), lim.get("max_total_q", max(b.total_q, 1)),
+                        lim.get("max_kv_pages", max(int(b.kv_indptr[-1]), 1)))
+    h = api.plan_create_host(kind, params, limits, num_sms)
+    _, host_bytes = api.plan_workspace_bytes(h)
+    ws = torch.empty(host_bytes + 64, dtype=torch.uint8)
+    off = (-ws.data_ptr()) % 64
+    return h, ws[off:off + host_bytes]
+
+
+def compute(h, ws, b, **over):
+    args = dict(batch=b.batch, qo=b.qo_indptr, ip=b.kv_indptr, ix=b.kv_indices, last=b.kv_last_page_len,
+                num_pages=b.num_pages)
+    args.update(over)
+    api.plan_compute(h, args["batch"], args["qo"], args["ip"], args["ix"], args["last"], args["num_pages"], ws)
+
+
+def table_batch(kv_lens, qo_lens=None, page_size=16, hq=32, hkv=8, d=128, causal=False):
+    """A paged batch with tiny data: only the index arrays matter to the plan."""
+    qo_lens = qo_lens or [1] * len(kv_lens)
+    b = W.make_paged_batch(qo_lens=[1] * len(kv_lens), kv_lens=kv_lens, num_qo_heads=1, num_kv_heads=1,
+                           head_dim=8, page_size=page_size, dtype=torch.bfloat16, seed=0, causal=causal)
+    b.num_qo_heads, b.num_kv_heads, b.head_dim = hq, hkv, d
+    b.qo_lens = list(qo_lens)
+    qo = torch.zeros(len(qo_lens) + 1, dtype=torch.int32)
+    qo[1:] = torch.cumsum(torch.tensor(qo_lens), 0)
+    b.qo_indptr = qo
+    b.q = torch.empty(int(qo[-1]), 1, 1)
+    return b
+
+
+# --------------------------------------------------------------------------- decode plan
+def check_decode_plan(h, b, num_sms=152):
+    info = api.plan_get_info(h)
+    work = api.plan_get_work(h)
+    P, hkv = b.page_size, b.num_kv_heads
+    counts = (b.kv_indptr[1:] - b.kv_indptr[:-1]).tolist()
+    covered = {}
+    per_worker = {}
+    slots = set()
+    for w, bb, kvh, p0, n, last, slot, _ in work.tolist():
+        per_worker[w] = per_worker.get(w, 0) + n
+        for p in range(p0, p0 + n):
+            key = (bb, kvh, p)
+            assert key not in covered, f"page {key} covered twice"
+            covered[key] = slot
+        if n:
+            assert last == (b.kv_last_page_len[bb].item() if p0 + n == counts[bb] else P)
+        if slot >= 0:
+            assert slot not in slots
+            slots.add(slot)
+    want = {(bb, kvh, p) for bb in range(b.batch) for kvh in range(hkv) for p in range(counts[bb])}
+    assert set(covered) == want
+    # workers appear in non-decreasing order and the runs are equal chunks
+    ws_ = work[:, 0].tolist()
+    assert ws_ == sorted(ws_)
+    total = sum(counts) * hkv
+    assert info.total_cost == total
+    if total:
+        run = max(-(-total // (num_sms * 6)), 8)
+        assert info.max_cost <= run
+        assert max(per_worker.values()) == info.max_cost
+    assert info.num_slots == len(slots)
+    # an empty request still gets exactly one entry per kv head (it writes o = 0)
+    for bb, n in enumerate(counts):
+        if n == 0:
+            assert sum(1 for r in work.tolist() if r[1] == bb) == hkv
+    return info, work
+
+
+def test_decode_plan_llama3_batch(lib):
+    b = table_batch([int(x) for x in torch.randint(512, 4097, (64,), generator=torch.Generator().manual_seed(1))])
+    h, ws = host_plan(b, api.PLAN_DECODE)
+    compute(h, ws, b)
+    info, work = check_decode_plan(h, b)
+    assert info.active_workers <= 152 * 6
+    assert info.max_cost * info.active_workers >= info.total_cost
+    api.plan_destroy(h)
+
+
+def test_decode_plan_skewed_batch_splits_the_long_request(lib):
+    b = table_batch([1024] * 31 + [131072])
+    h, ws = host_plan(b, api.PLAN_DECODE)
+    compute(h, ws, b)
+    info, work = check_decode_plan(h, b)
+    long_slots = [r for r in work.tolist() if r[1] == 31]
+    assert len(long_slots) > 8 * 50  # the long request is spread over most workers
+    assert info.num_merge >= 8
+    api.plan_destroy(h)
+
+
+@pytest.mark.parametrize("kv_lens,P", [([0, 5, 0, 17], 16), ([1, 15, 16, 17, 33], 16), ([7, 100, 3], 1),
+                                       ([130, 64, 0], 64), ([0, 0], 16), ([1], 16)])
+def test_decode_plan_edge_lengths(lib, kv_lens, P):
+    b = table_batch(kv_lens, page_size=P, hq=8, hkv=2)
+    h, ws = host_plan(b, api.PLAN_DECODE, num_sms=4)
+    compute(h, ws, b)
+    check_decode_plan(h, b, num_sms=4)
+    api.plan_destroy(h)
+
+
+def test_decode_plan_is_deterministic(lib):
+    b = table_batch([300, 2000, 17, 4096, 1])
+    h, ws = host_plan(b, api.PLAN_DECODE)
+    compute(h, ws, b)
+    w1 = api.plan_get_work(h).clone()
+    bytes1 = ws.clone()
+    compute(h, ws, b)
+    assert torch.equal(w1, api.plan_get_work(h))
+    assert torch.equal(bytes1, ws)
+    api.plan_destroy(h)
+
+
+# --------------------------------------------------------------------------- validation
+def test_plan_rejects_malformed_index_arrays(lib):
+    b = table_batch([40, 17, 3])
+    h, ws = host_plan(b, api.PLAN_DECODE)
+    ip = b.kv_indptr.tolist()
+    bad_ip = torch.tensor([ip[0], ip[2], ip[1], ip[3]], dtype=torch.int32)
+    cases = [
+        dict(ip=bad_ip),                                                    # non-monotone indptr
+        dict(ix=torch.where(torch.arange(b.kv_indices.numel()) == 0, b.num_pages, b.kv_indices)),  # id = pool size
+        dict(ix=torch.where(torch.arange(b.kv_indices.numel()) == 1, -1, b.kv_indices)),          # negative id
+        dict(last=torch.tensor([16, 0, 3], dtype=torch.int32)),             # last_page_len 0 with pages
+        dict(last=torch.tensor([16, 17, 3], dtype=torch.int32)),            # last_page_len > page_size
+        dict(ip=torch.cat([torch.tensor([1], dtype=torch.int32), b.kv_indptr[1:]])),  # indptr[0] != 0
+    ]
+    for over in cases:
+        with pytest.raises(api.PkvError) as e:
+            compute(h, ws, b, **over)
+        assert e.value.status == -2, over
+    with pytest.raises(api.PkvError) as e:                                  # more requests than the limits
+        api.plan_compute(h, 4, None, torch.zeros(5, dtype=torch.int32), None, torch.zeros(4, dtype=torch.int32),
+                         10, ws)
+    assert e.value.status == -4
+    with pytest.raises(api.PkvError) as e:                                  # host buffer too small
+        api.plan_compute(h, b.batch, None, b.kv_indptr, b.kv_indices, b.kv_last_page_len, b.num_pages, ws[:64])
+    assert e.value.status == -4
+    api.plan_destroy(h)
+
+
+def test_plan_create_rejects_bad_params(lib):
+    lim = api.Limits(4, 4, 100)
+    for params, st in [
+        (api.make_params(6, 4, 128, 16, torch.bfloat16, 0.1), -1),   # heads not a multiple
+        (api.make_params(8, 2, 96, 16, torch.bfloat16, 0.1), -3),    # head_dim not built
+        (api.make_params(8, 2, 128, 24, torch.bfloat16, 0.1), -3),   # page size neither <=16 nor 16k
+        (api.make_params(8, 2, 128, 16, torch.float32, 0.1), -3),    # fp32 storage
+        (api.make_params(48, 2, 128, 16, torch.bfloat16, 0.1), -3),  # group 24
+        (api.make_params(8, 2, 128, 16, torch.bfloat16, 0.0), -1),   # scale 0
+    ]:
+        with pytest.raises(api.PkvError) as e:
+            api.plan_create_host(api.PLAN_DECODE, params, lim, 152)
+        assert e.value.status == st
+
+
+def test_run_calls_refuse_host_only_plans(lib):
+    b = table_batch([40])
+    h, ws = host_plan(b, api.PLAN_DECODE)
+    compute(h, ws, b)
+    dummy = torch.empty(64, dtype=torch.uint8)
+    with pytest.raises(api.PkvError):
+        api.batch_decode_paged(h, dummy, dummy, dummy, dummy, dummy, dummy, None, dummy, stream=0)
+    api.plan_destroy(h)
