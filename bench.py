@@ -417,7 +417,8 @@ def run_own(args):
     secondary = {}
     e2e = None
     if world == 1:
-        e2e = decode_e2e(b, args.e2e_steps)
+        if args.e2e_steps > 0:
+            e2e = decode_e2e(b, args.e2e_steps)
         if not args.no_secondary:
             sk = W.skewed_decode(seed=1002)
             r3 = decode_measure(sk, max(20, args.steps // 10), 5, peaks)

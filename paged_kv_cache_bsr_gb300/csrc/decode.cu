@@ -134,6 +134,65 @@ __device__ __forceinline__ bool producer_issue(Producer& p, const DecodeArgs& a,
   return false;
 }
 
+// Head owned by lane slice `sub` after reduce_scatter<G, LPT>.
+template <int G, int LPT>
+__device__ __forceinline__ int owned_head(int sub) {
+  int h = 0, n = G;
+#pragma unroll
+  for (int o = LPT / 2; o >= 1; o >>= 1)
+    if (n > 1) {
+      if (sub & o) h += n / 2;
+      n /= 2;
+    }
+  return h;
+}
+
+// Lane slice (within a token group) that owns head g.
+template <int G, int LPT>
+__device__ __forceinline__ int owner_of_head(int g) {
+  int sub = 0, n = G;
+#pragma unroll
+  for (int o = LPT / 2; o >= 1; o >>= 1)
+    if (n > 1) {
+      if (g >= n / 2) {
+        sub |= o;
+        g -= n / 2;
+      }
+      n /= 2;
+    }
+  return sub;
+}
+
+// Sum G per-head partial dots over the LPT lanes of a token group.  Each
+// xor-round halves the number of heads a lane carries (it keeps one half and
+// sends the other), so G heads cost G-1 + log2(LPT/G) shuffles instead of
+// G*log2(LPT); the lane ends with the full sum of head owned_head<G,LPT>(sub).
+template <int G, int LPT>
+__device__ __forceinline__ float reduce_scatter(const float (&v)[G], int sub) {
+  float cur[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) cur[g] = v[g];
+  int n = G;
+#pragma unroll
+  for (int o = LPT / 2; o >= 1; o >>= 1) {
+    if (n > 1) {
+      const bool upper = (sub & o) != 0;
+#pragma unroll
+      for (int i = 0; i < G / 2; ++i) {
+        if (i < n / 2) {
+          const float send = upper ? cur[i] : cur[i + n / 2];
+          const float keep = upper ? cur[i + n / 2] : cur[i];
+          cur[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+      }
+      n /= 2;
+    } else {
+      cur[0] += __shfl_xor_sync(kFull, cur[0], o);
+    }
+  }
+  return cur[0];
+}
+
 template <int D, int G, int LPT, typename T, bool CAP>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
   using Shape = DecodeShape<D, T>;
@@ -144,6 +203,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
   constexpr int STEPS = kDecodeTileRows / TPS;
   static_assert(CH >= 1 && VEC % 8 == 0, "lane slice must be whole 16-byte chunks");
   static_assert(kDecodeTileRows % TPS == 0, "steps must tile the 16 rows");
+  static_assert(G <= LPT, "every head needs an owning lane in the token group");
 
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kDecodeWarps][S];
@@ -152,6 +212,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
   const int lane = threadIdx.x & 31;
   const int sub = lane % LPT;   // dim slice of this lane
   const int grp = lane / LPT;   // token slot of this lane within a step
+  const int my_head = owned_head<G, LPT>(sub);
   uint8_t* ring = smem + warp * kDecodeWarpSmem;
   const uint32_t bar0 = smem_addr(&bars[warp][0]);
 
@@ -188,26 +249,27 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
     int indptr_seen = 0;
     if (lane == 0) indptr_seen = __ldg(a.kv_indptr + sg.b);
 
-    // Query rows of the head group, pre-scaled (log2 domain without a cap).
-    float qf[G][VEC];
+    // Query rows of the head group as fp32 pairs, pre-scaled (log2 domain without a cap).
+    float2 qf[G][VEC / 2];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const T* qrow = q_all + (static_cast<int64_t>(sg.b) * a.num_qo_heads + hq0 + g) * D;
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
-        float f[8];
-        to_float8<T>(ld_nc_v4(qrow + (sub + c * LPT) * 8), f);
+        float2 f[4];
+        to_float2x4<T>(ld_nc_v4(qrow + (sub + c * LPT) * 8), f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qf[g][c * 8 + e] = f[e] * a.q_scale;
+        for (int e = 0; e < 4; ++e) qf[g][c * 4 + e] = make_float2(f[e].x * a.q_scale, f[e].y * a.q_scale);
       }
     }
-    float m[G], l[G], acc[G][VEC];
+    float m[G];        // running max per head (warp-uniform)
+    float l_own = 0.f; // running sum of the owned head over this lane's tokens
+    float2 acc[G][VEC / 2];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       m[g] = -INFINITY;
-      l[g] = 0.f;
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) acc[g][v] = 0.f;
+      for (int v = 0; v < VEC / 2; ++v) acc[g][v] = make_float2(0.f, 0.f);
     }
 
     for (int pg = 0; pg < sg.n_pages && ok; ++pg) {
@@ -222,68 +284,71 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
         const T* ks = reinterpret_cast<const T*>(ring + stage * Shape::kStageBytes);
         const T* vs = ks + kDecodeTileRows * D;
 
-        float sc[STEPS][G];
+        // Scores of the owned head, one per step (token st*TPS + grp).
+        float sc[STEPS];
 #pragma unroll
         for (int st = 0; st < STEPS; ++st) {
           const int tok = st * TPS + grp;
+          float2 part2[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) part2[g] = make_float2(0.f, 0.f);
+          if (tok < rows) {
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+              float2 kf[4];
+              to_float2x4<T>(*reinterpret_cast<const uint4*>(ks + tok * D + (sub + c * LPT) * 8), kf);
+#pragma unroll
+              for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) part2[g] = ffma2(qf[g][c * 4 + e], kf[e], part2[g]);
+            }
+          }
           float part[G];
 #pragma unroll
-          for (int g = 0; g < G; ++g) part[g] = 0.f;
-          if (tok < rows) {
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-              float kf[8];
-              to_float8<T>(*reinterpret_cast<const uint4*>(ks + tok * D + (sub + c * LPT) * 8), kf);
-#pragma unroll
-              for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) part[g] = fmaf(qf[g][c * 8 + e], kf[e], part[g]);
-            }
-          }
-#pragma unroll
-          for (int o = LPT / 2; o >= 1; o >>= 1)
-#pragma unroll
-            for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(kFull, part[g], o);
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float x = part[g];
-            if constexpr (CAP) x = a.cap * tanhf(x / a.cap) * kLog2e;
-            sc[st][g] = tok < rows ? x : -INFINITY;
-          }
+          for (int g = 0; g < G; ++g) part[g] = part2[g].x + part2[g].y;
+          float x = reduce_scatter<G, LPT>(part, sub);
+          if constexpr (CAP) x = a.cap * tanhf(x / a.cap) * kLog2e;
+          sc[st] = tok < rows ? x : -INFINITY;
         }
-        // Tile max per head over all tokens of the tile; rescale only when it grows.
+        // Tile max of every head, known to all lanes; rescale only when it grows.
+        float mx = sc[0];
+#pragma unroll
+        for (int st = 1; st < STEPS; ++st) mx = fmaxf(mx, sc[st]);
+        mx = warp_max(mx, 16, LPT);
+        float m_own = -INFINITY;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float mx = sc[0][g];
+          const float mg = __shfl_sync(kFull, mx, owner_of_head<G, LPT>(g));
+          if (mg > m[g]) {
+            const float alpha = fast_exp2(m[g] - mg);
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int st = 1; st < STEPS; ++st) mx = fmaxf(mx, sc[st][g]);
-          mx = warp_max(mx, 16, LPT);
-          if (mx > m[g]) {
-            const float alpha = fast_exp2(m[g] - mx);
-            l[g] *= alpha;
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) acc[g][v] *= alpha;
-            m[g] = mx;
+            for (int v = 0; v < VEC / 2; ++v) acc[g][v] = fmul2(acc[g][v], a2);
+            if (g == my_head) l_own *= alpha;
+            m[g] = mg;
           }
+          if (g == my_head) m_own = m[g];
         }
 #pragma unroll
         for (int st = 0; st < STEPS; ++st) {
           const int tok = st * TPS + grp;
-          if (tok < rows) {
-            float p[G];
+          const float p_own = fast_exp2(sc[st] - m_own);  // 0 for a masked token
+          l_own += p_own;
+          float2 p2[G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              p[g] = fast_exp2(sc[st][g] - m[g]);
-              l[g] += p[g];
-            }
+          for (int g = 0; g < G; ++g) {
+            const float pg_ = __shfl_sync(kFull, p_own, grp * LPT + owner_of_head<G, LPT>(g));
+            p2[g] = make_float2(pg_, pg_);
+          }
+          if (tok < rows) {
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
-              float vf[8];
-              to_float8<T>(*reinterpret_cast<const uint4*>(vs + tok * D + (sub + c * LPT) * 8), vf);
+              float2 vf[4];
+              to_float2x4<T>(*reinterpret_cast<const uint4*>(vs + tok * D + (sub + c * LPT) * 8), vf);
 #pragma unroll
               for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[g][c * 8 + e] = fmaf(p[g], vf[e], acc[g][c * 8 + e]);
+                for (int e = 0; e < 4; ++e) acc[g][c * 4 + e] = ffma2(p2[g], vf[e], acc[g][c * 4 + e]);
             }
           }
         }
@@ -294,31 +359,39 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
     }
     if (!ok) break;
 
-    // Combine the token groups: every lane ends with the full sums of its dims.
+    // Combine the token groups: every lane ends with the full sums of its dims,
+    // and the owner lanes with the full softmax denominator of their head.
 #pragma unroll
-    for (int o = LPT; o < 32; o <<= 1)
+    for (int o = LPT; o < 32; o <<= 1) {
+      l_own += __shfl_xor_sync(kFull, l_own, o);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        l[g] += __shfl_xor_sync(kFull, l[g], o);
+      for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) acc[g][v] += __shfl_xor_sync(kFull, acc[g][v], o);
-      }
+        for (int v = 0; v < VEC / 2; ++v) {
+          acc[g][v].x += __shfl_xor_sync(kFull, acc[g][v].x, o);
+          acc[g][v].y += __shfl_xor_sync(kFull, acc[g][v].y, o);
+        }
+    }
 
     if (lane == 0 && indptr_seen != sg.idx_begin - sg.page_begin) atomicOr(a.err, kErrIndptrMismatch);
 
+    const bool empty = sg.n_pages == 0;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
+      const float lg = __shfl_sync(kFull, l_own, owner_of_head<G, LPT>(g));
       if (g % TPS != grp) continue;
-      const bool empty = sg.n_pages == 0;
-      const float inv = empty ? 0.f : 1.f / l[g];
-      const float lse_v = empty ? -INFINITY : (m[g] + log2f(l[g])) * kLn2;
+      const float inv = empty ? 0.f : 1.f / lg;
+      const float lse_v = empty ? -INFINITY : (m[g] + log2f(lg)) * kLn2;
       if (sg.slot < 0) {
         T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(sg.b) * a.num_qo_heads + hq0 + g) * D;
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
           float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = acc[g][c * 8 + e] * inv;
+          for (int e = 0; e < 4; ++e) {
+            f[2 * e] = acc[g][c * 4 + e].x * inv;
+            f[2 * e + 1] = acc[g][c * 4 + e].y * inv;
+          }
           *reinterpret_cast<uint4*>(orow + (sub + c * LPT) * 8) = from_float8<T>(f);
         }
         if (sub == 0 && a.lse) a.lse[static_cast<int64_t>(sg.b) * a.num_qo_heads + hq0 + g] = lse_v;
@@ -327,10 +400,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
           float4* dst = reinterpret_cast<float4*>(prow + (sub + c * LPT) * 8);
-          dst[0] = make_float4(acc[g][c * 8 + 0] * inv, acc[g][c * 8 + 1] * inv,
-                               acc[g][c * 8 + 2] * inv, acc[g][c * 8 + 3] * inv);
-          dst[1] = make_float4(acc[g][c * 8 + 4] * inv, acc[g][c * 8 + 5] * inv,
-                               acc[g][c * 8 + 6] * inv, acc[g][c * 8 + 7] * inv);
+          dst[0] = make_float4(acc[g][c * 4 + 0].x * inv, acc[g][c * 4 + 0].y * inv,
+                               acc[g][c * 4 + 1].x * inv, acc[g][c * 4 + 1].y * inv);
+          dst[1] = make_float4(acc[g][c * 4 + 2].x * inv, acc[g][c * 4 + 2].y * inv,
+                               acc[g][c * 4 + 3].x * inv, acc[g][c * 4 + 3].y * inv);
         }
         if (sub == 0) a.part_lse[static_cast<int64_t>(sg.slot) * G + g] = lse_v;
       }
@@ -346,79 +419,80 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
 }
 
 // n-way merge of the partial states of split (request, kv head) sequences:
-// one CTA per (item, head of the group); warps take slots, lanes take dims.
+// one warp per (item, head of the group), lanes over head_dim, the slot loop
+// unrolled so that several partial rows are in flight per lane.
 template <int D, int G, typename T>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
-  constexpr int NW = kMergeThreads / 32;
   constexpr int PER = D / 32;  // dims per lane
-  __shared__ float s_acc[NW][D];
-  __shared__ float s_w[NW];
-  __shared__ float s_max[NW];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int U = 8;         // slots in flight per lane
+  const int lane = threadIdx.x & 31;
+  const int warp_id = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
+  const int n_warps = gridDim.x * (kMergeThreads / 32);
   const int pairs = a.hdr->num_merge * G;
-  for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x) {
+  for (int pair = warp_id; pair < pairs; pair += n_warps) {
     const MergeItem it = a.merge[pair / G];
     const int g = pair % G;
+    const float* lse_p = a.part_lse + static_cast<int64_t>(it.slot_begin) * G + g;
     float mx = -INFINITY;
-    for (int i = threadIdx.x; i < it.n_slots; i += kMergeThreads)
-      mx = fmaxf(mx, a.part_lse[static_cast<int64_t>(it.slot_begin + i) * G + g]);
+    for (int i = lane; i < it.n_slots; i += 32) mx = fmaxf(mx, lse_p[static_cast<int64_t>(i) * G]);
     mx = warp_max(mx);
-    if (lane == 0) s_max[warp] = mx;
-    __syncthreads();
-    mx = s_max[0];
-#pragma unroll
-    for (int w = 1; w < NW; ++w) mx = fmaxf(mx, s_max[w]);
     float acc[PER];
 #pragma unroll
     for (int v = 0; v < PER; ++v) acc[v] = 0.f;
     float wsum = 0.f;
     if (mx != -INFINITY) {
-      for (int i = warp; i < it.n_slots; i += NW) {
-        const int64_t slot = it.slot_begin + i;
-        const float w = fast_exp2((a.part_lse[slot * G + g] - mx) * kLog2e);
-        const float* src = a.part_o + (slot * G + g) * D + lane * PER;
-        float v4[PER];
-        if constexpr (PER == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(src);
-          v4[0] = t.x; v4[1] = t.y; v4[2] = t.z; v4[3] = t.w;
-        } else {
+      const float* o_p = a.part_o + (static_cast<int64_t>(it.slot_begin) * G + g) * D + lane * PER;
+      for (int i0 = 0; i0 < it.n_slots; i0 += 32) {
+        // lane j holds the weight of slot i0 + j
+        const float w_lane = (i0 + lane < it.n_slots)
+                                 ? fast_exp2((lse_p[static_cast<int64_t>(i0 + lane) * G] - mx) * kLog2e)
+                                 : 0.f;
+        const int cnt = min(32, it.n_slots - i0);
+        for (int j0 = 0; j0 < cnt; j0 += U) {
+          float vals[U][PER];
 #pragma unroll
-          for (int v = 0; v < PER; ++v) v4[v] = src[v];
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + j0 + u;
+            if (j0 + u < cnt) {
+              const float* src = o_p + static_cast<int64_t>(i) * G * D;
+              if constexpr (PER == 4) {
+                const float4 t = *reinterpret_cast<const float4*>(src);
+                vals[u][0] = t.x; vals[u][1] = t.y; vals[u][2] = t.z; vals[u][3] = t.w;
+              } else {
+                const float2 t = *reinterpret_cast<const float2*>(src);
+                vals[u][0] = t.x; vals[u][1] = t.y;
+              }
+            } else {
+#pragma unroll
+              for (int v = 0; v < PER; ++v) vals[u][v] = 0.f;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const float w = __shfl_sync(kFull, w_lane, (j0 + u) & 31);
+            if (j0 + u < cnt) {
+#pragma unroll
+              for (int v = 0; v < PER; ++v) acc[v] = fmaf(w, vals[u][v], acc[v]);
+              wsum += w;
+            }
+          }
         }
-#pragma unroll
-        for (int v = 0; v < PER; ++v) acc[v] = fmaf(w, v4[v], acc[v]);
-        wsum += w;
       }
     }
+    const int hq = it.kvh * G + g;
+    T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(it.b) * a.num_qo_heads + hq) * D;
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-    for (int v = 0; v < PER; ++v) s_acc[warp][lane * PER + v] = acc[v];
-    if (lane == 0) s_w[warp] = wsum;
-    __syncthreads();
-    if (warp == 0) {
-      float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) tot += s_w[w];
-      const int hq = it.kvh * G + g;
-      T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(it.b) * a.num_qo_heads + hq) * D;
-      const float inv = tot > 0.f ? 1.f / tot : 0.f;
-#pragma unroll
-      for (int v = 0; v < PER; ++v) {
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) s += s_acc[w][lane * PER + v];
-        orow[lane * PER + v] = from_float<T>(s * inv);
-      }
-      if (lane == 0 && a.lse)
-        a.lse[static_cast<int64_t>(it.b) * a.num_qo_heads + hq] =
-            tot > 0.f ? mx + logf(tot) : -INFINITY;
-    }
-    __syncthreads();
+    for (int v = 0; v < PER; ++v) orow[lane * PER + v] = from_float<T>(acc[v] * inv);
+    if (lane == 0 && a.lse)
+      a.lse[static_cast<int64_t>(it.b) * a.num_qo_heads + hq] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
   }
 }
 
 template <int D, int G, int LPT, typename T>
 cudaError_t launch_decode_t(const DecodeArgs& a, bool cap, int grid, cudaStream_t stream) {
   const int smem = kDecodeWarps * kDecodeWarpSmem;
+  static_assert(kDecodeWarps * kDecodeWarpSmem <= 200 * 1024, "decode ring exceeds shared memory");
   auto kern = cap ? decode_kernel<D, G, LPT, T, true> : decode_kernel<D, G, LPT, T, false>;
   cudaError_t e = ensure_smem_limit(kern, smem);
   if (e != cudaSuccess) return e;

@@ -41,9 +41,9 @@ inline cudaError_t ensure_smem_limit(Kernel kern, int bytes) {
 }
 
 // Warps per decode CTA; each warp streams its own pages (one CTA per SM).
-constexpr int kDecodeWarps = 6;
+constexpr int kDecodeWarps = 8;
 // Shared memory each decode warp uses for its ring of page tiles.
-constexpr int kDecodeWarpSmem = 32 * 1024;
+constexpr int kDecodeWarpSmem = 24 * 1024;
 constexpr int kDecodeTileRows = 16;
 constexpr int kMergeThreads = 256;
 

@@ -105,7 +105,7 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
     pl->max_merge = static_cast<int>(std::min<int64_t>((int64_t)limits->max_batch * hkv, pl->workers) + 1);
     pl->max_slots = 2 * pl->workers;
     pl->rows_per_slot = pl->group;
-    pl->merge_grid = num_sms * 2;
+    pl->merge_grid = num_sms * 4;
   } else {
     const int mp = pkv::kPrefillRows / pl->group;  // query positions per tile
     pl->grid_ctas = num_sms;

@@ -132,7 +132,7 @@ def test_cuda_graph_replay_after_replanning():
     """Capture plan-independent run calls once; re-plan another batch into the same
     workspace and buffers; replaying the graph gives that batch's result."""
     hq, hkv, d, P = 16, 4, 128, 16
-    pool = 600
+    pool = 800
     gen = torch.Generator().manual_seed(11)
     kv = torch.randn(pool, 2, hkv, P, d, generator=gen).to(torch.bfloat16)
     max_b, max_pages = 6, pool
