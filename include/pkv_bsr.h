@@ -221,6 +221,38 @@ pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const in
                                    void* o, float* lse, void* dev_ws, void* stream);
 
 /*
+ * Batch decode for callers that cannot allocate device memory: plug-ins whose
+ * host framework owns all device memory through its own allocator, services
+ * under a fixed device-memory budget, and code paths that must not pay the
+ * implicit device synchronisation a cudaMalloc can cause.  The FlashInfer
+ * pages have no counterpart of this call.
+ * It computes exactly what pkv_batch_decode_paged computes, but the plan
+ * tables and the fp32 partial states live in one static 8 MiB device array
+ * inside this library (present on every device that loads it, until the
+ * process exits) instead of a caller workspace, and the call allocates
+ * nothing.
+ *  - plan: a decode plan whose tables pkv_plan_compute wrote into
+ *    host_tables (pageable or pinned host memory of host_tables_bytes, at
+ *    least the plan's host_bytes).  The call copies them into the static array
+ *    on `stream`; pinned host_tables must stay unchanged until that copy runs.
+ *  - A plan whose device workspace (dev_bytes of pkv_plan_workspace_bytes)
+ *    exceeds 8 MiB is rejected with PKV_ERR_WORKSPACE.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents (each call rewrites the tables, with a zeroed error word, before
+ *    its kernels read them).  Calls whose work overlaps on the GPU (on other
+ *    streams, or from several host threads) race on the array: serialise them.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - The device error word lives in the static array and is not reported.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_WORKSPACE, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const void* host_tables,
+                                          size_t host_tables_bytes, const void* q, const void* kv_data,
+                                          const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
+                                          const int32_t* kv_last_page_len_d, void* o, float* lse,
+                                          void* stream);
+
+/*
  * merge_state (guide section 3, "Cascade Attention": the two partial results
  * are combined with the online-softmax correction).  For each of n_rows *
  * num_heads rows with states (o_a, lse_a) and (o_b, lse_b) over disjoint key

@@ -56,7 +56,7 @@ EXPORTS = [
     "pkv_status_string", "pkv_version", "pkv_plan_create", "pkv_plan_create_host", "pkv_plan_destroy",
     "pkv_plan_workspace_bytes", "pkv_plan_compute", "pkv_plan_run", "pkv_plan_get_info", "pkv_plan_get_work",
     "pkv_batch_decode_paged", "pkv_batch_prefill_paged", "pkv_merge_state", "pkv_get_device_error",
-    "pkv_plan_set_timing_events",
+    "pkv_plan_set_timing_events", "pkv_batch_decode_paged_noalloc",
 ]
 
 
@@ -91,6 +91,7 @@ def load(path: Optional[str] = None):
             "pkv_merge_state": (i32, [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp]),
             "pkv_get_device_error": (i32, [vp, vp, ctypes.POINTER(i32), i32, vp]),
             "pkv_plan_set_timing_events": (i32, [vp, vp, vp]),
+            "pkv_batch_decode_paged_noalloc": (i32, [vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -209,6 +210,19 @@ def batch_decode_paged(h, q, kv_data, kv_indices, kv_indptr, kv_last_page_len, o
     _check(load().pkv_batch_decode_paged(h, _ptr(q), _ptr(kv_data), _ptr(kv_indices), _ptr(kv_indptr),
                                          _ptr(kv_last_page_len), _ptr(o), _ptr(lse), _ptr(dev_ws),
                                          _stream(stream)), "pkv_batch_decode_paged")
+
+
+def batch_decode_paged_noalloc(h, host_tables, q, kv_data, kv_indices, kv_indptr, kv_last_page_len, o, lse,
+                               stream=None) -> None:
+    """Decode with the library's static device scratch instead of a caller workspace.
+
+    ``host_tables`` is the host buffer ``plan_compute`` filled for this plan.
+    """
+    _check(load().pkv_batch_decode_paged_noalloc(h, _ptr(host_tables),
+                                                 host_tables.numel() * host_tables.element_size(), _ptr(q),
+                                                 _ptr(kv_data), _ptr(kv_indices), _ptr(kv_indptr),
+                                                 _ptr(kv_last_page_len), _ptr(o), _ptr(lse), _stream(stream)),
+           "pkv_batch_decode_paged_noalloc")
 
 
 def batch_prefill_paged(h, q, qo_indptr, kv_data, kv_indices, kv_indptr, kv_last_page_len, o, lse, dev_ws,
