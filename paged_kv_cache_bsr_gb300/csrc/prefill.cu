@@ -1,19 +1,541 @@
-// prefill.cu -- causal ragged batch prefill over a paged KV cache (tcgen05).
+// prefill.cu -- causal ragged batch prefill over a paged KV cache on tcgen05.
+//
+// Method (FlashInfer pages): batch_prefill with causal=True over the same
+// page table as decode ("FlashInfer" guide, "The Interface"); the kernel
+// gathers scattered pages into contiguous shared memory before using tensor
+// cores (fdeinterviews, "One format for every KV layout"); query heads that
+// share a kv head are packed into one row block (greptalks, "Head Group
+// Packing"); with causal off and every request's query in one row block it is
+// the shared-prefix half of cascade attention (guide section 3, "Cascade
+// Attention"; fdeinterviews, composable formats with a large row block).
+//
+// GB300 design.  One CTA per SM walks the plan's list of work tiles.  A tile
+// is 128 packed query rows (128/G query positions x the G heads of one kv
+// head) against a key range, visited 128 keys (128/P pages) at a time:
+//   warp 0      producer: TMA loads the Q box once per tile and, per key
+//               block, one 64-column box per (page, half) for K and for V,
+//               128B-swizzled into shared memory (two stages each).  Pages
+//               past the request come from an out-of-range page coordinate,
+//               which TMA fills with zeros; V rows past kv_last_page_len of
+//               the last page are zeroed before the MMA may read them.
+//   warp 1      one thread issues the tcgen05 MMAs: S_j = Q K_j^T into one of
+//               two TMEM buffers (so S_{j+1} overlaps the softmax of S_j),
+//               then O += P_j V_j into a third TMEM region.
+//   warps 2-5   softmax: thread = query row = TMEM lane.  Each reads its S
+//               row from TMEM, scales (and soft-caps), masks, keeps a running
+//               max and sum, writes P as bf16/fp16 into shared memory (the A
+//               operand of the P V MMA) and rescales O in TMEM only when its
+//               max grows by more than 2^8.  The epilogue divides O by the sum
+//               and writes o and the natural-log lse (or an fp32 partial state
+//               when the plan split the key range).
+// Every wait is bounded; a wait that runs out records kErrWaitTimeout and
+// makes all roles leave their loops, the MMA thread waits for its issued
+// MMAs, and TMEM is released.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+#include <type_traits>
 
 #include "pkv_bsr.h"
+#include "pkv_device.cuh"
 #include "pkv_launch.h"
 
 namespace pkv {
+namespace {
 
-bool prefill_supported(int, int, int, int) { return false; }
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kD = 128;                 // head_dim of the prefill kernel
+constexpr int kBM = kPrefillRows;       // packed query rows per tile
+constexpr int kBN = kPrefillKeys;       // keys per block
+constexpr int kThreads = 192;           // producer, MMA, 4 softmax warps
+constexpr uint32_t kTile = 32768;       // 128 rows x 128 16-bit values
+constexpr uint32_t kHalf = 16384;       // one 64-column half of a tile
+// Shared-memory map (offsets from a 1024-aligned base).
+constexpr uint32_t kOffQ = 0, kOffK = kTile, kOffV = 3 * kTile, kOffP = 5 * kTile, kOffBar = 6 * kTile;
+constexpr int kSmemBytes = 6 * kTile + 256 + 1024;
+// Barrier slots.
+enum { Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = 4, V_FULL = 6, V_EMPTY = 8, S_FULL = 10, P_FULL = 12,
+       O_DONE = 13, O_FREE = 14, V_LOAD = 15, DRAIN = 17, NUM_BARS = 18 };
+constexpr uint32_t kSoftmaxThreads = 128;
+constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t kColO = 256;
 
-cudaError_t launch_prefill(const PrefillArgs&, int, int, int, bool, int, int64_t, int64_t, cudaStream_t) {
-  return cudaErrorInvalidValue;
+struct Waiter {
+  int32_t* err;
+  volatile int* abort_flag;
+  // Bounded wait; false when it ran out (recorded) or another role gave up.
+  __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(err, kErrWaitTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return a <= 0 ? 0 : (a + b - 1) / b; }
+
+template <int G, typename T, bool CAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
+                   const __grid_constant__ CUtensorMap tkv) {
+  constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t base = smem_addr(sm);
+  const uint32_t sQ = base + kOffQ, sP = base + kOffP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
+  auto bar = [&](int i) { return base + kOffBar + 8u * i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NUM_BARS; ++i)
+      mbar_init(bar(i), (i == P_FULL || i == O_FREE) ? kSoftmaxThreads : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter wait{a.err, abort_flag};
+
+  const PlanHeader* hdr = a.hdr;
+  int t_begin = 0, t_end = 0;
+  if (static_cast<int>(blockIdx.x) < hdr->num_workers) {
+    t_begin = a.worker_ptr[blockIdx.x];
+    t_end = a.worker_ptr[blockIdx.x + 1];
+  }
+  const int num_pages = static_cast<int>(hdr->num_pages);
+  const int P = a.page_size;
+  const int ppt = kBN / P;  // pages per key block
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int kvc = 0;
+    uint32_t vload_phase[2] = {0, 0};
+    bool ok = true;
+    for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
+      const PrefillTile t = a.tiles[ti];
+      if (tn > 0) {
+        ok = __all_sync(kFull, wait(bar(Q_EMPTY), (tn - 1) & 1));
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(Q_FULL), kTile);
+        tma_load_3d(sQ, &tq, 0, t.kvh * G, t.q_row0, bar(Q_FULL));
+        tma_load_3d(sQ + kHalf, &tq, 64, t.kvh * G, t.q_row0, bar(Q_FULL));
+      }
+      const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
+      const int n_pages_req = ceil_div_i(t.kv_len, P);
+      auto page_of = [&](int j) {
+        const int rel = (t.kv_begin + j * kBN) / P + lane;
+        int id = num_pages;  // past the pool: TMA fills the box with zeros
+        if (lane < ppt && rel < n_pages_req) {
+          const int v = __ldg(a.kv_indices + t.idx_base + rel);
+          if (v >= 0 && v < num_pages)
+            id = v;
+          else
+            atomicOr(a.err, kErrPageIndex);
+        }
+        return id;
+      };
+      int id_next = n > 0 ? page_of(0) : num_pages;
+      for (int j = 0; j < n; ++j) {
+        const int id = id_next;
+        if (j + 1 < n) id_next = page_of(j + 1);  // the next block's page ids load during this one
+        const int s = kvc & 1;
+        const uint32_t ph = (kvc >> 1) & 1;
+        const uint32_t sK = base + kOffK + s * kTile, sV = base + kOffV + s * kTile;
+        if (kvc >= 2) {
+          ok = __all_sync(kFull, wait(bar(K_EMPTY + s), ph ^ 1));
+          if (!ok) break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL + s), kTile);
+        __syncwarp();
+        if (lane < ppt)
+          for (int h = 0; h < 2; ++h)
+            tma_load_5d(sK + h * kHalf + lane * P * 128, &tkv, h * 64, 0, t.kvh, 0, id, bar(K_FULL + s));
+        if (kvc >= 2) {
+          ok = __all_sync(kFull, wait(bar(V_EMPTY + s), ph ^ 1));
+          if (!ok) break;
+        }
+        const int rel0 = (t.kv_begin + j * kBN) / P;
+        const int last_rel = n_pages_req - 1 - rel0;
+        const bool partial = t.last_rows < P && last_rel >= 0 && last_rel < ppt;
+        const uint32_t vbar = partial ? bar(V_LOAD + s) : bar(V_FULL + s);
+        if (lane == 0) mbar_arrive_expect_tx(vbar, kTile);
+        __syncwarp();
+        if (lane < ppt)
+          for (int h = 0; h < 2; ++h) tma_load_5d(sV + h * kHalf + lane * P * 128, &tkv, h * 64, 0, t.kvh, 1, id, vbar);
+        if (partial) {
+          // The last page's slots past kv_last_page_len may hold anything; the
+          // P V product must see zeros there (0 * NaN would poison O).
+          ok = __all_sync(kFull, wait(bar(V_LOAD + s), vload_phase[s]));
+          if (!ok) break;
+          vload_phase[s] ^= 1;
+          const int chunks = (P - t.last_rows) * 8;  // 16-byte chunks per half
+          uint8_t* vgen = sm + kOffV + s * kTile;
+          for (int i = lane; i < 2 * chunks; i += 32) {
+            const int h = i / chunks, c = i % chunks;
+            *reinterpret_cast<uint4*>(vgen + h * kHalf + (last_rel * P + t.last_rows) * 128 + c * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(V_FULL + s));
+        }
+        ++kvc;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = umma_idesc_f16(kFmt, kBM, kBN, 0);
+      const uint32_t id_o = umma_idesc_f16(kFmt, kBM, kD, 1);
+      int kvc = 0, pc = 0;
+      bool ok = true;
+      // O += P_c V_c for the key block with global count c (the i-th of its tile).
+      auto pv = [&](int c, int i) -> bool {
+        if (!wait(bar(P_FULL), pc & 1)) return false;
+        ++pc;
+        const int s = c & 1;
+        if (!wait(bar(V_FULL + s), (c >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t sV = base + kOffV + s * kTile;
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_f16(tmem + kColO, sw128_desc(sP + (kk / 4) * kHalf + (kk % 4) * 32, 16, 1024),
+                   sw128_desc(sV + kk * 2048, kHalf, 1024), id_o, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(V_EMPTY + s));
+        umma_commit(bar(O_DONE));
+        return true;
+      };
+      for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
+        const PrefillTile t = a.tiles[ti];
+        const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
+        if (tn > 0 && !(ok = wait(bar(O_FREE), (tn - 1) & 1))) break;
+        if (!(ok = wait(bar(Q_FULL), tn & 1))) break;
+        tc_fence_after();
+        for (int j = 0; j < n; ++j) {
+          const int s = kvc & 1;
+          if (!(ok = wait(bar(K_FULL + s), (kvc >> 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t sK = base + kOffK + s * kTile;
+          const uint32_t d_s = tmem + (kvc & 1) * kBN;
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t koff = (kk / 4) * kHalf + (kk % 4) * 32;
+            umma_f16(d_s, sw128_desc(sQ + koff, 16, 1024), sw128_desc(sK + koff, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(S_FULL + (kvc & 1)));
+          umma_commit(bar(K_EMPTY + s));
+          if (j >= 1 && !(ok = pv(kvc - 1, j - 1))) break;
+          ++kvc;
+        }
+        if (!ok) break;
+        if (n >= 1 && !(ok = pv(kvc - 1, n - 1))) break;
+        umma_commit(bar(Q_EMPTY));
+      }
+      // Every MMA issued so far must finish before TMEM is released.
+      umma_commit(bar(DRAIN));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(bar(DRAIN), 0))
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(a.err, kErrWaitTimeout);
+          break;
+        }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float scale = CAP ? a.sm_scale : a.sm_scale * kLog2e;
+    uint8_t* pgen = sm + kOffP;
+    int kvc = 0, odc = 0;
+    bool ok = true;
+    for (int ti = t_begin; ti < t_end && ok; ++ti) {
+      const PrefillTile t = a.tiles[ti];
+      const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
+      const int rpos = r / G;
+      const bool row_valid = rpos < t.n_pos;
+      const int pos = t.q_pos0 + rpos;
+      int limit = t.kv_len, lim0 = t.kv_len;  // keys < limit are visible to this row / to every row
+      if (a.causal) {
+        limit = min(limit, pos + 1 + t.kv_len - t.qo_len);
+        lim0 = min(lim0, t.q_pos0 + 1 + t.kv_len - t.qo_len);
+      }
+      limit = min(limit, t.kv_end);
+      lim0 = min(lim0, t.kv_end);
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        const int b = kvc & 1;
+        if (!(ok = __all_sync(kFull, wait(bar(S_FULL + b), (kvc >> 1) & 1)))) break;
+        tc_fence_after();
+        float x[kBN];
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32_sync(tmem + lane_off + b * kBN + c * 32, rr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]);
+        }
+        const int key0 = t.kv_begin + j * kBN;
+        const bool full = key0 + kBN <= lim0;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) {
+          float v = x[i] * scale;
+          if constexpr (CAP) v = a.cap * tanhf(v / a.cap) * kLog2e;
+          if (!full && key0 + i >= limit) v = -INFINITY;
+          x[i] = v;
+          mx = fmaxf(mx, v);
+        }
+        const float m_new = fmaxf(m_ref, mx);
+        const bool resc = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_ref + 8.f);
+        float alpha = 1.f;
+        if (resc) {
+          alpha = fast_exp2(m_ref - m_new);
+          m_ref = m_new;
+          l *= alpha;
+        }
+        const float sub = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float lsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) {
+          x[i] = fast_exp2(x[i] - sub);
+          lsum += x[i];
+        }
+        l += lsum;
+        if (j >= 1) {
+          // P V of the previous block must be done before O is rescaled and P overwritten.
+          if (!(ok = __all_sync(kFull, wait(bar(O_DONE), odc & 1)))) break;
+          ++odc;
+          tc_fence_after();
+          if (__any_sync(kFull, resc)) {
+#pragma unroll
+            for (int c = 0; c < kD / 32; ++c) {
+              uint32_t rr[32];
+              const uint32_t addr = tmem + lane_off + kColO + c * 32;
+              tmem_ld32_sync(addr, rr);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+              tmem_st32(addr, rr);
+            }
+            tmem_wait_st();
+          }
+        }
+        // P row -> shared memory, 128B-swizzled K-major (the A operand of O += P V).
+#pragma unroll
+        for (int c16 = 0; c16 < kBN / 8; ++c16) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = x[c16 * 8 + e];
+          const int half = c16 / 8, cc = c16 % 8;
+          *reinterpret_cast<uint4*>(pgen + half * kHalf + r * 128 + ((cc ^ (r & 7)) << 4)) = from_float8<T>(f);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(P_FULL));
+        ++kvc;
+      }
+      if (!ok) break;
+      if (n >= 1) {
+        if (!(ok = __all_sync(kFull, wait(bar(O_DONE), odc & 1)))) break;
+        ++odc;
+        tc_fence_after();
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse_v = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+      const int64_t orow = static_cast<int64_t>(t.q_row0 + rpos) * a.num_qo_heads + t.kvh * G + (r % G);
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        float ov[32];
+        if (n >= 1) {
+          uint32_t rr[32];
+          tmem_ld32_sync(tmem + lane_off + kColO + c * 32, rr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(rr[i]) * inv;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+        }
+        if (t.slot < 0) {
+          if (row_valid) {
+            T* dst = static_cast<T*>(a.o) + orow * kD + c * 32;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = ov[q * 8 + e];
+              reinterpret_cast<uint4*>(dst)[q] = from_float8<T>(f);
+            }
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(t.slot) * kBM + r) * kD + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dst[q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+        }
+      }
+      if (t.slot < 0) {
+        if (row_valid && a.lse) a.lse[orow] = lse_v;
+      } else {
+        a.part_lse[static_cast<int64_t>(t.slot) * kBM + r] = lse_v;
+      }
+      tc_fence_before();
+      mbar_arrive(bar(O_FREE));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_prefill_merge(const PrefillArgs&, int, int, int, int, cudaStream_t) {
-  return cudaErrorInvalidValue;
+// Rows of query tiles whose key range the plan split: one warp per packed row,
+// lanes over head_dim, log-sum-exp merge of the chunks' fp32 partial states.
+template <typename T>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constant__ PrefillArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int warp_id = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int n_warps = gridDim.x * 8;
+  const int G = a.num_qo_heads / a.num_kv_heads;
+  const int pairs = a.hdr->num_merge * kBM;
+  for (int pair = warp_id; pair < pairs; pair += n_warps) {
+    const PrefillMerge it = a.merge[pair / kBM];
+    const int r = pair % kBM;
+    if (r / G >= it.n_pos) continue;
+    float mx = -INFINITY;
+    for (int i = lane; i < it.n_slots; i += 32)
+      mx = fmaxf(mx, a.part_lse[static_cast<int64_t>(it.slot_begin + i) * kBM + r]);
+    mx = warp_max(mx);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float wsum = 0.f;
+    if (mx != -INFINITY) {
+      for (int i = 0; i < it.n_slots; ++i) {
+        const int64_t row = static_cast<int64_t>(it.slot_begin + i) * kBM + r;
+        const float w = fast_exp2((a.part_lse[row] - mx) * kLog2e);
+        if (w > 0.f) {
+          const float4 v = reinterpret_cast<const float4*>(a.part_o + row * kD)[lane];
+          acc[0] = fmaf(w, v.x, acc[0]);
+          acc[1] = fmaf(w, v.y, acc[1]);
+          acc[2] = fmaf(w, v.z, acc[2]);
+          acc[3] = fmaf(w, v.w, acc[3]);
+          wsum += w;
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int64_t orow = static_cast<int64_t>(it.q_row0 + r / G) * a.num_qo_heads + it.kvh * G + (r % G);
+    T* dst = static_cast<T*>(a.o) + orow * kD + lane * 4;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) dst[v] = from_float<T>(acc[v] * inv);
+    if (lane == 0 && a.lse) a.lse[orow] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+template <typename T>
+cudaError_t launch_t(const PrefillArgs& a, int G, bool cap, int grid, const CUtensorMap& tq, const CUtensorMap& tkv,
+                     cudaStream_t s) {
+  void (*kern)(PrefillArgs, CUtensorMap, CUtensorMap) = nullptr;
+#define PKV_PF_CASE(GG)                                                                      \
+  case GG:                                                                                   \
+    kern = cap ? prefill_kernel<GG, T, true> : prefill_kernel<GG, T, false>;                 \
+    break;
+  switch (G) {
+    PKV_PF_CASE(1) PKV_PF_CASE(2) PKV_PF_CASE(4) PKV_PF_CASE(8)
+    default: return cudaErrorInvalidValue;
+  }
+#undef PKV_PF_CASE
+  cudaError_t e = ensure_smem_limit(kern, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, kSmemBytes, s>>>(a, tq, tkv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_supported(int head_dim, int group, int dtype, int page_size) {
+  return head_dim == kD && (group == 1 || group == 2 || group == 4 || group == 8) &&
+         (dtype == PKV_F16 || dtype == PKV_BF16) &&
+         (page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64 || page_size == 128);
+}
+
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dtype, bool cap, int grid,
+                           int64_t total_q, int64_t num_pages, cudaStream_t stream) {
+  if (!prefill_supported(head_dim, group, dtype, a.page_size)) return cudaErrorInvalidValue;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt = dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t hq = a.num_qo_heads, hkv = a.num_kv_heads, P = a.page_size;
+  CUtensorMap tq, tkv;
+  {
+    // q [total_q, Hq, D]: box = 64 columns x the G heads of a group x 128/G positions.
+    cuuint64_t dims[3] = {kD, hq, static_cast<cuuint64_t>(total_q > 0 ? total_q : 1)};
+    cuuint64_t strides[2] = {kD * 2, hq * kD * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(kBM / group)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&tq, dt, 3, const_cast<void*>(a.q), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // kv_data [num_pages, 2, Hkv, P, D]: box = 64 columns x the P rows of one (page, K|V, head).
+    cuuint64_t dims[5] = {kD, P, hkv, 2, static_cast<cuuint64_t>(num_pages > 0 ? num_pages : 1)};
+    cuuint64_t strides[4] = {kD * 2, P * kD * 2, hkv * P * kD * 2, 2 * hkv * P * kD * 2};
+    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(P), 1, 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (encode(&tkv, dt, 5, const_cast<void*>(a.kv), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (dtype == PKV_BF16) return launch_t<__nv_bfloat16>(a, group, cap, grid, tq, tkv, stream);
+  return launch_t<__half>(a, group, cap, grid, tq, tkv, stream);
+}
+
+cudaError_t launch_prefill_merge(const PrefillArgs& a, int head_dim, int group, int dtype, int grid,
+                                 cudaStream_t stream) {
+  if (head_dim != kD || group <= 0) return cudaErrorInvalidValue;
+  if (dtype == PKV_BF16)
+    prefill_merge_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a);
+  else if (dtype == PKV_F16)
+    prefill_merge_kernel<__half><<<grid, 256, 0, stream>>>(a);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -1,0 +1,130 @@
+"""GPU parity of the tcgen05 paged prefill (causal ragged, split key ranges) and of
+cascade attention (prefix row block + per-request suffix + merge_state) against the
+fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_bsr_gb300 import api, runner, workloads as W
+from gpu_util import assert_matches_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_bsr_gb300 import build
+    build.build()
+    oracle.build()
+    api.load()
+    torch.cuda.set_device(0)
+
+
+def prefill_vs_oracle(b, what="", rows=None, **limits):
+    db = runner.DeviceBatch.from_host(b)
+    plan = runner.make_plan(b, api.PLAN_PREFILL, **limits)
+    runner.plan_batch(plan, b)
+    o, lse = runner.prefill(db, plan)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    ref_o, ref_lse = oracle.attention_of(b, rows=rows)
+    if rows is not None:
+        idx = torch.as_tensor(rows, dtype=torch.long, device=o.device)
+        o, lse = o[idx], lse[idx]
+    assert_matches_oracle(o, lse, ref_o, ref_lse, b.dtype, what)
+    return plan
+
+
+def batch(qo_lens, prefix, hq=8, hkv=2, P=16, dtype=torch.bfloat16, causal=True, seed=0, cap=0.0):
+    kv = [q + p for q, p in zip(qo_lens, prefix)]
+    return W.make_paged_batch(qo_lens=qo_lens, kv_lens=kv, num_qo_heads=hq, num_kv_heads=hkv, head_dim=128,
+                              page_size=P, dtype=dtype, seed=seed, causal=causal, logits_cap=cap, poison=True)
+
+
+def test_small_ragged_causal():
+    prefill_vs_oracle(batch([1, 37, 200], [0, 5, 100], seed=1), "small causal")
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_group_sizes(group):
+    prefill_vs_oracle(batch([130, 7, 300], [17, 0, 64], hq=2 * group, hkv=2, seed=group), f"g{group}")
+
+
+def test_fp16():
+    prefill_vs_oracle(batch([100, 129], [3, 200], dtype=torch.float16, seed=2), "fp16")
+
+
+def test_non_causal():
+    prefill_vs_oracle(batch([50, 128, 300], [10, 70, 1], causal=False, seed=3), "non-causal")
+
+
+@pytest.mark.parametrize("page_size", [8, 32, 64, 128])
+def test_page_sizes(page_size):
+    prefill_vs_oracle(batch([90, 257], [33, 5], P=page_size, seed=page_size), f"page {page_size}")
+
+
+def test_rows_that_see_no_key_and_empty_requests():
+    # causal with more rows than keys: the first qo - kv rows see nothing (o = 0, lse = -inf)
+    b = W.make_paged_batch(qo_lens=[10, 0, 3, 40], kv_lens=[5, 9, 3, 1], num_qo_heads=8, num_kv_heads=2,
+                           head_dim=128, page_size=16, dtype=torch.bfloat16, seed=4, causal=True, poison=True)
+    prefill_vs_oracle(b, "no keys")
+
+
+def test_softcap_prefill():
+    prefill_vs_oracle(batch([77, 200], [100, 0], seed=5, cap=30.0), "softcap")
+
+
+def test_split_key_range_is_merged():
+    """Few query tiles and long keys: the plan cuts key ranges into chunks (partials + merge)."""
+    b = W.make_paged_batch(qo_lens=[64], kv_lens=[9000], num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                           page_size=16, dtype=torch.bfloat16, seed=6, causal=False, poison=True)
+    plan = prefill_vs_oracle(b, "split")
+    assert plan.info().num_merge > 0 and plan.info().num_slots > 8
+
+
+@pytest.mark.slow
+def test_ragged_causal_prefill_full_size_sampled_rows():
+    """Batch 16, qo ~ U[128, 2048], kv = qo + U[0, 1024], 32/8 heads: 3000 sampled rows."""
+    b = W.ragged_prefill(seed=1003, poison=True)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(b.total_q, size=3000, replace=False))
+    # always include each request's first and last row
+    ends = np.concatenate([b.qo_indptr[:-1].numpy(), b.qo_indptr[1:].numpy() - 1])
+    rows = np.unique(np.concatenate([rows, ends]))
+    prefill_vs_oracle(b, "ragged full size", rows=rows)
+
+
+@pytest.mark.slow
+def test_cascade_softcap_full_size_equals_full_attention():
+    """64 requests sharing a 2048-token prefix (one large row block), suffixes U[50, 200],
+    soft-cap 30: prefix prefill + suffix decode + merge_state vs non-cascade attention."""
+    cb = W.cascade_decode(seed=1004, poison=True)
+    kv = cb.full.kv_data.cuda()
+    dp = runner.DeviceBatch.from_host(cb.prefix, kv_data=kv)
+    ds = runner.DeviceBatch.from_host(cb.suffix, kv_data=kv)
+    pplan = runner.make_plan(cb.prefix, api.PLAN_PREFILL)
+    splan = runner.make_plan(cb.suffix, api.PLAN_DECODE)
+    runner.plan_batch(pplan, cb.prefix)
+    runner.plan_batch(splan, cb.suffix)
+    o, lse = runner.cascade(dp, ds, pplan, splan)
+    torch.cuda.synchronize()
+    assert pplan.device_error() == 0 and splan.device_error() == 0
+    ref_o, ref_lse = oracle.attention_of(cb.full)
+    assert_matches_oracle(o, lse, ref_o, ref_lse, torch.bfloat16, "cascade")
+
+
+def test_prefill_page_permutation_is_bit_exact():
+    b = batch([300, 45], [60, 200], seed=8)
+    db = runner.DeviceBatch.from_host(b)
+    plan = runner.make_plan(b, api.PLAN_PREFILL)
+    runner.plan_batch(plan, b)
+    o1, l1 = runner.prefill(db, plan)
+    perm = torch.randperm(b.num_pages, generator=torch.Generator().manual_seed(5))
+    kv2 = torch.empty_like(b.kv_data)
+    kv2[perm] = b.kv_data
+    b2 = W.PagedBatch(**{**b.__dict__, "kv_data": kv2, "kv_indices": perm[b.kv_indices.long()].to(torch.int32)})
+    runner.plan_batch(plan, b2)
+    o2, l2 = runner.prefill(runner.DeviceBatch.from_host(b2), plan)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
