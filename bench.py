@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--no-secondary", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--only", choices=["prefill", "cascade", "skewed"], default=None,
+                   help="time one secondary measurement alone (for profiling) and print it")
     return p.parse_args()
 
 
@@ -343,6 +345,10 @@ def prefill_measure(peaks, steps=20, warmup=3):
 
 
 def cascade_measure(steps=50, warmup=5):
+    """Cascade (prefix prefill over one large row block + suffix decode + merge_state)
+    vs non-cascade decode over prefix + suffix pages.  Plans are made once (the batch
+    does not change); the run calls of each variant are captured in a CUDA graph and
+    replayed, so the comparison is GPU time, not Python launch overhead."""
     import torch
     from paged_kv_cache_bsr_gb300 import runner, api, workloads as W
     cb = W.cascade_decode(seed=1004)
@@ -356,23 +362,64 @@ def cascade_measure(steps=50, warmup=5):
     dp = runner.DeviceBatch.from_host(cb.prefix, kv_data=kv)
     ds = runner.DeviceBatch.from_host(cb.suffix, kv_data=kv)
     df = runner.DeviceBatch.from_host(cb.full, kv_data=kv)
-    s = torch.cuda.current_stream()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        runner.plan_batch(pplan, cb.prefix, stream=s)
+        runner.plan_batch(splan, cb.suffix, stream=s)
+        runner.plan_batch(fplan, cb.full, stream=s)
+        o_p = torch.empty_like(dp.q)
+        l_p = torch.empty(dp.q.shape[:2], dtype=torch.float32, device=dp.q.device)
+        o_s, l_s = torch.empty_like(o_p), torch.empty_like(l_p)
+        o_f, l_f = torch.empty_like(o_p), torch.empty_like(l_p)
 
-    def casc(_):
-        runner.plan_batch(pplan, cb.prefix)
-        runner.plan_batch(splan, cb.suffix)
-        runner.cascade(dp, ds, pplan, splan)
+        def casc():
+            pplan.run(dp.q, kv, dp.kv_indices, dp.kv_indptr, dp.kv_last_page_len, o_p, l_p,
+                      qo_indptr=dp.qo_indptr, stream=s)
+            splan.run(ds.q, kv, ds.kv_indices, ds.kv_indptr, ds.kv_last_page_len, o_s, l_s, stream=s)
+            api.merge_state(o_p, l_p, o_s, l_s, o_p, l_p, stream=s)
 
-    def full(_):
-        runner.plan_batch(fplan, cb.full)
-        runner.decode(df, fplan)
+        def full():
+            fplan.run(df.q, kv, df.kv_indices, df.kv_indptr, df.kv_last_page_len, o_f, l_f, stream=s)
 
-    c_ms, _ = time_steps(casc, steps, warmup, s)
-    f_ms, _ = time_steps(full, steps, warmup, s)
-    c_ms, f_ms = c_ms / steps, f_ms / steps
-    return {"workload": "cascade_softcap_decode", "cascade_us": round(c_ms * 1e3, 2),
-            "non_cascade_us": round(f_ms * 1e3, 2), "speedup": round(f_ms / c_ms, 3),
-            "non_cascade_kv_GBps": round(cb.full.kv_bytes() / (f_ms * 1e-3) / 1e9, 1)}
+        casc()
+        full()
+    s.synchronize()
+    out = {"workload": "cascade_softcap_decode"}
+    for name, fn in (("cascade", casc), ("non_cascade", full)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(steps):
+                g.replay()
+            b.record(s)
+        b.synchronize()
+        out[name + "_us"] = round(a.elapsed_time(b) / steps * 1e3, 2)
+    out["speedup"] = round(out["non_cascade_us"] / out["cascade_us"], 3)
+    out["non_cascade_kv_GBps"] = round(cb.full.kv_bytes() / (out["non_cascade_us"] * 1e-6) / 1e9, 1)
+    out["timing"] = "CUDA-graph replay of the run calls; plans made once outside the timed loop"
+    return out
+
+
+def run_only(args):
+    import torch
+    from paged_kv_cache_bsr_gb300 import build, api, workloads as W
+    torch.cuda.set_device(0)
+    build.build()
+    api.load()
+    peaks = measured_peaks()
+    if args.only == "prefill":
+        res = prefill_measure(peaks, steps=args.steps, warmup=args.warmup)
+    elif args.only == "cascade":
+        res = cascade_measure(steps=args.steps, warmup=args.warmup)
+    else:
+        r = decode_measure(W.skewed_decode(seed=1002), args.steps, args.warmup, peaks)
+        res = {"value": round(r["value"], 1), "unit": "GB/s", "roofline": r["roofline"]}
+    print(json.dumps({"only": args.only, **res}), flush=True)
 
 
 def run_own(args):
@@ -464,6 +511,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_own(args)
 

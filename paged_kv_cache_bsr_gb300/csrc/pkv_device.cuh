@@ -129,6 +129,34 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   return d;
 }
 
+// Packed fp32 add on a pair: d = a + b.
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// 2^x on the FMA pipe, for x <= 2^22: x = j + f with j the nearest integer
+// (added to and subtracted from 1.5 * 2^23, which rounds to an integer) and
+// f in [-1/2, 1/2]; 2^f by a cubic fitted here by least squares on Chebyshev
+// nodes of [-1/2, 1/2] (largest relative error 7.8e-5); 2^j added to the
+// exponent field.  Inputs below -126 (masked logits are -inf) give exactly 0.
+__device__ __forceinline__ float exp2_poly3(float x_in) {
+  const float x = fmaxf(x_in, -126.f);
+  const float t = x + 12582912.f;
+  const float f = x - (t - 12582912.f);
+  float p = fmaf(0.05508868396282196f, f, 0.24260404706001282f);
+  p = fmaf(p, f, 0.6932762265205383f);
+  p = fmaf(p, f, 0.9999289512634277f);
+  const int j = __float_as_int(t) - 0x4B400000;
+  const float r = __int_as_float(__float_as_int(p) + (j << 23));
+  return x_in < -126.f ? 0.f : r;
+}
+
 // Four 16-bit pairs (one 16-byte chunk) to four fp32 pairs.
 template <typename T>
 __device__ __forceinline__ void to_float2x4(const uint4& raw, float2 (&f)[4]);
@@ -307,6 +335,44 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
       : "r"(taddr)
       : "memory");
 }
+// 128 consecutive fp32 columns of this thread's TMEM lane: four loads, one wait.
+__device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "{\n\t.reg .b32 a1, a2, a3;\n\t"
+      "add.u32 a1, %128, 32;\n\tadd.u32 a2, %128, 64;\n\tadd.u32 a3, %128, 96;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [a1];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, "
+      "%77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, [a2];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, "
+      "%107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, "
+      "%124, %125, %126, %127}, [a3];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t}"
+      : PKV_R32(r), PKV_R32((r + 32)), PKV_R32((r + 64)), PKV_R32((r + 96))
+      : "r"(taddr)
+      : "memory");
+}
+// 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait.
+__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "{\n\t.reg .b32 a1;\n\tadd.u32 a1, %64, 32;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [a1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t}"
+      : PKV_R32(r), PKV_R32((r + 32))
+      : "r"(taddr)
+      : "memory");
+}
+
+// Barrier over `threads` threads (a multiple of 32) with id 1..15 (0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

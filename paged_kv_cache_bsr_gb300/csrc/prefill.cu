@@ -12,22 +12,28 @@
 // GB300 design.  One CTA per SM walks the plan's list of work tiles.  A tile
 // is 128 packed query rows (128/G query positions x the G heads of one kv
 // head) against a key range, visited 128 keys (128/P pages) at a time:
-//   warp 0      producer: TMA loads the Q box once per tile and, per key
-//               block, one 64-column box per (page, half) for K and for V,
-//               128B-swizzled into shared memory (two stages each).  Pages
-//               past the request come from an out-of-range page coordinate,
-//               which TMA fills with zeros; V rows past kv_last_page_len of
-//               the last page are zeroed before the MMA may read them.
+//   warps 0, 6  producers: TMA loads the Q box once per tile and, per key
+//               block, one 64-column box per (page, half) for K (warp 0,
+//               three stages) and for V (warp 6, two stages), 128B-swizzled
+//               into shared memory.  K and V run independently, so the page
+//               gather of K is never held back by the P V of older blocks.
+//               Pages past the request come from an out-of-range page
+//               coordinate, which TMA fills with zeros; V rows past
+//               kv_last_page_len of the last page are zeroed before the MMA
+//               may read them.
 //   warp 1      one thread issues the tcgen05 MMAs: S_j = Q K_j^T into one of
 //               two TMEM buffers (so S_{j+1} overlaps the softmax of S_j),
 //               then O += P_j V_j into a third TMEM region.
-//   warps 2-5   softmax: thread = query row = TMEM lane.  Each reads its S
-//               row from TMEM, scales (and soft-caps), masks, keeps a running
-//               max and sum, writes P as bf16/fp16 into shared memory (the A
-//               operand of the P V MMA) and rescales O in TMEM only when its
-//               max grows by more than 2^8.  The epilogue divides O by the sum
-//               and writes o and the natural-log lse (or an fp32 partial state
-//               when the plan split the key range).
+//   warps 2-9   softmax: two warps per query row block quarter, each thread
+//               one query row (= TMEM lane) and one half (64 keys) of it.  It
+//               reads its half of S from TMEM, scales (and soft-caps), masks,
+//               exchanges the half-row max with its partner warp through
+//               shared memory, keeps a running max and sum, writes its half of
+//               P as bf16/fp16 into shared memory (the A operand of the P V
+//               MMA) and rescales its half of O in TMEM only when the max grows
+//               by more than 2^8.  The epilogue divides O by the sum and writes
+//               o and the natural-log lse (or an fp32 partial state when the
+//               plan split the key range).
 // Every wait is bounded; a wait that runs out records kErrWaitTimeout and
 // makes all roles leave their loops, the MMA thread waits for its issued
 // MMAs, and TMEM is released.
@@ -50,16 +56,25 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kD = 128;                 // head_dim of the prefill kernel
 constexpr int kBM = kPrefillRows;       // packed query rows per tile
 constexpr int kBN = kPrefillKeys;       // keys per block
-constexpr int kThreads = 192;           // producer, MMA, 4 softmax warps
+constexpr int kThreads = 352;           // K producer, MMA, 8 softmax warps, V producer
+constexpr int kVWarp = 10;              // the V producer
 constexpr uint32_t kTile = 32768;       // 128 rows x 128 16-bit values
 constexpr uint32_t kHalf = 16384;       // one 64-column half of a tile
+constexpr int kKStages = 3;             // K blocks in flight (gather latency is ~2 key blocks)
+constexpr int kVStages = 2;
 // Shared-memory map (offsets from a 1024-aligned base).
-constexpr uint32_t kOffQ = 0, kOffK = kTile, kOffV = 3 * kTile, kOffP = 5 * kTile, kOffBar = 6 * kTile;
-constexpr int kSmemBytes = 6 * kTile + 256 + 1024;
+constexpr uint32_t kOffQ = 0, kOffK = kTile, kOffV = kOffK + kKStages * kTile, kOffP = kOffV + kVStages * kTile,
+                   kOffBar = kOffP + kTile, kOffRed = kOffBar + 256;
+// The tiles need 1024-byte alignment and the budget leaves no slack to align
+// by hand: the kernel checks that dynamic shared memory starts aligned.
+constexpr int kSmemBytes = kOffRed + 2 * 2 * kPrefillRows * 4;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 // Barrier slots.
-enum { Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = 4, V_FULL = 6, V_EMPTY = 8, S_FULL = 10, P_FULL = 12,
-       O_DONE = 13, O_FREE = 14, V_LOAD = 15, DRAIN = 17, NUM_BARS = 18 };
-constexpr uint32_t kSoftmaxThreads = 128;
+enum { Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages,
+       V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, P_FULL = S_FULL + 2, O_DONE = P_FULL + 1,
+       O_FREE = O_DONE + 1, V_LOAD = O_FREE + 1, DRAIN = V_LOAD + kVStages, NUM_BARS = DRAIN + 1 };
+static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
+constexpr uint32_t kSoftmaxThreads = 256;
 constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384)
 constexpr uint32_t kColO = 256;
 
@@ -89,9 +104,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
                    const __grid_constant__ CUtensorMap tkv) {
   constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   const uint32_t base = smem_addr(sm);
+  if (base & 1023u) {  // never expected; refuse rather than misread swizzled tiles
+    if (threadIdx.x == 0) atomicOr(a.err, kErrTmemAlloc);
+    return;
+  }
   const uint32_t sQ = base + kOffQ, sP = base + kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
@@ -125,10 +144,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int P = a.page_size;
   const int ppt = kBN / P;  // pages per key block
 
+  auto page_of = [&](const PrefillTile& t, int j, int n_pages_req) {
+    const int rel = (t.kv_begin + j * kBN) / P + lane;
+    int id = num_pages;  // past the pool: TMA fills the box with zeros
+    if (lane < ppt && rel < n_pages_req) {
+      const int v = __ldg(a.kv_indices + t.idx_base + rel);
+      if (v >= 0 && v < num_pages)
+        id = v;
+      else
+        atomicOr(a.err, kErrPageIndex);
+    }
+    return id;
+  };
+
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ Q and K producer
     int kvc = 0;
-    uint32_t vload_phase[2] = {0, 0};
     bool ok = true;
     for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
       const PrefillTile t = a.tiles[ti];
@@ -143,38 +174,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
       const int n_pages_req = ceil_div_i(t.kv_len, P);
-      auto page_of = [&](int j) {
-        const int rel = (t.kv_begin + j * kBN) / P + lane;
-        int id = num_pages;  // past the pool: TMA fills the box with zeros
-        if (lane < ppt && rel < n_pages_req) {
-          const int v = __ldg(a.kv_indices + t.idx_base + rel);
-          if (v >= 0 && v < num_pages)
-            id = v;
-          else
-            atomicOr(a.err, kErrPageIndex);
-        }
-        return id;
-      };
-      int id_next = n > 0 ? page_of(0) : num_pages;
+      int id_next = n > 0 ? page_of(t, 0, n_pages_req) : num_pages;
       for (int j = 0; j < n; ++j) {
         const int id = id_next;
-        if (j + 1 < n) id_next = page_of(j + 1);  // the next block's page ids load during this one
-        const int s = kvc & 1;
-        const uint32_t ph = (kvc >> 1) & 1;
-        const uint32_t sK = base + kOffK + s * kTile, sV = base + kOffV + s * kTile;
-        if (kvc >= 2) {
-          ok = __all_sync(kFull, wait(bar(K_EMPTY + s), ph ^ 1));
+        if (j + 1 < n) id_next = page_of(t, j + 1, n_pages_req);  // next block's page ids load meanwhile
+        const int s = kvc % kKStages;
+        if (kvc >= kKStages) {
+          ok = __all_sync(kFull, wait(bar(K_EMPTY + s), ((kvc / kKStages) - 1) & 1));
           if (!ok) break;
         }
         if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL + s), kTile);
         __syncwarp();
+        const uint32_t sK = base + kOffK + s * kTile;
         if (lane < ppt)
           for (int h = 0; h < 2; ++h)
             tma_load_5d(sK + h * kHalf + lane * P * 128, &tkv, h * 64, 0, t.kvh, 0, id, bar(K_FULL + s));
-        if (kvc >= 2) {
-          ok = __all_sync(kFull, wait(bar(V_EMPTY + s), ph ^ 1));
+        ++kvc;
+      }
+    }
+  } else if (warp == kVWarp) {
+    // ------------------------------------------------------------ V producer
+    int kvc = 0;
+    uint32_t vload_bits = 0;  // phase parity of each V_LOAD barrier
+    bool ok = true;
+    for (int ti = t_begin; ti < t_end && ok; ++ti) {
+      const PrefillTile t = a.tiles[ti];
+      const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
+      const int n_pages_req = ceil_div_i(t.kv_len, P);
+      int id_next = n > 0 ? page_of(t, 0, n_pages_req) : num_pages;
+      for (int j = 0; j < n; ++j) {
+        const int id = id_next;
+        if (j + 1 < n) id_next = page_of(t, j + 1, n_pages_req);
+        const int s = kvc % kVStages;
+        if (kvc >= kVStages) {
+          ok = __all_sync(kFull, wait(bar(V_EMPTY + s), ((kvc / kVStages) - 1) & 1));
           if (!ok) break;
         }
+        const uint32_t sV = base + kOffV + s * kTile;
         const int rel0 = (t.kv_begin + j * kBN) / P;
         const int last_rel = n_pages_req - 1 - rel0;
         const bool partial = t.last_rows < P && last_rel >= 0 && last_rel < ppt;
@@ -186,9 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (partial) {
           // The last page's slots past kv_last_page_len may hold anything; the
           // P V product must see zeros there (0 * NaN would poison O).
-          ok = __all_sync(kFull, wait(bar(V_LOAD + s), vload_phase[s]));
+          ok = __all_sync(kFull, wait(bar(V_LOAD + s), (vload_bits >> s) & 1));
           if (!ok) break;
-          vload_phase[s] ^= 1;
+          vload_bits ^= 1u << s;
           const int chunks = (P - t.last_rows) * 8;  // 16-byte chunks per half
           uint8_t* vgen = sm + kOffV + s * kTile;
           for (int i = lane; i < 2 * chunks; i += 32) {
@@ -208,14 +244,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = umma_idesc_f16(kFmt, kBM, kBN, 0);
       const uint32_t id_o = umma_idesc_f16(kFmt, kBM, kD, 1);
-      int kvc = 0, pc = 0;
+      int kvc = 0, pc = 0, ofree = 0;
+      bool o_used = false;  // an earlier tile accumulated into O: wait for its epilogue first
       bool ok = true;
       // O += P_c V_c for the key block with global count c (the i-th of its tile).
       auto pv = [&](int c, int i) -> bool {
+        if (i == 0 && o_used) {
+          if (!wait(bar(O_FREE), ofree & 1)) return false;
+          ++ofree;
+        }
         if (!wait(bar(P_FULL), pc & 1)) return false;
         ++pc;
-        const int s = c & 1;
-        if (!wait(bar(V_FULL + s), (c >> 1) & 1)) return false;
+        const int s = c % kVStages;
+        if (!wait(bar(V_FULL + s), (c / kVStages) & 1)) return false;
         tc_fence_after();
         const uint32_t sV = base + kOffV + s * kTile;
         for (int kk = 0; kk < kBN / 16; ++kk)
@@ -223,17 +264,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                    sw128_desc(sV + kk * 2048, kHalf, 1024), id_o, (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(V_EMPTY + s));
         umma_commit(bar(O_DONE));
+        o_used = true;
         return true;
       };
       for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
         const PrefillTile t = a.tiles[ti];
         const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
-        if (tn > 0 && !(ok = wait(bar(O_FREE), (tn - 1) & 1))) break;
         if (!(ok = wait(bar(Q_FULL), tn & 1))) break;
         tc_fence_after();
         for (int j = 0; j < n; ++j) {
-          const int s = kvc & 1;
-          if (!(ok = wait(bar(K_FULL + s), (kvc >> 1) & 1))) break;
+          const int s = kvc % kKStages;
+          if (!(ok = wait(bar(K_FULL + s), (kvc / kKStages) & 1))) break;
           tc_fence_after();
           const uint32_t sK = base + kOffK + s * kTile;
           const uint32_t d_s = tmem + (kvc & 1) * kBN;
@@ -243,12 +284,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit(bar(S_FULL + (kvc & 1)));
           umma_commit(bar(K_EMPTY + s));
+          if (j == n - 1) umma_commit(bar(Q_EMPTY));  // Q is free once the tile's last S is done
           if (j >= 1 && !(ok = pv(kvc - 1, j - 1))) break;
           ++kvc;
         }
         if (!ok) break;
-        if (n >= 1 && !(ok = pv(kvc - 1, n - 1))) break;
-        umma_commit(bar(Q_EMPTY));
+        if (n >= 1) {
+          if (!(ok = pv(kvc - 1, n - 1))) break;
+        } else {
+          umma_commit(bar(Q_EMPTY));
+        }
       }
       // Every MMA issued so far must finish before TMEM is released.
       umma_commit(bar(DRAIN));
@@ -262,11 +307,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int hf = (warp - 2) >> 2;          // which 64 keys / O columns of the row
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t pair_bar = 1 + quarter;   // the two warps of this lane quarter
+    float* red = reinterpret_cast<float*>(sm + kOffRed);  // [parity][half][row] half-row maxima / sums
     const float scale = CAP ? a.sm_scale : a.sm_scale * kLog2e;
     uint8_t* pgen = sm + kOffP;
+    constexpr int kH = kBN / 2;
     int kvc = 0, odc = 0;
     bool ok = true;
     for (int ti = t_begin; ti < t_end && ok; ++ti) {
@@ -282,30 +331,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       limit = min(limit, t.kv_end);
       lim0 = min(lim0, t.kv_end);
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;  // l: this half-row's share of the sum
       for (int j = 0; j < n; ++j) {
         const int b = kvc & 1;
         if (!(ok = __all_sync(kFull, wait(bar(S_FULL + b), (kvc >> 1) & 1)))) break;
         tc_fence_after();
-        float x[kBN];
+        uint32_t sr[kH];
+        tmem_ld64_sync(tmem + lane_off + b * kBN + hf * kH, sr);
+        const int key0 = t.kv_begin + j * kBN + hf * kH;
+        const bool full = key0 + kH <= lim0;
+        // Logits in log2 units are x * mul; the max is taken on x (mul > 0).
+        float mul = scale;
+        if constexpr (CAP) {
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32_sync(tmem + lane_off + b * kBN + c * 32, rr);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(rr[i]);
+          for (int i = 0; i < kH; ++i)
+            sr[i] = __float_as_uint(a.cap * tanhf(__uint_as_float(sr[i]) * scale / a.cap) * kLog2e);
+          mul = 1.f;
         }
-        const int key0 = t.kv_begin + j * kBN;
-        const bool full = key0 + kBN <= lim0;
-        float mx = -INFINITY;
+        if (!full) {
 #pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          float v = x[i] * scale;
-          if constexpr (CAP) v = a.cap * tanhf(v / a.cap) * kLog2e;
-          if (!full && key0 + i >= limit) v = -INFINITY;
-          x[i] = v;
-          mx = fmaxf(mx, v);
+          for (int i = 0; i < kH; ++i)
+            if (key0 + i >= limit) sr[i] = 0xff800000u;  // -inf
         }
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(sr[k]);
+#pragma unroll
+        for (int i = 8; i < kH; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+        const float mx_half = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * mul;
+        // Whole-row max from the partner warp (slots alternate by block parity).
+        red[(b * 2 + hf) * kBM + r] = mx_half;
+        named_bar_sync(pair_bar, 64);
+        const float mx = fmaxf(mx_half, red[(b * 2 + (hf ^ 1)) * kBM + r]);
         const float m_new = fmaxf(m_ref, mx);
         const bool resc = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_ref + 8.f);
         float alpha = 1.f;
@@ -315,13 +373,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
         }
         const float sub = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float lsum = 0.f;
+        // p = 2^(x * mul - sub): packed FMAs, three of every four exponentials on the
+        // SFU and one on the FMA pipe, sum in four packed partial sums.
+        float x[kH];
+        const float2 mul2 = make_float2(mul, mul), nsub2 = make_float2(-sub, -sub);
+        float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          x[i] = fast_exp2(x[i] - sub);
-          lsum += x[i];
+        for (int i = 0; i < kH; i += 2) {
+          float2 v = ffma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), mul2, nsub2);
+          v.x = fast_exp2(v.x);
+          v.y = ((i >> 1) & 1) ? exp2_poly3(v.y) : fast_exp2(v.y);
+          x[i] = v.x;
+          x[i + 1] = v.y;
+          sum4[(i >> 1) & 3] = fadd2(sum4[(i >> 1) & 3], v);
         }
-        l += lsum;
+        const float2 s4 = fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3]));
+        l += s4.x + s4.y;
         if (j >= 1) {
           // P V of the previous block must be done before O is rescaled and P overwritten.
           if (!(ok = __all_sync(kFull, wait(bar(O_DONE), odc & 1)))) break;
@@ -329,9 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (__any_sync(kFull, resc)) {
 #pragma unroll
-            for (int c = 0; c < kD / 32; ++c) {
+            for (int c = 0; c < kH / 32; ++c) {
               uint32_t rr[32];
-              const uint32_t addr = tmem + lane_off + kColO + c * 32;
+              const uint32_t addr = tmem + lane_off + kColO + hf * kH + c * 32;
               tmem_ld32_sync(addr, rr);
 #pragma unroll
               for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
@@ -340,14 +408,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
           }
         }
-        // P row -> shared memory, 128B-swizzled K-major (the A operand of O += P V).
+        // This half of the P row -> shared memory, 128B-swizzled K-major: keys
+        // 0-63 are the first 64-column half of the operand, keys 64-127 the second.
 #pragma unroll
-        for (int c16 = 0; c16 < kBN / 8; ++c16) {
+        for (int cc = 0; cc < kH / 8; ++cc) {
           float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = x[c16 * 8 + e];
-          const int half = c16 / 8, cc = c16 % 8;
-          *reinterpret_cast<uint4*>(pgen + half * kHalf + r * 128 + ((cc ^ (r & 7)) << 4)) = from_float8<T>(f);
+          for (int e = 0; e < 8; ++e) f[e] = x[cc * 8 + e];
+          *reinterpret_cast<uint4*>(pgen + hf * kHalf + r * 128 + ((cc ^ (r & 7)) << 4)) = from_float8<T>(f);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -360,15 +428,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++odc;
         tc_fence_after();
       }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse_v = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+      // Whole-row sum: the parity slot of the next block is free; a second barrier
+      // keeps the partner from reusing it before both have read.
+      const int pb = kvc & 1;
+      red[(pb * 2 + hf) * kBM + r] = l;
+      named_bar_sync(pair_bar, 64);
+      const float l_row = l + red[(pb * 2 + (hf ^ 1)) * kBM + r];
+      named_bar_sync(pair_bar, 64);
+      const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+      const float lse_v = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
       const int64_t orow = static_cast<int64_t>(t.q_row0 + rpos) * a.num_qo_heads + t.kvh * G + (r % G);
 #pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
+      for (int c = 0; c < kH / 32; ++c) {
+        const int col = hf * kH + c * 32;
         float ov[32];
         if (n >= 1) {
           uint32_t rr[32];
-          tmem_ld32_sync(tmem + lane_off + kColO + c * 32, rr);
+          tmem_ld32_sync(tmem + lane_off + kColO + col, rr);
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(rr[i]) * inv;
         } else {
@@ -377,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (t.slot < 0) {
           if (row_valid) {
-            T* dst = static_cast<T*>(a.o) + orow * kD + c * 32;
+            T* dst = static_cast<T*>(a.o) + orow * kD + col;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               float f[8];
@@ -387,18 +463,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(t.slot) * kBM + r) * kD + c * 32);
+          float4* dst = reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(t.slot) * kBM + r) * kD + col);
 #pragma unroll
           for (int q = 0; q < 8; ++q) dst[q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
         }
       }
-      if (t.slot < 0) {
-        if (row_valid && a.lse) a.lse[orow] = lse_v;
-      } else {
-        a.part_lse[static_cast<int64_t>(t.slot) * kBM + r] = lse_v;
+      if (hf == 0) {
+        if (t.slot < 0) {
+          if (row_valid && a.lse) a.lse[orow] = lse_v;
+        } else {
+          a.part_lse[static_cast<int64_t>(t.slot) * kBM + r] = lse_v;
+        }
       }
-      tc_fence_before();
-      mbar_arrive(bar(O_FREE));
+      if (n >= 1) {  // this tile's O is free for the next tile's P V
+        tc_fence_before();
+        mbar_arrive(bar(O_FREE));
+      }
     }
   }
 
