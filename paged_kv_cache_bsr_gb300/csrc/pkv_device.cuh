@@ -59,6 +59,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking probe of phase `parity` (try_wait may suspend the thread for a while).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for phase `parity` of a barrier to complete, giving up after
 // kWaitLimitNs.  Returns false (and records kErrWaitTimeout) on give-up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err) {
@@ -240,6 +253,20 @@ template <>
 __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
 template <>
 __device__ __forceinline__ float from_float<float>(float x) { return x; }
+
+// Two fp32 values to one 32-bit pair of 16-bit values (round to nearest even), low half first.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;

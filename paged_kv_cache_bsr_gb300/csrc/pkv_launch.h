@@ -61,8 +61,9 @@ cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* 
 
 bool decode_supported(int head_dim, int group, int dtype);
 
-// Prefill work tile: kPrefillRows packed query rows x kPrefillKeys keys.
-constexpr int kPrefillRows = 128;
+// Prefill work tile: kPrefillRows packed query rows (two 128-row UMMA tiles),
+// visited kPrefillKeys keys at a time.
+constexpr int kPrefillRows = 256;
 constexpr int kPrefillKeys = 128;
 
 bool prefill_supported(int head_dim, int group, int dtype, int page_size);

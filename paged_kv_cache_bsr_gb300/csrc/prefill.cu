@@ -9,34 +9,34 @@
 // the shared-prefix half of cascade attention (guide section 3, "Cascade
 // Attention"; fdeinterviews, composable formats with a large row block).
 //
-// GB300 design.  One CTA per SM walks the plan's list of work tiles.  A tile
-// is 128 packed query rows (128/G query positions x the G heads of one kv
-// head) against a key range, visited 128 keys (128/P pages) at a time:
-//   warps 0, 6  producers: TMA loads the Q box once per tile and, per key
-//               block, one 64-column box per (page, half) for K (warp 0,
-//               three stages) and for V (warp 6, two stages), 128B-swizzled
-//               into shared memory.  K and V run independently, so the page
-//               gather of K is never held back by the P V of older blocks.
+// GB300 design.  One CTA per SM walks the plan's list of work tiles.  A work
+// tile is 256 packed query rows (256/G query positions x the G heads of one
+// kv head) held as two 128-row UMMA tiles, A and B, against one key range
+// visited 128 keys (128/P pages) at a time; every K/V block that lands in
+// shared memory serves both tiles.
+//   warps 0, 10 producers: TMA loads the two Q boxes once per tile and, per
+//               key block, one 64-column box per (page, half) for K (warp 0,
+//               three stages) and for V (warp 10, two stages), 128B-swizzled.
 //               Pages past the request come from an out-of-range page
 //               coordinate, which TMA fills with zeros; V rows past
 //               kv_last_page_len of the last page are zeroed before the MMA
 //               may read them.
-//   warp 1      one thread issues the tcgen05 MMAs: S_j = Q K_j^T into one of
-//               two TMEM buffers (so S_{j+1} overlaps the softmax of S_j),
-//               then O += P_j V_j into a third TMEM region.
-//   warps 2-9   softmax: two warps per query row block quarter, each thread
-//               one query row (= TMEM lane) and one half (64 keys) of it.  It
-//               reads its half of S from TMEM, scales (and soft-caps), masks,
-//               exchanges the half-row max with its partner warp through
-//               shared memory, keeps a running max and sum, writes its half of
-//               P as bf16/fp16 into shared memory (the A operand of the P V
-//               MMA) and rescales its half of O in TMEM only when the max grows
-//               by more than 2^8.  The epilogue divides O by the sum and writes
-//               o and the natural-log lse (or an fp32 partial state when the
-//               plan split the key range).
+//   warp 1      one thread issues the tcgen05 MMAs, alternating the tiles:
+//               P_A V -> O_A, S_A(next) = Q_A K^T, P_B V -> O_B, S_B(next).
+//               S, P and O stay in tensor memory: S_A, S_B, O_A, O_B take the
+//               512 columns, and each P (bf16/fp16) overwrites the first 64
+//               columns of its S, the A operand of its P V MMA.
+//   warps 2-5   softmax of tile A, warps 6-9 of tile B (two warps per
+//               scheduler, so one group's softmax overlaps the other group's
+//               MMAs): thread = query row = TMEM lane.  Each reads its S row,
+//               scales (and soft-caps), masks, keeps a running max and sum,
+//               writes P back to tensor memory and rescales O only when the
+//               max grows by more than 2^8.  The epilogue divides O by the sum
+//               and writes o and the natural-log lse (or an fp32 partial state
+//               when the plan split the key range).
 // Every wait is bounded; a wait that runs out records kErrWaitTimeout and
 // makes all roles leave their loops, the MMA thread waits for its issued
-// MMAs, and TMEM is released.
+// MMAs, and tensor memory is released.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -54,29 +54,30 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kD = 128;                 // head_dim of the prefill kernel
-constexpr int kBM = kPrefillRows;       // packed query rows per tile
+constexpr int kTM = 128;                // rows of one UMMA tile
+constexpr int kWR = kPrefillRows;       // rows of a work tile: two UMMA tiles
+static_assert(kWR == 2 * kTM, "a work tile is two UMMA tiles");
 constexpr int kBN = kPrefillKeys;       // keys per block
-constexpr int kThreads = 352;           // K producer, MMA, 8 softmax warps, V producer
-constexpr int kVWarp = 10;              // the V producer
+constexpr int kThreads = 352;           // K producer, MMA, 2 x 4 softmax warps, V producer
+constexpr int kVWarp = 10;
 constexpr uint32_t kTile = 32768;       // 128 rows x 128 16-bit values
 constexpr uint32_t kHalf = 16384;       // one 64-column half of a tile
-constexpr int kKStages = 3;             // K blocks in flight (gather latency is ~2 key blocks)
+constexpr int kKStages = 2;             // K has its own producer: two blocks of lead cover the gather
 constexpr int kVStages = 2;
-// Shared-memory map (offsets from a 1024-aligned base).
-constexpr uint32_t kOffQ = 0, kOffK = kTile, kOffV = kOffK + kKStages * kTile, kOffP = kOffV + kVStages * kTile,
-                   kOffBar = kOffP + kTile, kOffRed = kOffBar + 256;
-// The tiles need 1024-byte alignment and the budget leaves no slack to align
-// by hand: the kernel checks that dynamic shared memory starts aligned.
-constexpr int kSmemBytes = kOffRed + 2 * 2 * kPrefillRows * 4;
+// Shared-memory map; dynamic shared memory must start 1024-aligned (checked).
+// The staging area gives each softmax warp 4 KB to turn its 32 rows into
+// row-contiguous global stores in the epilogue.
+constexpr uint32_t kOffQ = 0, kOffK = 2 * kTile, kOffV = kOffK + kKStages * kTile,
+                   kOffStage = kOffV + kVStages * kTile, kOffBar = kOffStage + 8 * 4096;
+constexpr int kSmemBytes = kOffBar + 256;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-// Barrier slots.
 enum { Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages,
-       V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, P_FULL = S_FULL + 2, O_DONE = P_FULL + 1,
-       O_FREE = O_DONE + 1, V_LOAD = O_FREE + 1, DRAIN = V_LOAD + kVStages, NUM_BARS = DRAIN + 1 };
+       V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, P_FULL = S_FULL + 2, O_DONE = P_FULL + 2,
+       O_FREE = O_DONE + 2, V_LOAD = O_FREE + 2, DRAIN = V_LOAD + kVStages, NUM_BARS = DRAIN + 1 };
 static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
-constexpr uint32_t kSoftmaxThreads = 256;
-constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384)
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kGroupThreads = 128;  // softmax threads of one tile
+constexpr uint32_t kTmemCols = 512;      // S_A, S_B, O_A, O_B
+constexpr uint32_t kColS = 0, kColO = 256;
 
 struct Waiter {
   int32_t* err;
@@ -99,11 +100,34 @@ struct Waiter {
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return a <= 0 ? 0 : (a + b - 1) / b; }
 
+// D[tmem] (+)= A * B with both shared-memory descriptors given as their low
+// words and a common high word (every descriptor here has the same stride
+// field, version and swizzle), so issuing an MMA costs two 32-bit adds in the
+// caller.  In the TS form the A operand is read from tensor memory (K-major,
+// 16-bit pairs per 32-bit column, even k in the low half).
+template <bool ACC>
+__device__ __forceinline__ void umma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b64 da, db;\n\tmov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, %5;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC ? 1 : 0)
+      : "memory");
+}
+template <bool ACC>
+__device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b64 db;\n\tmov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, %5;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC ? 1 : 0)
+      : "memory");
+}
+
 template <int G, typename T, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
                    const __grid_constant__ CUtensorMap tkv) {
   constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  constexpr int MP = kTM / G;  // query positions per UMMA tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   const uint32_t base = smem_addr(sm);
@@ -111,7 +135,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicOr(a.err, kErrTmemAlloc);
     return;
   }
-  const uint32_t sQ = base + kOffQ, sP = base + kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
@@ -120,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NUM_BARS; ++i)
-      mbar_init(bar(i), (i == P_FULL || i == O_FREE) ? kSoftmaxThreads : 1);
+      mbar_init(bar(i), (i == P_FULL || i == P_FULL + 1 || i == O_FREE || i == O_FREE + 1) ? kGroupThreads : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -168,9 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(Q_FULL), kTile);
-        tma_load_3d(sQ, &tq, 0, t.kvh * G, t.q_row0, bar(Q_FULL));
-        tma_load_3d(sQ + kHalf, &tq, 64, t.kvh * G, t.q_row0, bar(Q_FULL));
+        mbar_arrive_expect_tx(bar(Q_FULL), 2 * kTile);
+        for (int x = 0; x < 2; ++x)
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(base + kOffQ + x * kTile + h * kHalf, &tq, h * 64, t.kvh * G, t.q_row0 + x * MP,
+                        bar(Q_FULL));
       }
       const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
       const int n_pages_req = ceil_div_i(t.kv_len, P);
@@ -242,60 +267,94 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = umma_idesc_f16(kFmt, kBM, kBN, 0);
-      const uint32_t id_o = umma_idesc_f16(kFmt, kBM, kD, 1);
-      int kvc = 0, pc = 0, ofree = 0;
-      bool o_used = false;  // an earlier tile accumulated into O: wait for its epilogue first
+      const uint32_t id_s = umma_idesc_f16(kFmt, kTM, kBN, 0);
+      const uint32_t id_o = umma_idesc_f16(kFmt, kTM, kD, 1);
+      int kvc = 0;
+      int pc[2] = {0, 0}, ofree[2] = {0, 0};
+      bool o_used[2] = {false, false};  // an earlier tile accumulated into O_x
       bool ok = true;
-      // O += P_c V_c for the key block with global count c (the i-th of its tile).
-      auto pv = [&](int c, int i) -> bool {
-        if (i == 0 && o_used) {
-          if (!wait(bar(O_FREE), ofree & 1)) return false;
-          ++ofree;
+      // Descriptors are built once; a K step or a stage only adds to the start
+      // address field of the low word (addresses stay below 2^18, so no carry
+      // leaves it), and all of them share one high word.  Issuing an MMA then
+      // takes a few instructions, well under the 64 cycles an M=128, N=128, K=16
+      // MMA runs, even while this warp shares its scheduler with softmax warps.
+      const uint64_t dq = sw128_desc(base + kOffQ, 16, 1024);
+      const uint64_t dk = sw128_desc(base + kOffK, 16, 1024);
+      const uint64_t dv = sw128_desc(base + kOffV, kHalf, 1024);
+      const uint32_t hi = static_cast<uint32_t>(dq >> 32);
+      const uint32_t q_lo = static_cast<uint32_t>(dq), k_lo = static_cast<uint32_t>(dk),
+                     v_lo = static_cast<uint32_t>(dv);
+      constexpr uint32_t kTile16 = kTile >> 4, kHalf16 = kHalf >> 4;
+      // S_x = Q_x K_c^T into tensor memory.
+      auto mma_s = [&](int x, int c) {
+        const uint32_t a0 = q_lo + x * kTile16;
+        const uint32_t b0 = k_lo + (c % kKStages) * kTile16;
+        const uint32_t d = tmem + kColS + x * kTM;
+        umma_ss_lo<false>(d, a0, b0, hi, id_s);
+#pragma unroll
+        for (int kk = 1; kk < kD / 16; ++kk) {
+          const uint32_t koff = (kk / 4) * kHalf16 + (kk % 4) * 2;
+          umma_ss_lo<true>(d, a0 + koff, b0 + koff, hi, id_s);
         }
-        if (!wait(bar(P_FULL), pc & 1)) return false;
-        ++pc;
-        const int s = c % kVStages;
-        if (!wait(bar(V_FULL + s), (c / kVStages) & 1)) return false;
-        tc_fence_after();
-        const uint32_t sV = base + kOffV + s * kTile;
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_f16(tmem + kColO, sw128_desc(sP + (kk / 4) * kHalf + (kk % 4) * 32, 16, 1024),
-                   sw128_desc(sV + kk * 2048, kHalf, 1024), id_o, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(V_EMPTY + s));
-        umma_commit(bar(O_DONE));
-        o_used = true;
-        return true;
+        umma_commit(bar(S_FULL + x));
+      };
+      // O_x += P_x V_c, P_x from tensor memory; the tile's last one signals the epilogue.
+      auto mma_pv = [&](int x, int c, bool acc, bool last) {
+        const uint32_t b0 = v_lo + (c % kVStages) * kTile16;
+        const uint32_t d = tmem + kColO + x * kTM, p = tmem + kColS + x * kTM;
+        if (acc)
+          umma_ts_lo<true>(d, p, b0, hi, id_o);
+        else
+          umma_ts_lo<false>(d, p, b0, hi, id_o);
+#pragma unroll
+        for (int kk = 1; kk < kBN / 16; ++kk) umma_ts_lo<true>(d, p + kk * 8, b0 + kk * (2048 >> 4), hi, id_o);
+        if (last) umma_commit(bar(O_DONE + x));
       };
       for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
         const PrefillTile t = a.tiles[ti];
         const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
         if (!(ok = wait(bar(Q_FULL), tn & 1))) break;
         tc_fence_after();
-        for (int j = 0; j < n; ++j) {
-          const int s = kvc % kKStages;
-          if (!(ok = wait(bar(K_FULL + s), (kvc / kKStages) & 1))) break;
-          tc_fence_after();
-          const uint32_t sK = base + kOffK + s * kTile;
-          const uint32_t d_s = tmem + (kvc & 1) * kBN;
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t koff = (kk / 4) * kHalf + (kk % 4) * 32;
-            umma_f16(d_s, sw128_desc(sQ + koff, 16, 1024), sw128_desc(sK + koff, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(S_FULL + (kvc & 1)));
-          umma_commit(bar(K_EMPTY + s));
-          if (j == n - 1) umma_commit(bar(Q_EMPTY));  // Q is free once the tile's last S is done
-          if (j >= 1 && !(ok = pv(kvc - 1, j - 1))) break;
-          ++kvc;
-        }
-        if (!ok) break;
-        if (n >= 1) {
-          if (!(ok = pv(kvc - 1, n - 1))) break;
-        } else {
+        if (n == 0) {
           umma_commit(bar(Q_EMPTY));
+          continue;
         }
+        if (!(ok = wait(bar(K_FULL + kvc % kKStages), (kvc / kKStages) & 1))) break;
+        tc_fence_after();
+        mma_s(0, kvc);
+        mma_s(1, kvc);
+        umma_commit(bar(K_EMPTY + kvc % kKStages));
+        if (n == 1) umma_commit(bar(Q_EMPTY));
+        for (int j = 0; j < n && ok; ++j) {
+          const int c = kvc + j;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (!(ok = wait(bar(P_FULL + x), pc[x] & 1))) break;
+            ++pc[x];
+            if (j == 0 && o_used[x]) {  // the previous tile's epilogue has read O_x
+              if (!(ok = wait(bar(O_FREE + x), ofree[x] & 1))) break;
+              ++ofree[x];
+            }
+            if (x == 0 && !(ok = wait(bar(V_FULL + c % kVStages), (c / kVStages) & 1))) break;
+            tc_fence_after();
+            mma_pv(x, c, j > 0, j == n - 1);
+            o_used[x] = true;
+            if (x == 1) umma_commit(bar(V_EMPTY + c % kVStages));  // both P V of block c issued
+            if (j + 1 < n) {
+              if (x == 0) {
+                if (!(ok = wait(bar(K_FULL + (c + 1) % kKStages), ((c + 1) / kKStages) & 1))) break;
+                tc_fence_after();
+              }
+              mma_s(x, c + 1);
+              if (x == 1) {
+                umma_commit(bar(K_EMPTY + (c + 1) % kKStages));  // both S of block c + 1 issued
+                if (j + 1 == n - 1) umma_commit(bar(Q_EMPTY));
+              }
+            }
+          }
+        }
+        kvc += n;
       }
-      // Every MMA issued so far must finish before TMEM is released.
+      // Every MMA issued so far must finish before tensor memory is released.
       umma_commit(bar(DRAIN));
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(bar(DRAIN), 0))
@@ -307,63 +366,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    const int x = (warp - 2) >> 2;           // UMMA tile of this warp group
     const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int hf = (warp - 2) >> 2;          // which 64 keys / O columns of the row
-    const int r = quarter * 32 + lane;
+    const int r = quarter * 32 + lane;       // row within the UMMA tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t pair_bar = 1 + quarter;   // the two warps of this lane quarter
-    float* red = reinterpret_cast<float*>(sm + kOffRed);  // [parity][half][row] half-row maxima / sums
+    const uint32_t col_s = tmem + lane_off + kColS + x * kTM;
+    const uint32_t col_o = tmem + lane_off + kColO + x * kTM;
     const float scale = CAP ? a.sm_scale : a.sm_scale * kLog2e;
-    uint8_t* pgen = sm + kOffP;
-    constexpr int kH = kBN / 2;
-    int kvc = 0, odc = 0;
+    int sc = 0, odc = 0;
     bool ok = true;
     for (int ti = t_begin; ti < t_end && ok; ++ti) {
       const PrefillTile t = a.tiles[ti];
       const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
-      const int rpos = r / G;
+      const int rpos = x * MP + r / G;     // position of this row within the work tile
       const bool row_valid = rpos < t.n_pos;
       const int pos = t.q_pos0 + rpos;
-      int limit = t.kv_len, lim0 = t.kv_len;  // keys < limit are visible to this row / to every row
+      int limit = t.kv_len, lim0 = t.kv_len;  // keys < limit are visible to this row / to every row of x
       if (a.causal) {
         limit = min(limit, pos + 1 + t.kv_len - t.qo_len);
-        lim0 = min(lim0, t.q_pos0 + 1 + t.kv_len - t.qo_len);
+        lim0 = min(lim0, t.q_pos0 + x * MP + 1 + t.kv_len - t.qo_len);
       }
       limit = min(limit, t.kv_end);
       lim0 = min(lim0, t.kv_end);
-      float m_ref = -INFINITY, l = 0.f;  // l: this half-row's share of the sum
+      float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
-        const int b = kvc & 1;
-        if (!(ok = __all_sync(kFull, wait(bar(S_FULL + b), (kvc >> 1) & 1)))) break;
+        if (!(ok = __all_sync(kFull, wait(bar(S_FULL + x), sc & 1)))) break;
+        ++sc;
         tc_fence_after();
-        uint32_t sr[kH];
-        tmem_ld64_sync(tmem + lane_off + b * kBN + hf * kH, sr);
-        const int key0 = t.kv_begin + j * kBN + hf * kH;
-        const bool full = key0 + kH <= lim0;
-        // Logits in log2 units are x * mul; the max is taken on x (mul > 0).
+        const int key0 = t.kv_begin + j * kBN;
+        const bool full = key0 + kBN <= lim0;
+        uint32_t sr[kBN];
+        tmem_ld128_sync(col_s, sr);
+        // Logits in log2 units are v * mul (the cap, when on, is applied to v first).
         float mul = scale;
         if constexpr (CAP) {
 #pragma unroll
-          for (int i = 0; i < kH; ++i)
+          for (int i = 0; i < kBN; ++i)
             sr[i] = __float_as_uint(a.cap * tanhf(__uint_as_float(sr[i]) * scale / a.cap) * kLog2e);
           mul = 1.f;
         }
         if (!full) {
 #pragma unroll
-          for (int i = 0; i < kH; ++i)
+          for (int i = 0; i < kBN; ++i)
             if (key0 + i >= limit) sr[i] = 0xff800000u;  // -inf
         }
         float mx8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(sr[k]);
 #pragma unroll
-        for (int i = 8; i < kH; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
-        const float mx_half = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * mul;
-        // Whole-row max from the partner warp (slots alternate by block parity).
-        red[(b * 2 + hf) * kBM + r] = mx_half;
-        named_bar_sync(pair_bar, 64);
-        const float mx = fmaxf(mx_half, red[(b * 2 + (hf ^ 1)) * kBM + r]);
+        for (int i = 8; i < kBN; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * mul;
         const float m_new = fmaxf(m_ref, mx);
         const bool resc = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_ref + 8.f);
         float alpha = 1.f;
@@ -373,111 +426,120 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
         }
         const float sub = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // p = 2^(x * mul - sub): packed FMAs, three of every four exponentials on the
-        // SFU and one on the FMA pipe, sum in four packed partial sums.
-        float x[kH];
+        // p = 2^(v * mul - sub): packed FMAs and the SFU exponential (the SFU has
+        // room at this rate: two tiles' rows share it with the tensor pipe's time);
+        // packed in place to 16-bit pairs.
         const float2 mul2 = make_float2(mul, mul), nsub2 = make_float2(-sub, -sub);
         float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int i = 0; i < kH; i += 2) {
+        for (int i = 0; i < kBN; i += 2) {
           float2 v = ffma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), mul2, nsub2);
           v.x = fast_exp2(v.x);
-          v.y = ((i >> 1) & 1) ? exp2_poly3(v.y) : fast_exp2(v.y);
-          x[i] = v.x;
-          x[i + 1] = v.y;
+          v.y = fast_exp2(v.y);
           sum4[(i >> 1) & 3] = fadd2(sum4[(i >> 1) & 3], v);
+          sr[i >> 1] = pack2<T>(v.x, v.y);
         }
         const float2 s4 = fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3]));
         l += s4.x + s4.y;
+        // P over the first 64 columns of this tile's S (already read).
+        tmem_st32(col_s, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_st32(col_s + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         if (j >= 1) {
-          // P V of the previous block must be done before O is rescaled and P overwritten.
-          if (!(ok = __all_sync(kFull, wait(bar(O_DONE), odc & 1)))) break;
-          ++odc;
-          tc_fence_after();
+          // P V of the previous block was issued before this S, so the S_FULL
+          // wait above already covers it: O is complete and can be rescaled
+          // before the next P V adds to it.
           if (__any_sync(kFull, resc)) {
 #pragma unroll
-            for (int c = 0; c < kH / 32; ++c) {
+            for (int c = 0; c < kD / 32; ++c) {
               uint32_t rr[32];
-              const uint32_t addr = tmem + lane_off + kColO + hf * kH + c * 32;
-              tmem_ld32_sync(addr, rr);
+              tmem_ld32_sync(col_o + c * 32, rr);
 #pragma unroll
               for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-              tmem_st32(addr, rr);
+              tmem_st32(col_o + c * 32, rr);
             }
-            tmem_wait_st();
           }
         }
-        // This half of the P row -> shared memory, 128B-swizzled K-major: keys
-        // 0-63 are the first 64-column half of the operand, keys 64-127 the second.
-#pragma unroll
-        for (int cc = 0; cc < kH / 8; ++cc) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = x[cc * 8 + e];
-          *reinterpret_cast<uint4*>(pgen + hf * kHalf + r * 128 + ((cc ^ (r & 7)) << 4)) = from_float8<T>(f);
-        }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(P_FULL));
-        ++kvc;
+        mbar_arrive(bar(P_FULL + x));
       }
       if (!ok) break;
       if (n >= 1) {
-        if (!(ok = __all_sync(kFull, wait(bar(O_DONE), odc & 1)))) break;
+        if (!(ok = __all_sync(kFull, wait(bar(O_DONE + x), odc & 1)))) break;
         ++odc;
         tc_fence_after();
       }
-      // Whole-row sum: the parity slot of the next block is free; a second barrier
-      // keeps the partner from reusing it before both have read.
-      const int pb = kvc & 1;
-      red[(pb * 2 + hf) * kBM + r] = l;
-      named_bar_sync(pair_bar, 64);
-      const float l_row = l + red[(pb * 2 + (hf ^ 1)) * kBM + r];
-      named_bar_sync(pair_bar, 64);
-      const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-      const float lse_v = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse_v = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
       const int64_t orow = static_cast<int64_t>(t.q_row0 + rpos) * a.num_qo_heads + t.kvh * G + (r % G);
+      const int srow = x * kTM + r;  // row of the work tile, for a partial-state slot
+      if (t.slot < 0) {
+        // Final output: through this warp's staging slab, half a row (64 values) per pass,
+        // so each store instruction writes four whole 128-byte row segments.
+        uint8_t* stg = sm + kOffStage + (warp - 2) * 4096;
 #pragma unroll
-      for (int c = 0; c < kH / 32; ++c) {
-        const int col = hf * kH + c * 32;
-        float ov[32];
-        if (n >= 1) {
-          uint32_t rr[32];
-          tmem_ld32_sync(tmem + lane_off + kColO + col, rr);
+        for (int hp = 0; hp < 2; ++hp) {
+          uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(rr[i]) * inv;
-        } else {
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t rr[32];
+            if (n >= 1) {
+              tmem_ld32_sync(col_o + (hp * 2 + cc) * 32, rr);
+            } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = 0.f;
-        }
-        if (t.slot < 0) {
-          if (row_valid) {
-            T* dst = static_cast<T*>(a.o) + orow * kD + col;
+              for (int i = 0; i < 32; ++i) rr[i] = 0u;
+            }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float f[8];
+            for (int i = 0; i < 16; ++i)
+              pk[cc * 16 + i] = pack2<T>(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
+          }
 #pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] = ov[q * 8 + e];
-              reinterpret_cast<uint4*>(dst)[q] = from_float8<T>(f);
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int rr_ = it * 4 + (lane >> 3), piece = lane & 7;  // a row of this warp, a 16-byte piece
+            const int r2 = quarter * 32 + rr_;
+            const int rpos2 = x * MP + r2 / G;
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr_ * 128 + ((piece ^ (rr_ & 7)) << 4));
+            if (rpos2 < t.n_pos) {
+              const int64_t orow2 =
+                  static_cast<int64_t>(t.q_row0 + rpos2) * a.num_qo_heads + t.kvh * G + (r2 % G);
+              reinterpret_cast<uint4*>(static_cast<T*>(a.o) + orow2 * kD + hp * 64)[piece] = v;
             }
           }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(t.slot) * kBM + r) * kD + col);
+          __syncwarp();
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+          float ov[32];
+          if (n >= 1) {
+            uint32_t rr[32];
+            tmem_ld32_sync(col_o + c * 32, rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(rr[i]) * inv;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+          }
+          float4* dst =
+              reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(t.slot) * kWR + srow) * kD + c * 32);
 #pragma unroll
           for (int q = 0; q < 8; ++q) dst[q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
         }
       }
-      if (hf == 0) {
-        if (t.slot < 0) {
-          if (row_valid && a.lse) a.lse[orow] = lse_v;
-        } else {
-          a.part_lse[static_cast<int64_t>(t.slot) * kBM + r] = lse_v;
-        }
+      if (t.slot < 0) {
+        if (row_valid && a.lse) a.lse[orow] = lse_v;
+      } else {
+        a.part_lse[static_cast<int64_t>(t.slot) * kWR + srow] = lse_v;
       }
       if (n >= 1) {  // this tile's O is free for the next tile's P V
         tc_fence_before();
-        mbar_arrive(bar(O_FREE));
+        mbar_arrive(bar(O_FREE + x));
       }
     }
   }
@@ -496,20 +558,20 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constan
   const int warp_id = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int n_warps = gridDim.x * 8;
   const int G = a.num_qo_heads / a.num_kv_heads;
-  const int pairs = a.hdr->num_merge * kBM;
+  const int pairs = a.hdr->num_merge * kWR;
   for (int pair = warp_id; pair < pairs; pair += n_warps) {
-    const PrefillMerge it = a.merge[pair / kBM];
-    const int r = pair % kBM;
+    const PrefillMerge it = a.merge[pair / kWR];
+    const int r = pair % kWR;
     if (r / G >= it.n_pos) continue;
     float mx = -INFINITY;
     for (int i = lane; i < it.n_slots; i += 32)
-      mx = fmaxf(mx, a.part_lse[static_cast<int64_t>(it.slot_begin + i) * kBM + r]);
+      mx = fmaxf(mx, a.part_lse[static_cast<int64_t>(it.slot_begin + i) * kWR + r]);
     mx = warp_max(mx);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float wsum = 0.f;
     if (mx != -INFINITY) {
       for (int i = 0; i < it.n_slots; ++i) {
-        const int64_t row = static_cast<int64_t>(it.slot_begin + i) * kBM + r;
+        const int64_t row = static_cast<int64_t>(it.slot_begin + i) * kWR + r;
         const float w = fast_exp2((a.part_lse[row] - mx) * kLog2e);
         if (w > 0.f) {
           const float4 v = reinterpret_cast<const float4*>(a.part_o + row * kD)[lane];
@@ -584,7 +646,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dt
     // q [total_q, Hq, D]: box = 64 columns x the G heads of a group x 128/G positions.
     cuuint64_t dims[3] = {kD, hq, static_cast<cuuint64_t>(total_q > 0 ? total_q : 1)};
     cuuint64_t strides[2] = {kD * 2, hq * kD * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(kBM / group)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(kTM / group)};
     cuuint32_t es[3] = {1, 1, 1};
     if (encode(&tq, dt, 3, const_cast<void*>(a.q), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
