@@ -149,6 +149,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(win)}
 
 
+def combine_over_ranks(ms_per_step: float, nbytes: float):
+    """Whole-job figures under torch.distributed: the slowest rank's step time and the
+    bytes all ranks processed (each rank streams its own batch; no data moves between
+    ranks).  Returns (max ms per step, total bytes)."""
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    nb = torch.tensor([nbytes], dtype=torch.float64, device=dev)
+    dist.all_reduce(nb, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(nb.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Seed of the decode batch a rank streams (weak scaling: one batch per rank)."""
+    return 1001 + rank
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -433,7 +452,7 @@ def run_own(args):
     build.build()
     api.load()
     peaks = measured_peaks()
-    b = W.llama3_decode(seed=1001 + rank)
+    b = W.llama3_decode(seed=rank_seed(rank))
     clocks = ClockSampler(local)
     clocks.start()
     if world > 1:
@@ -444,12 +463,7 @@ def run_own(args):
     t_wall1 = time.time()
     ms = res["ms_per_step"]
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        nb = torch.tensor([res["bytes"]], dtype=torch.float64, device="cuda")
-        dist.all_reduce(nb, op=dist.ReduceOp.SUM)
-        total_bytes = float(nb.item())
+        ms, total_bytes = combine_over_ranks(ms, res["bytes"])
         dist.barrier()
     else:
         total_bytes = res["bytes"]
