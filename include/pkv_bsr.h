@@ -211,8 +211,10 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
  * tcgen05 tensor-core MMAs (bf16 and fp16) and fp32 TMEM accumulators.
  * q and o: [total_q, Hq, d]; lse: [total_q, Hq] fp32 (may be NULL).
  * With causal = 0 and one request whose rows are many requests' queries, this
- * is the shared-prefix half of cascade attention.  Graph-capturable as long as
- * kv_data and num_pages stay the same.
+ * is the shared-prefix half of cascade attention.  The kernel's TMA tensor maps
+ * are built at launch from q, kv_data, the total query rows and num_pages of
+ * the current plan, so a captured CUDA graph can be replayed after re-planning
+ * a batch with the same q and kv_data buffers, total query rows and pool size.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  */
 pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,

@@ -214,3 +214,75 @@ def test_run_calls_refuse_host_only_plans(lib):
     with pytest.raises(api.PkvError):
         api.batch_decode_paged(h, dummy, dummy, dummy, dummy, dummy, dummy, None, dummy, stream=0)
     api.plan_destroy(h)
+
+
+# --------------------------------------------------------------------------- prefill plan
+def check_prefill_plan(h, b, num_sms=152, rows_per_tile=256):
+    """Every (request, kv head, query position) gets exactly one tile family whose key
+    chunks cover [0, causal limit of the family's last row) once, in 128-key blocks."""
+    info = api.plan_get_info(h)
+    work = api.plan_get_work(h).tolist()
+    g = b.num_qo_heads // b.num_kv_heads
+    mp_ = rows_per_tile // g
+    fam = {}
+    for w, bb, kvh, pos0, npos, kb, ke, slot in work:
+        fam.setdefault((bb, kvh, pos0), []).append((kb, ke, slot, npos, w))
+    for bb in range(b.batch):
+        qo, kv = b.qo_lens[bb], b.kv_lens[bb]
+        for kvh in range(b.num_kv_heads):
+            for pos0 in range(0, qo, mp_):
+                npos = min(mp_, qo - pos0)
+                chunks = sorted(fam.pop((bb, kvh, pos0)))
+                assert all(c[3] == npos for c in chunks)
+                end = kv if not b.causal else max(0, min(kv, pos0 + npos + kv - qo))
+                pos = 0
+                for kb, ke, slot, _, _ in chunks:
+                    assert kb == pos and kb % 128 == 0 and ke > kb or (kb == ke == 0 == end)
+                    pos = ke
+                assert pos == end
+                if len(chunks) == 1:
+                    assert chunks[0][2] == -1
+                else:
+                    slots = [c[2] for c in chunks]
+                    assert min(slots) >= 0 and slots == list(range(slots[0], slots[0] + len(slots)))
+    assert not fam, f"tiles for rows that do not exist: {list(fam)[:3]}"
+    # workers appear in non-decreasing order; LPT keeps the loads within one tile of each other
+    ws_ = [r[0] for r in work]
+    assert ws_ == sorted(ws_)
+    return info, work
+
+
+def test_prefill_plan_ragged_causal(lib):
+    b = W.ragged_prefill(seed=1003)
+    h, ws = host_plan(b, api.PLAN_PREFILL)
+    compute(h, ws, b)
+    info, work = check_prefill_plan(h, b)
+    costs = {}
+    for w, bb, kvh, pos0, npos, kb, ke, slot in work:
+        costs[w] = costs.get(w, 0) + -(-(ke - kb) // 128) + 1
+    biggest = max(-(-(ke - kb) // 128) + 1 for _, _, _, _, _, kb, ke, _ in work)
+    assert max(costs.values()) - min(costs.values()) <= biggest
+    assert info.num_merge == 0  # thousands of tiles: no key range needs splitting
+    api.plan_destroy(h)
+
+
+def test_prefill_plan_splits_long_keys_of_few_tiles(lib):
+    # the cascade prefix: one row block of 64 queries x 32 heads against 2048 shared keys
+    cb = W.cascade_decode(seed=1004, num_qo_heads=32, num_kv_heads=8)
+    b = cb.prefix
+    h, ws = host_plan(b, api.PLAN_PREFILL)
+    compute(h, ws, b)
+    info, work = check_prefill_plan(h, b)
+    assert info.num_merge == 8 and info.num_slots == len(work) and len(work) > 8 * 4
+    api.plan_destroy(h)
+
+
+@pytest.mark.parametrize("qo,kv,causal", [([5, 0, 300], [5, 9, 300], True), ([10, 3], [4, 3], True),
+                                          ([257, 1], [1000, 1], False)])
+def test_prefill_plan_edge_cases(lib, qo, kv, causal):
+    b = W.make_paged_batch(qo_lens=qo, kv_lens=kv, num_qo_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+                           dtype=torch.bfloat16, seed=1, causal=causal)
+    h, ws = host_plan(b, api.PLAN_PREFILL, num_sms=8)
+    compute(h, ws, b)
+    check_prefill_plan(h, b)
+    api.plan_destroy(h)

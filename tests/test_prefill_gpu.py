@@ -128,3 +128,63 @@ def test_prefill_page_permutation_is_bit_exact():
     o2, l2 = runner.prefill(runner.DeviceBatch.from_host(b2), plan)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_prefill_cuda_graph_replay_after_replanning():
+    """Capture the prefill run calls once; re-plan another batch (same total query rows,
+    same pool) into the same workspace and buffers; replay gives that batch's result."""
+    hq, hkv, d, P = 8, 2, 128, 16
+    pool = 160
+    gen = torch.Generator().manual_seed(21)
+    kv = torch.randn(pool, 2, hkv, P, d, generator=gen).to(torch.bfloat16)
+
+    def batch_with(qo_lens, kv_lens, seed):
+        g = torch.Generator().manual_seed(seed)
+        perm = torch.randperm(pool, generator=g)
+        ip, ix, last, _ = W.build_page_table(kv_lens, P, perm)
+        q = torch.randn(sum(qo_lens), hq, d, generator=g).to(torch.bfloat16)
+        qo = torch.zeros(len(qo_lens) + 1, dtype=torch.int32)
+        qo[1:] = torch.cumsum(torch.tensor(qo_lens), 0)
+        return W.PagedBatch(page_size=P, num_qo_heads=hq, num_kv_heads=hkv, head_dim=d, dtype=torch.bfloat16,
+                            q=q, kv_data=kv, qo_indptr=qo, kv_indptr=ip, kv_indices=ix, kv_last_page_len=last,
+                            qo_lens=list(qo_lens), kv_lens=list(kv_lens), sm_scale=d ** -0.5, causal=True)
+
+    a = batch_with([100, 300, 28], [150, 700, 28], 1)
+    bb = batch_with([228, 200, 0], [500, 210, 7], 2)
+    max_b, max_q = 3, 428
+    plan = runner.make_plan(a, api.PLAN_PREFILL, max_batch=max_b, max_total_q=max_q, max_kv_pages=pool)
+    dev = "cuda"
+    kv_d = kv.to(dev)
+    q_buf = torch.empty(max_q, hq, d, dtype=torch.bfloat16, device=dev)
+    o_buf = torch.empty_like(q_buf)
+    lse_buf = torch.empty(max_q, hq, dtype=torch.float32, device=dev)
+    qo_buf = torch.zeros(max_b + 1, dtype=torch.int32, device=dev)
+    ip_buf = torch.zeros(max_b + 1, dtype=torch.int32, device=dev)
+    ix_buf = torch.zeros(pool, dtype=torch.int32, device=dev)
+    last_buf = torch.zeros(max_b, dtype=torch.int32, device=dev)
+
+    def load(b):
+        q_buf.copy_(b.q)
+        qo_buf.copy_(b.qo_indptr)
+        ip_buf.copy_(b.kv_indptr)
+        ix_buf[: b.kv_indices.numel()].copy_(b.kv_indices)
+        last_buf.copy_(b.kv_last_page_len)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        load(a)
+        runner.plan_batch(plan, a, stream=s)
+        plan.run(q_buf, kv_d, ix_buf, ip_buf, last_buf, o_buf, lse_buf, qo_indptr=qo_buf, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.run(q_buf, kv_d, ix_buf, ip_buf, last_buf, o_buf, lse_buf, qo_indptr=qo_buf, stream=s)
+    for b in (bb, a, bb):
+        with torch.cuda.stream(s):
+            load(b)
+            runner.plan_batch(plan, b, stream=s)
+            g.replay()
+        s.synchronize()
+        ref_o, ref_lse = oracle.attention_of(b)
+        assert_matches_oracle(o_buf, lse_buf, ref_o, ref_lse, torch.bfloat16, "prefill graph replay")
+    assert plan.device_error() == 0
