@@ -48,7 +48,7 @@ def parse_args():
     p.add_argument("--no-secondary", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
-    p.add_argument("--only", choices=["prefill", "cascade", "skewed"], default=None,
+    p.add_argument("--only", choices=["prefill", "cascade", "multilevel", "skewed"], default=None,
                    help="time one secondary measurement alone (for profiling) and print it")
     return p.parse_args()
 
@@ -363,6 +363,24 @@ def prefill_measure(peaks, steps=20, warmup=3):
                          "peak_source": peaks["source"], "kernel": "prefill_kernel"}}
 
 
+def graph_us(fn, s, steps, warmup):
+    """Capture fn's launches on stream s in a CUDA graph; mean replay time in us."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(steps):
+            g.replay()
+        b.record(s)
+    b.synchronize()
+    return round(a.elapsed_time(b) / steps * 1e3, 2)
+
+
 def cascade_measure(steps=50, warmup=5):
     """Cascade (prefix prefill over one large row block + suffix decode + merge_state)
     vs non-cascade decode over prefix + suffix pages.  Plans are made once (the batch
@@ -405,21 +423,58 @@ def cascade_measure(steps=50, warmup=5):
     s.synchronize()
     out = {"workload": "cascade_softcap_decode"}
     for name, fn in (("cascade", casc), ("non_cascade", full)):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            fn()
-        with torch.cuda.stream(s):
-            for _ in range(warmup):
-                g.replay()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(s)
-            for _ in range(steps):
-                g.replay()
-            b.record(s)
-        b.synchronize()
-        out[name + "_us"] = round(a.elapsed_time(b) / steps * 1e3, 2)
+        out[name + "_us"] = graph_us(fn, s, steps, warmup)
     out["speedup"] = round(out["non_cascade_us"] / out["cascade_us"], 3)
     out["non_cascade_kv_GBps"] = round(cb.full.kv_bytes() / (out["non_cascade_us"] * 1e-6) / 1e9, 1)
+    out["timing"] = "CUDA-graph replay of the run calls; plans made once outside the timed loop"
+    return out
+
+
+def multilevel_measure(steps=50, warmup=5):
+    """Parallel generation over a three-level prefix tree (system prompt shared by 64
+    requests, 8 prompts shared by 8 samples each, own generated tokens): the levels
+    run in order on one stream, or concurrently on side streams, then merge_state;
+    against non-cascade decode over every request's whole page list.  Each variant's
+    run calls are replayed from a CUDA graph; plans are made once."""
+    import torch
+    from paged_kv_cache_bsr_gb300 import runner, api, workloads as W
+    mb = W.parallel_generation(seed=1005)
+    kv = mb.full.kv_data.cuda()
+    levels = [runner.DeviceBatch.from_host(lv, kv_data=kv) for lv in mb.levels]
+    df = runner.DeviceBatch.from_host(mb.full, kv_data=kv)
+    s = torch.cuda.Stream()
+    side = [torch.cuda.Stream() for _ in levels[1:]]
+    try:
+        plans = [runner.make_plan(lv, runner.level_kind(lv)) for lv in mb.levels]
+    except api.PkvError as e:
+        return {"unavailable": str(e)}
+    fplan = runner.make_plan(mb.full, api.PLAN_DECODE)
+    with torch.cuda.stream(s):
+        for p, lv in zip(plans, mb.levels):
+            runner.plan_batch(p, lv, stream=s)
+        runner.plan_batch(fplan, mb.full, stream=s)
+        o_f = torch.empty_like(df.q)
+        l_f = torch.empty(df.q.shape[:2], dtype=torch.float32, device=df.q.device)
+
+    def serial():
+        runner.multi_level_cascade(levels, plans, stream=s)
+
+    def concurrent():
+        runner.multi_level_cascade(levels, plans, stream=s, side_streams=side)
+
+    def full():
+        fplan.run(df.q, kv, df.kv_indices, df.kv_indptr, df.kv_last_page_len, o_f, l_f, stream=s)
+
+    out = {"workload": "parallel_generation_3_level"}
+    for name, fn in (("levels_serial", serial), ("levels_concurrent", concurrent), ("non_cascade", full)):
+        with torch.cuda.stream(s):
+            fn()
+        s.synchronize()
+        out[name + "_us"] = graph_us(fn, s, steps, warmup)
+    best = min(out["levels_serial_us"], out["levels_concurrent_us"])
+    out["speedup"] = round(out["non_cascade_us"] / best, 3)
+    out["unique_kv_MB"] = round(sum(lv.kv_bytes() for lv in mb.levels) / 1e6, 1)
+    out["non_cascade_kv_MB"] = round(mb.full.kv_bytes() / 1e6, 1)
     out["timing"] = "CUDA-graph replay of the run calls; plans made once outside the timed loop"
     return out
 
@@ -435,6 +490,8 @@ def run_only(args):
         res = prefill_measure(peaks, steps=args.steps, warmup=args.warmup)
     elif args.only == "cascade":
         res = cascade_measure(steps=args.steps, warmup=args.warmup)
+    elif args.only == "multilevel":
+        res = multilevel_measure(steps=args.steps, warmup=args.warmup)
     else:
         r = decode_measure(W.skewed_decode(seed=1002), args.steps, args.warmup, peaks)
         res = {"value": round(r["value"], 1), "unit": "GB/s", "roofline": r["roofline"]}
@@ -495,6 +552,7 @@ def run_own(args):
             del ident
             secondary["prefill"] = prefill_measure(peaks)
             secondary["cascade"] = cascade_measure()
+            secondary["multilevel_cascade"] = multilevel_measure()
     clocks.stop()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,

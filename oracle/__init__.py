@@ -223,13 +223,18 @@ def merge_states(os_, lses) -> Tuple[np.ndarray, np.ndarray]:
     return out.reshape(*lead, d), lout.reshape(lead)
 
 
-def cascade(prefix_batch, suffix_batch, threads: int = 0):
-    """Cascade (shared-prefix) attention: prefix row block + per-request suffix, merged.
+def cascade(*level_batches, threads: int = 0):
+    """Cascade (shared-prefix) attention over a prefix tree, level by level, merged.
 
-    ``prefix_batch`` holds every request's query as one row block against the
-    shared prefix pages; ``suffix_batch`` holds each request against its own pages.
-    Both view the same pool.  Returns (o, lse) per request row.
+    Two levels are the common case: a prefix batch holding every request's query as
+    one row block against the shared prefix pages, and a suffix batch holding each
+    request against its own pages.  More levels (a system prompt, per-group prompts,
+    per-request tokens) follow the same rule: each level's batch groups the request
+    rows into consecutive blocks, each block against its own pages.  All views index
+    the same pool.  Returns (o, lse) per request row: the merge of the levels'
+    states (FlashInfer pages: "Composable Formats for Shared Prefixes").
     """
-    o_p, l_p = attention_of(prefix_batch, threads=threads)
-    o_s, l_s = attention_of(suffix_batch, threads=threads)
-    return merge_states([o_p, o_s], [l_p, l_s])
+    if len(level_batches) < 1:
+        raise ValueError("cascade needs at least one level")
+    states = [attention_of(b, threads=threads) for b in level_batches]
+    return merge_states([s[0] for s in states], [s[1] for s in states])

@@ -1,13 +1,13 @@
 """Run paged-KV attention on a workload through the C ABI (device marshalling only).
 
-``DeviceBatch`` moves one paged batch to the GPU; ``decode``, ``prefill`` and
-``cascade`` plan and launch through ``api.Plan`` and return (o, lse) device
-tensors.  The arithmetic is all in libpkvbsr.so.
+``DeviceBatch`` moves one paged batch to the GPU; ``decode``, ``prefill``,
+``cascade`` and ``multi_level_cascade`` plan and launch through ``api.Plan`` and
+return (o, lse) device tensors.  The arithmetic is all in libpkvbsr.so.
 """
 from __future__ import annotations
 
 import dataclasses
-from typing import Optional, Tuple
+from typing import Optional, Sequence, Tuple
 
 import torch
 
@@ -83,3 +83,69 @@ def cascade(prefix: DeviceBatch, suffix: DeviceBatch, prefix_plan: Optional[api.
     o_s, l_s = decode(suffix, suffix_plan, stream)
     api.merge_state(o_p, l_p, o_s, l_s, o_p, l_p, stream=stream)
     return o_p, l_p
+
+
+def level_kind(b) -> int:
+    """A level whose nodes each hold one query row is plain decode; a level with
+    multi-row blocks (a prefix shared by several requests) runs on the prefill
+    kernel without a mask, so each node's KV is read once for all its rows."""
+    return api.PLAN_DECODE if all(n == 1 for n in b.qo_lens) else api.PLAN_PREFILL
+
+
+def multi_level_cascade(levels: Sequence[DeviceBatch], plans: Optional[Sequence[api.Plan]] = None,
+                        stream=None, side_streams: Optional[Sequence] = None
+                        ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Attention over a prefix tree stored as one BSR matrix per level.
+
+    Each level's batch groups the request rows into consecutive blocks (its nodes),
+    each block against that node's pages; every level covers every row once.  Each
+    level is computed on the GPU (prefill kernel for multi-row blocks, decode kernel
+    for single rows) and the states are folded into level 0's buffers with
+    merge_state.  With ``side_streams`` (one per level after the first) the levels
+    run concurrently and join before the merges; the whole call is capturable in
+    one CUDA graph.
+    """
+    if not levels:
+        raise ValueError("multi_level_cascade needs at least one level")
+    if plans is None:
+        plans = []
+        for db in levels:
+            p = make_plan(db.host, level_kind(db.host))
+            plan_batch(p, db.host, stream)
+            plans.append(p)
+    if len(plans) != len(levels):
+        raise ValueError("one plan per level")
+    if side_streams is not None and len(side_streams) < len(levels) - 1:
+        raise ValueError("one side stream per level after the first")
+    q = levels[0].q
+    outs = [(torch.empty_like(q), torch.empty(q.shape[:2], dtype=torch.float32, device=q.device))
+            for _ in levels]
+    main = stream if stream is not None else torch.cuda.current_stream()
+
+    def run(i, s):
+        db, p = levels[i], plans[i]
+        o, lse = outs[i]
+        p.run(db.q, db.kv_data, db.kv_indices, db.kv_indptr, db.kv_last_page_len, o, lse,
+              qo_indptr=db.qo_indptr if p.kind == api.PLAN_PREFILL else None, stream=s)
+
+    if side_streams is None:
+        for i in range(len(levels)):
+            run(i, main)
+    else:
+        fork = torch.cuda.Event()
+        fork.record(main)
+        joins = []
+        for i in range(1, len(levels)):
+            s = side_streams[i - 1]
+            s.wait_event(fork)
+            run(i, s)
+            ev = torch.cuda.Event()
+            ev.record(s)
+            joins.append(ev)
+        run(0, main)
+        for ev in joins:
+            main.wait_event(ev)
+    o0, l0 = outs[0]
+    for o, lse in outs[1:]:
+        api.merge_state(o0, l0, o, lse, o0, l0, stream=main)
+    return o0, l0

@@ -36,6 +36,8 @@ __all__ = [
     "skewed_decode",
     "ragged_prefill",
     "cascade_decode",
+    "MultiLevelBatch",
+    "parallel_generation",
     "WORKLOADS",
 ]
 
@@ -98,6 +100,22 @@ class CascadeBatch:
     suffix: PagedBatch
     prefix_len: int
     suffix_lens: List[int]
+
+
+@dataclasses.dataclass
+class MultiLevelBatch:
+    """A prefix tree of KV over one pool, seen per level (no data moves).
+
+    ``full``   : each request's page list = the pages of every level on its path.
+    ``levels`` : level l groups the requests into consecutive row blocks (its nodes);
+                 node n of level l attends, as one block of rows, to that node's own
+                 pages.  Every level covers every request row exactly once, so the
+                 merge of all levels' states is the full attention.
+    """
+
+    full: PagedBatch
+    levels: List[PagedBatch]
+    level_names: List[str]
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -321,10 +339,86 @@ def cascade_decode(seed: int = 1004, batch: int = 64, prefix_len: int = 2048,
                         suffix_lens=list(suffix_lens))
 
 
+def parallel_generation(seed: int = 1005, num_prompts: int = 8, samples: int = 8,
+                        system_len: int = 1024, prompt_lo: int = 512, prompt_hi: int = 2048,
+                        gen_lo: int = 50, gen_hi: int = 200, num_qo_heads: int = 32,
+                        num_kv_heads: int = 8, head_dim: int = 128, page_size: int = 16,
+                        dtype: torch.dtype = torch.bfloat16, logits_cap: float = 0.0,
+                        poison: bool = False) -> MultiLevelBatch:
+    """Parallel generation over a three-level prefix tree, one decode token per request.
+
+    Level 0: a ``system_len``-token system prompt shared by all
+    ``num_prompts * samples`` requests.  Level 1: ``num_prompts`` user prompts of
+    U[prompt_lo, prompt_hi] tokens (rounded down to whole pages), each shared by the
+    ``samples`` requests generated from it.  Level 2: each request's own generated
+    tokens, U[gen_lo, gen_hi].  Shared levels fill whole pages, so the full view is a
+    plain page table; only a request's last (private) page is partial.
+    """
+    if system_len % page_size:
+        raise ValueError("the shared system prompt must fill whole pages")
+    if gen_lo < 1:
+        raise ValueError("every request holds at least one generated token")
+    gen = _gen(seed)
+    batch = num_prompts * samples
+    n_sys = system_len // page_size
+    n_prompt = [max(1, x // page_size) for x in _uniform_ints(prompt_lo, prompt_hi, num_prompts, gen)]
+    gen_lens = _uniform_ints(gen_lo, gen_hi, batch, gen)
+    n_gen = [(g + page_size - 1) // page_size for g in gen_lens]
+    pool = n_sys + sum(n_prompt) + sum(n_gen)
+    perm = torch.randperm(pool, generator=gen).to(torch.int32)
+    off = 0
+
+    def take(n):
+        nonlocal off
+        t = perm[off:off + n]
+        off += n
+        return t
+
+    sys_pages = take(n_sys)
+    prompt_pages = [take(n) for n in n_prompt]
+    gen_pages = [take(n) for n in n_gen]
+    q = _randn((batch, num_qo_heads, head_dim), gen, dtype)
+    kv = _randn((pool, 2, num_kv_heads, page_size, head_dim), gen, dtype)
+    gen_last = torch.tensor([g - (n - 1) * page_size for g, n in zip(gen_lens, n_gen)], dtype=torch.int32)
+
+    def indptr_of(counts):
+        t = torch.zeros(len(counts) + 1, dtype=torch.int32)
+        t[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int64), 0).to(torch.int32)
+        return t
+
+    owner = [r // samples for r in range(batch)]
+    full_pages = [torch.cat([sys_pages, prompt_pages[owner[r]], gen_pages[r]]) for r in range(batch)]
+    full_indices = torch.cat(full_pages)
+    full_indptr = indptr_of([p.numel() for p in full_pages])
+    if poison:
+        _poison_(kv, full_indices, full_indptr, gen_last, page_size)
+    common = dict(page_size=page_size, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                  head_dim=head_dim, dtype=dtype, kv_data=kv, sm_scale=1.0 / math.sqrt(head_dim),
+                  logits_cap=logits_cap, causal=False)
+    full = PagedBatch(q=q, qo_indptr=indptr_of([1] * batch), kv_indptr=full_indptr, kv_indices=full_indices,
+                      kv_last_page_len=gen_last.clone(), qo_lens=[1] * batch,
+                      kv_lens=[system_len + n_prompt[owner[r]] * page_size + gen_lens[r] for r in range(batch)],
+                      name="parallel_generation_full", **common)
+    system = PagedBatch(q=q, qo_indptr=torch.tensor([0, batch], dtype=torch.int32),
+                        kv_indptr=torch.tensor([0, n_sys], dtype=torch.int32), kv_indices=sys_pages.clone(),
+                        kv_last_page_len=torch.tensor([page_size], dtype=torch.int32), qo_lens=[batch],
+                        kv_lens=[system_len], name="parallel_generation_system", **common)
+    prompts = PagedBatch(q=q, qo_indptr=indptr_of([samples] * num_prompts), kv_indptr=indptr_of(n_prompt),
+                         kv_indices=torch.cat(prompt_pages),
+                         kv_last_page_len=torch.full((num_prompts,), page_size, dtype=torch.int32),
+                         qo_lens=[samples] * num_prompts, kv_lens=[n * page_size for n in n_prompt],
+                         name="parallel_generation_prompts", **common)
+    own = PagedBatch(q=q, qo_indptr=indptr_of([1] * batch), kv_indptr=indptr_of(n_gen),
+                     kv_indices=torch.cat(gen_pages), kv_last_page_len=gen_last.clone(), qo_lens=[1] * batch,
+                     kv_lens=list(gen_lens), name="parallel_generation_own", **common)
+    return MultiLevelBatch(full=full, levels=[system, prompts, own], level_names=["system", "prompt", "own"])
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama3_8b_decode": llama3_decode,
     "skewed_decode": skewed_decode,
     "ragged_causal_prefill": ragged_prefill,
     "cascade_softcap_decode": cascade_decode,
+    "parallel_generation": parallel_generation,
 }

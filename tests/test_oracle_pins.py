@@ -348,6 +348,29 @@ def test_cascade_equals_full_attention():
     np.testing.assert_allclose(l_c, l_f, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("cap", [0.0, 20.0])
+def test_multi_level_cascade_equals_full_attention(cap):
+    """Three levels (system prompt, per-group prompts, own tokens): the merge of the
+    levels' states is attention over each request's whole path."""
+    mb = W.parallel_generation(seed=42, num_prompts=3, samples=4, system_len=32, prompt_lo=8, prompt_hi=60,
+                               gen_lo=1, gen_hi=30, num_qo_heads=4, num_kv_heads=2, head_dim=16, page_size=8,
+                               logits_cap=cap, poison=True)
+    batch = mb.full.batch
+    for lv in mb.levels:
+        assert int(lv.qo_indptr[-1]) == batch and lv.total_q == batch
+    path_len = [0] * batch
+    for lv in mb.levels:
+        for n in range(lv.batch):
+            for r in range(int(lv.qo_indptr[n]), int(lv.qo_indptr[n + 1])):
+                path_len[r] += lv.kv_lens[n]
+    assert path_len == mb.full.kv_lens
+    o_c, l_c = oracle.cascade(*mb.levels)
+    o_f, l_f = oracle.attention_of(mb.full)
+    assert np.all(np.isfinite(o_f))
+    np.testing.assert_allclose(o_c, o_f, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l_c, l_f, rtol=0, atol=1e-12)
+
+
 # --------------------------------------------------------------------------- merge_state forms
 def test_merge_state_closed_forms():
     rng = np.random.default_rng(0)
