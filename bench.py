@@ -48,7 +48,7 @@ def parse_args():
     p.add_argument("--no-secondary", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
-    p.add_argument("--only", choices=["prefill", "cascade", "multilevel", "skewed"], default=None,
+    p.add_argument("--only", choices=["prefill", "cascade", "multilevel", "append", "skewed"], default=None,
                    help="time one secondary measurement alone (for profiling) and print it")
     return p.parse_args()
 
@@ -479,6 +479,49 @@ def multilevel_measure(steps=50, warmup=5):
     return out
 
 
+def append_bytes(b) -> int:
+    """Algorithmic bytes of one append + RoPE launch: every new token's query read and
+    written, its K and V read and written into the pool (index arrays not counted)."""
+    e = b.kv_data.element_size()
+    per_token = (2 * b.num_qo_heads + 4 * b.num_kv_heads) * b.head_dim * e
+    return b.total_q * per_token
+
+
+def append_measure(peaks, steps=50, warmup=5, per_graph=20):
+    """Append stage with RoPE of keys and queries: the ragged prefill batch's new
+    tokens (bandwidth: ~0.5 GB per launch, larger than L2) and one decode step of the
+    Llama-3-8B-shaped batch (64 tokens, latency).  ``per_graph`` launches are captured
+    in one CUDA graph and replayed, so host launch overhead is not timed; the figure
+    is per launch."""
+    import torch
+    from paged_kv_cache_bsr_gb300 import runner, workloads as W
+    out = {}
+    for name, b in (("ragged_prefill_append", W.ragged_prefill(seed=1003)),
+                    ("decode_step_append", W.llama3_decode(seed=1001))):
+        k_new, v_new = W.new_kv_rows(b)
+        db = runner.DeviceBatch.from_host(b)
+        kn, vn = k_new.cuda(), v_new.cuda()
+        q_out = torch.empty_like(db.q)
+        s = torch.cuda.Stream()
+
+        def launches():
+            for _ in range(per_graph):
+                runner.append_kv(db, kn, vn, 500000.0, q_out=q_out, stream=s)
+
+        with torch.cuda.stream(s):
+            launches()
+        s.synchronize()
+        us = graph_us(launches, s, steps, warmup) / per_graph
+        nbytes = append_bytes(b)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"new_tokens": b.total_q, "us": round(us, 2), "bytes": nbytes, "GBps": round(gbs, 1),
+                     "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)}
+        del db, kn, vn, q_out
+    out["rope_theta"] = 500000.0
+    out["timing"] = f"CUDA-graph replay of {per_graph} back-to-back launches; per-launch time"
+    return out
+
+
 def run_only(args):
     import torch
     from paged_kv_cache_bsr_gb300 import build, api, workloads as W
@@ -492,6 +535,8 @@ def run_only(args):
         res = cascade_measure(steps=args.steps, warmup=args.warmup)
     elif args.only == "multilevel":
         res = multilevel_measure(steps=args.steps, warmup=args.warmup)
+    elif args.only == "append":
+        res = append_measure(peaks, steps=args.steps, warmup=args.warmup)
     else:
         r = decode_measure(W.skewed_decode(seed=1002), args.steps, args.warmup, peaks)
         res = {"value": round(r["value"], 1), "unit": "GB/s", "roofline": r["roofline"]}
@@ -553,6 +598,7 @@ def run_own(args):
             secondary["prefill"] = prefill_measure(peaks)
             secondary["cascade"] = cascade_measure()
             secondary["multilevel_cascade"] = multilevel_measure()
+            secondary["append_rope"] = append_measure(peaks)
     clocks.stop()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,

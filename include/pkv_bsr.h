@@ -271,6 +271,49 @@ pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b,
                            int dtype, void* stream);
 
 /*
+ * Append new tokens' K and V into their pages, with the rotary position
+ * embedding (RoPE) of the keys and of the queries fused into the same pass.
+ * Serving appends each step's new tokens to the KV cache (fdeinterviews,
+ * "Dynamic Problem Shapes": the prefill, decode and append stages), and RoPE
+ * is one of the query/key transforms an attention variant fuses
+ * (fdeinterviews summary, "Customizable attention, compiled just in time").
+ *
+ * params       : num_qo_heads, num_kv_heads, head_dim (64 or 128), page_size
+ *                and dtype (PKV_F16 / PKV_BF16) are used; the rest is ignored.
+ * batch, nnz   : requests, and new tokens over all requests.
+ * num_pages    : pool size; page ids outside [0, num_pages) are not written.
+ * append_indptr_d  [batch + 1] int32 device: new rows of request b are
+ *                append_indptr[b] .. append_indptr[b+1]-1 (append_indptr[0] = 0,
+ *                append_indptr[batch] = nnz).
+ * kv_indptr_d, kv_indices_d, kv_last_page_len_d: the page table as for the
+ *                attention calls, already INCLUDING the new tokens: the n_b new
+ *                tokens of request b are its last n_b tokens, so new token i sits
+ *                at position kv_len_b - n_b + i, in page
+ *                kv_indices[kv_indptr[b] + pos / page_size], slot pos % page_size.
+ * k_new, v_new [nnz, num_kv_heads, head_dim] device, dtype.
+ * kv_data      [num_pages, 2, num_kv_heads, page_size, head_dim] device: only the
+ *                new tokens' slots are written.
+ * q_in, q_out  [nnz, num_qo_heads, head_dim] device, dtype, or both NULL.  Row t
+ *                of q is the query of new token t and turns by the same position.
+ *                q_out may equal q_in (in place).
+ * rope_theta   : > 0: keys and queries are rotated, "rotate half" pairing (element
+ *                i < head_dim/2 with i + head_dim/2) by the angle
+ *                pos * rope_theta^(-2i/head_dim); 0: copied unchanged.  Positions
+ *                must be below 2^24.  V is never rotated.
+ * error_d      : device int32 or NULL; OR-ed with 1 (a page id out of range) and
+ *                16 (a row outside every request's new rows, more new tokens than
+ *                kv_len, or a last-page length outside [1, page_size]).  Such
+ *                tokens are skipped.  The caller clears it.
+ * Errors: PKV_ERR_INVALID_ARG (null or misaligned pointer, bad size or theta),
+ * PKV_ERR_UNSUPPORTED (head_dim, dtype), PKV_ERR_CUDA.  nnz = 0 is a no-op.
+ */
+pkv_status pkv_append_paged_kv(const pkv_params* params, int batch, int64_t nnz, int64_t num_pages,
+                               const int32_t* append_indptr_d, const int32_t* kv_indptr_d,
+                               const int32_t* kv_indices_d, const int32_t* kv_last_page_len_d,
+                               const void* k_new, const void* v_new, void* kv_data, const void* q_in,
+                               void* q_out, double rope_theta, int32_t* error_d, void* stream);
+
+/*
  * Read (and, with clear != 0, reset) the device error word a plan's kernels
  * write when a check fails (page id out of range, indptr mismatch, a bounded
  * wait that ran out).  Synchronises `stream`.  *code = 0 means no error.

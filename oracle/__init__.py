@@ -21,7 +21,13 @@ arguments through ctypes.  Every function follows the FlashInfer pages:
 * ``cascade``       -- shared-prefix attention computed once for the whole
                        row block, per-request suffix attention, then a merge
                        (guide section 3, "Cascade Attention"; fdeinterviews
-                       "One format", composable formats).
+                       "One format", composable formats); any number of levels.
+* ``rope``, ``append_positions``, ``append_paged_kv`` -- the append stage that
+                       writes new tokens into their pages (fdeinterviews,
+                       "Dynamic Problem Shapes") with the rotary query/key
+                       transform (fdeinterviews summary, "Customizable
+                       attention"), in plain numpy fp64.
+* ``encode16``      -- fp64 -> fp16/bf16 storage, round to nearest even.
 
 Parity pins: see tests/test_oracle_pins.py.  Every function here is pinned.
 """
@@ -238,3 +244,103 @@ def cascade(*level_batches, threads: int = 0):
         raise ValueError("cascade needs at least one level")
     states = [attention_of(b, threads=threads) for b in level_batches]
     return merge_states([s[0] for s in states], [s[1] for s in states])
+
+
+# ----------------------------------------------------------------------------- append stage
+def encode16(x, dtype: str) -> np.ndarray:
+    """Round fp64 values to the nearest fp16 / bf16 value, ties to even (the IEEE
+    default), returned as fp64 holding exactly representable values.
+
+    A finite x = m * 2^e with m in [0.5, 1) has its unit in the last place at
+    2^(e - bits) for a format of ``bits`` significant bits, but never below the
+    format's smallest subnormal; values past the largest finite one become inf.
+    """
+    bits, min_exp, max_finite = {"bf16": (8, -133, 3.3895313892515355e38),
+                                 "f16": (11, -24, 65504.0)}[dtype]
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x, copy=True)
+    fin = np.isfinite(x) & (x != 0)
+    _, e = np.frexp(x[fin])
+    ulp_exp = np.maximum(e - bits, min_exp).astype(np.int64)
+    r = np.ldexp(np.rint(np.ldexp(x[fin], -ulp_exp)), ulp_exp)
+    # past the largest finite value by half an ulp or more: infinity
+    top_ulp = 2.0 ** (int(np.frexp(max_finite)[1]) - bits)
+    r = np.where(np.abs(x[fin]) >= max_finite + top_ulp / 2, np.copysign(np.inf, x[fin]), r)
+    out[fin] = r
+    return out
+
+
+def rope(x, positions, theta: float, dtype: Optional[str] = None) -> np.ndarray:
+    """Rotary position embedding (RoFormer), "rotate half" pairing, in fp64.
+
+    x [n, H, d] (16-bit storage decoded exactly, or any float array); row t turns by
+    positions[t]: element i < d/2 pairs with i + d/2 and the pair turns by the angle
+    positions[t] * theta^(-2i/d):  (a, b) -> (a cos - b sin, b cos + a sin).
+    """
+    xv = _as_f64(x, dtype)
+    n, _, d = xv.shape
+    half = d // 2
+    inv_freq = float(theta) ** (-2.0 * np.arange(half, dtype=np.float64) / d)
+    ang = np.asarray(positions, dtype=np.float64).reshape(n)[:, None] * inv_freq[None, :]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    a, b = xv[..., :half], xv[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def _as_f64(x, dtype: Optional[str]) -> np.ndarray:
+    """16-bit storage decoded exactly; any other float array as fp64."""
+    name = str(getattr(x, "dtype", ""))
+    if dtype is not None or "float16" in name:
+        return decode16(x, dtype)
+    return np.asarray(x, dtype=np.float64)
+
+
+def append_positions(append_indptr, kv_indptr, kv_last_page_len, kv_indices, page_size: int):
+    """Where each new token goes.  The page table already holds the new tokens, and
+    request b's n_b new tokens are its last n_b: token i of them sits at position
+    kv_len_b - n_b + i, in page kv_indices[kv_indptr[b] + pos // P], slot pos % P.
+
+    Returns (request, position, page, slot), one entry per new token.
+    """
+    ap, ip, ix, last = _i32(append_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(kv_last_page_len)
+    batch = ip.size - 1
+    if ap.size != batch + 1 or ap[0] != 0 or np.any(np.diff(ap) < 0):
+        raise ValueError("append_indptr must start at 0 and be non-decreasing, one entry per request + 1")
+    req, pos, page, slot = [], [], [], []
+    for b in range(batch):
+        n_pages = int(ip[b + 1] - ip[b])
+        kv_len = (n_pages - 1) * page_size + int(last[b]) if n_pages > 0 else 0
+        n_new = int(ap[b + 1] - ap[b])
+        if n_new > kv_len:
+            raise ValueError(f"request {b}: {n_new} new tokens but kv_len {kv_len}")
+        for i in range(n_new):
+            p = kv_len - n_new + i
+            req.append(b)
+            pos.append(p)
+            page.append(int(ix[ip[b] + p // page_size]))
+            slot.append(p % page_size)
+    as64 = lambda v: np.asarray(v, dtype=np.int64)
+    return as64(req), as64(pos), as64(page), as64(slot)
+
+
+def append_paged_kv(kv_data, append_indptr, kv_indptr, kv_indices, kv_last_page_len, k_new, v_new,
+                    rope_theta: float = 0.0):
+    """The KV pool after appending new tokens, in fp64.
+
+    kv_data [num_pages, 2, Hkv, P, d] (16-bit storage); k_new, v_new [nnz, Hkv, d].
+    The keys turn by their positions when rope_theta > 0 (``rope``); values never do.
+    Returns (kv fp64 with the new tokens written, page [nnz], slot [nnz]).
+    """
+    kv = decode16(kv_data)
+    page_size = kv.shape[3]
+    _, pos, page, slot = append_positions(append_indptr, kv_indptr, kv_last_page_len, kv_indices, page_size)
+    if len(set(zip(page.tolist(), slot.tolist()))) != page.size:
+        raise ValueError("two new tokens map to the same page slot")
+    if np.any(page < 0) or np.any(page >= kv.shape[0]):
+        raise ValueError("page id out of range")
+    k = rope(k_new, pos, rope_theta) if rope_theta > 0 else decode16(k_new)
+    v = decode16(v_new)
+    kv[page, 0, :, slot, :] = k
+    kv[page, 1, :, slot, :] = v
+    return kv, page, slot

@@ -56,7 +56,7 @@ EXPORTS = [
     "pkv_status_string", "pkv_version", "pkv_plan_create", "pkv_plan_create_host", "pkv_plan_destroy",
     "pkv_plan_workspace_bytes", "pkv_plan_compute", "pkv_plan_run", "pkv_plan_get_info", "pkv_plan_get_work",
     "pkv_batch_decode_paged", "pkv_batch_prefill_paged", "pkv_merge_state", "pkv_get_device_error",
-    "pkv_plan_set_timing_events", "pkv_batch_decode_paged_noalloc",
+    "pkv_plan_set_timing_events", "pkv_batch_decode_paged_noalloc", "pkv_append_paged_kv",
 ]
 
 
@@ -92,6 +92,8 @@ def load(path: Optional[str] = None):
             "pkv_get_device_error": (i32, [vp, vp, ctypes.POINTER(i32), i32, vp]),
             "pkv_plan_set_timing_events": (i32, [vp, vp, vp]),
             "pkv_batch_decode_paged_noalloc": (i32, [vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "pkv_append_paged_kv": (i32, [ctypes.POINTER(Params), i32, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          vp, ctypes.c_double, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -239,6 +241,20 @@ def merge_state(o_a, lse_a, o_b, lse_b, o_out, lse_out=None, stream=None) -> Non
     n, hh, d = o_a.shape
     _check(load().pkv_merge_state(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o_out), _ptr(lse_out),
                                   n, hh, d, dtype_code(o_a.dtype), _stream(stream)), "pkv_merge_state")
+
+
+def append_paged_kv(params: Params, append_indptr, kv_indptr, kv_indices, kv_last_page_len, k_new, v_new,
+                    kv_data, q_in=None, q_out=None, rope_theta: float = 0.0, error=None, stream=None) -> None:
+    """Write new tokens' K/V into their pages (page table already including them);
+    with rope_theta > 0 rotate the keys and, when given, the queries (q_out may be q_in)."""
+    batch = int(append_indptr.numel()) - 1
+    nnz = int(k_new.shape[0])
+    if q_in is not None and q_out is None:
+        q_out = q_in
+    _check(load().pkv_append_paged_kv(ctypes.byref(params), batch, nnz, int(kv_data.shape[0]), _ptr(append_indptr),
+                                      _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len), _ptr(k_new),
+                                      _ptr(v_new), _ptr(kv_data), _ptr(q_in), _ptr(q_out), float(rope_theta),
+                                      _ptr(error), _stream(stream)), "pkv_append_paged_kv")
 
 
 def plan_set_timing_events(h, start=None, stop=None) -> None:

@@ -18,6 +18,8 @@ enum : int {
   kErrIndptrMismatch = 2,// kv_indptr on the device differs from the plan's host copy
   kErrWaitTimeout = 4,   // a bounded wait on an mbarrier ran out
   kErrTmemAlloc = 8,     // tensor-memory allocation failed
+  kErrAppendLayout = 16, // append: a row outside every request's new rows, more new
+                         // tokens than the request's kv_len, or a bad last-page length
 };
 
 struct alignas(64) PlanHeader {

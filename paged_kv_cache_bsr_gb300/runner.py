@@ -85,6 +85,23 @@ def cascade(prefix: DeviceBatch, suffix: DeviceBatch, prefix_plan: Optional[api.
     return o_p, l_p
 
 
+def append_kv(db: DeviceBatch, k_new: torch.Tensor, v_new: torch.Tensor, rope_theta: float = 0.0,
+              q_out: Optional[torch.Tensor] = None, rotate_q: bool = True, error: Optional[torch.Tensor] = None,
+              stream=None) -> Optional[torch.Tensor]:
+    """Append stage: write the batch's new tokens (one per query row, rows by
+    qo_indptr) into ``db.kv_data`` at the end of each request's page list, turning
+    the keys (and the queries, into ``q_out`` or a new tensor) by RoPE when
+    rope_theta > 0.  Returns the rotated queries (None with rotate_q False)."""
+    b = db.host
+    params = api.make_params(b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.dtype, b.sm_scale)
+    if rotate_q and q_out is None:
+        q_out = torch.empty_like(db.q)
+    api.append_paged_kv(params, db.qo_indptr, db.kv_indptr, db.kv_indices, db.kv_last_page_len, k_new, v_new,
+                        db.kv_data, db.q if rotate_q else None, q_out if rotate_q else None, rope_theta,
+                        error=error, stream=stream)
+    return q_out if rotate_q else None
+
+
 def level_kind(b) -> int:
     """A level whose nodes each hold one query row is plain decode; a level with
     multi-row blocks (a prefix shared by several requests) runs on the prefill

@@ -38,6 +38,7 @@ __all__ = [
     "cascade_decode",
     "MultiLevelBatch",
     "parallel_generation",
+    "new_kv_rows",
     "WORKLOADS",
 ]
 
@@ -412,6 +413,16 @@ def parallel_generation(seed: int = 1005, num_prompts: int = 8, samples: int = 8
                      kv_indices=torch.cat(gen_pages), kv_last_page_len=gen_last.clone(), qo_lens=[1] * batch,
                      kv_lens=list(gen_lens), name="parallel_generation_own", **common)
     return MultiLevelBatch(full=full, levels=[system, prompts, own], level_names=["system", "prompt", "own"])
+
+
+def new_kv_rows(b: PagedBatch, seed: int = 7) -> "tuple[torch.Tensor, torch.Tensor]":
+    """K and V of the new tokens of a batch, one per query row: [total_q, Hkv, d] each,
+    N(0, 1) in the batch's dtype.  With the batch's page table (which already counts
+    them) and ``qo_indptr`` as the append row pointer, these are the inputs of the
+    append stage: request b's qo_len new tokens are the last of its kv_len."""
+    gen = _gen(seed)
+    shape = (b.total_q, b.num_kv_heads, b.head_dim)
+    return _randn(shape, gen, b.dtype), _randn(shape, gen, b.dtype)
 
 
 WORKLOADS = {

@@ -409,3 +409,109 @@ def test_poisoned_pool_never_reaches_outputs():
     assert torch.isnan(b.kv_data.float()).any()
     o, lse = oracle.attention_of(b)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+# --------------------------------------------------------------------------- append stage: rope, positions
+def test_rope_closed_forms_fix_pairing_sign_and_frequencies():
+    """Unit vectors: e_0 turns into (cos m, sin m) on the pair (0, d/2) (frequency 1);
+    e_{d/2} into (-sin m, cos m); e_1 turns by m * theta^(-2/d)."""
+    d, theta = 8, 10000.0
+    m = np.array([0.0, 1.0, 7.0, 1000.0])
+    e = np.zeros((4, 3, d))
+    e[:, 0, 0] = 1.0
+    e[:, 1, d // 2] = 1.0
+    e[:, 2, 1] = 1.0
+    r = oracle.rope(e, m, theta)
+    np.testing.assert_allclose(r[:, 0, 0], np.cos(m), atol=1e-15)
+    np.testing.assert_allclose(r[:, 0, d // 2], np.sin(m), atol=1e-15)
+    np.testing.assert_allclose(r[:, 1, 0], -np.sin(m), atol=1e-15)
+    np.testing.assert_allclose(r[:, 1, d // 2], np.cos(m), atol=1e-15)
+    a1 = m * theta ** (-2.0 / d)  # = m / 10
+    np.testing.assert_allclose(r[:, 2, 1], np.cos(a1), atol=1e-15)
+    np.testing.assert_allclose(r[:, 2, 1 + d // 2], np.sin(a1), atol=1e-15)
+    # every other coordinate of the three rows stays zero
+    mask = np.ones_like(r, dtype=bool)
+    mask[:, 0, [0, d // 2]] = mask[:, 1, [0, d // 2]] = mask[:, 2, [1, 1 + d // 2]] = False
+    assert np.all(r[mask] == 0)
+
+
+def test_rope_is_a_rotation_by_relative_position():
+    """Position 0 is the identity, norms of each pair are kept, rotations compose
+    (m then n is m + n), and <R(m) q, R(n) k> depends on m - n only."""
+    rng = np.random.default_rng(3)
+    d, theta = 16, 500.0
+    x = rng.normal(size=(6, 2, d))
+    np.testing.assert_array_equal(oracle.rope(x, np.zeros(6), theta), x)
+    m = rng.integers(0, 5000, size=6).astype(np.float64)
+    n = rng.integers(0, 5000, size=6).astype(np.float64)
+    rx = oracle.rope(x, m, theta)
+    pair_norm = lambda v: v[..., : d // 2] ** 2 + v[..., d // 2:] ** 2
+    np.testing.assert_allclose(pair_norm(rx), pair_norm(x), rtol=1e-12)
+    np.testing.assert_allclose(oracle.rope(rx, n, theta), oracle.rope(x, m + n, theta), atol=1e-9)
+    q, k = rng.normal(size=(6, 1, d)), rng.normal(size=(6, 1, d))
+    dots = lambda a, b: np.sum(oracle.rope(q, a, theta) * oracle.rope(k, b, theta), axis=-1)
+    np.testing.assert_allclose(dots(m, n), dots(m + 37, n + 37), atol=1e-9)
+    assert not np.allclose(dots(m, n), dots(m + 37, n))
+
+
+def test_append_positions_worked_example():
+    """P = 4.  Request 0: 2 pages, last 3 (kv_len 7), 2 new tokens -> positions 5, 6 =
+    slots 1, 2 of its second page.  Request 1: 1 page, last 1, 1 new token -> position 0.
+    Request 2: 3 full pages, nothing new.  Request 3: 2 pages, last 4, 5 new -> 3..7."""
+    kv_indptr = [0, 2, 3, 6, 8]
+    kv_indices = [9, 4, 7, 0, 1, 2, 5, 3]
+    last = [3, 1, 4, 4]
+    append_indptr = [0, 2, 3, 3, 8]
+    req, pos, page, slot = oracle.append_positions(append_indptr, kv_indptr, last, kv_indices, 4)
+    assert req.tolist() == [0, 0, 1, 3, 3, 3, 3, 3]
+    assert pos.tolist() == [5, 6, 0, 3, 4, 5, 6, 7]
+    assert page.tolist() == [4, 4, 7, 5, 3, 3, 3, 3]
+    assert slot.tolist() == [1, 2, 0, 3, 0, 1, 2, 3]
+    with pytest.raises(ValueError):
+        oracle.append_positions([0, 9, 9, 9, 9], kv_indptr, last, kv_indices, 4)
+
+
+def test_append_then_gather_reads_old_tokens_then_new():
+    """After the append, the page-table gather of each request returns its earlier
+    tokens unchanged followed by the new ones (rotated keys, plain values)."""
+    b = W.make_paged_batch(qo_lens=[3, 1, 0, 9], kv_lens=[20, 1, 5, 9], num_qo_heads=4, num_kv_heads=2,
+                           head_dim=16, page_size=8, dtype=torch.bfloat16, seed=11, poison=True)
+    gen = torch.Generator().manual_seed(12)
+    k_new = torch.randn(b.total_q, 2, 16, generator=gen).to(torch.bfloat16)
+    v_new = torch.randn(b.total_q, 2, 16, generator=gen).to(torch.bfloat16)
+    theta = 10000.0
+    kv, page, slot = oracle.append_paged_kv(b.kv_data, b.qo_indptr, b.kv_indptr, b.kv_indices,
+                                            b.kv_last_page_len, k_new, v_new, rope_theta=theta)
+    req, pos, _, _ = oracle.append_positions(b.qo_indptr, b.kv_indptr, b.kv_last_page_len, b.kv_indices, 8)
+    k_rot = oracle.rope(k_new, pos, theta)
+    for r in range(b.batch):
+        n_new = b.qo_lens[r]
+        rows = np.nonzero(req == r)[0]
+        for h in range(2):
+            before_k = oracle.gather(b.kv_data, b.kv_indptr, b.kv_indices, b.kv_last_page_len, r, 0, h)
+            p0, p1 = int(b.kv_indptr[r]), int(b.kv_indptr[r + 1])
+            pages = b.kv_indices[p0:p1].long().numpy()
+            after_k = kv[pages, 0, h].reshape(-1, 16)[: b.kv_lens[r]]
+            after_v = kv[pages, 1, h].reshape(-1, 16)[: b.kv_lens[r]]
+            old = b.kv_lens[r] - n_new
+            np.testing.assert_array_equal(after_k[:old], before_k[:old])
+            np.testing.assert_array_equal(after_k[old:], k_rot[rows, h])
+            np.testing.assert_array_equal(after_v[old:], oracle.decode16(v_new)[rows, h])
+
+
+def test_encode16_rounds_to_nearest_even():
+    """Values a 32-bit float holds exactly round like torch's float -> bf16 / fp16
+    conversion (round to nearest even); halfway cases go to the even neighbour;
+    representable values and the special values come back unchanged."""
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.normal(size=4000) * 10.0 ** rng.integers(-6, 5, size=4000),
+                        [0.0, -0.0, np.inf, -np.inf, 65504.0, 65520.0, 1e-8, 6e-8]]).astype(np.float32)
+    for name, td in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        ref = torch.from_numpy(v).to(td).double().numpy()
+        np.testing.assert_array_equal(oracle.encode16(v.astype(np.float64), name), ref)
+    # 1 + 2^-8 is halfway between bf16 neighbours 1 and 1 + 2^-7: ties to even -> 1
+    assert oracle.encode16(np.array([1 + 2.0 ** -8]), "bf16")[0] == 1.0
+    assert oracle.encode16(np.array([1 + 3 * 2.0 ** -8]), "bf16")[0] == 1 + 2 * 2.0 ** -7
+    # fp16: 1 + 2^-11 halfway -> 1, 2049 -> 2048 (ties to even), nan stays nan
+    assert oracle.encode16(np.array([1 + 2.0 ** -11, 2049.0]), "f16").tolist() == [1.0, 2048.0]
+    assert np.isnan(oracle.encode16(np.array([np.nan]), "bf16")[0])
