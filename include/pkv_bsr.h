@@ -273,8 +273,9 @@ pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b,
 /*
  * Append new tokens' K and V into their pages, with the rotary position
  * embedding (RoPE) of the keys and of the queries fused into the same pass.
- * Serving appends each step's new tokens to the KV cache (fdeinterviews,
- * "Dynamic Problem Shapes": the prefill, decode and append stages), and RoPE
+ * Serving appends each step's new tokens to the KV cache (greptalks MLSys
+ * 2025 talk summary, Background, "Dynamic Problem Shapes": the prefill,
+ * decode and append stages), and RoPE
  * is one of the query/key transforms an attention variant fuses
  * (fdeinterviews summary, "Customizable attention, compiled just in time").
  *

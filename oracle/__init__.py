@@ -23,10 +23,11 @@ arguments through ctypes.  Every function follows the FlashInfer pages:
                        (guide section 3, "Cascade Attention"; fdeinterviews
                        "One format", composable formats); any number of levels.
 * ``rope``, ``append_positions``, ``append_paged_kv`` -- the append stage that
-                       writes new tokens into their pages (fdeinterviews,
-                       "Dynamic Problem Shapes") with the rotary query/key
-                       transform (fdeinterviews summary, "Customizable
-                       attention"), in plain numpy fp64.
+                       writes new tokens into their pages (greptalks
+                       summary, Background, "Dynamic Problem Shapes") with
+                       the rotary query/key transform (fdeinterviews
+                       summary, "Customizable attention"), in plain numpy
+                       fp64.
 * ``encode16``      -- fp64 -> fp16/bf16 storage, round to nearest even.
 
 Parity pins: see tests/test_oracle_pins.py.  Every function here is pinned.
@@ -238,7 +239,8 @@ def cascade(*level_batches, threads: int = 0):
     per-request tokens) follow the same rule: each level's batch groups the request
     rows into consecutive blocks, each block against its own pages.  All views index
     the same pool.  Returns (o, lse) per request row: the merge of the levels'
-    states (FlashInfer pages: "Composable Formats for Shared Prefixes").
+    states (greptalks summary, "Composable Formats for Shared Prefixes": one
+    block-sparse matrix decomposed into several of different block sizes).
     """
     if len(level_batches) < 1:
         raise ValueError("cascade needs at least one level")

@@ -3,10 +3,11 @@
 // same pass.
 //
 // The pages name both steps: serving has an "append" stage that adds the new
-// tokens to the KV cache (fdeinterviews, "Dynamic Problem Shapes"), and the
-// query/key transforms of an attention variant include RoPE, which FlashInfer
-// fuses instead of running as a separate pass (fdeinterviews summary,
-// "Customizable attention, compiled just in time").  Neither page fixes the
+// tokens to the KV cache (greptalks MLSys 2025 talk summary, Background,
+// "Dynamic Problem Shapes"), and the query/key transforms of an attention
+// variant include RoPE, which FlashInfer fuses instead of running as a
+// separate pass (fdeinterviews summary, "Customizable attention, compiled
+// just in time").  Neither page fixes the
 // rotation, so the embedding is the RoFormer one in its "rotate half" form:
 // element i < D/2 of a head row pairs with element i + D/2, and the pair at
 // position `pos` turns by the angle pos * theta^(-2i/D):

@@ -112,7 +112,10 @@ def level_kind(b) -> int:
 def multi_level_cascade(levels: Sequence[DeviceBatch], plans: Optional[Sequence[api.Plan]] = None,
                         stream=None, side_streams: Optional[Sequence] = None
                         ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Attention over a prefix tree stored as one BSR matrix per level.
+    """Attention over a prefix tree stored as one BSR matrix per level (greptalks
+    summary, "Composable Formats for Shared Prefixes": one block-sparse matrix
+    decomposed into several with different row-block sizes; fdeinterviews summary,
+    "One format": shared prefixes as large row blocks, no data moved).
 
     Each level's batch groups the request rows into consecutive blocks (its nodes),
     each block against that node's pages; every level covers every row once.  Each

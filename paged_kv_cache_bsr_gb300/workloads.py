@@ -346,7 +346,8 @@ def parallel_generation(seed: int = 1005, num_prompts: int = 8, samples: int = 8
                         num_kv_heads: int = 8, head_dim: int = 128, page_size: int = 16,
                         dtype: torch.dtype = torch.bfloat16, logits_cap: float = 0.0,
                         poison: bool = False) -> MultiLevelBatch:
-    """Parallel generation over a three-level prefix tree, one decode token per request.
+    """Parallel generation over a three-level prefix tree, one decode token per request
+    (the parallel-generation scenario of the fdeinterviews summary, composable formats).
 
     Level 0: a ``system_len``-token system prompt shared by all
     ``num_prompts * samples`` requests.  Level 1: ``num_prompts`` user prompts of
