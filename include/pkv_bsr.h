@@ -223,6 +223,34 @@ pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const in
                                    void* o, float* lse, void* dev_ws, void* stream);
 
 /*
+ * Batch prefill with a custom attention mask, for tree attention (speculative
+ * decoding verifies a tree of draft tokens: each draft sees the cached prefix
+ * and its own ancestors) and any other block-sparse pattern finer than a
+ * page.  The pages list masks among the pieces a variant supplies
+ * (fdeinterviews summary, "Customizable attention, compiled just in time")
+ * and the token trees of speculative decoding among the KV layouts the BSR
+ * format covers (greptalks summary, "Radix Tree / Token Tree").
+ * packed_mask_d: device bits, request b's boolean matrix [qo_len_b, kv_len_b]
+ *   row-major, the requests back to back from bit 0 with no padding between
+ *   them (request b starts at bit sum over b' < b of qo_len_b' * kv_len_b');
+ *   bit k of 32-bit word w is bit 32 w + k (little-endian bytes, least
+ *   significant bit first).  1 = the query row sees the key.
+ * mask_bytes: size of that buffer; it must hold whole 32-bit words covering all
+ *   bits (4 * ceil(total_bits / 32) bytes) and be 4-byte aligned.  The kernel
+ *   never reads past mask_bytes.
+ * The mask applies on top of params->causal (both must allow a key).  A row
+ * that sees no key gets o = 0, lse = -inf.  Other arguments, layouts and graph
+ * capture as for pkv_batch_prefill_paged.
+ * Errors: PKV_ERR_INVALID_ARG (also for a short or misaligned mask),
+ * PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+pkv_status pkv_batch_prefill_paged_masked(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
+                                          const void* kv_data, const int32_t* kv_indices_d,
+                                          const int32_t* kv_indptr_d, const int32_t* kv_last_page_len_d,
+                                          const uint8_t* packed_mask_d, size_t mask_bytes, void* o, float* lse,
+                                          void* dev_ws, void* stream);
+
+/*
  * Batch decode for callers that cannot allocate device memory: plug-ins whose
  * host framework owns all device memory through its own allocator, services
  * under a fixed device-memory budget, and code paths that must not pay the

@@ -79,7 +79,7 @@ def _load():
             lib.pkv_oracle_attention.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 u16p, ctypes.c_int64, i32p, u16p, ctypes.c_int64, i32p, i32p, i32p,
-                ctypes.c_int, ctypes.c_double, ctypes.c_double, i64p, ctypes.c_int64,
+                ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_void_p, i64p, ctypes.c_int64,
                 f64p, f64p, ctypes.c_int]
             lib.pkv_oracle_gather.restype = ctypes.c_int
             lib.pkv_oracle_gather.argtypes = [
@@ -169,12 +169,14 @@ def gather(kv_data, kv_indptr, kv_indices, kv_last_page_len, b: int, kv_sel: int
 def attention(q, kv_data, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, *,
               sm_scale: float, causal: bool = False, logits_cap: float = 0.0,
               rows: Optional[Sequence[int]] = None, threads: int = 0,
-              dtype: Optional[str] = None) -> Tuple[np.ndarray, np.ndarray]:
+              dtype: Optional[str] = None, mask=None) -> Tuple[np.ndarray, np.ndarray]:
     """fp64 attention over the paged KV cache.
 
     q [total_q, Hq, d], kv_data [num_pages, 2, Hkv, page_size, d] (16-bit storage).
     Returns (o [n, Hq, d], lse [n, Hq]) for the listed global rows (all rows when
     ``rows`` is None); lse is the natural log-sum-exp of the (capped) logits.
+    ``mask``: packed custom-mask bytes (request b's [qo_len, kv_len] boolean matrix,
+    row-major, least significant bit first, requests back to back from bit 0), or None.
     """
     code = _dtype_code(q, dtype)
     qa, kv = _u16(q), _u16(kv_data)
@@ -190,6 +192,16 @@ def attention(q, kv_data, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, *,
     else:
         row_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         n = row_arr.size
+    mask_arr = None
+    if mask is not None:
+        if hasattr(mask, "detach"):
+            mask = mask.detach().cpu().numpy()
+        mask_arr = np.ascontiguousarray(np.asarray(mask).view(np.uint8).reshape(-1))
+        kv_lens = [((int(indptr[b + 1]) - int(indptr[b])) - 1) * page_size + int(last[b])
+                   if indptr[b + 1] > indptr[b] else 0 for b in range(batch)]
+        bits = sum((int(qo[b + 1]) - int(qo[b])) * kv_lens[b] for b in range(batch))
+        if mask_arr.size * 8 < bits:
+            raise ValueError(f"mask holds {mask_arr.size * 8} bits, the batch needs {bits}")
     o = np.empty((n, hq, d), dtype=np.float64)
     lse = np.empty((n, hq), dtype=np.float64)
     st = _load().pkv_oracle_attention(
@@ -197,6 +209,7 @@ def attention(q, kv_data, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, *,
         _ptr(qo, ctypes.c_int32), _ptr(kv, ctypes.c_uint16), num_pages,
         _ptr(indptr, ctypes.c_int32), _ptr(indices, ctypes.c_int32), _ptr(last, ctypes.c_int32),
         int(bool(causal)), float(sm_scale), float(logits_cap),
+        None if mask_arr is None else mask_arr.ctypes.data_as(ctypes.c_void_p),
         None if row_arr is None else _ptr(row_arr, ctypes.c_int64), n,
         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double), int(threads))
     if st != 0:
@@ -204,11 +217,11 @@ def attention(q, kv_data, qo_indptr, kv_indptr, kv_indices, kv_last_page_len, *,
     return o, lse
 
 
-def attention_of(batch, rows=None, threads: int = 0):
+def attention_of(batch, rows=None, threads: int = 0, mask=None):
     """``attention`` on a workload object with the fields of a paged batch."""
     return attention(batch.q, batch.kv_data, batch.qo_indptr, batch.kv_indptr, batch.kv_indices,
                      batch.kv_last_page_len, sm_scale=batch.sm_scale, causal=batch.causal,
-                     logits_cap=batch.logits_cap, rows=rows, threads=threads)
+                     logits_cap=batch.logits_cap, rows=rows, threads=threads, mask=mask)
 
 
 def merge_states(os_, lses) -> Tuple[np.ndarray, np.ndarray]:

@@ -19,6 +19,12 @@
  *  - Causal prefill ("The Interface", causal=True): row i of a request with
  *    qo_len rows and kv_len keys may see keys t <= i + kv_len - qo_len
  *    (the mask aligned to the end of the KV sequence).
+ *  - Custom mask (the mask a variant supplies, fdeinterviews "Customizable
+ *    attention"; token trees of speculative decoding, greptalks "Radix Tree /
+ *    Token Tree"): request b's boolean matrix [qo_len, kv_len], row-major,
+ *    packed one bit per entry (least significant bit first in each byte),
+ *    the requests back to back from bit 0; row i sees key t only if its bit
+ *    is 1, in addition to the causal rule.
  *  - merge_state (guide section 3, "Cascade Attention" and "FlashDecoding"):
  *    states (o_i, lse_i) over disjoint key sets combine as
  *    lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.
@@ -155,8 +161,8 @@ int pkv_oracle_attention(int batch, int num_qo_heads, int num_kv_heads, int head
                          const int32_t* qo_indptr, const uint16_t* kv_data, int64_t num_pages,
                          const int32_t* kv_indptr, const int32_t* kv_indices,
                          const int32_t* kv_last_page_len, int causal, double sm_scale,
-                         double logits_cap, const int64_t* rows, int64_t n_rows, double* o,
-                         double* lse, int num_threads) {
+                         double logits_cap, const uint8_t* mask, const int64_t* rows, int64_t n_rows,
+                         double* o, double* lse, int num_threads) {
     paged_kv c = {batch, num_qo_heads, num_kv_heads, head_dim, page_size, dtype, kv_data,
                   num_pages, kv_indptr, kv_indices, kv_last_page_len};
     int st = check_table(&c);
@@ -174,6 +180,15 @@ int pkv_oracle_attention(int batch, int num_qo_heads, int num_kv_heads, int head
     }
     const int group = num_qo_heads / num_kv_heads;
     const int64_t jobs = n_out * num_qo_heads;
+    /* first bit of each request's mask block */
+    int64_t* mask_off = NULL;
+    if (mask) {
+        mask_off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(batch + 1));
+        if (!mask_off) return ORACLE_NO_MEM;
+        mask_off[0] = 0;
+        for (int b = 0; b < batch; ++b)
+            mask_off[b + 1] = mask_off[b] + ((int64_t)qo_indptr[b + 1] - qo_indptr[b]) * kv_len_of(&c, b);
+    }
     int failed = 0;
 #ifdef _OPENMP
     if (num_threads <= 0) num_threads = omp_get_max_threads();
@@ -208,13 +223,17 @@ int pkv_oracle_attention(int batch, int num_qo_heads, int num_kv_heads, int head
                 for (int k = 0; k < head_dim; ++k) qv[k] = decode(qr[k], dtype);
                 double* orow = o + (out_row * num_qo_heads + h) * head_dim;
                 double* lrow = lse + out_row * num_qo_heads + h;
-                if (visible == 0) {
-                    for (int k = 0; k < head_dim; ++k) orow[k] = 0.0;
-                    *lrow = -INFINITY;
-                    continue;
-                }
+                int64_t n_seen = 0;
                 double mx = -INFINITY;
                 for (int64_t t = 0; t < visible; ++t) {
+                    if (mask) {
+                        int64_t bit = mask_off[b] + i * kv_len + t;
+                        if (!((mask[bit >> 3] >> (bit & 7)) & 1)) {
+                            s[t] = -INFINITY;
+                            continue;
+                        }
+                    }
+                    ++n_seen;
                     const uint16_t* kr = token_row(&c, b, t, 0, kvh);
                     double dot = 0.0;
                     for (int k = 0; k < head_dim; ++k) dot += qv[k] * decode(kr[k], dtype);
@@ -223,11 +242,18 @@ int pkv_oracle_attention(int batch, int num_qo_heads, int num_kv_heads, int head
                     s[t] = logit;
                     if (logit > mx) mx = logit;
                 }
+                if (n_seen == 0) {
+                    for (int k = 0; k < head_dim; ++k) orow[k] = 0.0;
+                    *lrow = -INFINITY;
+                    continue;
+                }
                 double sum = 0.0;
-                for (int64_t t = 0; t < visible; ++t) sum += exp(s[t] - mx);
+                for (int64_t t = 0; t < visible; ++t)
+                    if (s[t] != -INFINITY) sum += exp(s[t] - mx);
                 double l = mx + log(sum);
                 for (int k = 0; k < head_dim; ++k) acc[k] = 0.0;
                 for (int64_t t = 0; t < visible; ++t) {
+                    if (s[t] == -INFINITY) continue;
                     double w = exp(s[t] - l);
                     const uint16_t* vr = token_row(&c, b, t, 1, kvh);
                     for (int k = 0; k < head_dim; ++k) acc[k] += w * decode(vr[k], dtype);
@@ -240,6 +266,7 @@ int pkv_oracle_attention(int batch, int num_qo_heads, int num_kv_heads, int head
         free(qv);
         free(acc);
     }
+    free(mask_off);
     return failed ? ORACLE_NO_MEM : ORACLE_OK;
 }
 

@@ -57,6 +57,7 @@ EXPORTS = [
     "pkv_plan_workspace_bytes", "pkv_plan_compute", "pkv_plan_run", "pkv_plan_get_info", "pkv_plan_get_work",
     "pkv_batch_decode_paged", "pkv_batch_prefill_paged", "pkv_merge_state", "pkv_get_device_error",
     "pkv_plan_set_timing_events", "pkv_batch_decode_paged_noalloc", "pkv_append_paged_kv",
+    "pkv_batch_prefill_paged_masked",
 ]
 
 
@@ -92,6 +93,7 @@ def load(path: Optional[str] = None):
             "pkv_get_device_error": (i32, [vp, vp, ctypes.POINTER(i32), i32, vp]),
             "pkv_plan_set_timing_events": (i32, [vp, vp, vp]),
             "pkv_batch_decode_paged_noalloc": (i32, [vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "pkv_batch_prefill_paged_masked": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
             "pkv_append_paged_kv": (i32, [ctypes.POINTER(Params), i32, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
                                           vp, ctypes.c_double, vp, vp]),
         }
@@ -234,6 +236,16 @@ def batch_prefill_paged(h, q, qo_indptr, kv_data, kv_indices, kv_indptr, kv_last
                                           _ptr(dev_ws), _stream(stream)), "pkv_batch_prefill_paged")
 
 
+def batch_prefill_paged_masked(h, q, qo_indptr, kv_data, kv_indices, kv_indptr, kv_last_page_len, packed_mask,
+                               o, lse, dev_ws, stream=None) -> None:
+    """Prefill with a packed custom mask (uint8 device tensor, whole 32-bit words)."""
+    _check(load().pkv_batch_prefill_paged_masked(h, _ptr(q), _ptr(qo_indptr), _ptr(kv_data), _ptr(kv_indices),
+                                                 _ptr(kv_indptr), _ptr(kv_last_page_len), _ptr(packed_mask),
+                                                 packed_mask.numel() * packed_mask.element_size(), _ptr(o),
+                                                 _ptr(lse), _ptr(dev_ws), _stream(stream)),
+           "pkv_batch_prefill_paged_masked")
+
+
 def merge_state(o_a, lse_a, o_b, lse_b, o_out, lse_out=None, stream=None) -> None:
     """merge_state over [n_rows, num_heads, head_dim] states (dtype fp16/bf16/fp32)."""
     if o_a.dim() != 3:
@@ -318,8 +330,13 @@ class Plan:
         self.num_pages = int(num_pages)
 
     def run(self, q, kv_data, kv_indices, kv_indptr, kv_last_page_len, o, lse=None, *, qo_indptr=None,
-            stream=None) -> None:
-        if self.kind == PLAN_DECODE:
+            mask=None, stream=None) -> None:
+        if mask is not None:
+            if self.kind != PLAN_PREFILL:
+                raise ValueError("a custom mask needs a prefill plan")
+            batch_prefill_paged_masked(self.handle, q, qo_indptr, kv_data, kv_indices, kv_indptr, kv_last_page_len,
+                                       mask, o, lse, self.dev_ws, stream)
+        elif self.kind == PLAN_DECODE:
             batch_decode_paged(self.handle, q, kv_data, kv_indices, kv_indptr, kv_last_page_len, o, lse,
                                self.dev_ws, stream)
         else:

@@ -125,11 +125,16 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
   return PKV_OK;
 }
 
-pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
-                                   const void* kv_data, const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
-                                   const int32_t* kv_last_page_len_d, void* o, float* lse, void* dev_ws,
-                                   void* stream) {
+static pkv_status prefill_run(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d, const void* kv_data,
+                              const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
+                              const int32_t* kv_last_page_len_d, const uint8_t* mask, size_t mask_bytes, void* o,
+                              float* lse, void* dev_ws, void* stream) {
   if (!plan || plan->kind != PKV_PLAN_PREFILL || !plan->planned) return PKV_ERR_INVALID_ARG;
+  if (mask) {
+    // whole 32-bit words covering every request's [qo_len, kv_len] block
+    if (!aligned(mask, 4) || mask_bytes / 4 < static_cast<size_t>((plan->mask_bits + 31) / 32))
+      return PKV_ERR_INVALID_ARG;
+  }
   if (!q || !qo_indptr_d || !kv_data || !kv_indices_d || !kv_indptr_d || !kv_last_page_len_d || !o || !dev_ws)
     return PKV_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_data, 16) || !aligned(o, 16) || !aligned(dev_ws, 256) ||
@@ -155,6 +160,8 @@ pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const in
   const bool cap = p.logits_cap > 0.f;
   a.sm_scale = p.sm_scale;
   a.cap = cap ? p.logits_cap : 0.f;
+  a.mask = reinterpret_cast<const uint32_t*>(mask);
+  a.mask_words = mask ? static_cast<int64_t>(mask_bytes / 4) : 0;
   auto s = static_cast<cudaStream_t>(stream);
   if (plan->time_start) cudaEventRecord(plan->time_start, s);
   cudaError_t e = pkv::launch_prefill(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas,
@@ -167,6 +174,24 @@ pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const in
     return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
   }
   return PKV_OK;
+}
+
+pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
+                                   const void* kv_data, const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
+                                   const int32_t* kv_last_page_len_d, void* o, float* lse, void* dev_ws,
+                                   void* stream) {
+  return prefill_run(plan, q, qo_indptr_d, kv_data, kv_indices_d, kv_indptr_d, kv_last_page_len_d, nullptr, 0, o, lse,
+                     dev_ws, stream);
+}
+
+pkv_status pkv_batch_prefill_paged_masked(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
+                                          const void* kv_data, const int32_t* kv_indices_d,
+                                          const int32_t* kv_indptr_d, const int32_t* kv_last_page_len_d,
+                                          const uint8_t* packed_mask_d, size_t mask_bytes, void* o, float* lse,
+                                          void* dev_ws, void* stream) {
+  if (!packed_mask_d) return PKV_ERR_INVALID_ARG;
+  return prefill_run(plan, q, qo_indptr_d, kv_data, kv_indices_d, kv_indptr_d, kv_last_page_len_d, packed_mask_d,
+                     mask_bytes, o, lse, dev_ws, stream);
 }
 
 pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o_out,

@@ -76,8 +76,8 @@ struct alignas(64) PrefillTile {
   int32_t idx_base;    // kv_indptr[b]
   int32_t last_rows;   // kv_last_page_len[b]
   int32_t slot;        // partial slot or -1
-  int32_t merge_row;   // unused by the kernel; keeps the record 64 bytes
-  int32_t pad[3];
+  int32_t pad[2];
+  int64_t mask_off;    // bit offset of the request's [qo_len, kv_len] custom-mask block
 };
 static_assert(sizeof(PrefillTile) == 64, "PrefillTile layout");
 

@@ -89,6 +89,8 @@ struct PrefillArgs {
   int causal;
   float sm_scale;
   float cap;                   // > 0 only in the capped instantiation
+  const uint32_t* mask;        // packed custom mask (bit k of word w = bit 32 w + k), or nullptr
+  int64_t mask_words;          // 32-bit words of the mask buffer
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dtype, bool cap, int grid,

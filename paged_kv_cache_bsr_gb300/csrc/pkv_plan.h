@@ -31,6 +31,7 @@ struct pkv_plan {
   int batch = 0;
   int64_t num_pages = 0;
   int64_t total_q = 0;
+  int64_t mask_bits = 0;    // prefill: sum over requests of qo_len * kv_len (custom-mask size)
   int active_workers = 0;
   int num_work = 0;
   int num_merge = 0;

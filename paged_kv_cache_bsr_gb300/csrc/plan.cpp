@@ -280,6 +280,12 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   };
   std::vector<Tile> tiles;
   int64_t total = 0;
+  // Request b's custom-mask block starts at bit sum over b' < b of qo_len * kv_len.
+  std::vector<int64_t> mask_off(batch + 1, 0);
+  for (int b = 0; b < batch; ++b)
+    mask_off[b + 1] = mask_off[b] + static_cast<int64_t>(qo_indptr[b + 1] - qo_indptr[b]) *
+                                        kv_len_of(kv_indptr, kv_last, b, P);
+  pl->mask_bits = mask_off[batch];
   for (int b = 0; b < batch; ++b) {
     const int qo = qo_indptr[b + 1] - qo_indptr[b];
     const int kv = static_cast<int>(kv_len_of(kv_indptr, kv_last, b, P));
@@ -305,6 +311,7 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
     pt.kv_len = t.kv;
     pt.idx_base = kv_indptr[t.b];
     pt.last_rows = kv_last[t.b];
+    pt.mask_off = mask_off[t.b];
     const int64_t nb = ceil_div(t.kv_end, BN);
     if (nb <= chunk) {
       pt.kv_begin = 0;

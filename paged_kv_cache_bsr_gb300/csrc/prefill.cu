@@ -1,554 +1,21 @@
-// prefill.cu -- causal ragged batch prefill over a paged KV cache on tcgen05.
-//
-// Method (FlashInfer pages): batch_prefill with causal=True over the same
-// page table as decode ("FlashInfer" guide, "The Interface"); the kernel
-// gathers scattered pages into contiguous shared memory before using tensor
-// cores (fdeinterviews, "One format for every KV layout"); query heads that
-// share a kv head are packed into one row block (greptalks, "Head Group
-// Packing"); with causal off and every request's query in one row block it is
-// the shared-prefix half of cascade attention (guide section 3, "Cascade
-// Attention"; fdeinterviews, composable formats with a large row block).
-//
-// GB300 design.  One CTA per SM walks the plan's list of work tiles.  A work
-// tile is 256 packed query rows (256/G query positions x the G heads of one
-// kv head) held as two 128-row UMMA tiles, A and B, against one key range
-// visited 128 keys (128/P pages) at a time; every K/V block that lands in
-// shared memory serves both tiles.
-//   warps 0, 10 producers: TMA loads the two Q boxes once per tile and, per
-//               key block, one 64-column box per (page, half) for K (warp 0,
-//               three stages) and for V (warp 10, two stages), 128B-swizzled.
-//               Pages past the request come from an out-of-range page
-//               coordinate, which TMA fills with zeros; V rows past
-//               kv_last_page_len of the last page are zeroed before the MMA
-//               may read them.
-//   warp 1      one thread issues the tcgen05 MMAs, alternating the tiles:
-//               P_A V -> O_A, S_A(next) = Q_A K^T, P_B V -> O_B, S_B(next).
-//               S, P and O stay in tensor memory: S_A, S_B, O_A, O_B take the
-//               512 columns, and each P (bf16/fp16) overwrites the first 64
-//               columns of its S, the A operand of its P V MMA.
-//   warps 2-5   softmax of tile A, warps 6-9 of tile B (two warps per
-//               scheduler, so one group's softmax overlaps the other group's
-//               MMAs): thread = query row = TMEM lane.  Each reads its S row,
-//               scales (and soft-caps), masks, keeps a running max and sum,
-//               writes P back to tensor memory and rescales O only when the
-//               max grows by more than 2^8.  The epilogue divides O by the sum
-//               and writes o and the natural-log lse (or an fp32 partial state
-//               when the plan split the key range).
-// Every wait is bounded; a wait that runs out records kErrWaitTimeout and
-// makes all roles leave their loops, the MMA thread waits for its issued
-// MMAs, and tensor memory is released.
-#include <cuda.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
-#include <math.h>
-
-#include <mutex>
-#include <type_traits>
-
-#include "pkv_bsr.h"
-#include "pkv_device.cuh"
-#include "pkv_launch.h"
+// prefill.cu -- causal ragged batch prefill over a paged KV cache: host launch
+// code, the merge of split key ranges, and the kernel instances without a
+// custom mask (the kernel itself is in prefill_kernel.cuh).
+#include "prefill_kernel.cuh"
 
 namespace pkv {
+namespace prefill_impl {
+
+template cudaError_t launch_kernel<__nv_bfloat16, false>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
+                                                        const CUtensorMap&, cudaStream_t);
+template cudaError_t launch_kernel<__half, false>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
+                                                 const CUtensorMap&, cudaStream_t);
+
+}  // namespace prefill_impl
+
+using namespace prefill_impl;
+
 namespace {
-
-constexpr unsigned kFull = 0xffffffffu;
-constexpr int kD = 128;                 // head_dim of the prefill kernel
-constexpr int kTM = 128;                // rows of one UMMA tile
-constexpr int kWR = kPrefillRows;       // rows of a work tile: two UMMA tiles
-static_assert(kWR == 2 * kTM, "a work tile is two UMMA tiles");
-constexpr int kBN = kPrefillKeys;       // keys per block
-constexpr int kThreads = 352;           // K producer, MMA, 2 x 4 softmax warps, V producer
-constexpr int kVWarp = 10;
-constexpr uint32_t kTile = 32768;       // 128 rows x 128 16-bit values
-constexpr uint32_t kHalf = 16384;       // one 64-column half of a tile
-constexpr int kKStages = 2;             // K has its own producer: two blocks of lead cover the gather
-constexpr int kVStages = 2;
-// Shared-memory map; dynamic shared memory must start 1024-aligned (checked).
-// The staging area gives each softmax warp 4 KB to turn its 32 rows into
-// row-contiguous global stores in the epilogue.
-constexpr uint32_t kOffQ = 0, kOffK = 2 * kTile, kOffV = kOffK + kKStages * kTile,
-                   kOffStage = kOffV + kVStages * kTile, kOffBar = kOffStage + 8 * 4096;
-constexpr int kSmemBytes = kOffBar + 256;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-enum { Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages,
-       V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, P_FULL = S_FULL + 2, O_DONE = P_FULL + 2,
-       O_FREE = O_DONE + 2, V_LOAD = O_FREE + 2, DRAIN = V_LOAD + kVStages, NUM_BARS = DRAIN + 1 };
-static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
-constexpr uint32_t kGroupThreads = 128;  // softmax threads of one tile
-constexpr uint32_t kTmemCols = 512;      // S_A, S_B, O_A, O_B
-constexpr uint32_t kColS = 0, kColO = 256;
-
-struct Waiter {
-  int32_t* err;
-  volatile int* abort_flag;
-  // Bounded wait; false when it ran out (recorded) or another role gave up.
-  __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        atomicOr(err, kErrWaitTimeout);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-    return true;
-  }
-};
-
-__device__ __forceinline__ int ceil_div_i(int a, int b) { return a <= 0 ? 0 : (a + b - 1) / b; }
-
-// D[tmem] (+)= A * B with both shared-memory descriptors given as their low
-// words and a common high word (every descriptor here has the same stride
-// field, version and swizzle), so issuing an MMA costs two 32-bit adds in the
-// caller.  In the TS form the A operand is read from tensor memory (K-major,
-// 16-bit pairs per 32-bit column, even k in the low half).
-template <bool ACC>
-__device__ __forceinline__ void umma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .b64 da, db;\n\tmov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, %5;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC ? 1 : 0)
-      : "memory");
-}
-template <bool ACC>
-__device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi, uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .b64 db;\n\tmov.b64 db, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, %5;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC ? 1 : 0)
-      : "memory");
-}
-
-template <int G, typename T, bool CAP>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
-                   const __grid_constant__ CUtensorMap tkv) {
-  constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-  constexpr int MP = kTM / G;  // query positions per UMMA tile
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* sm = smem_raw;
-  const uint32_t base = smem_addr(sm);
-  if (base & 1023u) {  // never expected; refuse rather than misread swizzled tiles
-    if (threadIdx.x == 0) atomicOr(a.err, kErrTmemAlloc);
-    return;
-  }
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS + 1);
-  auto bar = [&](int i) { return base + kOffBar + 8u * i; };
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NUM_BARS; ++i)
-      mbar_init(bar(i), (i == P_FULL || i == P_FULL + 1 || i == O_FREE || i == O_FREE + 1) ? kGroupThreads : 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const Waiter wait{a.err, abort_flag};
-
-  const PlanHeader* hdr = a.hdr;
-  int t_begin = 0, t_end = 0;
-  if (static_cast<int>(blockIdx.x) < hdr->num_workers) {
-    t_begin = a.worker_ptr[blockIdx.x];
-    t_end = a.worker_ptr[blockIdx.x + 1];
-  }
-  const int num_pages = static_cast<int>(hdr->num_pages);
-  const int P = a.page_size;
-  const int ppt = kBN / P;  // pages per key block
-
-  auto page_of = [&](const PrefillTile& t, int j, int n_pages_req) {
-    const int rel = (t.kv_begin + j * kBN) / P + lane;
-    int id = num_pages;  // past the pool: TMA fills the box with zeros
-    if (lane < ppt && rel < n_pages_req) {
-      const int v = __ldg(a.kv_indices + t.idx_base + rel);
-      if (v >= 0 && v < num_pages)
-        id = v;
-      else
-        atomicOr(a.err, kErrPageIndex);
-    }
-    return id;
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ Q and K producer
-    int kvc = 0;
-    bool ok = true;
-    for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
-      const PrefillTile t = a.tiles[ti];
-      if (tn > 0) {
-        ok = __all_sync(kFull, wait(bar(Q_EMPTY), (tn - 1) & 1));
-        if (!ok) break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(Q_FULL), 2 * kTile);
-        for (int x = 0; x < 2; ++x)
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(base + kOffQ + x * kTile + h * kHalf, &tq, h * 64, t.kvh * G, t.q_row0 + x * MP,
-                        bar(Q_FULL));
-      }
-      const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
-      const int n_pages_req = ceil_div_i(t.kv_len, P);
-      int id_next = n > 0 ? page_of(t, 0, n_pages_req) : num_pages;
-      for (int j = 0; j < n; ++j) {
-        const int id = id_next;
-        if (j + 1 < n) id_next = page_of(t, j + 1, n_pages_req);  // next block's page ids load meanwhile
-        const int s = kvc % kKStages;
-        if (kvc >= kKStages) {
-          ok = __all_sync(kFull, wait(bar(K_EMPTY + s), ((kvc / kKStages) - 1) & 1));
-          if (!ok) break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL + s), kTile);
-        __syncwarp();
-        const uint32_t sK = base + kOffK + s * kTile;
-        if (lane < ppt)
-          for (int h = 0; h < 2; ++h)
-            tma_load_5d(sK + h * kHalf + lane * P * 128, &tkv, h * 64, 0, t.kvh, 0, id, bar(K_FULL + s));
-        ++kvc;
-      }
-    }
-  } else if (warp == kVWarp) {
-    // ------------------------------------------------------------ V producer
-    int kvc = 0;
-    uint32_t vload_bits = 0;  // phase parity of each V_LOAD barrier
-    bool ok = true;
-    for (int ti = t_begin; ti < t_end && ok; ++ti) {
-      const PrefillTile t = a.tiles[ti];
-      const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
-      const int n_pages_req = ceil_div_i(t.kv_len, P);
-      int id_next = n > 0 ? page_of(t, 0, n_pages_req) : num_pages;
-      for (int j = 0; j < n; ++j) {
-        const int id = id_next;
-        if (j + 1 < n) id_next = page_of(t, j + 1, n_pages_req);
-        const int s = kvc % kVStages;
-        if (kvc >= kVStages) {
-          ok = __all_sync(kFull, wait(bar(V_EMPTY + s), ((kvc / kVStages) - 1) & 1));
-          if (!ok) break;
-        }
-        const uint32_t sV = base + kOffV + s * kTile;
-        const int rel0 = (t.kv_begin + j * kBN) / P;
-        const int last_rel = n_pages_req - 1 - rel0;
-        const bool partial = t.last_rows < P && last_rel >= 0 && last_rel < ppt;
-        const uint32_t vbar = partial ? bar(V_LOAD + s) : bar(V_FULL + s);
-        if (lane == 0) mbar_arrive_expect_tx(vbar, kTile);
-        __syncwarp();
-        if (lane < ppt)
-          for (int h = 0; h < 2; ++h) tma_load_5d(sV + h * kHalf + lane * P * 128, &tkv, h * 64, 0, t.kvh, 1, id, vbar);
-        if (partial) {
-          // The last page's slots past kv_last_page_len may hold anything; the
-          // P V product must see zeros there (0 * NaN would poison O).
-          ok = __all_sync(kFull, wait(bar(V_LOAD + s), (vload_bits >> s) & 1));
-          if (!ok) break;
-          vload_bits ^= 1u << s;
-          const int chunks = (P - t.last_rows) * 8;  // 16-byte chunks per half
-          uint8_t* vgen = sm + kOffV + s * kTile;
-          for (int i = lane; i < 2 * chunks; i += 32) {
-            const int h = i / chunks, c = i % chunks;
-            *reinterpret_cast<uint4*>(vgen + h * kHalf + (last_rel * P + t.last_rows) * 128 + c * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(V_FULL + s));
-        }
-        ++kvc;
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t id_s = umma_idesc_f16(kFmt, kTM, kBN, 0);
-      const uint32_t id_o = umma_idesc_f16(kFmt, kTM, kD, 1);
-      int kvc = 0;
-      int pc[2] = {0, 0}, ofree[2] = {0, 0};
-      bool o_used[2] = {false, false};  // an earlier tile accumulated into O_x
-      bool ok = true;
-      // Descriptors are built once; a K step or a stage only adds to the start
-      // address field of the low word (addresses stay below 2^18, so no carry
-      // leaves it), and all of them share one high word.  Issuing an MMA then
-      // takes a few instructions, well under the 64 cycles an M=128, N=128, K=16
-      // MMA runs, even while this warp shares its scheduler with softmax warps.
-      const uint64_t dq = sw128_desc(base + kOffQ, 16, 1024);
-      const uint64_t dk = sw128_desc(base + kOffK, 16, 1024);
-      const uint64_t dv = sw128_desc(base + kOffV, kHalf, 1024);
-      const uint32_t hi = static_cast<uint32_t>(dq >> 32);
-      const uint32_t q_lo = static_cast<uint32_t>(dq), k_lo = static_cast<uint32_t>(dk),
-                     v_lo = static_cast<uint32_t>(dv);
-      constexpr uint32_t kTile16 = kTile >> 4, kHalf16 = kHalf >> 4;
-      // S_x = Q_x K_c^T into tensor memory.
-      auto mma_s = [&](int x, int c) {
-        const uint32_t a0 = q_lo + x * kTile16;
-        const uint32_t b0 = k_lo + (c % kKStages) * kTile16;
-        const uint32_t d = tmem + kColS + x * kTM;
-        umma_ss_lo<false>(d, a0, b0, hi, id_s);
-#pragma unroll
-        for (int kk = 1; kk < kD / 16; ++kk) {
-          const uint32_t koff = (kk / 4) * kHalf16 + (kk % 4) * 2;
-          umma_ss_lo<true>(d, a0 + koff, b0 + koff, hi, id_s);
-        }
-        umma_commit(bar(S_FULL + x));
-      };
-      // O_x += P_x V_c, P_x from tensor memory; the tile's last one signals the epilogue.
-      auto mma_pv = [&](int x, int c, bool acc, bool last) {
-        const uint32_t b0 = v_lo + (c % kVStages) * kTile16;
-        const uint32_t d = tmem + kColO + x * kTM, p = tmem + kColS + x * kTM;
-        if (acc)
-          umma_ts_lo<true>(d, p, b0, hi, id_o);
-        else
-          umma_ts_lo<false>(d, p, b0, hi, id_o);
-#pragma unroll
-        for (int kk = 1; kk < kBN / 16; ++kk) umma_ts_lo<true>(d, p + kk * 8, b0 + kk * (2048 >> 4), hi, id_o);
-        if (last) umma_commit(bar(O_DONE + x));
-      };
-      for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
-        const PrefillTile t = a.tiles[ti];
-        const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
-        if (!(ok = wait(bar(Q_FULL), tn & 1))) break;
-        tc_fence_after();
-        if (n == 0) {
-          umma_commit(bar(Q_EMPTY));
-          continue;
-        }
-        if (!(ok = wait(bar(K_FULL + kvc % kKStages), (kvc / kKStages) & 1))) break;
-        tc_fence_after();
-        mma_s(0, kvc);
-        mma_s(1, kvc);
-        umma_commit(bar(K_EMPTY + kvc % kKStages));
-        if (n == 1) umma_commit(bar(Q_EMPTY));
-        for (int j = 0; j < n && ok; ++j) {
-          const int c = kvc + j;
-          for (int x = 0; x < 2 && ok; ++x) {
-            if (!(ok = wait(bar(P_FULL + x), pc[x] & 1))) break;
-            ++pc[x];
-            if (j == 0 && o_used[x]) {  // the previous tile's epilogue has read O_x
-              if (!(ok = wait(bar(O_FREE + x), ofree[x] & 1))) break;
-              ++ofree[x];
-            }
-            if (x == 0 && !(ok = wait(bar(V_FULL + c % kVStages), (c / kVStages) & 1))) break;
-            tc_fence_after();
-            mma_pv(x, c, j > 0, j == n - 1);
-            o_used[x] = true;
-            if (x == 1) umma_commit(bar(V_EMPTY + c % kVStages));  // both P V of block c issued
-            if (j + 1 < n) {
-              if (x == 0) {
-                if (!(ok = wait(bar(K_FULL + (c + 1) % kKStages), ((c + 1) / kKStages) & 1))) break;
-                tc_fence_after();
-              }
-              mma_s(x, c + 1);
-              if (x == 1) {
-                umma_commit(bar(K_EMPTY + (c + 1) % kKStages));  // both S of block c + 1 issued
-                if (j + 1 == n - 1) umma_commit(bar(Q_EMPTY));
-              }
-            }
-          }
-        }
-        kvc += n;
-      }
-      // Every MMA issued so far must finish before tensor memory is released.
-      umma_commit(bar(DRAIN));
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(bar(DRAIN), 0))
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-          atomicOr(a.err, kErrWaitTimeout);
-          break;
-        }
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int x = (warp - 2) >> 2;           // UMMA tile of this warp group
-    const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int r = quarter * 32 + lane;       // row within the UMMA tile
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t col_s = tmem + lane_off + kColS + x * kTM;
-    const uint32_t col_o = tmem + lane_off + kColO + x * kTM;
-    const float scale = CAP ? a.sm_scale : a.sm_scale * kLog2e;
-    int sc = 0, odc = 0;
-    bool ok = true;
-    for (int ti = t_begin; ti < t_end && ok; ++ti) {
-      const PrefillTile t = a.tiles[ti];
-      const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
-      const int rpos = x * MP + r / G;     // position of this row within the work tile
-      const bool row_valid = rpos < t.n_pos;
-      const int pos = t.q_pos0 + rpos;
-      int limit = t.kv_len, lim0 = t.kv_len;  // keys < limit are visible to this row / to every row of x
-      if (a.causal) {
-        limit = min(limit, pos + 1 + t.kv_len - t.qo_len);
-        lim0 = min(lim0, t.q_pos0 + x * MP + 1 + t.kv_len - t.qo_len);
-      }
-      limit = min(limit, t.kv_end);
-      lim0 = min(lim0, t.kv_end);
-      float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < n; ++j) {
-        if (!(ok = __all_sync(kFull, wait(bar(S_FULL + x), sc & 1)))) break;
-        ++sc;
-        tc_fence_after();
-        const int key0 = t.kv_begin + j * kBN;
-        const bool full = key0 + kBN <= lim0;
-        uint32_t sr[kBN];
-        tmem_ld128_sync(col_s, sr);
-        // Logits in log2 units are v * mul (the cap, when on, is applied to v first).
-        float mul = scale;
-        if constexpr (CAP) {
-#pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            sr[i] = __float_as_uint(a.cap * tanhf(__uint_as_float(sr[i]) * scale / a.cap) * kLog2e);
-          mul = 1.f;
-        }
-        if (!full) {
-#pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            if (key0 + i >= limit) sr[i] = 0xff800000u;  // -inf
-        }
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(sr[k]);
-#pragma unroll
-        for (int i = 8; i < kBN; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * mul;
-        const float m_new = fmaxf(m_ref, mx);
-        const bool resc = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new > m_ref + 8.f);
-        float alpha = 1.f;
-        if (resc) {
-          alpha = fast_exp2(m_ref - m_new);
-          m_ref = m_new;
-          l *= alpha;
-        }
-        const float sub = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // p = 2^(v * mul - sub): packed FMAs and the SFU exponential (the SFU has
-        // room at this rate: two tiles' rows share it with the tensor pipe's time);
-        // packed in place to 16-bit pairs.
-        const float2 mul2 = make_float2(mul, mul), nsub2 = make_float2(-sub, -sub);
-        float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int i = 0; i < kBN; i += 2) {
-          float2 v = ffma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), mul2, nsub2);
-          v.x = fast_exp2(v.x);
-          v.y = fast_exp2(v.y);
-          sum4[(i >> 1) & 3] = fadd2(sum4[(i >> 1) & 3], v);
-          sr[i >> 1] = pack2<T>(v.x, v.y);
-        }
-        const float2 s4 = fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3]));
-        l += s4.x + s4.y;
-        // P over the first 64 columns of this tile's S (already read).
-        tmem_st32(col_s, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_st32(col_s + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-        if (j >= 1) {
-          // P V of the previous block was issued before this S, so the S_FULL
-          // wait above already covers it: O is complete and can be rescaled
-          // before the next P V adds to it.
-          if (__any_sync(kFull, resc)) {
-#pragma unroll
-            for (int c = 0; c < kD / 32; ++c) {
-              uint32_t rr[32];
-              tmem_ld32_sync(col_o + c * 32, rr);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-              tmem_st32(col_o + c * 32, rr);
-            }
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(P_FULL + x));
-      }
-      if (!ok) break;
-      if (n >= 1) {
-        if (!(ok = __all_sync(kFull, wait(bar(O_DONE + x), odc & 1)))) break;
-        ++odc;
-        tc_fence_after();
-      }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse_v = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-      const int64_t orow = static_cast<int64_t>(t.q_row0 + rpos) * a.num_qo_heads + t.kvh * G + (r % G);
-      const int srow = x * kTM + r;  // row of the work tile, for a partial-state slot
-      if (t.slot < 0) {
-        // Final output: through this warp's staging slab, half a row (64 values) per pass,
-        // so each store instruction writes four whole 128-byte row segments.
-        uint8_t* stg = sm + kOffStage + (warp - 2) * 4096;
-#pragma unroll
-        for (int hp = 0; hp < 2; ++hp) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t rr[32];
-            if (n >= 1) {
-              tmem_ld32_sync(col_o + (hp * 2 + cc) * 32, rr);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) rr[i] = 0u;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[cc * 16 + i] = pack2<T>(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
-                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int rr_ = it * 4 + (lane >> 3), piece = lane & 7;  // a row of this warp, a 16-byte piece
-            const int r2 = quarter * 32 + rr_;
-            const int rpos2 = x * MP + r2 / G;
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + rr_ * 128 + ((piece ^ (rr_ & 7)) << 4));
-            if (rpos2 < t.n_pos) {
-              const int64_t orow2 =
-                  static_cast<int64_t>(t.q_row0 + rpos2) * a.num_qo_heads + t.kvh * G + (r2 % G);
-              reinterpret_cast<uint4*>(static_cast<T*>(a.o) + orow2 * kD + hp * 64)[piece] = v;
-            }
-          }
-          __syncwarp();
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
-          float ov[32];
-          if (n >= 1) {
-            uint32_t rr[32];
-            tmem_ld32_sync(col_o + c * 32, rr);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(rr[i]) * inv;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = 0.f;
-          }
-          float4* dst =
-              reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(t.slot) * kWR + srow) * kD + c * 32);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) dst[q] = make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
-        }
-      }
-      if (t.slot < 0) {
-        if (row_valid && a.lse) a.lse[orow] = lse_v;
-      } else {
-        a.part_lse[static_cast<int64_t>(t.slot) * kWR + srow] = lse_v;
-      }
-      if (n >= 1) {  // this tile's O is free for the next tile's P V
-        tc_fence_before();
-        mbar_arrive(bar(O_FREE + x));
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-}
 
 // Rows of query tiles whose key range the plan split: one warp per packed row,
 // lanes over head_dim, log-sum-exp merge of the chunks' fp32 partial states.
@@ -607,25 +74,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <typename T>
-cudaError_t launch_t(const PrefillArgs& a, int G, bool cap, int grid, const CUtensorMap& tq, const CUtensorMap& tkv,
-                     cudaStream_t s) {
-  void (*kern)(PrefillArgs, CUtensorMap, CUtensorMap) = nullptr;
-#define PKV_PF_CASE(GG)                                                                      \
-  case GG:                                                                                   \
-    kern = cap ? prefill_kernel<GG, T, true> : prefill_kernel<GG, T, false>;                 \
-    break;
-  switch (G) {
-    PKV_PF_CASE(1) PKV_PF_CASE(2) PKV_PF_CASE(4) PKV_PF_CASE(8)
-    default: return cudaErrorInvalidValue;
-  }
-#undef PKV_PF_CASE
-  cudaError_t e = ensure_smem_limit(kern, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, kSmemBytes, s>>>(a, tq, tkv);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 bool prefill_supported(int head_dim, int group, int dtype, int page_size) {
@@ -664,8 +112,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dt
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  if (dtype == PKV_BF16) return launch_t<__nv_bfloat16>(a, group, cap, grid, tq, tkv, stream);
-  return launch_t<__half>(a, group, cap, grid, tq, tkv, stream);
+  const bool masked = a.mask != nullptr;
+  if (dtype == PKV_BF16)
+    return masked ? launch_kernel<__nv_bfloat16, true>(a, group, cap, grid, tq, tkv, stream)
+                  : launch_kernel<__nv_bfloat16, false>(a, group, cap, grid, tq, tkv, stream);
+  return masked ? launch_kernel<__half, true>(a, group, cap, grid, tq, tkv, stream)
+                : launch_kernel<__half, false>(a, group, cap, grid, tq, tkv, stream);
 }
 
 cudaError_t launch_prefill_merge(const PrefillArgs& a, int head_dim, int group, int dtype, int grid,

@@ -62,7 +62,10 @@ def decode(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None) -> Tup
     return o, lse
 
 
-def prefill(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+def prefill(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None,
+            mask: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Batch prefill; ``mask`` is an optional packed custom mask on the device
+    (``workloads.pack_mask`` layout), applied on top of the batch's causal flag."""
     b = db.host
     if plan is None:
         plan = make_plan(b, api.PLAN_PREFILL)
@@ -70,7 +73,7 @@ def prefill(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None) -> Tu
     o = torch.empty_like(db.q)
     lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.q.device)
     plan.run(db.q, db.kv_data, db.kv_indices, db.kv_indptr, db.kv_last_page_len, o, lse,
-             qo_indptr=db.qo_indptr, stream=stream)
+             qo_indptr=db.qo_indptr, mask=mask, stream=stream)
     return o, lse
 
 

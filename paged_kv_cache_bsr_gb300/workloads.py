@@ -39,6 +39,9 @@ __all__ = [
     "MultiLevelBatch",
     "parallel_generation",
     "new_kv_rows",
+    "pack_mask",
+    "TreeBatch",
+    "tree_verify",
     "WORKLOADS",
 ]
 
@@ -426,6 +429,61 @@ def new_kv_rows(b: PagedBatch, seed: int = 7) -> "tuple[torch.Tensor, torch.Tens
     return _randn(shape, gen, b.dtype), _randn(shape, gen, b.dtype)
 
 
+def pack_mask(matrices: Sequence) -> torch.Tensor:
+    """Pack per-request boolean masks [qo_len_b, kv_len_b] into the custom-mask format:
+    row-major, requests back to back from bit 0, least significant bit first in each
+    byte, zero-padded to whole 32-bit words.  Returns a uint8 tensor."""
+    import numpy as np
+    flat = [np.asarray(m, dtype=bool).reshape(-1) for m in matrices]
+    bits = np.concatenate(flat) if flat else np.zeros(0, dtype=bool)
+    packed = np.packbits(bits, bitorder="little")
+    pad = (-packed.size) % 4
+    if pad or packed.size == 0:
+        packed = np.concatenate([packed, np.zeros(pad if packed.size else 4, dtype=np.uint8)])
+    return torch.from_numpy(packed.copy())
+
+
+@dataclasses.dataclass
+class TreeBatch:
+    """Tree verification for speculative decoding: each request's draft tree nodes are
+    its query rows and its last keys; ``mask`` lets node i see the cached prefix and
+    its own ancestors (and itself)."""
+
+    batch: PagedBatch
+    mask: torch.Tensor            # packed, see pack_mask
+    parents: List[List[int]]      # parents[b][i] < i, -1 for the root
+    prefix_lens: List[int]
+    matrices: list                # the unpacked boolean masks, [qo_len, kv_len] each
+
+
+def tree_verify(seed: int = 1006, batch: int = 16, prefix_lo: int = 512, prefix_hi: int = 4096,
+                nodes: int = 64, num_qo_heads: int = 32, num_kv_heads: int = 8, head_dim: int = 128,
+                page_size: int = 16, dtype: torch.dtype = torch.bfloat16, poison: bool = False) -> TreeBatch:
+    """Speculative-decoding tree verification: ``batch`` requests, each with a cached
+    prefix of U[prefix_lo, prefix_hi] tokens and a draft tree of ``nodes`` tokens whose
+    parent pointers are drawn uniformly among the earlier nodes (node 0 is the root).
+    The tree's tokens are the query rows and the request's last ``nodes`` keys."""
+    import numpy as np
+    gen = _gen(seed)
+    prefix = _uniform_ints(prefix_lo, prefix_hi, batch, gen)
+    parents, mats = [], []
+    for b in range(batch):
+        par = [-1] + [int(torch.randint(0, i, (1,), generator=gen)) for i in range(1, nodes)]
+        m = np.zeros((nodes, prefix[b] + nodes), dtype=bool)
+        m[:, :prefix[b]] = True
+        for i in range(nodes):
+            j = i
+            while j >= 0:
+                m[i, prefix[b] + j] = True
+                j = par[j]
+        parents.append(par)
+        mats.append(m)
+    pb = make_paged_batch(qo_lens=[nodes] * batch, kv_lens=[p + nodes for p in prefix], num_qo_heads=num_qo_heads,
+                          num_kv_heads=num_kv_heads, head_dim=head_dim, page_size=page_size, dtype=dtype,
+                          seed=seed + 1, causal=False, poison=poison, name="tree_verify")
+    return TreeBatch(batch=pb, mask=pack_mask(mats), parents=parents, prefix_lens=prefix, matrices=mats)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama3_8b_decode": llama3_decode,
@@ -433,4 +491,5 @@ WORKLOADS = {
     "ragged_causal_prefill": ragged_prefill,
     "cascade_softcap_decode": cascade_decode,
     "parallel_generation": parallel_generation,
+    "tree_verify": tree_verify,
 }

@@ -50,8 +50,9 @@ def _scatter_to_pool(ks, vs, page_size, num_pages, gen, dtype, poison=True):
             torch.tensor(indices, dtype=torch.int32), torch.tensor(last, dtype=torch.int32))
 
 
-def _sdpa_reference(q, ks, vs, qo_lens, scale, causal):
-    """torch SDPA in fp64 on contiguous K/V, one request at a time (GQA by repetition)."""
+def _sdpa_reference(q, ks, vs, qo_lens, scale, causal, masks=None):
+    """torch SDPA in fp64 on contiguous K/V, one request at a time (GQA by repetition);
+    ``masks``: optional boolean [qo_len, kv_len] per request, AND-ed with the causal rule."""
     hq = q.shape[1]
     outs = []
     row = 0
@@ -66,6 +67,8 @@ def _sdpa_reference(q, ks, vs, qo_lens, scale, causal):
             i = torch.arange(n_q)[:, None]
             j = torch.arange(kv_len)[None, :]
             mask = j <= i + (kv_len - n_q)
+        if masks is not None:
+            mask = mask & torch.as_tensor(masks[len(outs)], dtype=torch.bool)
         o = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=scale)
         outs.append(o.permute(1, 0, 2))
         row += n_q
@@ -515,3 +518,99 @@ def test_encode16_rounds_to_nearest_even():
     # fp16: 1 + 2^-11 halfway -> 1, 2049 -> 2048 (ties to even), nan stays nan
     assert oracle.encode16(np.array([1 + 2.0 ** -11, 2049.0]), "f16").tolist() == [1.0, 2048.0]
     assert np.isnan(oracle.encode16(np.array([np.nan]), "bf16")[0])
+
+
+# --------------------------------------------------------------------------- custom (tree) masks
+def _random_masks(rng, qo_lens, kv_lens, causal, p=0.6):
+    """Random boolean masks in which every row keeps at least one key the causal rule allows."""
+    out = []
+    for n_q, kv in zip(qo_lens, kv_lens):
+        m = rng.random((n_q, kv)) < p
+        for i in range(n_q):
+            m[i, i + kv - n_q if causal else rng.integers(0, kv)] = True
+        out.append(m)
+    return out
+
+
+@pytest.mark.parametrize("qo_lens,kv_lens,hq,hkv,P,causal", [
+    ([3, 5, 1], [7, 40, 9], 4, 2, 4, False),
+    ([6, 2], [6, 19], 2, 1, 1, True),       # page size 1 (column vectors), causal AND mask
+    ([9], [33], 4, 4, 16, False),
+])
+def test_custom_mask_matches_sdpa_with_boolean_mask(qo_lens, kv_lens, hq, hkv, P, causal):
+    """The packed mask (least significant bit first, requests back to back) selects
+    exactly the keys a boolean attn_mask selects in torch SDPA."""
+    q, ks, vs, pool, qo_indptr, indptr, indices, last = _random_case(
+        31 + sum(kv_lens), qo_lens, kv_lens, hq, hkv, 16, P, torch.bfloat16)
+    masks = _random_masks(np.random.default_rng(len(qo_lens)), qo_lens, kv_lens, causal)
+    packed = W.pack_mask(masks)
+    assert packed.numel() % 4 == 0
+    o, lse = oracle.attention(q, pool, qo_indptr, indptr, indices, last, sm_scale=0.25, causal=causal, mask=packed)
+    ref = _sdpa_reference(q, ks, vs, qo_lens, 0.25, causal, masks=masks)
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+    # the mask changes the result: dropping it gives something else
+    o2, _ = oracle.attention(q, pool, qo_indptr, indptr, indices, last, sm_scale=0.25, causal=causal)
+    assert np.abs(o2 - o).max() > 1e-3
+
+
+def test_mask_of_ones_is_no_mask_and_lower_triangle_is_causal():
+    qo_lens, kv_lens = [4, 7], [10, 7]
+    q, ks, vs, pool, qo_indptr, indptr, indices, last = _random_case(5, qo_lens, kv_lens, 4, 2, 16, 4,
+                                                                      torch.float16)
+    ones = W.pack_mask([np.ones((a, b), bool) for a, b in zip(qo_lens, kv_lens)])
+    tri = W.pack_mask([np.arange(b)[None, :] <= np.arange(a)[:, None] + (b - a) for a, b in zip(qo_lens, kv_lens)])
+    args = (q, pool, qo_indptr, indptr, indices, last)
+    plain = oracle.attention(*args, sm_scale=0.3)
+    causal = oracle.attention(*args, sm_scale=0.3, causal=True)
+    for got, ref in ((oracle.attention(*args, sm_scale=0.3, mask=ones), plain),
+                     (oracle.attention(*args, sm_scale=0.3, mask=tri), causal)):
+        np.testing.assert_array_equal(got[0], ref[0])
+        np.testing.assert_array_equal(got[1], ref[1])
+
+
+def test_row_with_every_key_masked_gives_zero_and_minus_inf():
+    qo_lens, kv_lens = [3], [9]
+    q, ks, vs, pool, qo_indptr, indptr, indices, last = _random_case(6, qo_lens, kv_lens, 2, 2, 8, 4,
+                                                                      torch.bfloat16)
+    m = np.ones((3, 9), bool)
+    m[1] = False
+    o, lse = oracle.attention(q, pool, qo_indptr, indptr, indices, last, sm_scale=0.3, mask=W.pack_mask([m]))
+    assert np.all(o[1] == 0) and np.all(np.isneginf(lse[1]))
+    assert np.all(np.isfinite(lse[[0, 2]]))
+
+
+def test_pack_mask_bit_order():
+    """Bit k of byte j is entry 8 j + k (least significant first); requests follow
+    each other with no padding; the buffer is padded to whole 32-bit words."""
+    m1 = np.zeros((1, 3), bool)
+    m1[0, 1] = True                      # entry 1
+    m2 = np.zeros((2, 4), bool)
+    m2[1, 2] = True                      # entry 3 + 4 + 2 = 9
+    packed = W.pack_mask([m1, m2]).numpy()
+    assert packed.tolist() == [0b10, 0b10, 0, 0]
+    np.testing.assert_array_equal(np.unpackbits(packed, bitorder="little")[:11],
+                                  np.concatenate([m1.reshape(-1), m2.reshape(-1)]))
+
+
+def test_tree_verify_mask_is_prefix_plus_ancestors():
+    """Tree verification: node i sees the whole prefix and exactly its ancestors and
+    itself; against SDPA with the same boolean masks; a chain tree is causal."""
+    tb = W.tree_verify(seed=3, batch=3, prefix_lo=5, prefix_hi=30, nodes=9, num_qo_heads=4, num_kv_heads=2,
+                       head_dim=16, page_size=4, poison=True)
+    for par, pre, m in zip(tb.parents, tb.prefix_lens, tb.matrices):
+        for i in range(len(par)):
+            anc = {i}
+            j = par[i]
+            while j >= 0:
+                anc.add(j)
+                j = par[j]
+            assert m[i, :pre].all()
+            assert set(np.nonzero(m[i, pre:])[0].tolist()) == anc
+    o, _ = oracle.attention_of(tb.batch, mask=tb.mask)
+    assert np.isfinite(o).all()
+    chain = [np.arange(p + 9)[None, :] <= np.arange(9)[:, None] + p for p in tb.prefix_lens]
+    oc, lc = oracle.attention_of(tb.batch, mask=W.pack_mask(chain))
+    causal = W.PagedBatch(**{**tb.batch.__dict__, "causal": True})
+    ocr, lcr = oracle.attention_of(causal)
+    np.testing.assert_array_equal(oc, ocr)
+    np.testing.assert_array_equal(lc, lcr)
