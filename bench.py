@@ -48,7 +48,7 @@ def parse_args():
     p.add_argument("--no-secondary", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
-    p.add_argument("--only", choices=["prefill", "cascade", "multilevel", "append", "skewed"], default=None,
+    p.add_argument("--only", choices=["prefill", "cascade", "multilevel", "append", "tree", "skewed"], default=None,
                    help="time one secondary measurement alone (for profiling) and print it")
     return p.parse_args()
 
@@ -327,10 +327,10 @@ def decode_e2e(b, steps):
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
 
 
-def prefill_measure(peaks, steps=20, warmup=3):
+def prefill_measure(peaks, steps=20, warmup=3, page_size=16):
     import torch
     from paged_kv_cache_bsr_gb300 import runner, api, workloads as W
-    b = W.ragged_prefill(seed=1003)
+    b = W.ragged_prefill(seed=1003, page_size=page_size)
     try:
         plan = runner.make_plan(b, api.PLAN_PREFILL)
     except api.PkvError as e:
@@ -348,6 +348,9 @@ def prefill_measure(peaks, steps=20, warmup=3):
 
     total_ms, kern_ms = time_steps(step, steps, warmup, torch.cuda.current_stream(), kernel_events=True)
     plan.set_timing_events(None, None)
+    err = plan.device_error()
+    if err:
+        return {"workload": "ragged_causal_prefill", "page_size": page_size, "error": f"device error word {err}"}
     pairs = 0
     for qo, kv in zip(b.qo_lens, b.kv_lens):
         pre = kv - qo
@@ -355,12 +358,51 @@ def prefill_measure(peaks, steps=20, warmup=3):
     flops = pairs * b.num_qo_heads * 4 * b.head_dim
     ms = total_ms / steps
     achieved = flops / (kern_ms * 1e-3) / 1e12
-    traffic = recorded_traffic("prefill_kernel_ragged_causal_prefill.txt", source_hash("prefill.cu"))
-    return {"workload": "ragged_causal_prefill", "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    traffic = recorded_traffic("prefill_kernel_ragged_causal_prefill.txt", source_hash("prefill_kernel.cuh"))
+    traffic = traffic if page_size == 16 else None
+    return {"workload": "ragged_causal_prefill", "page_size": page_size,
+            "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "kernel_ms": round(kern_ms, 4), "flops": flops,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
                          "peak_source": peaks["source"], "kernel": "prefill_kernel"}}
+
+
+def tree_measure(peaks, steps=20, warmup=3):
+    """Speculative-decoding tree verification: 16 requests, prefix U[512, 4096], 64-node
+    draft trees, custom-mask prefill; TFLOP/s over the query-key pairs the mask keeps."""
+    import torch
+    from paged_kv_cache_bsr_gb300 import runner, api, workloads as W
+    tb = W.tree_verify(seed=1006)
+    b = tb.batch
+    plan = runner.make_plan(b, api.PLAN_PREFILL)
+    db = runner.DeviceBatch.from_host(b)
+    mask = tb.mask.cuda()
+    o = torch.empty_like(db.q)
+    lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.q.device)
+    runner.plan_batch(plan, b)
+
+    def step(ev):
+        if ev is not None:
+            plan.set_timing_events(*ev)
+        plan.run(db.q, db.kv_data, db.kv_indices, db.kv_indptr, db.kv_last_page_len, o, lse,
+                 qo_indptr=db.qo_indptr, mask=mask)
+
+    total_ms, kern_ms = time_steps(step, steps, warmup, torch.cuda.current_stream(), kernel_events=True)
+    plan.set_timing_events(None, None)
+    err = plan.device_error()
+    if err:
+        return {"workload": "tree_verify", "error": f"device error word {err}"}
+    pairs = int(sum(int(m.sum()) for m in tb.matrices))
+    flops = pairs * b.num_qo_heads * 4 * b.head_dim
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    kv_bytes = b.kv_bytes()
+    return {"workload": "tree_verify", "requests": b.batch, "nodes": 64, "kernel_ms": round(kern_ms, 4),
+            "ms_per_step": round(total_ms / steps, 4), "TFLOPs": round(achieved, 1),
+            "tensor_frac": round(achieved / peaks["bf16_tflops"], 4),
+            "kv_GBps": round(kv_bytes / (kern_ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(kv_bytes / (kern_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "note": "64 query rows x 4 heads per kv head: one 256-row tile per (request, kv head); KV-read bound"}
 
 
 def graph_us(fn, s, steps, warmup):
@@ -537,6 +579,9 @@ def run_only(args):
         res = multilevel_measure(steps=args.steps, warmup=args.warmup)
     elif args.only == "append":
         res = append_measure(peaks, steps=args.steps, warmup=args.warmup)
+    elif args.only == "tree":
+        res = {"tree": tree_measure(peaks, steps=args.steps, warmup=args.warmup),
+               "page_size_1": prefill_measure(peaks, steps=args.steps, warmup=args.warmup, page_size=1)}
     else:
         r = decode_measure(W.skewed_decode(seed=1002), args.steps, args.warmup, peaks)
         res = {"value": round(r["value"], 1), "unit": "GB/s", "roofline": r["roofline"]}
@@ -599,6 +644,8 @@ def run_own(args):
             secondary["cascade"] = cascade_measure()
             secondary["multilevel_cascade"] = multilevel_measure()
             secondary["append_rope"] = append_measure(peaks)
+            secondary["tree_verify"] = tree_measure(peaks)
+            secondary["prefill_page_size_1"] = prefill_measure(peaks, page_size=1)
     clocks.stop()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,

@@ -209,6 +209,9 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
  * Batch prefill over the paged KV cache ("The Interface", step 2), ragged
  * query rows given by qo_indptr_d, causal per params->causal, computed with
  * tcgen05 tensor-core MMAs (bf16 and fp16) and fp32 TMEM accumulators.
+ * Built for head_dim 128, groups 1/2/4/8 and page sizes 1, 2, 4, 8, 16, 32,
+ * 64 and 128 (pages of 1-4 rows, the column-vector BSR of sparse patterns,
+ * are gathered row by row; larger pages by one tensor copy per page).
  * q and o: [total_q, Hq, d]; lse: [total_q, Hq] fp32 (may be NULL).
  * With causal = 0 and one request whose rows are many requests' queries, this
  * is the shared-prefix half of cascade attention.  The kernel's TMA tensor maps

@@ -1,15 +1,16 @@
 // prefill.cu -- causal ragged batch prefill over a paged KV cache: host launch
-// code, the merge of split key ranges, and the kernel instances without a
-// custom mask (the kernel itself is in prefill_kernel.cuh).
+// code, the merge of split key ranges, and the kernel instances for pages of 8
+// rows or more without a custom mask (the kernel itself is in
+// prefill_kernel.cuh).
 #include "prefill_kernel.cuh"
 
 namespace pkv {
 namespace prefill_impl {
 
-template cudaError_t launch_kernel<__nv_bfloat16, false>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
+template cudaError_t launch_kernel<__nv_bfloat16, false, false>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
+                                                               const CUtensorMap&, cudaStream_t);
+template cudaError_t launch_kernel<__half, false, false>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
                                                         const CUtensorMap&, cudaStream_t);
-template cudaError_t launch_kernel<__half, false>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
-                                                 const CUtensorMap&, cudaStream_t);
 
 }  // namespace prefill_impl
 
@@ -79,7 +80,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool prefill_supported(int head_dim, int group, int dtype, int page_size) {
   return head_dim == kD && (group == 1 || group == 2 || group == 4 || group == 8) &&
          (dtype == PKV_F16 || dtype == PKV_BF16) &&
-         (page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64 || page_size == 128);
+         (page_size == 1 || page_size == 2 || page_size == 4 || page_size == 8 || page_size == 16 ||
+          page_size == 32 || page_size == 64 || page_size == 128);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dtype, bool cap, int grid,
@@ -112,12 +114,16 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dt
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const bool masked = a.mask != nullptr;
+  const bool masked = a.mask != nullptr, small = a.page_size < 8;
+  using L = cudaError_t (*)(const PrefillArgs&, int, bool, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+  L fn;
   if (dtype == PKV_BF16)
-    return masked ? launch_kernel<__nv_bfloat16, true>(a, group, cap, grid, tq, tkv, stream)
-                  : launch_kernel<__nv_bfloat16, false>(a, group, cap, grid, tq, tkv, stream);
-  return masked ? launch_kernel<__half, true>(a, group, cap, grid, tq, tkv, stream)
-                : launch_kernel<__half, false>(a, group, cap, grid, tq, tkv, stream);
+    fn = masked ? (small ? launch_kernel<__nv_bfloat16, true, true> : launch_kernel<__nv_bfloat16, true, false>)
+                : (small ? launch_kernel<__nv_bfloat16, false, true> : launch_kernel<__nv_bfloat16, false, false>);
+  else
+    fn = masked ? (small ? launch_kernel<__half, true, true> : launch_kernel<__half, true, false>)
+                : (small ? launch_kernel<__half, false, true> : launch_kernel<__half, false, false>);
+  return fn(a, group, cap, grid, tq, tkv, stream);
 }
 
 cudaError_t launch_prefill_merge(const PrefillArgs& a, int head_dim, int group, int dtype, int grid,

@@ -24,7 +24,12 @@
 //               Pages past the request come from an out-of-range page
 //               coordinate, which TMA fills with zeros; V rows past
 //               kv_last_page_len of the last page are zeroed before the MMA
-//               may read them.
+//               may read them.  Pages of 1, 2 or 4 rows (column-vector BSR)
+//               are gathered instead with 16-byte cp.async, half a warp per
+//               256-byte row, into the same swizzled layout, zero-filled past
+//               the request; a block's barrier is signalled once the producer
+//               has issued the next block of the same tile (or finished the
+//               tile) and its own copies have landed.
 //   warp 1      one thread issues the tcgen05 MMAs, alternating the tiles:
 //               P_A V -> O_A, S_A(next) = Q_A K^T, P_B V -> O_B, S_B(next).
 //               S, P and O stay in tensor memory: S_A, S_B, O_A, O_B take the
@@ -75,10 +80,13 @@ constexpr int kVStages = 2;
 // Shared-memory map; dynamic shared memory must start 1024-aligned (checked).
 // The staging area gives each softmax warp 4 KB to turn its 32 rows into
 // row-contiguous global stores in the epilogue.
+// The two page-id arrays serve the cp.async gather of pages smaller than 8 rows
+// (only those instances reserve them).
 constexpr uint32_t kOffQ = 0, kOffK = 2 * kTile, kOffV = kOffK + kKStages * kTile,
-                   kOffStage = kOffV + kVStages * kTile, kOffBar = kOffStage + 8 * 4096;
+                   kOffStage = kOffV + kVStages * kTile, kOffBar = kOffStage + 8 * 4096, kOffIds = kOffBar + 256;
 constexpr int kSmemBytes = kOffBar + 256;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr int kSmemBytesSmall = kOffIds + 2 * kBN * 4;
+static_assert(kSmemBytesSmall <= 232448, "shared memory budget");
 enum { Q_FULL = 0, Q_EMPTY = 1, K_FULL = 2, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages,
        V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, P_FULL = S_FULL + 2, O_DONE = P_FULL + 2,
        O_FREE = O_DONE + 2, V_LOAD = O_FREE + 2, DRAIN = V_LOAD + kVStages, NUM_BARS = DRAIN + 1 };
@@ -130,7 +138,9 @@ __device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
-template <int G, typename T, bool CAP, bool MASK>
+// SMALL: pages of fewer than 8 rows, gathered with cp.async (its own instance set,
+// so the tensor-copy path of larger pages carries none of that code).
+template <int G, typename T, bool CAP, bool MASK, bool SMALL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
                    const __grid_constant__ CUtensorMap tkv) {
@@ -149,9 +159,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return base + kOffBar + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  constexpr bool small = SMALL;  // cp.async gather: every producer lane arrives on the FULL barriers
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NUM_BARS; ++i)
-      mbar_init(bar(i), (i == P_FULL || i == P_FULL + 1 || i == O_FREE || i == O_FREE + 1) ? kGroupThreads : 1);
+    for (int i = 0; i < NUM_BARS; ++i) {
+      uint32_t count = 1;
+      if (i == P_FULL || i == P_FULL + 1 || i == O_FREE || i == O_FREE + 1) count = kGroupThreads;
+      if (small && ((i >= K_FULL && i < K_FULL + kKStages) || (i >= V_FULL && i < V_FULL + kVStages))) count = 32;
+      mbar_init(bar(i), count);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -188,9 +203,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     return id;
   };
 
+  // Pages smaller than 8 rows: copy block j's K (kv_sel 0) or V (1) rows of tile t
+  // into the swizzled stage at `dst` with cp.async, 16 bytes a lane, rows past the
+  // request zero-filled; commits one cp.async group.
+  auto gather_block = [&](const PrefillTile& t, int j, int kv_sel, uint32_t dst, int32_t* ids) {
+    const int key0 = t.kv_begin + j * kBN;
+    const int rel0 = key0 / P;
+    const int n_pages_req = ceil_div_i(t.kv_len, P);
+    for (int k = lane; k < ppt; k += 32) {
+      int id = -1;
+      if (rel0 + k < n_pages_req) {
+        const int v = __ldg(a.kv_indices + t.idx_base + rel0 + k);
+        if (v >= 0 && v < num_pages)
+          id = v;
+        else
+          atomicOr(a.err, kErrPageIndex);
+      }
+      ids[k] = id;
+    }
+    __syncwarp();
+    const int lp = __ffs(P) - 1;     // P is a power of two
+    const int c = lane & 15;         // 16-byte chunk of the 256-byte row
+    const uint32_t dst_c = dst + (c >> 3) * kHalf;
+    const int cc = c & 7;
+    const T* kvp = static_cast<const T*>(a.kv);
+    for (int i = 0; i < kBN / 2; ++i) {
+      const int r = 2 * i + (lane >> 4);
+      const int id = ids[r >> lp];
+      const bool valid = id >= 0 && key0 + r < t.kv_len;
+      const T* src = kvp;
+      if (valid)
+        src = kvp + ((((int64_t)id * 2 + kv_sel) * a.num_kv_heads + t.kvh) * P + (r & (P - 1))) * kD + c * 8;
+      cp_async_16(dst_c + r * 128 + ((cc ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+    }
+    cp_async_commit();
+    __syncwarp();  // every lane has read ids before the next block rewrites them
+  };
+  // Signal the FULL barrier of the block gathered before the one just issued, once
+  // this lane's copies of it have landed (at most one group left in flight).
+  auto gather_signal = [&](int full_bar, bool last) {
+    if (last)
+      cp_async_wait<0>();
+    else
+      cp_async_wait<1>();
+    fence_proxy_async_smem();
+    mbar_arrive(bar(full_bar));
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ Q and K producer
     int kvc = 0;
+    int pend = -1;  // cp.async gather: stage whose FULL barrier is still to be signalled
     bool ok = true;
     for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
       const PrefillTile t = a.tiles[ti];
@@ -207,14 +270,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
       const int n_pages_req = ceil_div_i(t.kv_len, P);
-      int id_next = n > 0 ? page_of(t, 0, n_pages_req) : num_pages;
+      int id_next = (n > 0 && !small) ? page_of(t, 0, n_pages_req) : num_pages;
       for (int j = 0; j < n; ++j) {
         const int id = id_next;
-        if (j + 1 < n) id_next = page_of(t, j + 1, n_pages_req);  // next block's page ids load meanwhile
+        if (j + 1 < n && !small) id_next = page_of(t, j + 1, n_pages_req);  // next block's page ids load meanwhile
         const int s = kvc % kKStages;
         if (kvc >= kKStages) {
           ok = __all_sync(kFull, wait(bar(K_EMPTY + s), ((kvc / kKStages) - 1) & 1));
           if (!ok) break;
+        }
+        if (small) {
+          gather_block(t, j, 0, base + kOffK + s * kTile, reinterpret_cast<int32_t*>(sm + kOffIds));
+          if (pend >= 0) gather_signal(K_FULL + pend, false);
+          pend = s;
+          ++kvc;
+          continue;
         }
         if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL + s), kTile);
         __syncwarp();
@@ -224,26 +294,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_5d(sK + h * kHalf + lane * P * 128, &tkv, h * 64, 0, t.kvh, 0, id, bar(K_FULL + s));
         ++kvc;
       }
+      // The tile's last block is signalled before the next tile's Q_EMPTY wait:
+      // Q_EMPTY needs the MMA to have issued that block's S, so holding the
+      // signal back until the next block would block both roles.
+      if (small && pend >= 0) {
+        gather_signal(K_FULL + pend, true);
+        pend = -1;
+      }
     }
+    if (small && pend >= 0) gather_signal(K_FULL + pend, true);
   } else if (warp == kVWarp) {
     // ------------------------------------------------------------ V producer
     int kvc = 0;
+    int pend = -1;            // cp.async gather: stage whose FULL barrier is still to be signalled
     uint32_t vload_bits = 0;  // phase parity of each V_LOAD barrier
     bool ok = true;
     for (int ti = t_begin; ti < t_end && ok; ++ti) {
       const PrefillTile t = a.tiles[ti];
       const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
       const int n_pages_req = ceil_div_i(t.kv_len, P);
-      int id_next = n > 0 ? page_of(t, 0, n_pages_req) : num_pages;
+      int id_next = (n > 0 && !small) ? page_of(t, 0, n_pages_req) : num_pages;
       for (int j = 0; j < n; ++j) {
         const int id = id_next;
-        if (j + 1 < n) id_next = page_of(t, j + 1, n_pages_req);
+        if (j + 1 < n && !small) id_next = page_of(t, j + 1, n_pages_req);
         const int s = kvc % kVStages;
         if (kvc >= kVStages) {
           ok = __all_sync(kFull, wait(bar(V_EMPTY + s), ((kvc / kVStages) - 1) & 1));
           if (!ok) break;
         }
         const uint32_t sV = base + kOffV + s * kTile;
+        if (small) {
+          gather_block(t, j, 1, sV, reinterpret_cast<int32_t*>(sm + kOffIds) + kBN);
+          if (pend >= 0) gather_signal(V_FULL + pend, false);
+          pend = s;
+          ++kvc;
+          continue;
+        }
         const int rel0 = (t.kv_begin + j * kBN) / P;
         const int last_rel = n_pages_req - 1 - rel0;
         const bool partial = t.last_rows < P && last_rel >= 0 && last_rel < ppt;
@@ -271,7 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++kvc;
       }
+      if (small && pend >= 0) {  // the tile's last block does not wait for the next tile
+        gather_signal(V_FULL + pend, true);
+        pend = -1;
+      }
     }
+    if (small && pend >= 0) gather_signal(V_FULL + pend, true);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -582,34 +673,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
 // Launch one instance of the kernel (group size and cap chosen at run time).
-template <typename T, bool MASK>
+template <typename T, bool MASK, bool SMALL>
 cudaError_t launch_kernel(const PrefillArgs& a, int G, bool cap, int grid, const CUtensorMap& tq,
                           const CUtensorMap& tkv, cudaStream_t s) {
   void (*kern)(PrefillArgs, CUtensorMap, CUtensorMap) = nullptr;
-#define PKV_PF_CASE(GG)                                                                        \
-  case GG:                                                                                     \
-    kern = cap ? prefill_kernel<GG, T, true, MASK> : prefill_kernel<GG, T, false, MASK>;       \
+#define PKV_PF_CASE(GG)                                                                                \
+  case GG:                                                                                             \
+    kern = cap ? prefill_kernel<GG, T, true, MASK, SMALL> : prefill_kernel<GG, T, false, MASK, SMALL>; \
     break;
   switch (G) {
     PKV_PF_CASE(1) PKV_PF_CASE(2) PKV_PF_CASE(4) PKV_PF_CASE(8)
     default: return cudaErrorInvalidValue;
   }
 #undef PKV_PF_CASE
-  cudaError_t e = ensure_smem_limit(kern, kSmemBytes);
+  constexpr int smem = SMALL ? kSmemBytesSmall : kSmemBytes;
+  cudaError_t e = ensure_smem_limit(kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, kSmemBytes, s>>>(a, tq, tkv);
+  kern<<<grid, kThreads, smem, s>>>(a, tq, tkv);
   return cudaGetLastError();
 }
 
 // Each instance set is compiled in its own translation unit.
-extern template cudaError_t launch_kernel<__nv_bfloat16, false>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
-                                                               const CUtensorMap&, cudaStream_t);
-extern template cudaError_t launch_kernel<__half, false>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
-                                                        const CUtensorMap&, cudaStream_t);
-extern template cudaError_t launch_kernel<__nv_bfloat16, true>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
-                                                              const CUtensorMap&, cudaStream_t);
-extern template cudaError_t launch_kernel<__half, true>(const PrefillArgs&, int, bool, int, const CUtensorMap&,
-                                                       const CUtensorMap&, cudaStream_t);
+extern template cudaError_t launch_kernel<__nv_bfloat16, false, false>(const PrefillArgs&, int, bool, int,
+                                                     const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+extern template cudaError_t launch_kernel<__half, false, false>(const PrefillArgs&, int, bool, int,
+                                                     const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+extern template cudaError_t launch_kernel<__nv_bfloat16, false, true>(const PrefillArgs&, int, bool, int,
+                                                     const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+extern template cudaError_t launch_kernel<__half, false, true>(const PrefillArgs&, int, bool, int,
+                                                     const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+extern template cudaError_t launch_kernel<__nv_bfloat16, true, false>(const PrefillArgs&, int, bool, int,
+                                                     const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+extern template cudaError_t launch_kernel<__half, true, false>(const PrefillArgs&, int, bool, int,
+                                                     const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+extern template cudaError_t launch_kernel<__nv_bfloat16, true, true>(const PrefillArgs&, int, bool, int,
+                                                     const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+extern template cudaError_t launch_kernel<__half, true, true>(const PrefillArgs&, int, bool, int,
+                                                     const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 
 }  // namespace prefill_impl
 }  // namespace pkv

@@ -268,7 +268,7 @@ def skewed_decode(seed: int = 1002, long_len: int = 131072, short_len: int = 102
 
 def ragged_prefill(seed: int = 1003, batch: int = 16, qo_lo: int = 128, qo_hi: int = 2048,
                    prefix_lo: int = 0, prefix_hi: int = 1024, poison: bool = False,
-                   num_qo_heads: int = 32, num_kv_heads: int = 8) -> PagedBatch:
+                   num_qo_heads: int = 32, num_kv_heads: int = 8, page_size: int = 16) -> PagedBatch:
     """Ragged causal batch prefill: qo_len ~ U[128, 2048], kv_len = qo_len + prefix with
     prefix ~ U[0, 1024], 32 q / 8 kv heads, head_dim 128, page 16, bf16."""
     gen = _gen(seed)
@@ -276,7 +276,7 @@ def ragged_prefill(seed: int = 1003, batch: int = 16, qo_lo: int = 128, qo_hi: i
     prefix = _uniform_ints(prefix_lo, prefix_hi, batch, gen)
     kv_lens = [a + b for a, b in zip(qo_lens, prefix)]
     return make_paged_batch(qo_lens=qo_lens, kv_lens=kv_lens, num_qo_heads=num_qo_heads,
-                            num_kv_heads=num_kv_heads, head_dim=128, page_size=16,
+                            num_kv_heads=num_kv_heads, head_dim=128, page_size=page_size,
                             dtype=torch.bfloat16, seed=seed + 1, causal=True, poison=poison,
                             name="ragged_causal_prefill")
 

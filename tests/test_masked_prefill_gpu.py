@@ -132,3 +132,11 @@ def test_short_mask_is_rejected():
     short = torch.zeros(8, dtype=torch.uint8, device="cuda")  # 64 bits < 400
     with pytest.raises(api.PkvError):
         runner.prefill(db, plan, mask=short)
+
+
+def test_tree_verify_on_single_token_pages():
+    """Column-vector BSR (page size 1) with the tree mask: the tree's tokens and the
+    prefix are single-token pages scattered over the pool."""
+    tb = W.tree_verify(seed=8, batch=3, prefix_lo=50, prefix_hi=400, nodes=24, num_qo_heads=8, num_kv_heads=2,
+                       page_size=1, poison=True)
+    masked_vs_oracle(tb.batch, tb.matrices, "tree, page 1")

@@ -188,3 +188,27 @@ def test_prefill_cuda_graph_replay_after_replanning():
         ref_o, ref_lse = oracle.attention_of(b)
         assert_matches_oracle(o_buf, lse_buf, ref_o, ref_lse, torch.bfloat16, "prefill graph replay")
     assert plan.device_error() == 0
+
+
+@pytest.mark.parametrize("page_size", [1, 2, 4])
+def test_column_vector_pages(page_size):
+    """Pages of 1, 2 or 4 rows (column-vector BSR) take the row-gather path."""
+    prefill_vs_oracle(batch([90, 257, 1], [33, 5, 300], P=page_size, seed=20 + page_size), f"page {page_size}")
+
+
+def test_column_vector_pages_split_and_softcap():
+    b = W.make_paged_batch(qo_lens=[40], kv_lens=[5000], num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                           page_size=1, dtype=torch.float16, seed=24, causal=True, logits_cap=30.0, poison=True)
+    plan = prefill_vs_oracle(b, "page 1 split")
+    assert plan.info().num_merge > 0
+
+
+@pytest.mark.parametrize("page_size", [1, 4])
+def test_column_vector_pages_full_ragged_batch(page_size):
+    """The full ragged batch on 1- and 4-row pages: every CTA walks several tiles, so
+    each tile's last gathered block must be released before the next tile starts."""
+    b = W.ragged_prefill(seed=1003, poison=True, page_size=page_size)
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(b.total_q, size=1500, replace=False))
+    plan = prefill_vs_oracle(b, f"ragged full size, page {page_size}", rows=rows)
+    assert plan.info().active_workers > 0
