@@ -48,7 +48,7 @@ def parse_args():
     p.add_argument("--no-secondary", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
-    p.add_argument("--only", choices=["prefill", "cascade", "multilevel", "append", "tree", "skewed"], default=None,
+    p.add_argument("--only", choices=["prefill", "prefill1", "cascade", "multilevel", "append", "tree", "skewed"], default=None,
                    help="time one secondary measurement alone (for profiling) and print it")
     return p.parse_args()
 
@@ -573,6 +573,8 @@ def run_only(args):
     peaks = measured_peaks()
     if args.only == "prefill":
         res = prefill_measure(peaks, steps=args.steps, warmup=args.warmup)
+    elif args.only == "prefill1":
+        res = prefill_measure(peaks, steps=args.steps, warmup=args.warmup, page_size=1)
     elif args.only == "cascade":
         res = cascade_measure(steps=args.steps, warmup=args.warmup)
     elif args.only == "multilevel":

@@ -27,9 +27,9 @@
 //               may read them.  Pages of 1, 2 or 4 rows (column-vector BSR)
 //               are gathered instead with 16-byte cp.async, half a warp per
 //               256-byte row, into the same swizzled layout, zero-filled past
-//               the request; a block's barrier is signalled once the producer
-//               has issued the next block of the same tile (or finished the
-//               tile) and its own copies have landed.
+//               the request; each lane waits for its own copies, fences them
+//               for the tensor cores and arrives on the block's barrier, while
+//               the next block's page ids load.
 //   warp 1      one thread issues the tcgen05 MMAs, alternating the tiles:
 //               P_A V -> O_A, S_A(next) = Q_A K^T, P_B V -> O_B, S_B(next).
 //               S, P and O stay in tensor memory: S_A, S_B, O_A, O_B take the
@@ -203,24 +203,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     return id;
   };
 
-  // Pages smaller than 8 rows: copy block j's K (kv_sel 0) or V (1) rows of tile t
-  // into the swizzled stage at `dst` with cp.async, 16 bytes a lane, rows past the
-  // request zero-filled; commits one cp.async group.
-  auto gather_block = [&](const PrefillTile& t, int j, int kv_sel, uint32_t dst, int32_t* ids) {
-    const int key0 = t.kv_begin + j * kBN;
-    const int rel0 = key0 / P;
+  // Pages smaller than 8 rows.  gather_ids loads the page ids of block j of tile t
+  // (up to 128, four per lane; -1 past the request); gather_block copies that
+  // block's K (kv_sel 0) or V (1) rows into the swizzled stage at `dst` with
+  // cp.async, 16 bytes a lane and half a warp per 256-byte row, zero-filling rows
+  // past the request, waits for this lane's copies, fences them for the tensor
+  // cores and arrives on `full_bar`.  The caller loads the next block's ids in
+  // between (`next`), so their latency hides behind the copies.
+  auto gather_ids = [&](const PrefillTile& t, int j, int (&idr)[4]) {
+    const int rel0 = (t.kv_begin + j * kBN) / P;
     const int n_pages_req = ceil_div_i(t.kv_len, P);
-    for (int k = lane; k < ppt; k += 32) {
-      int id = -1;
-      if (rel0 + k < n_pages_req) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int k = lane + 32 * m;
+      idr[m] = -1;
+      if (k < ppt && rel0 + k < n_pages_req) {
         const int v = __ldg(a.kv_indices + t.idx_base + rel0 + k);
         if (v >= 0 && v < num_pages)
-          id = v;
+          idr[m] = v;
         else
           atomicOr(a.err, kErrPageIndex);
       }
-      ids[k] = id;
     }
+  };
+  auto gather_block = [&](const PrefillTile& t, int j, int kv_sel, uint32_t dst, int32_t* ids, const int (&idr)[4],
+                          int full_bar, auto&& next) {
+    const int key0 = t.kv_begin + j * kBN;
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      if (lane + 32 * m < ppt) ids[lane + 32 * m] = idr[m];
     __syncwarp();
     const int lp = __ffs(P) - 1;     // P is a power of two
     const int c = lane & 15;         // 16-byte chunk of the 256-byte row
@@ -237,23 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async_16(dst_c + r * 128 + ((cc ^ (r & 7)) << 4), src, valid ? 16u : 0u);
     }
     cp_async_commit();
-    __syncwarp();  // every lane has read ids before the next block rewrites them
-  };
-  // Signal the FULL barrier of the block gathered before the one just issued, once
-  // this lane's copies of it have landed (at most one group left in flight).
-  auto gather_signal = [&](int full_bar, bool last) {
-    if (last)
-      cp_async_wait<0>();
-    else
-      cp_async_wait<1>();
+    next();
+    cp_async_wait<0>();
     fence_proxy_async_smem();
     mbar_arrive(bar(full_bar));
+    __syncwarp();  // every lane has read ids before the next block rewrites them
   };
 
   if (warp == 0) {
     // ------------------------------------------------------------ Q and K producer
     int kvc = 0;
-    int pend = -1;  // cp.async gather: stage whose FULL barrier is still to be signalled
     bool ok = true;
     for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
       const PrefillTile t = a.tiles[ti];
@@ -271,6 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
       const int n_pages_req = ceil_div_i(t.kv_len, P);
       int id_next = (n > 0 && !small) ? page_of(t, 0, n_pages_req) : num_pages;
+      int idr[4] = {-1, -1, -1, -1};  // cp.async gather: page ids of the block being issued
+      if (small && n > 0) gather_ids(t, 0, idr);
       for (int j = 0; j < n; ++j) {
         const int id = id_next;
         if (j + 1 < n && !small) id_next = page_of(t, j + 1, n_pages_req);  // next block's page ids load meanwhile
@@ -279,10 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(kFull, wait(bar(K_EMPTY + s), ((kvc / kKStages) - 1) & 1));
           if (!ok) break;
         }
-        if (small) {
-          gather_block(t, j, 0, base + kOffK + s * kTile, reinterpret_cast<int32_t*>(sm + kOffIds));
-          if (pend >= 0) gather_signal(K_FULL + pend, false);
-          pend = s;
+        if constexpr (SMALL) {
+          int idn[4];
+          gather_block(t, j, 0, base + kOffK + s * kTile, reinterpret_cast<int32_t*>(sm + kOffIds), idr, K_FULL + s,
+                       [&] {
+                         if (j + 1 < n) gather_ids(t, j + 1, idn);
+                       });
+#pragma unroll
+          for (int m = 0; m < 4; ++m) idr[m] = idn[m];
           ++kvc;
           continue;
         }
@@ -294,19 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_5d(sK + h * kHalf + lane * P * 128, &tkv, h * 64, 0, t.kvh, 0, id, bar(K_FULL + s));
         ++kvc;
       }
-      // The tile's last block is signalled before the next tile's Q_EMPTY wait:
-      // Q_EMPTY needs the MMA to have issued that block's S, so holding the
-      // signal back until the next block would block both roles.
-      if (small && pend >= 0) {
-        gather_signal(K_FULL + pend, true);
-        pend = -1;
-      }
     }
-    if (small && pend >= 0) gather_signal(K_FULL + pend, true);
   } else if (warp == kVWarp) {
     // ------------------------------------------------------------ V producer
     int kvc = 0;
-    int pend = -1;            // cp.async gather: stage whose FULL barrier is still to be signalled
     uint32_t vload_bits = 0;  // phase parity of each V_LOAD barrier
     bool ok = true;
     for (int ti = t_begin; ti < t_end && ok; ++ti) {
@@ -314,6 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
       const int n_pages_req = ceil_div_i(t.kv_len, P);
       int id_next = (n > 0 && !small) ? page_of(t, 0, n_pages_req) : num_pages;
+      int idr[4] = {-1, -1, -1, -1};  // cp.async gather: page ids of the block being issued
+      if (small && n > 0) gather_ids(t, 0, idr);
       for (int j = 0; j < n; ++j) {
         const int id = id_next;
         if (j + 1 < n && !small) id_next = page_of(t, j + 1, n_pages_req);
@@ -323,10 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         const uint32_t sV = base + kOffV + s * kTile;
-        if (small) {
-          gather_block(t, j, 1, sV, reinterpret_cast<int32_t*>(sm + kOffIds) + kBN);
-          if (pend >= 0) gather_signal(V_FULL + pend, false);
-          pend = s;
+        if constexpr (SMALL) {
+          int idn[4];
+          gather_block(t, j, 1, sV, reinterpret_cast<int32_t*>(sm + kOffIds) + kBN, idr, V_FULL + s, [&] {
+            if (j + 1 < n) gather_ids(t, j + 1, idn);
+          });
+#pragma unroll
+          for (int m = 0; m < 4; ++m) idr[m] = idn[m];
           ++kvc;
           continue;
         }
@@ -357,12 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++kvc;
       }
-      if (small && pend >= 0) {  // the tile's last block does not wait for the next tile
-        gather_signal(V_FULL + pend, true);
-        pend = -1;
-      }
     }
-    if (small && pend >= 0) gather_signal(V_FULL + pend, true);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
