@@ -48,7 +48,7 @@ def parse_args():
     p.add_argument("--no-secondary", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
-    p.add_argument("--only", choices=["prefill", "prefill1", "cascade", "multilevel", "append", "tree", "skewed"], default=None,
+    p.add_argument("--only", choices=["prefill", "prefill1", "cascade", "multilevel", "mixed", "append", "tree", "skewed"], default=None,
                    help="time one secondary measurement alone (for profiling) and print it")
     return p.parse_args()
 
@@ -564,6 +564,56 @@ def append_measure(peaks, steps=50, warmup=5, per_graph=20):
     return out
 
 
+def mixed_measure(steps=50, warmup=5):
+    """A continuous-batching step of 60 decode requests and 4 prompt chunks: the mixed
+    plan (decode and prefill kernels side by side on an SM split) against the two
+    halves run back to back and against one prefill plan for every request (the
+    128-row tile for single-row requests too).  CUDA-graph replay of the run calls."""
+    import torch
+    from paged_kv_cache_bsr_gb300 import runner, api, workloads as W
+    b = W.mixed_batch(seed=1007)
+    dec = [r for r in range(b.batch) if b.qo_lens[r] == 1]
+    pre = [r for r in range(b.batch) if b.qo_lens[r] > 1]
+    bd, bp = W.sub_batch(b, dec), W.sub_batch(b, pre)
+    kv = b.kv_data.cuda()
+    db, dd, dp = (runner.DeviceBatch.from_host(x, kv_data=kv) for x in (b, bd, bp))
+    pm = runner.make_plan(b, api.PLAN_MIXED)
+    pd = runner.make_plan(bd, api.PLAN_DECODE)
+    pp = runner.make_plan(bp, api.PLAN_PREFILL)
+    pu = runner.make_plan(b, api.PLAN_PREFILL)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for plan, x in ((pm, b), (pd, bd), (pp, bp), (pu, b)):
+            runner.plan_batch(plan, x, stream=s)
+        outs = {k: (torch.empty_like(x.q), torch.empty(x.q.shape[:2], dtype=torch.float32, device="cuda"))
+                for k, x in (("m", db), ("d", dd), ("p", dp), ("u", db))}
+
+    def run(plan, x, k):
+        o, lse = outs[k]
+        plan.run(x.q, kv, x.kv_indices, x.kv_indptr, x.kv_last_page_len, o, lse, qo_indptr=x.qo_indptr, stream=s)
+
+    variants = (("mixed", lambda: run(pm, db, "m")),
+                ("sequential", lambda: (run(pd, dd, "d"), run(pp, dp, "p"))),
+                ("decode_half_alone", lambda: run(pd, dd, "d")),
+                ("prefill_half_alone", lambda: run(pp, dp, "p")),
+                ("one_prefill_plan", lambda: run(pu, db, "u")))
+    out = {"workload": "mixed_batch", "decode_requests": len(dec), "prefill_requests": len(pre),
+           "prefill_rows": bp.total_q}
+    for name, fn in variants:
+        with torch.cuda.stream(s):
+            fn()
+        s.synchronize()
+        out[name + "_us"] = graph_us(fn, s, steps, warmup)
+    info = pm.info()
+    out["prefill_ctas"], out["decode_ctas"] = info.prefill_ctas, info.decode_ctas
+    out["speedup_vs_sequential"] = round(out["sequential_us"] / out["mixed_us"], 3)
+    err = pm.device_error()
+    if err:
+        out["error"] = f"device error word {err}"
+    out["timing"] = "CUDA-graph replay of the run calls; plans made once outside the timed loop"
+    return out
+
+
 def run_only(args):
     import torch
     from paged_kv_cache_bsr_gb300 import build, api, workloads as W
@@ -579,6 +629,8 @@ def run_only(args):
         res = cascade_measure(steps=args.steps, warmup=args.warmup)
     elif args.only == "multilevel":
         res = multilevel_measure(steps=args.steps, warmup=args.warmup)
+    elif args.only == "mixed":
+        res = mixed_measure(steps=args.steps, warmup=args.warmup)
     elif args.only == "append":
         res = append_measure(peaks, steps=args.steps, warmup=args.warmup)
     elif args.only == "tree":
@@ -647,6 +699,7 @@ def run_own(args):
             secondary["multilevel_cascade"] = multilevel_measure()
             secondary["append_rope"] = append_measure(peaks)
             secondary["tree_verify"] = tree_measure(peaks)
+            secondary["mixed_batch"] = mixed_measure()
             secondary["prefill_page_size_1"] = prefill_measure(peaks, page_size=1)
     clocks.stop()
     line = {

@@ -64,7 +64,11 @@ typedef enum {
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
 
-typedef enum { PKV_PLAN_DECODE = 0, PKV_PLAN_PREFILL = 1 } pkv_plan_kind;
+/* DECODE: one query row per request (CUDA cores, split-KV).  PREFILL: ragged
+ * query rows (tcgen05 tensor cores).  MIXED: a batch holding both; requests with
+ * one query row take the decode path, longer ones the prefill path, and one run
+ * call launches both on disjoint SMs (see pkv_batch_mixed_paged). */
+typedef enum { PKV_PLAN_DECODE = 0, PKV_PLAN_PREFILL = 1, PKV_PLAN_MIXED = 2 } pkv_plan_kind;
 
 /* Problem description shared by plan and run calls. */
 typedef struct {
@@ -164,6 +168,8 @@ typedef struct {
     int num_slots;       /* partial-state slots used */
     int64_t max_cost;    /* largest per-worker cost (decode: pages; prefill: KV blocks) */
     int64_t total_cost;  /* sum of the per-worker costs */
+    int prefill_ctas;    /* mixed plans: SMs the last plan gave the prefill half (0 otherwise) */
+    int decode_ctas;     /* mixed plans: SMs the last plan gave the decode half (0 otherwise) */
 } pkv_plan_info;
 
 pkv_status pkv_plan_get_info(const pkv_plan* plan, pkv_plan_info* info);
@@ -284,6 +290,29 @@ pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const void* host
                                           const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
                                           const int32_t* kv_last_page_len_d, void* o, float* lse,
                                           void* stream);
+
+/*
+ * Mixed batch: requests with one query row (decode) and requests with more
+ * (prefill: chunked prompts, new requests) in one call, on a plan of kind
+ * PKV_PLAN_MIXED.  The plan routes each request by its query-tile size: one
+ * row to the CUDA-core decode path (split-KV over warp workers), several rows
+ * to the tcgen05 prefill path (128-row tiles), and splits the SMs between the
+ * two halves in proportion to their estimated times.  The run call launches
+ * both persistent kernels, prefill on a side stream the plan owns, forked from
+ * and joined back into `stream`, so they run side by side on disjoint SMs
+ * (fdeinterviews summary: a batch mixes new prompts and single-token decodes;
+ * "Customizable attention": a query tile size from 1 to 128 picked per batch;
+ * greptalks "Runtime Scheduler").  Graph-capturable: the fork and join are
+ * event records and waits.
+ * Arguments and layouts as for pkv_batch_prefill_paged (qo_indptr_d covers
+ * every request; causal per params->causal applies to the prefill half, and a
+ * single-row request sees all its keys either way).
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+pkv_status pkv_batch_mixed_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
+                                 const void* kv_data, const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
+                                 const int32_t* kv_last_page_len_d, void* o, float* lse, void* dev_ws,
+                                 void* stream);
 
 /*
  * merge_state (guide section 3, "Cascade Attention": the two partial results

@@ -22,7 +22,7 @@ from . import build as _build
 
 PKV_OK = 0
 PKV_F16, PKV_BF16, PKV_F32 = 0, 1, 2
-PLAN_DECODE, PLAN_PREFILL = 0, 1
+PLAN_DECODE, PLAN_PREFILL, PLAN_MIXED = 0, 1, 2
 
 _DTYPES = {torch.float16: PKV_F16, torch.bfloat16: PKV_BF16, torch.float32: PKV_F32}
 
@@ -46,7 +46,8 @@ class Limits(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("grid_ctas", ctypes.c_int), ("workers", ctypes.c_int), ("active_workers", ctypes.c_int),
                 ("num_work", ctypes.c_int), ("num_merge", ctypes.c_int), ("num_slots", ctypes.c_int),
-                ("max_cost", ctypes.c_int64), ("total_cost", ctypes.c_int64)]
+                ("max_cost", ctypes.c_int64), ("total_cost", ctypes.c_int64),
+                ("prefill_ctas", ctypes.c_int), ("decode_ctas", ctypes.c_int)]
 
 
 _lib = None
@@ -57,7 +58,7 @@ EXPORTS = [
     "pkv_plan_workspace_bytes", "pkv_plan_compute", "pkv_plan_run", "pkv_plan_get_info", "pkv_plan_get_work",
     "pkv_batch_decode_paged", "pkv_batch_prefill_paged", "pkv_merge_state", "pkv_get_device_error",
     "pkv_plan_set_timing_events", "pkv_batch_decode_paged_noalloc", "pkv_append_paged_kv",
-    "pkv_batch_prefill_paged_masked",
+    "pkv_batch_prefill_paged_masked", "pkv_batch_mixed_paged",
 ]
 
 
@@ -94,6 +95,7 @@ def load(path: Optional[str] = None):
             "pkv_plan_set_timing_events": (i32, [vp, vp, vp]),
             "pkv_batch_decode_paged_noalloc": (i32, [vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_batch_prefill_paged_masked": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
+            "pkv_batch_mixed_paged": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_append_paged_kv": (i32, [ctypes.POINTER(Params), i32, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
                                           vp, ctypes.c_double, vp, vp]),
         }
@@ -246,6 +248,13 @@ def batch_prefill_paged_masked(h, q, qo_indptr, kv_data, kv_indices, kv_indptr, 
            "pkv_batch_prefill_paged_masked")
 
 
+def batch_mixed_paged(h, q, qo_indptr, kv_data, kv_indices, kv_indptr, kv_last_page_len, o, lse, dev_ws,
+                      stream=None) -> None:
+    _check(load().pkv_batch_mixed_paged(h, _ptr(q), _ptr(qo_indptr), _ptr(kv_data), _ptr(kv_indices),
+                                        _ptr(kv_indptr), _ptr(kv_last_page_len), _ptr(o), _ptr(lse), _ptr(dev_ws),
+                                        _stream(stream)), "pkv_batch_mixed_paged")
+
+
 def merge_state(o_a, lse_a, o_b, lse_b, o_out, lse_out=None, stream=None) -> None:
     """merge_state over [n_rows, num_heads, head_dim] states (dtype fp16/bf16/fp32)."""
     if o_a.dim() != 3:
@@ -291,7 +300,7 @@ def get_device_error(h, dev_ws, clear: bool = False, stream=None) -> int:
 class Plan:
     """A plan handle plus the caller-side buffers it needs.
 
-    ``kind`` is PLAN_DECODE or PLAN_PREFILL.  The device workspace and the
+    ``kind`` is PLAN_DECODE, PLAN_PREFILL or PLAN_MIXED.  The device workspace and the
     pinned host staging buffer are allocated once here, with torch, for the
     given limits; ``plan()`` re-plans a new batch into them and ``run()``
     launches the kernels.
@@ -336,6 +345,9 @@ class Plan:
                 raise ValueError("a custom mask needs a prefill plan")
             batch_prefill_paged_masked(self.handle, q, qo_indptr, kv_data, kv_indices, kv_indptr, kv_last_page_len,
                                        mask, o, lse, self.dev_ws, stream)
+        elif self.kind == PLAN_MIXED:
+            batch_mixed_paged(self.handle, q, qo_indptr, kv_data, kv_indices, kv_indptr, kv_last_page_len, o, lse,
+                              self.dev_ws, stream)
         elif self.kind == PLAN_DECODE:
             batch_decode_paged(self.handle, q, kv_data, kv_indices, kv_indptr, kv_last_page_len, o, lse,
                                self.dev_ws, stream)

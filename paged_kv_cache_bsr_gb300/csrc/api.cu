@@ -194,6 +194,48 @@ pkv_status pkv_batch_prefill_paged_masked(const pkv_plan* plan, const void* q, c
                      mask_bytes, o, lse, dev_ws, stream);
 }
 
+pkv_status pkv_batch_mixed_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
+                                 const void* kv_data, const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
+                                 const int32_t* kv_last_page_len_d, void* o, float* lse, void* dev_ws,
+                                 void* stream) {
+  if (!plan || plan->kind != PKV_PLAN_MIXED || !plan->planned || !dev_ws) return PKV_ERR_INVALID_ARG;
+  if (!aligned(dev_ws, 256)) return PKV_ERR_INVALID_ARG;
+  pkv_status st = check_device(plan);
+  if (st != PKV_OK) return st;
+  auto* base = static_cast<uint8_t*>(dev_ws);
+  void* dws = base + plan->dec_dev_off;
+  void* pws = base + plan->pre_dev_off;
+  const bool has_pre = plan->prefill_ctas > 0 && plan->sub_pre->num_work > 0;
+  const bool has_dec = plan->decode_ctas > 0 && plan->sub_dec->num_work > 0;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (has_pre && has_dec) {
+    // Prefill on the side stream, decode on the caller's: the two persistent
+    // grids find their work in the first prefill_ctas resp. decode_ctas CTAs,
+    // so they run side by side on disjoint SMs; the side stream joins back.
+    if (cudaEventRecord(plan->fork, s) != cudaSuccess || cudaStreamWaitEvent(plan->side, plan->fork, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+    st = prefill_run(plan->sub_pre, q, qo_indptr_d, kv_data, kv_indices_d, kv_indptr_d, kv_last_page_len_d, nullptr,
+                     0, o, lse, pws, plan->side);
+    pkv_status st2 = pkv_batch_decode_paged(plan->sub_dec, q, kv_data, kv_indices_d, kv_indptr_d,
+                                            kv_last_page_len_d, o, lse, dws, stream);
+    // Join even after a failed launch, so the caller's stream never runs ahead of the side stream.
+    if (cudaEventRecord(plan->join, plan->side) != cudaSuccess || cudaStreamWaitEvent(s, plan->join, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+    return st != PKV_OK ? st : st2;
+  }
+  if (has_pre)
+    return prefill_run(plan->sub_pre, q, qo_indptr_d, kv_data, kv_indices_d, kv_indptr_d, kv_last_page_len_d,
+                       nullptr, 0, o, lse, pws, stream);
+  if (has_dec)
+    return pkv_batch_decode_paged(plan->sub_dec, q, kv_data, kv_indices_d, kv_indptr_d, kv_last_page_len_d, o, lse,
+                                  dws, stream);
+  return PKV_OK;
+}
+
 pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o_out,
                            float* lse_out, int64_t n_rows, int num_heads, int head_dim, int dtype, void* stream) {
   if (n_rows < 0 || num_heads <= 0 || head_dim <= 0) return PKV_ERR_INVALID_ARG;
@@ -221,6 +263,14 @@ pkv_status pkv_plan_set_timing_events(pkv_plan* plan, void* start, void* stop) {
 
 pkv_status pkv_get_device_error(const pkv_plan* plan, void* dev_ws, int* code, int clear, void* stream) {
   if (!plan || !dev_ws || !code) return PKV_ERR_INVALID_ARG;
+  if (plan->kind == PKV_PLAN_MIXED) {  // the OR of both halves' words
+    int cd = 0, cp = 0;
+    auto* base = static_cast<uint8_t*>(dev_ws);
+    pkv_status st = pkv_get_device_error(plan->sub_dec, base + plan->dec_dev_off, &cd, clear, stream);
+    if (st == PKV_OK) st = pkv_get_device_error(plan->sub_pre, base + plan->pre_dev_off, &cp, clear, stream);
+    *code = cd | cp;
+    return st;
+  }
   auto s = static_cast<cudaStream_t>(stream);
   auto* word = static_cast<uint8_t*>(dev_ws) + plan->L.header + offsetof(pkv::PlanHeader, error);
   int32_t v = 0;

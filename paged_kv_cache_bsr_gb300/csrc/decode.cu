@@ -45,7 +45,7 @@ struct DecodeShape {
 };
 
 struct SegInfo {
-  int b, kvh, idx_begin, n_pages, last_rows, page_begin, slot;
+  int b, kvh, idx_begin, n_pages, last_rows, page_begin, slot, q_row;
 };
 
 __device__ __forceinline__ SegInfo load_seg(const DecodeSeg* segs, int i, int lane) {
@@ -58,6 +58,7 @@ __device__ __forceinline__ SegInfo load_seg(const DecodeSeg* segs, int i, int la
   s.last_rows = __shfl_sync(kFull, v, 4);
   s.page_begin = __shfl_sync(kFull, v, 5);
   s.slot = __shfl_sync(kFull, v, 6);
+  s.q_row = __shfl_sync(kFull, v, 7);
   return s;
 }
 
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
     float2 qf[G][VEC / 2];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const T* qrow = q_all + (static_cast<int64_t>(sg.b) * a.num_qo_heads + hq0 + g) * D;
+      const T* qrow = q_all + (static_cast<int64_t>(sg.q_row) * a.num_qo_heads + hq0 + g) * D;
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
         float2 f[4];
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
       const float inv = empty ? 0.f : 1.f / lg;
       const float lse_v = empty ? -INFINITY : (m[g] + log2f(lg)) * kLn2;
       if (sg.slot < 0) {
-        T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(sg.b) * a.num_qo_heads + hq0 + g) * D;
+        T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(sg.q_row) * a.num_qo_heads + hq0 + g) * D;
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
           float f[8];
@@ -394,7 +395,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
           }
           *reinterpret_cast<uint4*>(orow + (sub + c * LPT) * 8) = from_float8<T>(f);
         }
-        if (sub == 0 && a.lse) a.lse[static_cast<int64_t>(sg.b) * a.num_qo_heads + hq0 + g] = lse_v;
+        if (sub == 0 && a.lse) a.lse[static_cast<int64_t>(sg.q_row) * a.num_qo_heads + hq0 + g] = lse_v;
       } else {
         float* prow = a.part_o + (static_cast<int64_t>(sg.slot) * G + g) * D;
 #pragma unroll
@@ -480,12 +481,12 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __gri
       }
     }
     const int hq = it.kvh * G + g;
-    T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(it.b) * a.num_qo_heads + hq) * D;
+    T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(it.row) * a.num_qo_heads + hq) * D;
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
     for (int v = 0; v < PER; ++v) orow[lane * PER + v] = from_float<T>(acc[v] * inv);
     if (lane == 0 && a.lse)
-      a.lse[static_cast<int64_t>(it.b) * a.num_qo_heads + hq] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+      a.lse[static_cast<int64_t>(it.row) * a.num_qo_heads + hq] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
   }
 }
 

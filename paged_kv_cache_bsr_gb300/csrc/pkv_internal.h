@@ -46,13 +46,14 @@ struct alignas(32) DecodeSeg {
   int32_t last_rows;   // valid slots of the run's final page
   int32_t page_begin;  // position of the run's first page in the request
   int32_t slot;        // partial slot, or -1
-  int32_t pad;
+  int32_t q_row;       // row of q / o / lse (the request itself in a decode batch; its
+                       // qo_indptr entry in a mixed prefill + decode batch)
 };
 static_assert(sizeof(DecodeSeg) == 32, "DecodeSeg layout");
 
 // A (request, kv head) whose sequence was split into n_slots partial states.
 struct alignas(16) MergeItem {
-  int32_t b;
+  int32_t row;         // row of o / lse
   int32_t kvh;
   int32_t slot_begin;
   int32_t n_slots;

@@ -46,4 +46,16 @@ struct pkv_plan {
   // Caller events recorded around the main kernel (pkv_plan_set_timing_events).
   cudaEvent_t time_start = nullptr;
   cudaEvent_t time_stop = nullptr;
+  // Mixed plans: the decode and prefill halves (each a plan of its own kind,
+  // sharing this plan's device), where their tables and workspaces sit inside
+  // this plan's workspaces, the last SM split, and the side stream and events
+  // the run call forks the prefill half onto.
+  pkv_plan* sub_dec = nullptr;
+  pkv_plan* sub_pre = nullptr;
+  size_t dec_dev_off = 0, pre_dev_off = 0, dec_host_off = 0, pre_host_off = 0;
+  int prefill_ctas = 0;
+  int decode_ctas = 0;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join = nullptr;
 };

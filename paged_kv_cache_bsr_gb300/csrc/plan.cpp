@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <functional>
 #include <new>
@@ -49,7 +50,7 @@ bool is_pow2_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
 pkv_status check_params(int kind, const pkv_params* p, const pkv_limits* lim) {
   if (!p || !lim) return PKV_ERR_INVALID_ARG;
-  if (kind != PKV_PLAN_DECODE && kind != PKV_PLAN_PREFILL) return PKV_ERR_INVALID_ARG;
+  if (kind != PKV_PLAN_DECODE && kind != PKV_PLAN_PREFILL && kind != PKV_PLAN_MIXED) return PKV_ERR_INVALID_ARG;
   if (p->num_qo_heads <= 0 || p->num_kv_heads <= 0 || p->num_qo_heads % p->num_kv_heads)
     return PKV_ERR_INVALID_ARG;
   if (p->page_size <= 0 || (p->page_size > 16 && p->page_size % 16)) return PKV_ERR_UNSUPPORTED;
@@ -58,8 +59,8 @@ pkv_status check_params(int kind, const pkv_params* p, const pkv_limits* lim) {
   if (lim->max_kv_pages > INT32_MAX || lim->max_total_q > INT32_MAX) return PKV_ERR_INVALID_ARG;
   const int g = p->num_qo_heads / p->num_kv_heads;
   if (p->dtype != PKV_F16 && p->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-  if (kind == PKV_PLAN_DECODE && !pkv::decode_supported(p->head_dim, g, p->dtype)) return PKV_ERR_UNSUPPORTED;
-  if (kind == PKV_PLAN_PREFILL && !pkv::prefill_supported(p->head_dim, g, p->dtype, p->page_size))
+  if (kind != PKV_PLAN_PREFILL && !pkv::decode_supported(p->head_dim, g, p->dtype)) return PKV_ERR_UNSUPPORTED;
+  if (kind != PKV_PLAN_DECODE && !pkv::prefill_supported(p->head_dim, g, p->dtype, p->page_size))
     return PKV_ERR_UNSUPPORTED;
   if (!is_pow2_group(g)) return PKV_ERR_UNSUPPORTED;
   return PKV_OK;
@@ -96,6 +97,27 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
   pl->num_sms = num_sms;
   pl->group = params->num_qo_heads / params->num_kv_heads;
   const int64_t hkv = params->num_kv_heads;
+  if (kind == PKV_PLAN_MIXED) {
+    // Two plans of the same problem and limits; their workspaces are laid end to end.
+    pkv_status s1 = make_plan(&pl->sub_dec, PKV_PLAN_DECODE, params, limits, device, num_sms);
+    pkv_status s2 = s1 == PKV_OK ? make_plan(&pl->sub_pre, PKV_PLAN_PREFILL, params, limits, device, num_sms) : s1;
+    if (s2 != PKV_OK) {
+      delete pl->sub_dec;
+      delete pl->sub_pre;
+      delete pl;
+      return s2;
+    }
+    pl->grid_ctas = num_sms;
+    pl->workers = num_sms;
+    pl->dec_dev_off = 0;
+    pl->pre_dev_off = align_up(pl->sub_dec->L.total, 256);
+    pl->L.total = pl->pre_dev_off + pl->sub_pre->L.total;
+    pl->dec_host_off = 0;
+    pl->pre_host_off = align_up(pl->sub_dec->host_bytes, 256);
+    pl->host_bytes = pl->pre_host_off + pl->sub_pre->host_bytes;
+    *out = pl;
+    return PKV_OK;
+  }
   if (kind == PKV_PLAN_DECODE) {
     pl->grid_ctas = num_sms;
     pl->workers = num_sms * pkv::kDecodeWarps;
@@ -130,7 +152,7 @@ pkv_status validate(const pkv_plan* pl, int batch, const int32_t* qo_indptr, con
                     const int32_t* kv_indices, const int32_t* kv_last, int64_t num_pages) {
   if (batch < 0 || !kv_indptr || (batch > 0 && !kv_last)) return PKV_ERR_INVALID_ARG;
   if (batch > pl->lim.max_batch) return PKV_ERR_WORKSPACE;
-  if (pl->kind == PKV_PLAN_PREFILL && !qo_indptr) return PKV_ERR_INVALID_ARG;
+  if (pl->kind != PKV_PLAN_DECODE && !qo_indptr) return PKV_ERR_INVALID_ARG;
   if (num_pages < 0 || num_pages > INT32_MAX) return PKV_ERR_INVALID_ARG;
   if (kv_indptr[0] != 0) return PKV_ERR_BAD_INDEX;
   for (int b = 0; b < batch; ++b) {
@@ -160,17 +182,26 @@ int64_t kv_len_of(const int32_t* kv_indptr, const int32_t* kv_last, int b, int P
   return n > 0 ? (n - 1) * P + kv_last[b] : 0;
 }
 
+// Decode work over `W` warp workers.  With qo_indptr (a mixed batch) only the
+// requests holding exactly one query row take part, and each reads and writes
+// its row qo_indptr[b]; without it every request is one row, row b.
 pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, const int32_t* kv_last,
-                          uint8_t* host) {
+                          uint8_t* host, const int32_t* qo_indptr = nullptr, int W = 0) {
   const int P = pl->p.page_size;
   const int hkv = pl->p.num_kv_heads;
-  const int W = pl->workers;
+  if (W <= 0) W = pl->workers;
+  auto takes_part = [&](int b) { return !qo_indptr || qo_indptr[b + 1] - qo_indptr[b] == 1; };
   const int64_t pages_per_chunk = ceil_div(P, pkv::kDecodeTileRows);
   const int64_t min_run = std::max<int64_t>(1, 8 / pages_per_chunk);  // keep runs >= 8 tiles
   int64_t total = 0;
-  for (int b = 0; b < batch; ++b) total += (int64_t)(kv_indptr[b + 1] - kv_indptr[b]) * hkv;
+  int parts = 0;
+  for (int b = 0; b < batch; ++b)
+    if (takes_part(b)) {
+      total += (int64_t)(kv_indptr[b + 1] - kv_indptr[b]) * hkv;
+      ++parts;
+    }
   const int64_t run = total > 0 ? std::max<int64_t>(ceil_div(total, W), min_run) : 1;
-  const int active = total > 0 ? static_cast<int>(ceil_div(total, run)) : (batch > 0 ? 1 : 0);
+  const int active = total > 0 ? static_cast<int>(ceil_div(total, run)) : (parts > 0 ? 1 : 0);
 
   auto* hdr = reinterpret_cast<PlanHeader*>(host + pl->L.header);
   auto* wptr = reinterpret_cast<int32_t*>(host + pl->L.worker_ptr);
@@ -186,11 +217,14 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
   };
   int64_t x = 0;  // offset of the current page list in the concatenated sequence
   for (int b = 0; b < batch; ++b) {
+    if (!takes_part(b)) continue;
     const int32_t n = kv_indptr[b + 1] - kv_indptr[b];
+    const int32_t row = qo_indptr ? qo_indptr[b] : b;
     for (int h = 0; h < hkv; ++h) {
       DecodeSeg s{};
       s.b = b;
       s.kvh = h;
+      s.q_row = row;
       if (n == 0) {
         const int w = static_cast<int>(std::min<int64_t>(x / run, active - 1));
         s.idx_begin = kv_indptr[b];
@@ -211,7 +245,7 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
         s.slot = -1;
         emit(w0, s);
       } else {
-        MergeItem m{b, h, n_slot, w1 - w0 + 1};
+        MergeItem m{row, h, n_slot, w1 - w0 + 1};
         merge[n_merge++] = m;
         for (int w = w0; w <= w1; ++w) {
           const int64_t lo = std::max<int64_t>(x, (int64_t)w * run) - x;
@@ -260,14 +294,16 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
   return PKV_OK;
 }
 
+// Prefill work over `C` CTAs; with skip_single the requests holding one query
+// row are left out (they are the decode half of a mixed batch).
 pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
-                           const int32_t* kv_last, uint8_t* host) {
+                           const int32_t* kv_last, uint8_t* host, int C = 0, bool skip_single = false) {
   const int P = pl->p.page_size;
   const int hkv = pl->p.num_kv_heads;
   const int G = pl->group;
   const int mp = pkv::kPrefillRows / G;
   const int BN = pkv::kPrefillKeys;
-  const int C = pl->workers;
+  if (C <= 0) C = pl->workers;
 
   struct Item {
     PrefillTile t;
@@ -288,6 +324,7 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   pl->mask_bits = mask_off[batch];
   for (int b = 0; b < batch; ++b) {
     const int qo = qo_indptr[b + 1] - qo_indptr[b];
+    if (skip_single && qo == 1) continue;
     const int kv = static_cast<int>(kv_len_of(kv_indptr, kv_last, b, P));
     for (int h = 0; h < hkv; ++h)
       for (int pos0 = 0; pos0 < qo; pos0 += mp) {
@@ -400,6 +437,83 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   return PKV_OK;
 }
 
+// Throughputs of the two kernels on a whole GB300, measured on the two halves of
+// a 60-decode + 4-prompt-chunk batch (decode 4.98 TB/s of K/V, prefill 0.84
+// PFLOP/s of unmasked work); only their ratio matters: it turns each half's work
+// into time for the SM split.
+constexpr double kDecodeBytesPerSec = 4.98e12;
+constexpr double kPrefillFlopsPerSec = 0.84e15;
+
+// Mixed batch: single-row requests to the decode half, the rest to the prefill
+// half, and the SMs shared in proportion to the estimated time of each half
+// alone on the whole GPU, so both halves end together.
+pkv_status compute_mixed(pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                         const int32_t* kv_last, int64_t num_pages, uint8_t* host) {
+  const int P = pl->p.page_size;
+  const double elem = 2.0;
+  double dec_bytes = 0.0, pre_flops = 0.0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t qo = qo_indptr[b + 1] - qo_indptr[b];
+    const int64_t kv = kv_len_of(kv_indptr, kv_last, b, P);
+    if (qo == 1) {
+      dec_bytes += 2.0 * kv * pl->p.num_kv_heads * pl->p.head_dim * elem;
+    } else if (qo > 1) {
+      int64_t pairs = 0;
+      if (pl->p.causal) {
+        const int64_t pre = std::max<int64_t>(kv - qo, 0);
+        const int64_t seen = std::min<int64_t>(qo, kv);  // rows that see at least their prefix
+        pairs = seen * pre + seen * (seen + 1) / 2;
+      } else {
+        pairs = qo * kv;
+      }
+      pre_flops += 4.0 * pairs * pl->p.num_qo_heads * pl->p.head_dim;
+    }
+  }
+  const double t_dec = dec_bytes / kDecodeBytesPerSec, t_pre = pre_flops / kPrefillFlopsPerSec;
+  const int S = pl->num_sms;
+  int kp = 0;
+  bool any_pre = false, any_dec = false;
+  for (int b = 0; b < batch; ++b) {
+    const int qo = qo_indptr[b + 1] - qo_indptr[b];
+    any_dec |= qo == 1;
+    any_pre |= qo > 1;
+  }
+  if (any_pre && !any_dec) {
+    kp = S;
+  } else if (any_pre && any_dec) {
+    const double share = (t_pre + t_dec) > 0.0 ? t_pre / (t_pre + t_dec) : 0.5;
+    kp = static_cast<int>(std::lround(share * S));
+    kp = std::min(std::max(kp, 1), S - 1);
+  }
+  pl->prefill_ctas = kp;
+  pl->decode_ctas = any_dec ? S - kp : 0;
+  pkv_plan* d = pl->sub_dec;
+  pkv_plan* p = pl->sub_pre;
+  pkv_status st = compute_decode(d, batch, kv_indptr, kv_last, host + pl->dec_host_off, qo_indptr,
+                                 std::max(pl->decode_ctas, 1) * pkv::kDecodeWarps);
+  if (st != PKV_OK) return st;
+  st = compute_prefill(p, batch, qo_indptr, kv_indptr, kv_last, host + pl->pre_host_off, std::max(kp, 1), true);
+  if (st != PKV_OK) return st;
+  for (pkv_plan* q : {d, p}) {
+    uint8_t* h = host + (q == d ? pl->dec_host_off : pl->pre_host_off);
+    reinterpret_cast<PlanHeader*>(h + q->L.header)->num_pages = num_pages;
+    q->batch = batch;
+    q->num_pages = num_pages;
+    q->total_q = batch > 0 ? qo_indptr[batch] : 0;
+    q->planned = true;
+  }
+  pl->active_workers = p->active_workers + static_cast<int>(ceil_div(d->active_workers, pkv::kDecodeWarps));
+  pl->num_work = d->num_work + p->num_work;
+  pl->num_merge = d->num_merge + p->num_merge;
+  pl->num_slots = d->num_slots + p->num_slots;
+  pl->max_cost = 0;
+  pl->total_cost = 0;
+  pl->mask_bits = p->mask_bits;
+  pl->work_rows = d->work_rows;
+  pl->work_rows.insert(pl->work_rows.end(), p->work_rows.begin(), p->work_rows.end());
+  return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -419,9 +533,16 @@ pkv_status pkv_plan_create(pkv_plan** out, int kind, const pkv_params* params, c
   cudaGetDevice(&prev);
   cudaSetDevice(device);
   cudaError_t e = cudaEventCreateWithFlags(&(*out)->copy_done, cudaEventDisableTiming);
+  if (e == cudaSuccess && kind == PKV_PLAN_MIXED) {
+    // The run call forks the prefill half onto this stream and joins it back.
+    e = cudaStreamCreateWithFlags(&(*out)->side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&(*out)->fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&(*out)->join, cudaEventDisableTiming);
+  }
   cudaSetDevice(prev);
   if (e != cudaSuccess) {
-    delete *out;
+    cudaGetLastError();
+    pkv_plan_destroy(*out);
     *out = nullptr;
     return PKV_ERR_CUDA;
   }
@@ -439,6 +560,14 @@ pkv_status pkv_plan_destroy(pkv_plan* plan) {
     if (plan->copy_pending) cudaEventSynchronize(plan->copy_done);
     cudaEventDestroy(plan->copy_done);
   }
+  if (plan->side) {
+    cudaStreamSynchronize(plan->side);
+    cudaStreamDestroy(plan->side);
+  }
+  if (plan->fork) cudaEventDestroy(plan->fork);
+  if (plan->join) cudaEventDestroy(plan->join);
+  delete plan->sub_dec;
+  delete plan->sub_pre;
   delete plan;
   return PKV_OK;
 }
@@ -463,13 +592,15 @@ pkv_status pkv_plan_compute(pkv_plan* plan, int batch, const int32_t* qo_indptr_
     plan->copy_pending = false;
   }
   auto* host = static_cast<uint8_t*>(host_ws);
-  if (plan->kind == PKV_PLAN_DECODE) {
+  if (plan->kind == PKV_PLAN_MIXED) {
+    st = compute_mixed(plan, batch, qo_indptr_h, kv_indptr_h, kv_last_page_len_h, num_pages, host);
+  } else if (plan->kind == PKV_PLAN_DECODE) {
     st = compute_decode(plan, batch, kv_indptr_h, kv_last_page_len_h, host);
   } else {
     st = compute_prefill(plan, batch, qo_indptr_h, kv_indptr_h, kv_last_page_len_h, host);
   }
   if (st != PKV_OK) return st;
-  reinterpret_cast<PlanHeader*>(host + plan->L.header)->num_pages = num_pages;
+  if (plan->kind != PKV_PLAN_MIXED) reinterpret_cast<PlanHeader*>(host + plan->L.header)->num_pages = num_pages;
   plan->batch = batch;
   plan->num_pages = num_pages;
   plan->total_q = plan->kind == PKV_PLAN_DECODE ? batch : (batch > 0 ? qo_indptr_h[batch] : 0);
@@ -488,8 +619,18 @@ pkv_status pkv_plan_run(pkv_plan* plan, int batch, const int32_t* qo_indptr_h, c
                                    num_pages, host_ws, host_ws_bytes);
   if (st != PKV_OK) return st;
   auto s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(dev_ws, host_ws, plan->used_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaEventRecord(plan->copy_done, s) != cudaSuccess) {
+  bool ok = true;
+  if (plan->kind == PKV_PLAN_MIXED) {
+    auto* d = static_cast<uint8_t*>(dev_ws);
+    auto* h = static_cast<uint8_t*>(host_ws);
+    ok = cudaMemcpyAsync(d + plan->dec_dev_off, h + plan->dec_host_off, plan->sub_dec->used_bytes,
+                         cudaMemcpyHostToDevice, s) == cudaSuccess &&
+         cudaMemcpyAsync(d + plan->pre_dev_off, h + plan->pre_host_off, plan->sub_pre->used_bytes,
+                         cudaMemcpyHostToDevice, s) == cudaSuccess;
+  } else {
+    ok = cudaMemcpyAsync(dev_ws, host_ws, plan->used_bytes, cudaMemcpyHostToDevice, s) == cudaSuccess;
+  }
+  if (!ok || cudaEventRecord(plan->copy_done, s) != cudaSuccess) {
     cudaGetLastError();
     plan->planned = false;
     return PKV_ERR_CUDA;
@@ -508,6 +649,8 @@ pkv_status pkv_plan_get_info(const pkv_plan* plan, pkv_plan_info* info) {
   info->num_slots = plan->num_slots;
   info->max_cost = plan->max_cost;
   info->total_cost = plan->total_cost;
+  info->prefill_ctas = plan->kind == PKV_PLAN_MIXED ? plan->prefill_ctas : 0;
+  info->decode_ctas = plan->kind == PKV_PLAN_MIXED ? plan->decode_ctas : 0;
   return PKV_OK;
 }
 

@@ -47,7 +47,7 @@ def make_plan(b, kind: int, **limits) -> api.Plan:
 
 def plan_batch(plan: api.Plan, b, stream=None) -> None:
     plan.plan(b.kv_indptr, b.kv_last_page_len, b.num_pages,
-              qo_indptr_h=b.qo_indptr if plan.kind == api.PLAN_PREFILL else None,
+              qo_indptr_h=b.qo_indptr if plan.kind != api.PLAN_DECODE else None,
               kv_indices_h=b.kv_indices, stream=stream)
 
 
@@ -103,6 +103,20 @@ def append_kv(db: DeviceBatch, k_new: torch.Tensor, v_new: torch.Tensor, rope_th
                         db.kv_data, db.q if rotate_q else None, q_out if rotate_q else None, rope_theta,
                         error=error, stream=stream)
     return q_out if rotate_q else None
+
+
+def mixed(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """A batch mixing single-row (decode) and multi-row (prefill) requests in one
+    call: the plan routes each request by its row count and splits the SMs."""
+    b = db.host
+    if plan is None:
+        plan = make_plan(b, api.PLAN_MIXED)
+        plan_batch(plan, b, stream)
+    o = torch.empty_like(db.q)
+    lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.q.device)
+    plan.run(db.q, db.kv_data, db.kv_indices, db.kv_indptr, db.kv_last_page_len, o, lse,
+             qo_indptr=db.qo_indptr, stream=stream)
+    return o, lse
 
 
 def level_kind(b) -> int:

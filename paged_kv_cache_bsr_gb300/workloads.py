@@ -42,6 +42,8 @@ __all__ = [
     "pack_mask",
     "TreeBatch",
     "tree_verify",
+    "mixed_batch",
+    "sub_batch",
     "WORKLOADS",
 ]
 
@@ -484,6 +486,48 @@ def tree_verify(seed: int = 1006, batch: int = 16, prefix_lo: int = 512, prefix_
     return TreeBatch(batch=pb, mask=pack_mask(mats), parents=parents, prefix_lens=prefix, matrices=mats)
 
 
+def mixed_batch(seed: int = 1007, n_decode: int = 60, n_prefill: int = 4, decode_lo: int = 512,
+                decode_hi: int = 4096, qo_lo: int = 256, qo_hi: int = 2048, prefix_lo: int = 0,
+                prefix_hi: int = 1024, num_qo_heads: int = 32, num_kv_heads: int = 8, head_dim: int = 128,
+                page_size: int = 16, dtype: torch.dtype = torch.bfloat16, poison: bool = False) -> PagedBatch:
+    """One continuous-batching step: ``n_decode`` requests generating one token
+    (kv_len ~ U[decode_lo, decode_hi]) and ``n_prefill`` requests taking a prompt chunk
+    (qo_len ~ U[qo_lo, qo_hi] after a cached prefix ~ U[prefix_lo, prefix_hi]), in
+    random order, causal, 32 q / 8 kv heads, head_dim 128, page 16, bf16."""
+    gen = _gen(seed)
+    dec = _uniform_ints(decode_lo, decode_hi, n_decode, gen)
+    qo = _uniform_ints(qo_lo, qo_hi, n_prefill, gen)
+    pre = _uniform_ints(prefix_lo, prefix_hi, n_prefill, gen)
+    reqs = [(1, k) for k in dec] + [(q, q + p) for q, p in zip(qo, pre)]
+    order = torch.randperm(len(reqs), generator=gen).tolist()
+    reqs = [reqs[i] for i in order]
+    return make_paged_batch(qo_lens=[r[0] for r in reqs], kv_lens=[r[1] for r in reqs], num_qo_heads=num_qo_heads,
+                            num_kv_heads=num_kv_heads, head_dim=head_dim, page_size=page_size, dtype=dtype,
+                            seed=seed + 1, causal=True, poison=poison, name="mixed_batch")
+
+
+def sub_batch(b: PagedBatch, requests: Sequence[int], name: str = "") -> PagedBatch:
+    """The listed requests of a batch as a batch of their own over the same pool
+    (their query rows copied, page tables sliced; kv_data shared)."""
+    reqs = list(requests)
+    rows = [torch.arange(int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])) for r in reqs]
+    q = b.q[torch.cat(rows)] if rows else b.q[:0]
+    pages = [b.kv_indices[int(b.kv_indptr[r]):int(b.kv_indptr[r + 1])] for r in reqs]
+
+    def indptr_of(counts):
+        t = torch.zeros(len(counts) + 1, dtype=torch.int32)
+        if counts:
+            t[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int64), 0).to(torch.int32)
+        return t
+
+    return dataclasses.replace(
+        b, q=q, qo_indptr=indptr_of([b.qo_lens[r] for r in reqs]),
+        kv_indptr=indptr_of([p.numel() for p in pages]),
+        kv_indices=torch.cat(pages) if pages else b.kv_indices[:0],
+        kv_last_page_len=b.kv_last_page_len[reqs] if reqs else b.kv_last_page_len[:0],
+        qo_lens=[b.qo_lens[r] for r in reqs], kv_lens=[b.kv_lens[r] for r in reqs], name=name or b.name)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama3_8b_decode": llama3_decode,
@@ -492,4 +536,5 @@ WORKLOADS = {
     "cascade_softcap_decode": cascade_decode,
     "parallel_generation": parallel_generation,
     "tree_verify": tree_verify,
+    "mixed_batch": mixed_batch,
 }

@@ -286,3 +286,79 @@ def test_prefill_plan_edge_cases(lib, qo, kv, causal):
     compute(h, ws, b)
     check_prefill_plan(h, b)
     api.plan_destroy(h)
+
+
+# --------------------------------------------------------------------------- mixed plans
+def check_mixed_plan(h, b, num_sms=152):
+    """Decode entries (listed first) cover each single-row request's pages once per kv
+    head and read/write its own row; prefill tiles cover the other requests; the two
+    halves use disjoint SM counts that add up to the GPU."""
+    info = api.plan_get_info(h)
+    work = api.plan_get_work(h).tolist()
+    single = {i for i, q in enumerate(b.qo_lens) if q == 1}
+    multi = {i for i, q in enumerate(b.qo_lens) if q > 1}
+    n_dec = 0
+    while n_dec < len(work) and work[n_dec][1] in single:
+        n_dec += 1
+    dec, pre = work[:n_dec], work[n_dec:]
+    assert all(r[1] in multi for r in pre)
+    assert {r[1] for r in dec} == single and {r[1] for r in pre} == multi
+    # decode half: pages of each (request, kv head) covered exactly once
+    seen = {}
+    for w, bb, kvh, pb, npg, last, slot, _ in dec:
+        seen.setdefault((bb, kvh), []).append((pb, npg))
+        assert w < info.decode_ctas * 8
+    for bb in single:
+        n = int(b.kv_indptr[bb + 1] - b.kv_indptr[bb])
+        for kvh in range(b.num_kv_heads):
+            runs = sorted(seen.pop((bb, kvh)))
+            pos = 0
+            for pb, npg in runs:
+                assert pb == pos
+                pos += npg
+            assert pos == n
+    assert not seen
+    # prefill half: every tile of a multi-row request, on the prefill CTAs only
+    assert all(r[0] < info.prefill_ctas for r in pre)
+    fam = {(r[1], r[2], r[3]) for r in pre}
+    g = b.num_qo_heads // b.num_kv_heads
+    mp = 256 // g
+    for bb in multi:
+        for kvh in range(b.num_kv_heads):
+            for pos0 in range(0, b.qo_lens[bb], mp):
+                assert (bb, kvh, pos0) in fam
+    if single and multi:
+        assert info.prefill_ctas >= 1 and info.decode_ctas >= 1
+        assert info.prefill_ctas + info.decode_ctas == num_sms
+    return info
+
+
+def test_mixed_plan_routes_requests_by_row_count(lib):
+    b = W.mixed_batch(seed=1007)
+    h, ws = host_plan(b, api.PLAN_MIXED)
+    compute(h, ws, b)
+    info = check_mixed_plan(h, b)
+    # the split follows the work: more prefill rows take more SMs
+    b2 = W.mixed_batch(seed=1007, n_prefill=12)
+    h2, ws2 = host_plan(b2, api.PLAN_MIXED)
+    compute(h2, ws2, b2)
+    info2 = check_mixed_plan(h2, b2)
+    assert info2.prefill_ctas > info.prefill_ctas
+
+
+@pytest.mark.parametrize("n_decode,n_prefill", [(0, 3), (5, 0), (0, 0)])
+def test_mixed_plan_with_one_half_empty(lib, n_decode, n_prefill):
+    b = W.mixed_batch(seed=5, n_decode=n_decode, n_prefill=n_prefill, qo_lo=20, qo_hi=300, decode_lo=1,
+                      decode_hi=400)
+    h, ws = host_plan(b, api.PLAN_MIXED)
+    compute(h, ws, b)
+    info = check_mixed_plan(h, b)
+    assert (info.prefill_ctas > 0) == (n_prefill > 0)
+    assert (info.decode_ctas > 0) == (n_decode > 0)
+
+
+def test_mixed_plan_needs_qo_indptr(lib):
+    b = W.mixed_batch(seed=6, n_decode=3, n_prefill=1)
+    h, ws = host_plan(b, api.PLAN_MIXED)
+    with pytest.raises(api.PkvError):
+        compute(h, ws, b, qo=None)

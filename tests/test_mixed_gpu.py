@@ -1,0 +1,130 @@
+"""GPU parity of mixed batches (single-row decode requests and multi-row prefill
+requests in one call, routed by the plan to the CUDA-core decode kernel and the
+tcgen05 prefill kernel running side by side) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_bsr_gb300 import api, runner, workloads as W
+from gpu_util import assert_matches_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_bsr_gb300 import build
+    build.build()
+    oracle.build()
+    api.load()
+    torch.cuda.set_device(0)
+
+
+def mixed_vs_oracle(b, what, rows=None):
+    db = runner.DeviceBatch.from_host(b)
+    plan = runner.make_plan(b, api.PLAN_MIXED)
+    runner.plan_batch(plan, b)
+    o, lse = runner.mixed(db, plan)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    ref_o, ref_lse = oracle.attention_of(b, rows=rows)
+    if rows is not None:
+        idx = torch.as_tensor(rows, dtype=torch.long, device=o.device)
+        o, lse = o[idx], lse[idx]
+    assert_matches_oracle(o, lse, ref_o, ref_lse, b.dtype, what)
+    return plan
+
+
+def small_mixed(seed, hq=8, hkv=2, dtype=torch.bfloat16, n_decode=9, n_prefill=3):
+    return W.mixed_batch(seed=seed, n_decode=n_decode, n_prefill=n_prefill, decode_lo=1, decode_hi=700, qo_lo=2,
+                         qo_hi=300, prefix_lo=0, prefix_hi=200, num_qo_heads=hq, num_kv_heads=hkv, dtype=dtype,
+                         poison=True)
+
+
+@pytest.mark.parametrize("group,dtype", [(4, torch.bfloat16), (1, torch.float16), (8, torch.bfloat16)])
+def test_small_mixed_batches(group, dtype):
+    plan = mixed_vs_oracle(small_mixed(group, hq=2 * group, dtype=dtype), f"mixed g{group}")
+    info = plan.info()
+    assert info.prefill_ctas >= 1 and info.decode_ctas >= 1
+
+
+@pytest.mark.parametrize("n_decode,n_prefill", [(7, 0), (0, 4)])
+def test_mixed_batch_with_one_half(n_decode, n_prefill):
+    mixed_vs_oracle(small_mixed(11, n_decode=n_decode, n_prefill=n_prefill), f"{n_decode}+{n_prefill}")
+
+
+def test_mixed_with_softcap_and_split_decode():
+    b = W.mixed_batch(seed=12, n_decode=3, n_prefill=2, decode_lo=30000, decode_hi=40000, qo_lo=100, qo_hi=200,
+                      num_qo_heads=8, num_kv_heads=2, poison=True)
+    b = W.PagedBatch(**{**b.__dict__, "logits_cap": 30.0})
+    plan = mixed_vs_oracle(b, "mixed cap, long decodes")
+    assert plan.info().num_merge > 0
+
+
+def test_mixed_full_size():
+    """60 decode requests (kv U[512, 4096]) and 4 prompt chunks (qo U[256, 2048] after
+    a prefix U[0, 1024]), 32 q / 8 kv heads: every decode row and 2000 prefill rows."""
+    b = W.mixed_batch(seed=1007, poison=True)
+    dec_rows = [int(b.qo_indptr[r]) for r in range(b.batch) if b.qo_lens[r] == 1]
+    pre_rows = [i for r in range(b.batch) if b.qo_lens[r] > 1
+                for i in range(int(b.qo_indptr[r]), int(b.qo_indptr[r + 1]))]
+    rng = np.random.default_rng(0)
+    rows = np.sort(np.concatenate([dec_rows, rng.choice(pre_rows, size=2000, replace=False)]))
+    mixed_vs_oracle(b, "mixed full size", rows=rows)
+
+
+def test_mixed_graph_replay_after_replanning():
+    """Capture the mixed run (fork onto the plan's side stream, join back) once;
+    re-plan a batch with another decode/prefill mix of the same total rows; replay."""
+    a = small_mixed(20, n_decode=10, n_prefill=2)
+    total = a.total_q
+    bb = W.mixed_batch(seed=21, n_decode=total - 2 * 50, n_prefill=2, decode_lo=1, decode_hi=700, qo_lo=50,
+                       qo_hi=50, prefix_lo=0, prefix_hi=200, num_qo_heads=8, num_kv_heads=2, poison=True)
+    assert bb.total_q == total
+    pool = max(a.num_pages, bb.num_pages)
+
+    def on_pool(b):
+        kv = torch.zeros(pool, *b.kv_data.shape[1:], dtype=b.kv_data.dtype)
+        kv[: b.num_pages] = b.kv_data
+        return W.PagedBatch(**{**b.__dict__, "kv_data": kv})
+
+    a, bb = on_pool(a), on_pool(bb)
+    max_b = max(a.batch, bb.batch)
+    plan = runner.make_plan(a, api.PLAN_MIXED, max_batch=max_b, max_total_q=total,
+                            max_kv_pages=max(int(a.kv_indptr[-1]), int(bb.kv_indptr[-1])))
+    dev = "cuda"
+    q = torch.empty(total, 8, 128, dtype=torch.bfloat16, device=dev)
+    kv = torch.empty(pool, *a.kv_data.shape[1:], dtype=torch.bfloat16, device=dev)
+    o, lse = torch.empty_like(q), torch.empty(total, 8, dtype=torch.float32, device=dev)
+    qo = torch.zeros(max_b + 1, dtype=torch.int32, device=dev)
+    ip = torch.zeros(max_b + 1, dtype=torch.int32, device=dev)
+    ix = torch.zeros(plan.limits.max_kv_pages, dtype=torch.int32, device=dev)
+    last = torch.zeros(max_b, dtype=torch.int32, device=dev)
+
+    def load(b):
+        q.copy_(b.q)
+        kv.copy_(b.kv_data)
+        qo[: b.batch + 1].copy_(b.qo_indptr)
+        ip[: b.batch + 1].copy_(b.kv_indptr)
+        ix[: b.kv_indices.numel()].copy_(b.kv_indices)
+        last[: b.batch].copy_(b.kv_last_page_len)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        load(a)
+        runner.plan_batch(plan, a, stream=s)
+        plan.run(q, kv, ix, ip, last, o, lse, qo_indptr=qo, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.run(q, kv, ix, ip, last, o, lse, qo_indptr=qo, stream=s)
+    for b in (bb, a):
+        with torch.cuda.stream(s):
+            load(b)
+            runner.plan_batch(plan, b, stream=s)
+            g.replay()
+        s.synchronize()
+        ref_o, ref_lse = oracle.attention_of(b)
+        assert_matches_oracle(o, lse, ref_o, ref_lse, torch.bfloat16, "mixed graph replay")
+    assert plan.device_error() == 0
