@@ -194,6 +194,97 @@ __device__ __forceinline__ float reduce_scatter(const float (&v)[G], int sub) {
   return cur[0];
 }
 
+// One 16-row tile of K and V in shared memory: scores of the owned head per
+// step, the tile max, a rescale of O only when some head's max grows by more
+// than 2^8 over its reference (so p stays <= 256 and most tiles skip it), then
+// P V with packed FMAs.  FULL: all 16 rows valid, no per-token checks.
+template <int D, int G, int LPT, typename T, bool CAP, bool FULL>
+__device__ __forceinline__ void tile_step(const DecodeArgs& a, const T* ks, const T* vs, int rows, int sub, int grp,
+                                          int my_head, const float2 (&qf)[G][D / LPT / 2], float (&m)[G],
+                                          float& m_own, float& l_own, float2 (&acc)[G][D / LPT / 2]) {
+  constexpr int VEC = D / LPT;
+  constexpr int CH = VEC / 8;
+  constexpr int TPS = 32 / LPT;
+  constexpr int STEPS = kDecodeTileRows / TPS;
+  float sc[STEPS];
+#pragma unroll
+  for (int st = 0; st < STEPS; ++st) {
+    const int tok = st * TPS + grp;
+    // two partial sums per head: half-length FMA chains
+    float2 pa[G], pb[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) pa[g] = pb[g] = make_float2(0.f, 0.f);
+    if (FULL || tok < rows) {
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        float2 kf[4];
+        to_float2x4<T>(*reinterpret_cast<const uint4*>(ks + tok * D + (sub + c * LPT) * 8), kf);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          pa[g] = ffma2(qf[g][c * 4 + 0], kf[0], pa[g]);
+          pb[g] = ffma2(qf[g][c * 4 + 1], kf[1], pb[g]);
+          pa[g] = ffma2(qf[g][c * 4 + 2], kf[2], pa[g]);
+          pb[g] = ffma2(qf[g][c * 4 + 3], kf[3], pb[g]);
+        }
+      }
+    }
+    float part[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float2 t = fadd2(pa[g], pb[g]);
+      part[g] = t.x + t.y;
+    }
+    float x = reduce_scatter<G, LPT>(part, sub);
+    if constexpr (CAP) x = a.cap * tanhf(x / a.cap) * kLog2e;
+    sc[st] = (FULL || tok < rows) ? x : -INFINITY;
+  }
+  // Tile max of the owned head over the token groups.
+  float mx = sc[0];
+#pragma unroll
+  for (int st = 1; st < STEPS; ++st) mx = fmaxf(mx, sc[st]);
+  mx = warp_max(mx, 16, LPT);
+  const bool grow = (m_own == -INFINITY) ? (mx != -INFINITY) : (mx > m_own + 8.f);
+  if (__any_sync(kFull, grow)) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mg = __shfl_sync(kFull, mx, owner_of_head<G, LPT>(g));
+      const bool up = (m[g] == -INFINITY) ? (mg != -INFINITY) : (mg > m[g] + 8.f);
+      if (up) {
+        const float alpha = fast_exp2(m[g] - mg);  // 0 while m[g] is -inf
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+        for (int v = 0; v < VEC / 2; ++v) acc[g][v] = fmul2(acc[g][v], a2);
+        if (g == my_head) l_own *= alpha;
+        m[g] = mg;
+      }
+      if (g == my_head) m_own = m[g];
+    }
+  }
+#pragma unroll
+  for (int st = 0; st < STEPS; ++st) {
+    const int tok = st * TPS + grp;
+    const float p_own = fast_exp2(sc[st] - m_own);  // 0 for a masked token
+    l_own += p_own;
+    float2 p2[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float pg_ = __shfl_sync(kFull, p_own, grp * LPT + owner_of_head<G, LPT>(g));
+      p2[g] = make_float2(pg_, pg_);
+    }
+    if (FULL || tok < rows) {
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        float2 vf[4];
+        to_float2x4<T>(*reinterpret_cast<const uint4*>(vs + tok * D + (sub + c * LPT) * 8), vf);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[g][c * 4 + e] = ffma2(p2[g], vf[e], acc[g][c * 4 + e]);
+      }
+    }
+  }
+}
+
 template <int D, int G, int LPT, typename T, bool CAP>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
   using Shape = DecodeShape<D, T>;
@@ -263,7 +354,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
         for (int e = 0; e < 4; ++e) qf[g][c * 4 + e] = make_float2(f[e].x * a.q_scale, f[e].y * a.q_scale);
       }
     }
-    float m[G];        // running max per head (warp-uniform)
+    float m[G];        // reference max per head (warp-uniform), log2 units
+    float m_own = -INFINITY;  // m[] of the head this lane owns
     float l_own = 0.f; // running sum of the owned head over this lane's tokens
     float2 acc[G][VEC / 2];
 #pragma unroll
@@ -284,75 +376,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
         }
         const T* ks = reinterpret_cast<const T*>(ring + stage * Shape::kStageBytes);
         const T* vs = ks + kDecodeTileRows * D;
-
-        // Scores of the owned head, one per step (token st*TPS + grp).
-        float sc[STEPS];
-#pragma unroll
-        for (int st = 0; st < STEPS; ++st) {
-          const int tok = st * TPS + grp;
-          float2 part2[G];
-#pragma unroll
-          for (int g = 0; g < G; ++g) part2[g] = make_float2(0.f, 0.f);
-          if (tok < rows) {
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-              float2 kf[4];
-              to_float2x4<T>(*reinterpret_cast<const uint4*>(ks + tok * D + (sub + c * LPT) * 8), kf);
-#pragma unroll
-              for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) part2[g] = ffma2(qf[g][c * 4 + e], kf[e], part2[g]);
-            }
-          }
-          float part[G];
-#pragma unroll
-          for (int g = 0; g < G; ++g) part[g] = part2[g].x + part2[g].y;
-          float x = reduce_scatter<G, LPT>(part, sub);
-          if constexpr (CAP) x = a.cap * tanhf(x / a.cap) * kLog2e;
-          sc[st] = tok < rows ? x : -INFINITY;
-        }
-        // Tile max of every head, known to all lanes; rescale only when it grows.
-        float mx = sc[0];
-#pragma unroll
-        for (int st = 1; st < STEPS; ++st) mx = fmaxf(mx, sc[st]);
-        mx = warp_max(mx, 16, LPT);
-        float m_own = -INFINITY;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float mg = __shfl_sync(kFull, mx, owner_of_head<G, LPT>(g));
-          if (mg > m[g]) {
-            const float alpha = fast_exp2(m[g] - mg);
-            const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-            for (int v = 0; v < VEC / 2; ++v) acc[g][v] = fmul2(acc[g][v], a2);
-            if (g == my_head) l_own *= alpha;
-            m[g] = mg;
-          }
-          if (g == my_head) m_own = m[g];
-        }
-#pragma unroll
-        for (int st = 0; st < STEPS; ++st) {
-          const int tok = st * TPS + grp;
-          const float p_own = fast_exp2(sc[st] - m_own);  // 0 for a masked token
-          l_own += p_own;
-          float2 p2[G];
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float pg_ = __shfl_sync(kFull, p_own, grp * LPT + owner_of_head<G, LPT>(g));
-            p2[g] = make_float2(pg_, pg_);
-          }
-          if (tok < rows) {
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-              float2 vf[4];
-              to_float2x4<T>(*reinterpret_cast<const uint4*>(vs + tok * D + (sub + c * LPT) * 8), vf);
-#pragma unroll
-              for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[g][c * 4 + e] = ffma2(p2[g], vf[e], acc[g][c * 4 + e]);
-            }
-          }
-        }
+        // Full tiles (every tile but the last of a page list) skip the per-token checks.
+        if (rows == kDecodeTileRows)
+          tile_step<D, G, LPT, T, CAP, true>(a, ks, vs, rows, sub, grp, my_head, qf, m, m_own, l_own, acc);
+        else
+          tile_step<D, G, LPT, T, CAP, false>(a, ks, vs, rows, sub, grp, my_head, qf, m, m_own, l_own, acc);
         ++consumed;
         __syncwarp();
         producer_issue<D, T>(prod, a, ring, bar0, lane, num_pages, policy);
