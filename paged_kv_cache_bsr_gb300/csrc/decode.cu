@@ -292,7 +292,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
   constexpr int VEC = D / LPT;     // dims per lane
   constexpr int CH = VEC / 8;      // 16-byte chunks per lane per row
   constexpr int TPS = 32 / LPT;    // tokens per step
-  constexpr int STEPS = kDecodeTileRows / TPS;
   static_assert(CH >= 1 && VEC % 8 == 0, "lane slice must be whole 16-byte chunks");
   static_assert(kDecodeTileRows % TPS == 0, "steps must tile the 16 rows");
   static_assert(G <= LPT, "every head needs an owning lane in the token group");
@@ -314,6 +313,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
   }
   __syncwarp();
 
+  // The merge kernel that follows may be scheduled now; it waits for this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int worker = blockIdx.x * kDecodeWarps + warp;
   const PlanHeader* hdr = a.hdr;
   if (worker >= hdr->num_workers) return;
@@ -457,6 +458,9 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __gri
   const int lane = threadIdx.x & 31;
   const int warp_id = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
   const int n_warps = gridDim.x * (kMergeThreads / 32);
+  // Launched as a programmatic dependent of the decode kernel: wait until that
+  // grid has finished and its partial states are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int pairs = a.hdr->num_merge * G;
   for (int pair = warp_id; pair < pairs; pair += n_warps) {
     const MergeItem it = a.merge[pair / G];
@@ -551,10 +555,21 @@ cudaError_t dispatch_decode(const DecodeArgs& a, int D, int G, bool cap, int gri
 
 template <typename T>
 cudaError_t dispatch_merge(const DecodeArgs& a, int D, int G, int grid, cudaStream_t s) {
-#define PKV_MERGE_CASE(DD, GG)                                            \
-  if (D == DD && G == GG) {                                               \
-    decode_merge_kernel<DD, GG, T><<<grid, kMergeThreads, 0, s>>>(a);     \
-    return cudaGetLastError();                                            \
+// The merge kernel is a programmatic dependent of the decode kernel just
+// before it on the stream: its launch overlaps the decode grid's tail, and it
+// waits (griddepcontrol.wait) for that grid before reading partial states.
+#define PKV_MERGE_CASE(DD, GG)                                                              \
+  if (D == DD && G == GG) {                                                                 \
+    cudaLaunchConfig_t cfg = {};                                                            \
+    cfg.gridDim = dim3(grid);                                                               \
+    cfg.blockDim = dim3(kMergeThreads);                                                     \
+    cfg.stream = s;                                                                         \
+    cudaLaunchAttribute attr[1];                                                            \
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                        \
+    attr[0].val.programmaticStreamSerializationAllowed = 1;                                 \
+    cfg.attrs = attr;                                                                       \
+    cfg.numAttrs = 1;                                                                       \
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<DD, GG, T>, a);                     \
   }
   PKV_MERGE_CASE(128, 1) PKV_MERGE_CASE(128, 2) PKV_MERGE_CASE(128, 4) PKV_MERGE_CASE(128, 8)
   PKV_MERGE_CASE(64, 1) PKV_MERGE_CASE(64, 2) PKV_MERGE_CASE(64, 4) PKV_MERGE_CASE(64, 8)

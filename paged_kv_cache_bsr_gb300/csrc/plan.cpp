@@ -246,6 +246,7 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
         emit(w0, s);
       } else {
         MergeItem m{row, h, n_slot, w1 - w0 + 1};
+        if (n_merge >= pl->max_merge || n_slot + m.n_slots > pl->max_slots) return PKV_ERR_WORKSPACE;
         merge[n_merge++] = m;
         for (int w = w0; w <= w1; ++w) {
           const int64_t lo = std::max<int64_t>(x, (int64_t)w * run) - x;
