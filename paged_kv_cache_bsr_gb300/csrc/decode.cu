@@ -313,8 +313,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
   }
   __syncwarp();
 
-  // The merge kernel that follows may be scheduled now; it waits for this grid.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int worker = blockIdx.x * kDecodeWarps + warp;
   const PlanHeader* hdr = a.hdr;
   if (worker >= hdr->num_workers) return;
@@ -556,8 +554,10 @@ cudaError_t dispatch_decode(const DecodeArgs& a, int D, int G, bool cap, int gri
 template <typename T>
 cudaError_t dispatch_merge(const DecodeArgs& a, int D, int G, int grid, cudaStream_t s) {
 // The merge kernel is a programmatic dependent of the decode kernel just
-// before it on the stream: its launch overlaps the decode grid's tail, and it
-// waits (griddepcontrol.wait) for that grid before reading partial states.
+// before it on the stream: it is launched as the decode CTAs exit (the decode
+// kernel triggers no earlier, so waiting merge CTAs never hold SMs that work on
+// another stream needs), and it waits (griddepcontrol.wait) for the whole
+// grid before reading partial states.
 #define PKV_MERGE_CASE(DD, GG)                                                              \
   if (D == DD && G == GG) {                                                                 \
     cudaLaunchConfig_t cfg = {};                                                            \
