@@ -235,7 +235,7 @@ __device__ __forceinline__ void tile_step(const DecodeArgs& a, const T* ks, cons
       part[g] = t.x + t.y;
     }
     float x = reduce_scatter<G, LPT>(part, sub);
-    if constexpr (CAP) x = a.cap * tanhf(x / a.cap) * kLog2e;
+    if constexpr (CAP) x = a.cap * kLog2e * tanh_from_log2(x * (2.f * kLog2e / a.cap));
     sc[st] = (FULL || tok < rows) ? x : -INFINITY;
   }
   // Tile max of the owned head over the token groups.

@@ -120,6 +120,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh(y) from the identity tanh(y) = 1 - 2 / (e^(2y) + 1), with e^(2y) written as
+// 2^(y * 2 log2(e)): the caller passes t = y * 2 log2(e).  Two SFU operations and no
+// branch; it saturates to +1 (e^(2y) = inf) and -1 (e^(2y) = 0).  Near 0 the
+// subtraction loses relative accuracy but the absolute error stays ~1e-7.
+__device__ __forceinline__ float tanh_from_log2(float t) {
+  return 1.f - 2.f * fast_rcp(fast_exp2(t) + 1.f);
+}
+
 // Packed fp32 fused multiply-add on a pair (sm_100 family FFMA2): d = a * b + c.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 d;

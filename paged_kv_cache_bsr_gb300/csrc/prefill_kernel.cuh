@@ -515,9 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Logits in log2 units are v * mul (the cap, when on, is applied to v first).
         float mul = scale;
         if constexpr (CAP) {
+          // cap * tanh(s * scale / cap), already in log2 units
+          const float k_in = scale * 2.f * kLog2e / a.cap, k_out = a.cap * kLog2e;
 #pragma unroll
           for (int i = 0; i < kBN; ++i)
-            sr[i] = __float_as_uint(a.cap * tanhf(__uint_as_float(sr[i]) * scale / a.cap) * kLog2e);
+            sr[i] = __float_as_uint(k_out * tanh_from_log2(__uint_as_float(sr[i]) * k_in));
           mul = 1.f;
         }
         if (!full) {
