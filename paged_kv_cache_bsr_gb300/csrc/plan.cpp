@@ -192,7 +192,8 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
   if (W <= 0) W = pl->workers;
   auto takes_part = [&](int b) { return !qo_indptr || qo_indptr[b + 1] - qo_indptr[b] == 1; };
   const int64_t pages_per_chunk = ceil_div(P, pkv::kDecodeTileRows);
-  const int64_t min_run = std::max<int64_t>(1, 8 / pages_per_chunk);  // keep runs >= 8 tiles
+  // Runs of at least 4 tiles: shorter ones no longer help small batches (measured).
+  const int64_t min_run = std::max<int64_t>(1, 4 / pages_per_chunk);
   int64_t total = 0;
   int parts = 0;
   for (int b = 0; b < batch; ++b)
