@@ -264,7 +264,9 @@ def decode_measure(b, steps, warmup, peaks, profile_name=None):
     import torch
     from paged_kv_cache_bsr_gb300 import runner, api
     db = runner.DeviceBatch.from_host(b)
-    plan = runner.make_plan(b, api.PLAN_DECODE)
+    # A step loop re-plans every call: the pipelined plan copies each step's tables
+    # while the previous step's kernels run.
+    plan = runner.make_plan(b, api.PLAN_DECODE, pipelined=True)
     o = torch.empty_like(db.q)
     lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.q.device)
     stream = torch.cuda.current_stream()

@@ -196,6 +196,20 @@ pkv_status pkv_plan_get_work(const pkv_plan* plan, int32_t* out, int64_t capacit
 pkv_status pkv_plan_set_timing_events(pkv_plan* plan, void* start, void* stop);
 
 /*
+ * Pipelined planning, for a step loop that re-plans every call (a serving loop's
+ * decode steps).  The plan keeps two images of its tables, in two halves of the
+ * host workspace and in two regions of the device workspace (both sizes from
+ * pkv_plan_workspace_bytes already include them).  With on != 0 each
+ * pkv_plan_run fills the image the previous run is not reading and copies it on a
+ * stream the plan owns, so that copy overlaps the previous call's kernels; the next
+ * run call waits for it on its own stream.  Not for CUDA-graph capture of the run
+ * calls (the image a run reads alternates).  Call before the first pkv_plan_run;
+ * device plans of kind DECODE or PREFILL only.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA.
+ */
+pkv_status pkv_plan_set_pipelined(pkv_plan* plan, int on);
+
+/*
  * Batch decode over the paged KV cache ("The Interface", step 3; guide
  * section 3 "FlashDecoding"): one query row per request, all query heads.
  * q and o: [batch, Hq, d]; lse: [batch, Hq] fp32 (may be NULL).

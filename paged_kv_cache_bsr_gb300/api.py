@@ -58,7 +58,7 @@ EXPORTS = [
     "pkv_plan_workspace_bytes", "pkv_plan_compute", "pkv_plan_run", "pkv_plan_get_info", "pkv_plan_get_work",
     "pkv_batch_decode_paged", "pkv_batch_prefill_paged", "pkv_merge_state", "pkv_get_device_error",
     "pkv_plan_set_timing_events", "pkv_batch_decode_paged_noalloc", "pkv_append_paged_kv",
-    "pkv_batch_prefill_paged_masked", "pkv_batch_mixed_paged",
+    "pkv_batch_prefill_paged_masked", "pkv_batch_mixed_paged", "pkv_plan_set_pipelined",
 ]
 
 
@@ -96,6 +96,7 @@ def load(path: Optional[str] = None):
             "pkv_batch_decode_paged_noalloc": (i32, [vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_batch_prefill_paged_masked": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
             "pkv_batch_mixed_paged": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "pkv_plan_set_pipelined": (i32, [vp, i32]),
             "pkv_append_paged_kv": (i32, [ctypes.POINTER(Params), i32, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
                                           vp, ctypes.c_double, vp, vp]),
         }
@@ -309,7 +310,7 @@ class Plan:
     def __init__(self, kind: int, *, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                  dtype: torch.dtype, sm_scale: float, logits_cap: float = 0.0, causal: bool = False,
                  max_batch: int, max_total_q: Optional[int] = None, max_kv_pages: int,
-                 device: Optional[int] = None):
+                 device: Optional[int] = None, pipelined: bool = False):
         self.kind = kind
         self.device = torch.cuda.current_device() if device is None else int(device)
         self.params = make_params(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, sm_scale, logits_cap,
@@ -321,6 +322,8 @@ class Plan:
         self.dev_ws = torch.empty(dev_bytes, dtype=torch.uint8, device=f"cuda:{self.device}")
         self.host_ws = torch.empty(host_bytes, dtype=torch.uint8, pin_memory=True)
         self.num_pages = 0
+        if pipelined:
+            _check(load().pkv_plan_set_pipelined(self.handle, 1), "pkv_plan_set_pipelined")
 
     def __del__(self):
         h = getattr(self, "handle", None)

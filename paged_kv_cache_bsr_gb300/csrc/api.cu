@@ -54,14 +54,29 @@ pkv_status check_device(const pkv_plan* plan) {
   return cur == plan->device ? PKV_OK : PKV_ERR_INVALID_ARG;
 }
 
+// Offset of the table image the next run reads (pipelined plans alternate two).
+size_t table_off(const pkv_plan* plan) { return (plan->pipelined && plan->cur) ? plan->L.alt : 0; }
+
 template <typename Args>
 void fill_tables(Args& a, const pkv_plan* plan, void* dev_ws) {
   auto* base = static_cast<uint8_t*>(dev_ws);
-  a.hdr = reinterpret_cast<const pkv::PlanHeader*>(base + plan->L.header);
-  a.worker_ptr = reinterpret_cast<const int32_t*>(base + plan->L.worker_ptr);
+  auto* tb = base + table_off(plan);
+  a.hdr = reinterpret_cast<const pkv::PlanHeader*>(tb + plan->L.header);
+  a.worker_ptr = reinterpret_cast<const int32_t*>(tb + plan->L.worker_ptr);
   a.part_o = reinterpret_cast<float*>(base + plan->L.part_o);
   a.part_lse = reinterpret_cast<float*>(base + plan->L.part_lse);
-  a.err = reinterpret_cast<int32_t*>(base + plan->L.header + offsetof(pkv::PlanHeader, error));
+  a.err = reinterpret_cast<int32_t*>(tb + plan->L.header + offsetof(pkv::PlanHeader, error));
+}
+
+// Pipelined plans: the run waits for its table image's copy, and marks the image
+// free again once its kernels have finished.
+cudaError_t wait_tables(const pkv_plan* plan, cudaStream_t s) {
+  return plan->pipelined ? cudaStreamWaitEvent(s, plan->copy_ev[plan->cur], 0) : cudaSuccess;
+}
+cudaError_t release_tables(const pkv_plan* plan, cudaStream_t s) {
+  if (!plan->pipelined) return cudaSuccess;
+  const_cast<pkv_plan*>(plan)->used[plan->cur] = true;
+  return cudaEventRecord(plan->free_ev[plan->cur], s);
 }
 
 }  // namespace
@@ -100,8 +115,8 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
   pkv::DecodeArgs a{};
   fill_tables(a, plan, dev_ws);
   auto* base = static_cast<uint8_t*>(dev_ws);
-  a.segs = reinterpret_cast<const pkv::DecodeSeg*>(base + plan->L.segs);
-  a.merge = reinterpret_cast<const pkv::MergeItem*>(base + plan->L.merge);
+  a.segs = reinterpret_cast<const pkv::DecodeSeg*>(base + table_off(plan) + plan->L.segs);
+  a.merge = reinterpret_cast<const pkv::MergeItem*>(base + table_off(plan) + plan->L.merge);
   a.q = q;
   a.kv = kv_data;
   a.kv_indices = kv_indices_d;
@@ -114,10 +129,12 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
   a.q_scale = cap ? p.sm_scale : p.sm_scale * pkv::kLog2e;
   a.cap = cap ? p.logits_cap : 0.f;
   auto s = static_cast<cudaStream_t>(stream);
-  if (plan->time_start) cudaEventRecord(plan->time_start, s);
-  cudaError_t e = pkv::launch_decode(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, s);
+  cudaError_t e = wait_tables(plan, s);
+  if (plan->time_start && e == cudaSuccess) cudaEventRecord(plan->time_start, s);
+  if (e == cudaSuccess) e = pkv::launch_decode(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, s);
   if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
   if (e == cudaSuccess) e = pkv::launch_decode_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
+  if (e == cudaSuccess) e = release_tables(plan, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
@@ -146,8 +163,8 @@ static pkv_status prefill_run(const pkv_plan* plan, const void* q, const int32_t
   pkv::PrefillArgs a{};
   fill_tables(a, plan, dev_ws);
   auto* base = static_cast<uint8_t*>(dev_ws);
-  a.tiles = reinterpret_cast<const pkv::PrefillTile*>(base + plan->L.segs);
-  a.merge = reinterpret_cast<const pkv::PrefillMerge*>(base + plan->L.merge);
+  a.tiles = reinterpret_cast<const pkv::PrefillTile*>(base + table_off(plan) + plan->L.segs);
+  a.merge = reinterpret_cast<const pkv::PrefillMerge*>(base + table_off(plan) + plan->L.merge);
   a.q = q;
   a.kv = kv_data;
   a.kv_indices = kv_indices_d;
@@ -163,12 +180,15 @@ static pkv_status prefill_run(const pkv_plan* plan, const void* q, const int32_t
   a.mask = reinterpret_cast<const uint32_t*>(mask);
   a.mask_words = mask ? static_cast<int64_t>(mask_bytes / 4) : 0;
   auto s = static_cast<cudaStream_t>(stream);
-  if (plan->time_start) cudaEventRecord(plan->time_start, s);
-  cudaError_t e = pkv::launch_prefill(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas,
-                                      plan->total_q, plan->num_pages, s);
+  cudaError_t e = wait_tables(plan, s);
+  if (plan->time_start && e == cudaSuccess) cudaEventRecord(plan->time_start, s);
+  if (e == cudaSuccess)
+    e = pkv::launch_prefill(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, plan->total_q,
+                            plan->num_pages, s);
   if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
   if (e == cudaSuccess)
     e = pkv::launch_prefill_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
+  if (e == cudaSuccess) e = release_tables(plan, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
@@ -272,18 +292,23 @@ pkv_status pkv_get_device_error(const pkv_plan* plan, void* dev_ws, int* code, i
     return st;
   }
   auto s = static_cast<cudaStream_t>(stream);
-  auto* word = static_cast<uint8_t*>(dev_ws) + plan->L.header + offsetof(pkv::PlanHeader, error);
-  int32_t v = 0;
-  if (cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess) {
-    cudaGetLastError();
-    return PKV_ERR_CUDA;
-  }
-  *code = v;
-  if (clear && v) {
-    if (cudaMemsetAsync(word, 0, sizeof(int32_t), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+  *code = 0;
+  // Both table images of a pipelined plan carry an error word.
+  for (int r = 0; r < (plan->pipelined ? 2 : 1); ++r) {
+    auto* word = static_cast<uint8_t*>(dev_ws) + (r ? plan->L.alt : 0) + plan->L.header +
+                 offsetof(pkv::PlanHeader, error);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
       cudaGetLastError();
       return PKV_ERR_CUDA;
+    }
+    *code |= v;
+    if (clear && v) {
+      if (cudaMemsetAsync(word, 0, sizeof(int32_t), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+      }
     }
   }
   return PKV_OK;

@@ -56,7 +56,8 @@ extern "C" pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const
                                                      const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
                                                      const int32_t* kv_last_page_len_d, void* o, float* lse,
                                                      void* stream) {
-  if (!plan || plan->kind != PKV_PLAN_DECODE || !plan->planned || plan->device < 0) return PKV_ERR_INVALID_ARG;
+  if (!plan || plan->kind != PKV_PLAN_DECODE || !plan->planned || plan->device < 0 || plan->pipelined)
+    return PKV_ERR_INVALID_ARG;
   if (!host_tables || host_tables_bytes < plan->used_bytes) return PKV_ERR_INVALID_ARG;
   if (!q || !kv_data || !kv_indices_d || !kv_indptr_d || !kv_last_page_len_d || !o) return PKV_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_data, 16) || !aligned(o, 16) || !aligned(kv_indices_d, 4) ||

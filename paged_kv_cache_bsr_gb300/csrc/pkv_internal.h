@@ -104,6 +104,7 @@ struct WorkspaceLayout {
   size_t tables_end;   // everything above is copied from the pinned host buffer
   size_t part_o;       // fp32 [max_slots][rows_per_slot][head_dim]
   size_t part_lse;     // fp32 [max_slots][rows_per_slot]
+  size_t alt;          // a second copy of the tables [0, tables_end), for pipelined plans
   size_t total;
 };
 

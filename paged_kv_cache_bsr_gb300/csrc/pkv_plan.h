@@ -43,6 +43,17 @@ struct pkv_plan {
   // The copy of the tables out of the pinned buffer.
   cudaEvent_t copy_done = nullptr;
   bool copy_pending = false;
+  // Pipelined plans (pkv_plan_set_pipelined): the tables alternate between two
+  // images (host region r at r * tables_end, device region 0 at 0 and 1 at
+  // L.alt); each plan_run copies the next image on copy_stream while the
+  // previous run's kernels still read the other one.
+  bool pipelined = false;
+  int cur = 0;                       // image the next run reads
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t copy_ev[2] = {nullptr, nullptr};   // image r copied
+  cudaEvent_t free_ev[2] = {nullptr, nullptr};   // the last run reading image r has finished
+  bool copy_pend[2] = {false, false};
+  bool used[2] = {false, false};
   // Caller events recorded around the main kernel (pkv_plan_set_timing_events).
   cudaEvent_t time_start = nullptr;
   cudaEvent_t time_stop = nullptr;

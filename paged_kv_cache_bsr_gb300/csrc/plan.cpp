@@ -78,7 +78,8 @@ void set_layout(pkv_plan* pl) {
   L.tables_end = align_up(L.segs + work_bytes * std::max(pl->max_work, 1), 256);
   L.part_o = L.tables_end;
   L.part_lse = align_up(L.part_o + sizeof(float) * (size_t)pl->max_slots * pl->rows_per_slot * pl->p.head_dim, 256);
-  L.total = align_up(L.part_lse + sizeof(float) * (size_t)pl->max_slots * pl->rows_per_slot, 256);
+  L.alt = align_up(L.part_lse + sizeof(float) * (size_t)pl->max_slots * pl->rows_per_slot, 256);
+  L.total = L.alt + L.tables_end;
 }
 
 pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const pkv_limits* limits,
@@ -142,7 +143,7 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
     pl->merge_grid = num_sms * 4;
   }
   set_layout(pl);
-  pl->host_bytes = pl->L.tables_end;
+  pl->host_bytes = 2 * pl->L.tables_end;  // two table images: see pkv_plan_set_pipelined
   *out = pl;
   return PKV_OK;
 }
@@ -566,6 +567,14 @@ pkv_status pkv_plan_destroy(pkv_plan* plan) {
     cudaStreamSynchronize(plan->side);
     cudaStreamDestroy(plan->side);
   }
+  if (plan->copy_stream) {
+    cudaStreamSynchronize(plan->copy_stream);
+    cudaStreamDestroy(plan->copy_stream);
+  }
+  for (int r = 0; r < 2; ++r) {
+    if (plan->copy_ev[r]) cudaEventDestroy(plan->copy_ev[r]);
+    if (plan->free_ev[r]) cudaEventDestroy(plan->free_ev[r]);
+  }
   if (plan->fork) cudaEventDestroy(plan->fork);
   if (plan->join) cudaEventDestroy(plan->join);
   delete plan->sub_dec;
@@ -594,6 +603,15 @@ pkv_status pkv_plan_compute(pkv_plan* plan, int batch, const int32_t* qo_indptr_
     plan->copy_pending = false;
   }
   auto* host = static_cast<uint8_t*>(host_ws);
+  if (plan->pipelined) {
+    // Plan into the image the running kernels do not read; its last copy must be done.
+    const int r = plan->cur ^ 1;
+    if (plan->copy_pend[r]) {
+      cudaEventSynchronize(plan->copy_ev[r]);
+      plan->copy_pend[r] = false;
+    }
+    host += static_cast<size_t>(r) * plan->L.tables_end;
+  }
   if (plan->kind == PKV_PLAN_MIXED) {
     st = compute_mixed(plan, batch, qo_indptr_h, kv_indptr_h, kv_last_page_len_h, num_pages, host);
   } else if (plan->kind == PKV_PLAN_DECODE) {
@@ -622,6 +640,22 @@ pkv_status pkv_plan_run(pkv_plan* plan, int batch, const int32_t* qo_indptr_h, c
   if (st != PKV_OK) return st;
   auto s = static_cast<cudaStream_t>(stream);
   bool ok = true;
+  if (plan->pipelined) {
+    const int r = plan->cur ^ 1;
+    auto* dst = static_cast<uint8_t*>(dev_ws) + (r ? plan->L.alt : 0);
+    auto* src = static_cast<uint8_t*>(host_ws) + static_cast<size_t>(r) * plan->L.tables_end;
+    ok = (!plan->used[r] || cudaStreamWaitEvent(plan->copy_stream, plan->free_ev[r], 0) == cudaSuccess) &&
+         cudaMemcpyAsync(dst, src, plan->used_bytes, cudaMemcpyHostToDevice, plan->copy_stream) == cudaSuccess &&
+         cudaEventRecord(plan->copy_ev[r], plan->copy_stream) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      plan->planned = false;
+      return PKV_ERR_CUDA;
+    }
+    plan->copy_pend[r] = true;
+    plan->cur = r;
+    return PKV_OK;
+  }
   if (plan->kind == PKV_PLAN_MIXED) {
     auto* d = static_cast<uint8_t*>(dev_ws);
     auto* h = static_cast<uint8_t*>(host_ws);
@@ -638,6 +672,32 @@ pkv_status pkv_plan_run(pkv_plan* plan, int batch, const int32_t* qo_indptr_h, c
     return PKV_ERR_CUDA;
   }
   plan->copy_pending = true;
+  return PKV_OK;
+}
+
+pkv_status pkv_plan_set_pipelined(pkv_plan* plan, int on) {
+  if (!plan || plan->device < 0 || plan->kind == PKV_PLAN_MIXED || plan->planned) return PKV_ERR_INVALID_ARG;
+  if (!on) {
+    plan->pipelined = false;
+    return PKV_OK;
+  }
+  if (!plan->copy_stream) {
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(plan->device);
+    cudaError_t e = cudaStreamCreateWithFlags(&plan->copy_stream, cudaStreamNonBlocking);
+    for (int r = 0; r < 2 && e == cudaSuccess; ++r) {
+      e = cudaEventCreateWithFlags(&plan->copy_ev[r], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&plan->free_ev[r], cudaEventDisableTiming);
+    }
+    cudaSetDevice(prev);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+  }
+  plan->pipelined = true;
+  plan->cur = 1;  // the first plan_run fills image 0
   return PKV_OK;
 }
 

@@ -262,3 +262,31 @@ def test_split_decode_merged_with_merge_state_equals_unsplit():
     torch.cuda.synchronize()
     ref_o, ref_lse = oracle.attention_of(b)
     assert_matches_oracle(o1, l1, ref_o, ref_lse, torch.bfloat16, "split + merge_state")
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill"])
+def test_pipelined_plan_steps_without_sync(kind):
+    """A pipelined plan re-planned every step with no host sync in between: each step's
+    tables are copied on the plan's own stream while the previous step runs; every
+    step's output must still match its own batch."""
+    batches = []
+    for i, kvs in enumerate(([40, 300, 17], [41, 301, 18, 900], [42, 5], [43, 302, 19, 901, 60])):
+        qo = [1] * len(kvs) if kind == "decode" else [min(k, 37 + 11 * j) for j, k in enumerate(kvs)]
+        batches.append(W.make_paged_batch(qo_lens=qo, kv_lens=kvs, num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                                          page_size=16, dtype=torch.bfloat16, seed=70 + i, causal=kind == "prefill",
+                                          poison=True))
+    max_b = max(b.batch for b in batches)
+    max_q = max(b.total_q for b in batches)
+    max_p = max(int(b.kv_indptr[-1]) for b in batches)
+    k = api.PLAN_DECODE if kind == "decode" else api.PLAN_PREFILL
+    plan = runner.make_plan(batches[0], k, pipelined=True, max_batch=max_b, max_total_q=max_q, max_kv_pages=max_p)
+    dev = [runner.DeviceBatch.from_host(b) for b in batches]
+    outs = []
+    for b, d in zip(batches, dev):
+        runner.plan_batch(plan, b)
+        outs.append(runner.decode(d, plan) if kind == "decode" else runner.prefill(d, plan))
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    for b, (o, lse) in zip(batches, outs):
+        ref_o, ref_lse = oracle.attention_of(b)
+        assert_matches_oracle(o, lse, ref_o, ref_lse, b.dtype, f"pipelined {kind}")
