@@ -337,7 +337,7 @@ def prefill_measure(peaks, steps=20, warmup=3, page_size=16):
     from paged_kv_cache_bsr_gb300 import runner, api, workloads as W
     b = W.ragged_prefill(seed=1003, page_size=page_size)
     try:
-        plan = runner.make_plan(b, api.PLAN_PREFILL)
+        plan = runner.make_plan(b, api.PLAN_PREFILL, pipelined=True)
     except api.PkvError as e:
         return {"unavailable": str(e)}
     db = runner.DeviceBatch.from_host(b)
