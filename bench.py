@@ -4,13 +4,16 @@
 One step = one pass of the decode hot path over one batch of the
 Llama-3-8B-shaped decode workload (batch 64, 32 q / 8 kv heads, head_dim 128,
 page 16, bf16, kv_len ~ U[512, 4096], randomly permuted page pool): the host
-plan (validation + equal-chunk split) with its copy to the device, the
-split-KV decode kernel and the log-sum-exp merge kernel, all through the C ABI.
-Inputs are resident in HBM; the KV read per step (~0.63 GB) is larger than L2,
-so no flush is needed between steps.
+plan (validation + equal-chunk split) with its copy to the device (a pipelined
+plan: the copy overlaps the previous step's kernels), the split-KV decode kernel
+and the log-sum-exp merge kernel, all through the C ABI.  Inputs are resident in
+HBM; the KV read per step (~0.63 GB) is larger than L2, so no flush is needed
+between steps.
 
 The JSON line also carries the prefill (ragged causal, tensor cores), skewed
-long-context decode and cascade measurements under "secondary".
+long-context decode, cascade, multi-level cascade, append + RoPE, tree
+verification, mixed batch and column-vector prefill measurements under
+"secondary".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -470,10 +473,29 @@ def cascade_measure(steps=50, warmup=5):
         casc()
         full()
     s.synchronize()
+    # the same cascade as one mixed launch: prefix prefill beside the suffix decode
+    m = W.cascade_as_mixed(cb.prefix, cb.suffix)
+    dm = runner.DeviceBatch.from_host(m, kv_data=kv)
+    mplan = runner.make_plan(m, api.PLAN_MIXED)
+    with torch.cuda.stream(s):
+        runner.plan_batch(mplan, m, stream=s)
+        o_m = torch.empty_like(dm.q)
+        l_m = torch.empty(dm.q.shape[:2], dtype=torch.float32, device=dm.q.device)
+    B = cb.suffix.batch
+
+    def casc_mixed():
+        mplan.run(dm.q, kv, dm.kv_indices, dm.kv_indptr, dm.kv_last_page_len, o_m, l_m, qo_indptr=dm.qo_indptr,
+                  stream=s)
+        api.merge_state(o_m[B:], l_m[B:], o_m[:B], l_m[:B], o_m[B:], l_m[B:], stream=s)
+
+    with torch.cuda.stream(s):
+        casc_mixed()
+    s.synchronize()
     out = {"workload": "cascade_softcap_decode"}
-    for name, fn in (("cascade", casc), ("non_cascade", full)):
+    for name, fn in (("cascade", casc), ("cascade_one_mixed_launch", casc_mixed), ("non_cascade", full)):
         out[name + "_us"] = graph_us(fn, s, steps, warmup)
-    out["speedup"] = round(out["non_cascade_us"] / out["cascade_us"], 3)
+    out["best_cascade_us"] = min(out["cascade_us"], out["cascade_one_mixed_launch_us"])
+    out["speedup"] = round(out["non_cascade_us"] / out["best_cascade_us"], 3)
     out["non_cascade_kv_GBps"] = round(cb.full.kv_bytes() / (out["non_cascade_us"] * 1e-6) / 1e9, 1)
     out["timing"] = "CUDA-graph replay of the run calls; plans made once outside the timed loop"
     return out

@@ -119,6 +119,18 @@ def mixed(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None) -> Tupl
     return o, lse
 
 
+def cascade_mixed(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None
+                  ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Cascade attention as one mixed launch: ``db`` holds
+    ``workloads.cascade_as_mixed(prefix, suffix)``.  The prefix row block runs on the
+    prefill kernel and the suffixes on the decode kernel side by side, then one
+    merge_state folds the prefix states (rows 0..B-1) into the suffix states."""
+    o, lse = mixed(db, plan, stream)
+    B = db.host.batch - 1
+    api.merge_state(o[B:], lse[B:], o[:B], lse[:B], o[B:], lse[B:], stream=stream)
+    return o[B:], lse[B:]
+
+
 def level_kind(b) -> int:
     """A level whose nodes each hold one query row is plain decode; a level with
     multi-row blocks (a prefix shared by several requests) runs on the prefill

@@ -44,6 +44,7 @@ __all__ = [
     "tree_verify",
     "mixed_batch",
     "sub_batch",
+    "cascade_as_mixed",
     "WORKLOADS",
 ]
 
@@ -526,6 +527,25 @@ def sub_batch(b: PagedBatch, requests: Sequence[int], name: str = "") -> PagedBa
         kv_indices=torch.cat(pages) if pages else b.kv_indices[:0],
         kv_last_page_len=b.kv_last_page_len[reqs] if reqs else b.kv_last_page_len[:0],
         qo_lens=[b.qo_lens[r] for r in reqs], kv_lens=[b.kv_lens[r] for r in reqs], name=name or b.name)
+
+
+def cascade_as_mixed(prefix: PagedBatch, suffix: PagedBatch) -> PagedBatch:
+    """One mixed batch holding both halves of a cascade: request 0 is the prefix row
+    block (all B query rows against the shared pages), requests 1..B are the suffixes
+    (one row each).  The queries appear twice (rows 0..B-1 and B..2B-1), so the two
+    partial states land in separate output rows, ready for merge_state."""
+    B = suffix.batch
+    qo = torch.zeros(B + 2, dtype=torch.int32)
+    qo[1] = prefix.total_q
+    qo[2:] = prefix.total_q + torch.arange(1, B + 1, dtype=torch.int32)
+    n_pre = int(prefix.kv_indptr[-1])
+    kv_indptr = torch.cat([torch.tensor([0], dtype=torch.int32), n_pre + suffix.kv_indptr.to(torch.int32)])
+    return dataclasses.replace(
+        suffix, q=torch.cat([prefix.q, suffix.q]), qo_indptr=qo, kv_indptr=kv_indptr,
+        kv_indices=torch.cat([prefix.kv_indices, suffix.kv_indices]),
+        kv_last_page_len=torch.cat([prefix.kv_last_page_len, suffix.kv_last_page_len]),
+        qo_lens=[prefix.total_q] + list(suffix.qo_lens), kv_lens=list(prefix.kv_lens) + list(suffix.kv_lens),
+        causal=False, name="cascade_mixed")
 
 
 WORKLOADS = {

@@ -128,3 +128,20 @@ def test_mixed_graph_replay_after_replanning():
         ref_o, ref_lse = oracle.attention_of(b)
         assert_matches_oracle(o, lse, ref_o, ref_lse, torch.bfloat16, "mixed graph replay")
     assert plan.device_error() == 0
+
+
+def test_cascade_as_one_mixed_launch_full_size():
+    """The 64-request soft-capped cascade as one mixed launch (prefix row block on the
+    prefill kernel beside the suffixes on the decode kernel) + merge_state."""
+    cb = W.cascade_decode(seed=1004, poison=True)
+    m = W.cascade_as_mixed(cb.prefix, cb.suffix)
+    db = runner.DeviceBatch.from_host(m)
+    plan = runner.make_plan(m, api.PLAN_MIXED)
+    runner.plan_batch(plan, m)
+    o, lse = runner.cascade_mixed(db, plan)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    info = plan.info()
+    assert info.prefill_ctas >= 1 and info.decode_ctas >= 1
+    ref_o, ref_lse = oracle.attention_of(cb.full)
+    assert_matches_oracle(o, lse, ref_o, ref_lse, torch.bfloat16, "cascade as mixed")

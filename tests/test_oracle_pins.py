@@ -614,3 +614,17 @@ def test_tree_verify_mask_is_prefix_plus_ancestors():
     ocr, lcr = oracle.attention_of(causal)
     np.testing.assert_array_equal(oc, ocr)
     np.testing.assert_array_equal(lc, lcr)
+
+
+def test_cascade_as_one_mixed_batch_equals_full_attention():
+    """The mixed-batch form of a cascade (prefix row block + one-row suffix requests,
+    queries listed twice) gives both partial states; their merge is full attention."""
+    cb = W.cascade_decode(seed=43, batch=5, prefix_len=48, suffix_lo=2, suffix_hi=30, num_qo_heads=4,
+                          num_kv_heads=2, head_dim=16, logits_cap=20.0, poison=True)
+    m = W.cascade_as_mixed(cb.prefix, cb.suffix)
+    assert m.qo_lens == [5, 1, 1, 1, 1, 1] and m.total_q == 10
+    o, lse = oracle.attention_of(m)
+    om, lm = oracle.merge_states([o[5:], o[:5]], [lse[5:], lse[:5]])
+    of, lf = oracle.attention_of(cb.full)
+    np.testing.assert_allclose(om, of, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lm, lf, rtol=0, atol=1e-12)
