@@ -119,16 +119,25 @@ def mixed(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None) -> Tupl
     return o, lse
 
 
+def levels_mixed(db: DeviceBatch, n_levels: int, plan: Optional[api.Plan] = None, stream=None
+                 ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """A prefix tree (or a cascade, n_levels = 2) as one mixed launch: ``db`` holds
+    ``workloads.levels_as_mixed(levels)``.  Multi-row nodes run on the prefill kernel
+    and single-row nodes on the decode kernel side by side; merge_state then folds
+    every level's rows into the last level's."""
+    o, lse = mixed(db, plan, stream)
+    R = db.q.shape[0] // n_levels
+    o_out, l_out = o[(n_levels - 1) * R:], lse[(n_levels - 1) * R:]
+    for lvl in range(n_levels - 1):
+        api.merge_state(o_out, l_out, o[lvl * R:(lvl + 1) * R], lse[lvl * R:(lvl + 1) * R], o_out, l_out,
+                        stream=stream)
+    return o_out, l_out
+
+
 def cascade_mixed(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None
                   ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Cascade attention as one mixed launch: ``db`` holds
-    ``workloads.cascade_as_mixed(prefix, suffix)``.  The prefix row block runs on the
-    prefill kernel and the suffixes on the decode kernel side by side, then one
-    merge_state folds the prefix states (rows 0..B-1) into the suffix states."""
-    o, lse = mixed(db, plan, stream)
-    B = db.host.batch - 1
-    api.merge_state(o[B:], lse[B:], o[:B], lse[:B], o[B:], lse[B:], stream=stream)
-    return o[B:], lse[B:]
+    """Cascade attention as one mixed launch (``workloads.cascade_as_mixed``)."""
+    return levels_mixed(db, 2, plan, stream)
 
 
 def level_kind(b) -> int:

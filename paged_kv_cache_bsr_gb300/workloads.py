@@ -45,6 +45,7 @@ __all__ = [
     "mixed_batch",
     "sub_batch",
     "cascade_as_mixed",
+    "levels_as_mixed",
     "WORKLOADS",
 ]
 
@@ -529,23 +530,34 @@ def sub_batch(b: PagedBatch, requests: Sequence[int], name: str = "") -> PagedBa
         qo_lens=[b.qo_lens[r] for r in reqs], kv_lens=[b.kv_lens[r] for r in reqs], name=name or b.name)
 
 
-def cascade_as_mixed(prefix: PagedBatch, suffix: PagedBatch) -> PagedBatch:
-    """One mixed batch holding both halves of a cascade: request 0 is the prefix row
-    block (all B query rows against the shared pages), requests 1..B are the suffixes
-    (one row each).  The queries appear twice (rows 0..B-1 and B..2B-1), so the two
-    partial states land in separate output rows, ready for merge_state."""
-    B = suffix.batch
-    qo = torch.zeros(B + 2, dtype=torch.int32)
-    qo[1] = prefix.total_q
-    qo[2:] = prefix.total_q + torch.arange(1, B + 1, dtype=torch.int32)
-    n_pre = int(prefix.kv_indptr[-1])
-    kv_indptr = torch.cat([torch.tensor([0], dtype=torch.int32), n_pre + suffix.kv_indptr.to(torch.int32)])
+def levels_as_mixed(levels: Sequence[PagedBatch]) -> PagedBatch:
+    """One mixed batch holding every level of a prefix tree (or both halves of a
+    cascade): the levels' requests one after another, each level's query rows listed
+    again (level l's rows are l*R .. l*R + R - 1 for R request rows), so every level's
+    partial states land in their own output rows, ready for merge_state.  Multi-row
+    nodes go to the prefill kernel and single-row ones to the decode kernel."""
+    R = levels[0].total_q
+    qo_lens, kv_lens, qo_parts, kv_ptr, idx, last = [], [], [0], [0], [], []
+    for lv in levels:
+        if lv.total_q != R:
+            raise ValueError("every level must cover the same request rows")
+        qo_lens += list(lv.qo_lens)
+        kv_lens += list(lv.kv_lens)
+        base_q, base_p = qo_parts[-1], kv_ptr[-1]
+        qo_parts += [base_q + int(x) for x in lv.qo_indptr[1:]]
+        kv_ptr += [base_p + int(x) for x in lv.kv_indptr[1:]]
+        idx.append(lv.kv_indices)
+        last.append(lv.kv_last_page_len)
     return dataclasses.replace(
-        suffix, q=torch.cat([prefix.q, suffix.q]), qo_indptr=qo, kv_indptr=kv_indptr,
-        kv_indices=torch.cat([prefix.kv_indices, suffix.kv_indices]),
-        kv_last_page_len=torch.cat([prefix.kv_last_page_len, suffix.kv_last_page_len]),
-        qo_lens=[prefix.total_q] + list(suffix.qo_lens), kv_lens=list(prefix.kv_lens) + list(suffix.kv_lens),
-        causal=False, name="cascade_mixed")
+        levels[-1], q=torch.cat([lv.q for lv in levels]), qo_indptr=torch.tensor(qo_parts, dtype=torch.int32),
+        kv_indptr=torch.tensor(kv_ptr, dtype=torch.int32), kv_indices=torch.cat(idx),
+        kv_last_page_len=torch.cat(last), qo_lens=qo_lens, kv_lens=kv_lens, causal=False, name="levels_mixed")
+
+
+def cascade_as_mixed(prefix: PagedBatch, suffix: PagedBatch) -> PagedBatch:
+    """Both halves of a cascade as one mixed batch: request 0 is the prefix row block
+    (rows 0..B-1), requests 1..B the suffixes (rows B..2B-1); see levels_as_mixed."""
+    return levels_as_mixed([prefix, suffix])
 
 
 WORKLOADS = {

@@ -125,3 +125,18 @@ def test_graph_capture_with_side_streams_replays():
         g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o_g, o_e) and torch.equal(l_g, l_e)
+
+
+def test_parallel_generation_as_one_mixed_launch():
+    """The full-size 3-level tree as one mixed launch (system prompt and shared prompts
+    on the prefill kernel beside the own tokens on the decode kernel) + merge_state."""
+    mb = W.parallel_generation(seed=1005, poison=True)
+    m = W.levels_as_mixed(mb.levels)
+    db = runner.DeviceBatch.from_host(m)
+    plan = runner.make_plan(m, api.PLAN_MIXED)
+    runner.plan_batch(plan, m)
+    o, lse = runner.levels_mixed(db, 3, plan)
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    ref_o, ref_lse = oracle.attention_of(mb.full)
+    assert_matches_oracle(o, lse, ref_o, ref_lse, mb.full.dtype, "tree as one mixed launch")

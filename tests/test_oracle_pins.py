@@ -628,3 +628,19 @@ def test_cascade_as_one_mixed_batch_equals_full_attention():
     of, lf = oracle.attention_of(cb.full)
     np.testing.assert_allclose(om, of, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lm, lf, rtol=0, atol=1e-12)
+
+
+def test_prefix_tree_as_one_mixed_batch_equals_full_attention():
+    """Three levels of a prefix tree as one mixed batch (every level's rows listed
+    again): merging the levels' row blocks gives attention over each whole path."""
+    mb = W.parallel_generation(seed=44, num_prompts=3, samples=4, system_len=32, prompt_lo=8, prompt_hi=60,
+                               gen_lo=1, gen_hi=30, num_qo_heads=4, num_kv_heads=2, head_dim=16, page_size=8,
+                               poison=True)
+    m = W.levels_as_mixed(mb.levels)
+    R = mb.full.batch
+    assert m.total_q == 3 * R and m.batch == sum(lv.batch for lv in mb.levels)
+    o, lse = oracle.attention_of(m)
+    om, lm = oracle.merge_states([o[l * R:(l + 1) * R] for l in range(3)], [lse[l * R:(l + 1) * R] for l in range(3)])
+    of, lf = oracle.attention_of(mb.full)
+    np.testing.assert_allclose(om, of, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lm, lf, rtol=0, atol=1e-12)
