@@ -742,6 +742,11 @@ def run_own(args):
                 "identity_pages_ms": round(r_id["ms_per_step"], 4), "permuted_pages_ms": round(ms, 4),
                 "overhead_pct": round((ms / r_id["ms_per_step"] - 1) * 100, 2)}
             del ident
+            col = W.llama3_decode(seed=1001, page_size=1)
+            r1 = decode_measure(col, max(20, args.steps // 10), 5, peaks)
+            secondary["decode_page_size_1"] = {"value": round(r1["value"], 1), "unit": "GB/s",
+                                               "ms_per_step": round(r1["ms_per_step"], 4), "roofline": r1["roofline"]}
+            del col
             secondary["prefill"] = prefill_measure(peaks)
             secondary["cascade"] = cascade_measure()
             secondary["multilevel_cascade"] = multilevel_measure()

@@ -62,28 +62,32 @@ __device__ __forceinline__ SegInfo load_seg(const DecodeSeg* segs, int i, int la
   return s;
 }
 
-// The copy side of a warp's ring: walks the same (segment, page, 16-row chunk)
-// sequence as the compute side, S tiles ahead of it.  Page ids come from a
-// 32-entry window of kv_indices held one per lane.
+// The copy side of a warp's ring: walks the same (segment, 16-token tile)
+// sequence as the compute side, S tiles ahead of it.  A tile is 16 consecutive
+// tokens of the segment; with pages of 16 rows or more it lies in one page (one
+// bulk copy each for K and V), with smaller pages it spans several, one lane per
+// page.  Page ids come from a 32-entry window of kv_indices held one per lane.
 struct Producer {
   int seg, seg_end;
-  int page, chunk;
-  int idx_begin, n_pages, last_rows, kvh;
+  int tok, n_tok;
+  int idx_begin, kvh;
   int win_base, win;
   int issued;
 };
+
+__device__ __forceinline__ int seg_tokens(int n_pages, int last_rows, int P) {
+  return n_pages > 0 ? (n_pages - 1) * P + last_rows : 0;
+}
 
 template <int D, typename T>
 __device__ __forceinline__ void producer_enter(Producer& p, const DecodeArgs& a, int lane) {
   const SegInfo s = load_seg(a.segs, p.seg, lane);
   p.idx_begin = s.idx_begin;
-  p.n_pages = s.n_pages;
-  p.last_rows = s.last_rows;
+  p.n_tok = seg_tokens(s.n_pages, s.last_rows, a.page_size);
   p.kvh = s.kvh;
-  p.page = 0;
-  p.chunk = 0;
+  p.tok = 0;
   p.win_base = 0;
-  p.win = lane < p.n_pages ? __ldg(a.kv_indices + p.idx_begin + lane) : 0;
+  p.win = lane < s.n_pages ? __ldg(a.kv_indices + p.idx_begin + lane) : 0;
 }
 
 // Issue the next tile of the warp's stream into its stage; false when done.
@@ -93,40 +97,41 @@ __device__ __forceinline__ bool producer_issue(Producer& p, const DecodeArgs& a,
                                                uint64_t policy) {
   using Shape = DecodeShape<D, T>;
   while (p.seg < p.seg_end) {
-    if (p.page < p.n_pages) {
-      if (p.page - p.win_base >= 32) {
-        p.win_base = p.page;
-        p.win = (p.page + lane < p.n_pages) ? __ldg(a.kv_indices + p.idx_begin + p.page + lane) : 0;
-      }
-      int page_id = __shfl_sync(kFull, p.win, p.page - p.win_base);
+    if (p.tok < p.n_tok) {
       const int P = a.page_size;
-      const int rows_in_page = (p.page == p.n_pages - 1) ? p.last_rows : P;
-      const int r0 = p.chunk * kDecodeTileRows;
-      const int rows = min(kDecodeTileRows, rows_in_page - r0);
-      if (page_id < 0 || page_id >= num_pages) {
-        if (lane == 0) atomicOr(a.err, kErrPageIndex);
-        page_id = 0;
+      const int rows = min(kDecodeTileRows, p.n_tok - p.tok);
+      const int pa = p.tok / P, pb = (p.tok + rows - 1) / P;  // pages the tile overlaps
+      if (pb - p.win_base >= 32) {
+        p.win_base = pa;
+        const int n_pages = (p.n_tok + P - 1) / P;
+        p.win = (pa + lane < n_pages) ? __ldg(a.kv_indices + p.idx_begin + pa + lane) : 0;
       }
       const int stage = p.issued % Shape::kStages;
-      if (lane == 0) {
-        const uint32_t bytes = static_cast<uint32_t>(rows) * D * sizeof(T);
+      const uint32_t dst = smem_addr(ring + stage * Shape::kStageBytes);
+      const uint32_t bar = bar0 + 8 * stage;
+      if (lane == 0) mbar_arrive_expect_tx(bar, 2u * rows * D * sizeof(T));
+      __syncwarp();
+      const int k = pa + lane;  // this lane's page
+      int page_id = __shfl_sync(kFull, p.win, min(k - p.win_base, 31));
+      if (k <= pb) {
+        if (page_id < 0 || page_id >= num_pages) {
+          atomicOr(a.err, kErrPageIndex);
+          page_id = 0;
+        }
+        const int r_lo = max(p.tok, k * P) - k * P;           // rows of the page inside the tile
+        const int r_hi = min(p.tok + rows, (k + 1) * P) - k * P;
+        const uint32_t bytes = static_cast<uint32_t>(r_hi - r_lo) * D * sizeof(T);
+        const uint32_t off = static_cast<uint32_t>(k * P + r_lo - p.tok) * D * sizeof(T);
         const T* kv = static_cast<const T*>(a.kv);
         const int64_t head_rows = static_cast<int64_t>(P) * D;  // elements of one (page, K|V, head)
         const T* k_src = kv + ((static_cast<int64_t>(page_id) * 2 + 0) * a.num_kv_heads + p.kvh) * head_rows +
-                         static_cast<int64_t>(r0) * D;
+                         static_cast<int64_t>(r_lo) * D;
         const T* v_src = k_src + static_cast<int64_t>(a.num_kv_heads) * head_rows;
-        const uint32_t dst = smem_addr(ring + stage * Shape::kStageBytes);
-        const uint32_t bar = bar0 + 8 * stage;
-        mbar_arrive_expect_tx(bar, 2 * bytes);
-        bulk_copy_g2s_hint(dst, k_src, bytes, bar, policy);
-        bulk_copy_g2s_hint(dst + Shape::kTileBytes, v_src, bytes, bar, policy);
+        bulk_copy_g2s_hint(dst + off, k_src, bytes, bar, policy);
+        bulk_copy_g2s_hint(dst + Shape::kTileBytes + off, v_src, bytes, bar, policy);
       }
       ++p.issued;
-      ++p.chunk;
-      if (p.chunk * kDecodeTileRows >= rows_in_page) {
-        p.chunk = 0;
-        ++p.page;
-      }
+      p.tok += rows;
       return true;
     }
     ++p.seg;
@@ -364,26 +369,25 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
       for (int v = 0; v < VEC / 2; ++v) acc[g][v] = make_float2(0.f, 0.f);
     }
 
-    for (int pg = 0; pg < sg.n_pages && ok; ++pg) {
-      const int rows_in_page = (pg == sg.n_pages - 1) ? sg.last_rows : a.page_size;
-      for (int r0 = 0; r0 < rows_in_page; r0 += kDecodeTileRows) {
-        const int rows = min(kDecodeTileRows, rows_in_page - r0);
-        const int stage = consumed % S;
-        if (!mbar_wait(bar0 + 8 * stage, (consumed / S) & 1, a.err)) {
-          ok = false;
-          break;
-        }
-        const T* ks = reinterpret_cast<const T*>(ring + stage * Shape::kStageBytes);
-        const T* vs = ks + kDecodeTileRows * D;
-        // Full tiles (every tile but the last of a page list) skip the per-token checks.
-        if (rows == kDecodeTileRows)
-          tile_step<D, G, LPT, T, CAP, true>(a, ks, vs, rows, sub, grp, my_head, qf, m, m_own, l_own, acc);
-        else
-          tile_step<D, G, LPT, T, CAP, false>(a, ks, vs, rows, sub, grp, my_head, qf, m, m_own, l_own, acc);
-        ++consumed;
-        __syncwarp();
-        producer_issue<D, T>(prod, a, ring, bar0, lane, num_pages, policy);
+    // 16-token tiles of the segment, in the producer's order.
+    const int n_tok = seg_tokens(sg.n_pages, sg.last_rows, a.page_size);
+    for (int tok0 = 0; tok0 < n_tok; tok0 += kDecodeTileRows) {
+      const int rows = min(kDecodeTileRows, n_tok - tok0);
+      const int stage = consumed % S;
+      if (!mbar_wait(bar0 + 8 * stage, (consumed / S) & 1, a.err)) {
+        ok = false;
+        break;
       }
+      const T* ks = reinterpret_cast<const T*>(ring + stage * Shape::kStageBytes);
+      const T* vs = ks + kDecodeTileRows * D;
+      // Full tiles (every tile but the last of a segment) skip the per-token checks.
+      if (rows == kDecodeTileRows)
+        tile_step<D, G, LPT, T, CAP, true>(a, ks, vs, rows, sub, grp, my_head, qf, m, m_own, l_own, acc);
+      else
+        tile_step<D, G, LPT, T, CAP, false>(a, ks, vs, rows, sub, grp, my_head, qf, m, m_own, l_own, acc);
+      ++consumed;
+      __syncwarp();
+      producer_issue<D, T>(prod, a, ring, bar0, lane, num_pages, policy);
     }
     if (!ok) break;
 

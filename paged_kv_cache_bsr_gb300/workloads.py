@@ -247,13 +247,13 @@ def tiny_decode(seed: int = 1000, poison: bool = False) -> PagedBatch:
 
 
 def llama3_decode(seed: int = 1001, batch: int = 64, poison: bool = False,
-                  identity_pages: bool = False) -> PagedBatch:
+                  identity_pages: bool = False, page_size: int = 16) -> PagedBatch:
     """Llama-3-8B-shaped batch decode: 32 q / 8 kv heads, head_dim 128, page 16, bf16,
     kv_len ~ U[512, 4096], pool = exactly the pages used, randomly permuted."""
     gen = _gen(seed)
     kv_lens = _uniform_ints(512, 4096, batch, gen)
     return make_paged_batch(qo_lens=[1] * batch, kv_lens=kv_lens, num_qo_heads=32, num_kv_heads=8,
-                            head_dim=128, page_size=16, dtype=torch.bfloat16, seed=seed + 1,
+                            head_dim=128, page_size=page_size, dtype=torch.bfloat16, seed=seed + 1,
                             poison=poison, identity_pages=identity_pages, name="llama3_8b_decode")
 
 
