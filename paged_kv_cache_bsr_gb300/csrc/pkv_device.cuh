@@ -59,19 +59,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Non-blocking probe of phase `parity` (try_wait may suspend the thread for a while).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
 // Wait for phase `parity` of a barrier to complete, giving up after
 // kWaitLimitNs.  Returns false (and records kErrWaitTimeout) on give-up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err) {
@@ -84,17 +71,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
     }
   }
   return true;
-}
-
-// Non-tensor bulk copy global -> shared (TMA unit), completion counted in
-// bytes on `bar`.  dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                              uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
 }
 
 // Same, with an L2 eviction-priority hint (policy from createpolicy).
@@ -165,23 +141,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
-}
-
-// 2^x on the FMA pipe, for x <= 2^22: x = j + f with j the nearest integer
-// (added to and subtracted from 1.5 * 2^23, which rounds to an integer) and
-// f in [-1/2, 1/2]; 2^f by a cubic fitted here by least squares on Chebyshev
-// nodes of [-1/2, 1/2] (largest relative error 7.8e-5); 2^j added to the
-// exponent field.  Inputs below -126 (masked logits are -inf) give exactly 0.
-__device__ __forceinline__ float exp2_poly3(float x_in) {
-  const float x = fmaxf(x_in, -126.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  float p = fmaf(0.05508868396282196f, f, 0.24260404706001282f);
-  p = fmaf(p, f, 0.6932762265205383f);
-  p = fmaf(p, f, 0.9999289512634277f);
-  const int j = __float_as_int(t) - 0x4B400000;
-  const float r = __int_as_float(__float_as_int(p) + (j << 23));
-  return x_in < -126.f ? 0.f : r;
 }
 
 // Four 16-bit pairs (one 16-byte chunk) to four fp32 pairs.
@@ -338,15 +297,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (fp16 or bf16 operands, fp32 accumulate).
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -362,14 +312,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
     "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),        \
     "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
 
-// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32*(w%4)...).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : PKV_R32(r)
-      : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -406,26 +348,6 @@ __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[12
       : "r"(taddr)
       : "memory");
 }
-// 64 consecutive fp32 columns of this thread's TMEM lane: two loads, one wait.
-__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "{\n\t.reg .b32 a1;\n\tadd.u32 a1, %64, 32;\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
-      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [a1];\n\t"
-      "tcgen05.wait::ld.sync.aligned;\n\t}"
-      : PKV_R32(r), PKV_R32((r + 32))
-      : "r"(taddr)
-      : "memory");
-}
-
-// Barrier over `threads` threads (a multiple of 32) with id 1..15 (0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a 128B-swizzled operand tile whose
