@@ -290,7 +290,7 @@ def decode_measure(b, steps, warmup, peaks, profile_name=None):
     ms = total_ms / steps
     res = {"ms_per_step": ms, "kernel_ms": kern_ms, "bytes": nbytes, "value": nbytes / (ms * 1e-3) / 1e9,
            "info": plan.info()}
-    traffic = recorded_traffic(profile_name, source_hash("decode.cu")) if profile_name else None
+    traffic = recorded_traffic(profile_name, source_hash("decode.cu", "decode_kernel.cuh")) if profile_name else None
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     res["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
@@ -614,9 +614,10 @@ def append_measure(peaks, steps=50, warmup=5, per_graph=20):
 
 def mixed_measure(steps=50, warmup=5):
     """A continuous-batching step of 60 decode requests and 4 prompt chunks: the mixed
-    plan (decode and prefill kernels side by side on an SM split) against the two
-    halves run back to back and against one prefill plan for every request (the
-    128-row tile for single-row requests too).  CUDA-graph replay of the run calls."""
+    plan (one persistent launch, prefill CTAs beside decode CTAs on an SM split)
+    against the two halves run back to back and against one prefill plan for every
+    request (the 128-row tile for single-row requests too).  CUDA-graph replay of
+    the run calls."""
     import torch
     from paged_kv_cache_bsr_gb300 import runner, api, workloads as W
     b = W.mixed_batch(seed=1007)

@@ -66,8 +66,8 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
 
 /* DECODE: one query row per request (CUDA cores, split-KV).  PREFILL: ragged
  * query rows (tcgen05 tensor cores).  MIXED: a batch holding both; requests with
- * one query row take the decode path, longer ones the prefill path, and one run
- * call launches both on disjoint SMs (see pkv_batch_mixed_paged). */
+ * one query row take the decode path, longer ones the prefill path, and one
+ * persistent kernel serves both on disjoint SMs (see pkv_batch_mixed_paged). */
 typedef enum { PKV_PLAN_DECODE = 0, PKV_PLAN_PREFILL = 1, PKV_PLAN_MIXED = 2 } pkv_plan_kind;
 
 /* Problem description shared by plan and run calls. */
@@ -311,17 +311,19 @@ pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const void* host
  * PKV_PLAN_MIXED.  The plan routes each request by its query-tile size: one
  * row to the CUDA-core decode path (split-KV over warp workers), several rows
  * to the tcgen05 prefill path (128-row tiles), and splits the SMs between the
- * two halves in proportion to their estimated times.  The run call launches
- * both persistent kernels, prefill on a side stream the plan owns, forked from
- * and joined back into `stream`, so they run side by side on disjoint SMs
- * (fdeinterviews summary: a batch mixes new prompts and single-token decodes;
- * "Customizable attention": a query tile size from 1 to 128 picked per batch;
- * greptalks "Runtime Scheduler").  Graph-capturable: the fork and join are
- * event records and waits.
+ * two halves in proportion to their estimated times.  The run call makes one
+ * persistent launch on every SM: the CTAs below the split run the prefill
+ * half, the others the decode workers; then each half's merge of split
+ * sequences follows on `stream` ("FlashInfer" guide, "Prefill-Decode Mixing";
+ * fdeinterviews summary, "Customizable attention": a query tile size from 1 to
+ * 128 picked per batch; greptalks, "Future Directions and Features": mixed
+ * prefill and decode phases in one batch).  The split is read from the device
+ * tables, so a captured graph stays valid across re-planning within the limits.
  * Arguments and layouts as for pkv_batch_prefill_paged (qo_indptr_d covers
  * every request; causal per params->causal applies to the prefill half, and a
  * single-row request sees all its keys either way).
- * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ * Errors: PKV_ERR_INVALID_ARG (a null or misaligned pointer, a plan of another
+ * kind or not planned), PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  */
 pkv_status pkv_batch_mixed_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
                                  const void* kv_data, const int32_t* kv_indices_d, const int32_t* kv_indptr_d,

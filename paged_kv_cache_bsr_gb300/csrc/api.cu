@@ -79,6 +79,61 @@ cudaError_t release_tables(const pkv_plan* plan, cudaStream_t s) {
   return cudaEventRecord(plan->free_ev[plan->cur], s);
 }
 
+pkv::DecodeArgs decode_args(const pkv_plan* plan, void* dev_ws, const void* q, const void* kv_data,
+                            const int32_t* kv_indices_d, const int32_t* kv_indptr_d, void* o, float* lse) {
+  const pkv_params& p = plan->p;
+  const bool cap = p.logits_cap > 0.f;
+  pkv::DecodeArgs a{};
+  fill_tables(a, plan, dev_ws);
+  auto* tb = static_cast<uint8_t*>(dev_ws) + table_off(plan);
+  a.segs = reinterpret_cast<const pkv::DecodeSeg*>(tb + plan->L.segs);
+  a.merge = reinterpret_cast<const pkv::MergeItem*>(tb + plan->L.merge);
+  a.q = q;
+  a.kv = kv_data;
+  a.kv_indices = kv_indices_d;
+  a.kv_indptr = kv_indptr_d;
+  a.o = o;
+  a.lse = lse;
+  a.num_qo_heads = p.num_qo_heads;
+  a.num_kv_heads = p.num_kv_heads;
+  a.page_size = p.page_size;
+  a.q_scale = cap ? p.sm_scale : p.sm_scale * pkv::kLog2e;
+  a.cap = cap ? p.logits_cap : 0.f;
+  return a;
+}
+
+pkv::PrefillArgs prefill_args(const pkv_plan* plan, void* dev_ws, const void* q, const void* kv_data,
+                              const int32_t* kv_indices_d, const uint8_t* mask, size_t mask_bytes, void* o,
+                              float* lse) {
+  const pkv_params& p = plan->p;
+  const bool cap = p.logits_cap > 0.f;
+  pkv::PrefillArgs a{};
+  fill_tables(a, plan, dev_ws);
+  auto* tb = static_cast<uint8_t*>(dev_ws) + table_off(plan);
+  a.tiles = reinterpret_cast<const pkv::PrefillTile*>(tb + plan->L.segs);
+  a.merge = reinterpret_cast<const pkv::PrefillMerge*>(tb + plan->L.merge);
+  a.q = q;
+  a.kv = kv_data;
+  a.kv_indices = kv_indices_d;
+  a.o = o;
+  a.lse = lse;
+  a.num_qo_heads = p.num_qo_heads;
+  a.num_kv_heads = p.num_kv_heads;
+  a.page_size = p.page_size;
+  a.causal = p.causal;
+  a.sm_scale = p.sm_scale;
+  a.cap = cap ? p.logits_cap : 0.f;
+  a.mask = reinterpret_cast<const uint32_t*>(mask);
+  a.mask_words = mask ? static_cast<int64_t>(mask_bytes / 4) : 0;
+  return a;
+}
+
+pkv_status launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  cudaGetLastError();
+  return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -112,22 +167,7 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
   if (st != PKV_OK) return st;
   const pkv_params& p = plan->p;
   const bool cap = p.logits_cap > 0.f;
-  pkv::DecodeArgs a{};
-  fill_tables(a, plan, dev_ws);
-  auto* base = static_cast<uint8_t*>(dev_ws);
-  a.segs = reinterpret_cast<const pkv::DecodeSeg*>(base + table_off(plan) + plan->L.segs);
-  a.merge = reinterpret_cast<const pkv::MergeItem*>(base + table_off(plan) + plan->L.merge);
-  a.q = q;
-  a.kv = kv_data;
-  a.kv_indices = kv_indices_d;
-  a.kv_indptr = kv_indptr_d;
-  a.o = o;
-  a.lse = lse;
-  a.num_qo_heads = p.num_qo_heads;
-  a.num_kv_heads = p.num_kv_heads;
-  a.page_size = p.page_size;
-  a.q_scale = cap ? p.sm_scale : p.sm_scale * pkv::kLog2e;
-  a.cap = cap ? p.logits_cap : 0.f;
+  const pkv::DecodeArgs a = decode_args(plan, dev_ws, q, kv_data, kv_indices_d, kv_indptr_d, o, lse);
   auto s = static_cast<cudaStream_t>(stream);
   cudaError_t e = wait_tables(plan, s);
   if (plan->time_start && e == cudaSuccess) cudaEventRecord(plan->time_start, s);
@@ -135,11 +175,7 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
   if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
   if (e == cudaSuccess) e = pkv::launch_decode_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
   if (e == cudaSuccess) e = release_tables(plan, s);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
-  }
-  return PKV_OK;
+  return launch_status(e);
 }
 
 static pkv_status prefill_run(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d, const void* kv_data,
@@ -160,25 +196,8 @@ static pkv_status prefill_run(const pkv_plan* plan, const void* q, const int32_t
   pkv_status st = check_device(plan);
   if (st != PKV_OK) return st;
   const pkv_params& p = plan->p;
-  pkv::PrefillArgs a{};
-  fill_tables(a, plan, dev_ws);
-  auto* base = static_cast<uint8_t*>(dev_ws);
-  a.tiles = reinterpret_cast<const pkv::PrefillTile*>(base + table_off(plan) + plan->L.segs);
-  a.merge = reinterpret_cast<const pkv::PrefillMerge*>(base + table_off(plan) + plan->L.merge);
-  a.q = q;
-  a.kv = kv_data;
-  a.kv_indices = kv_indices_d;
-  a.o = o;
-  a.lse = lse;
-  a.num_qo_heads = p.num_qo_heads;
-  a.num_kv_heads = p.num_kv_heads;
-  a.page_size = p.page_size;
-  a.causal = p.causal;
   const bool cap = p.logits_cap > 0.f;
-  a.sm_scale = p.sm_scale;
-  a.cap = cap ? p.logits_cap : 0.f;
-  a.mask = reinterpret_cast<const uint32_t*>(mask);
-  a.mask_words = mask ? static_cast<int64_t>(mask_bytes / 4) : 0;
+  const pkv::PrefillArgs a = prefill_args(plan, dev_ws, q, kv_data, kv_indices_d, mask, mask_bytes, o, lse);
   auto s = static_cast<cudaStream_t>(stream);
   cudaError_t e = wait_tables(plan, s);
   if (plan->time_start && e == cudaSuccess) cudaEventRecord(plan->time_start, s);
@@ -189,11 +208,7 @@ static pkv_status prefill_run(const pkv_plan* plan, const void* q, const int32_t
   if (e == cudaSuccess)
     e = pkv::launch_prefill_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
   if (e == cudaSuccess) e = release_tables(plan, s);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
-  }
-  return PKV_OK;
+  return launch_status(e);
 }
 
 pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,
@@ -218,42 +233,34 @@ pkv_status pkv_batch_mixed_paged(const pkv_plan* plan, const void* q, const int3
                                  const void* kv_data, const int32_t* kv_indices_d, const int32_t* kv_indptr_d,
                                  const int32_t* kv_last_page_len_d, void* o, float* lse, void* dev_ws,
                                  void* stream) {
-  if (!plan || plan->kind != PKV_PLAN_MIXED || !plan->planned || !dev_ws) return PKV_ERR_INVALID_ARG;
-  if (!aligned(dev_ws, 256)) return PKV_ERR_INVALID_ARG;
+  if (!plan || plan->kind != PKV_PLAN_MIXED || !plan->planned) return PKV_ERR_INVALID_ARG;
+  if (!q || !qo_indptr_d || !kv_data || !kv_indices_d || !kv_indptr_d || !kv_last_page_len_d || !o || !dev_ws)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_data, 16) || !aligned(o, 16) || !aligned(dev_ws, 256) ||
+      !aligned(kv_indices_d, 4) || !aligned(kv_indptr_d, 4) || (lse && !aligned(lse, 4)))
+    return PKV_ERR_INVALID_ARG;
   pkv_status st = check_device(plan);
   if (st != PKV_OK) return st;
+  const pkv_params& p = plan->p;
+  const bool cap = p.logits_cap > 0.f;
   auto* base = static_cast<uint8_t*>(dev_ws);
-  void* dws = base + plan->dec_dev_off;
-  void* pws = base + plan->pre_dev_off;
-  const bool has_pre = plan->prefill_ctas > 0 && plan->sub_pre->num_work > 0;
-  const bool has_dec = plan->decode_ctas > 0 && plan->sub_dec->num_work > 0;
+  const pkv_plan* dp = plan->sub_dec;
+  const pkv_plan* pp = plan->sub_pre;
+  // Decode segments carry their row of q / o / lse, so both halves read and
+  // write the caller's tensors in place.
+  const pkv::DecodeArgs da =
+      decode_args(dp, base + plan->dec_dev_off, q, kv_data, kv_indices_d, kv_indptr_d, o, lse);
+  const pkv::PrefillArgs pa = prefill_args(pp, base + plan->pre_dev_off, q, kv_data, kv_indices_d, nullptr, 0, o, lse);
   auto s = static_cast<cudaStream_t>(stream);
-  if (has_pre && has_dec) {
-    // Prefill on the side stream, decode on the caller's: the two persistent
-    // grids find their work in the first prefill_ctas resp. decode_ctas CTAs,
-    // so they run side by side on disjoint SMs; the side stream joins back.
-    if (cudaEventRecord(plan->fork, s) != cudaSuccess || cudaStreamWaitEvent(plan->side, plan->fork, 0) != cudaSuccess) {
-      cudaGetLastError();
-      return PKV_ERR_CUDA;
-    }
-    st = prefill_run(plan->sub_pre, q, qo_indptr_d, kv_data, kv_indices_d, kv_indptr_d, kv_last_page_len_d, nullptr,
-                     0, o, lse, pws, plan->side);
-    pkv_status st2 = pkv_batch_decode_paged(plan->sub_dec, q, kv_data, kv_indices_d, kv_indptr_d,
-                                            kv_last_page_len_d, o, lse, dws, stream);
-    // Join even after a failed launch, so the caller's stream never runs ahead of the side stream.
-    if (cudaEventRecord(plan->join, plan->side) != cudaSuccess || cudaStreamWaitEvent(s, plan->join, 0) != cudaSuccess) {
-      cudaGetLastError();
-      return PKV_ERR_CUDA;
-    }
-    return st != PKV_OK ? st : st2;
-  }
-  if (has_pre)
-    return prefill_run(plan->sub_pre, q, qo_indptr_d, kv_data, kv_indices_d, kv_indptr_d, kv_last_page_len_d,
-                       nullptr, 0, o, lse, pws, stream);
-  if (has_dec)
-    return pkv_batch_decode_paged(plan->sub_dec, q, kv_data, kv_indices_d, kv_indptr_d, kv_last_page_len_d, o, lse,
-                                  dws, stream);
-  return PKV_OK;
+  // One persistent launch serves both halves (the CTA split is in the decode
+  // tables); then each half's merge of split sequences.
+  cudaError_t e = cudaSuccess;
+  if (plan->time_start) cudaEventRecord(plan->time_start, s);
+  e = pkv::launch_mixed(pa, da, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, pp->total_q, pp->num_pages, s);
+  if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
+  if (e == cudaSuccess) e = pkv::launch_prefill_merge(pa, p.head_dim, plan->group, p.dtype, pp->merge_grid, s);
+  if (e == cudaSuccess) e = pkv::launch_decode_merge(da, p.head_dim, plan->group, p.dtype, dp->merge_grid, s);
+  return launch_status(e);
 }
 
 pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o_out,

@@ -31,7 +31,9 @@ struct alignas(64) PlanHeader {
   int32_t num_slots;     // partial-state slots in use
   int64_t num_pages;     // pool size, for the device-side page-id check
   int32_t error;         // device error word; cleared by every plan_run
-  int32_t pad[5];
+  int32_t cta_offset;    // mixed plans, decode half: the first CTA of the mixed launch
+                         // that serves it (CTAs below it serve the prefill half); 0 otherwise
+  int32_t pad[4];
 };
 static_assert(sizeof(PlanHeader) == 64, "PlanHeader layout");
 

@@ -98,4 +98,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dt
 cudaError_t launch_prefill_merge(const PrefillArgs& a, int head_dim, int group, int dtype, int grid,
                                  cudaStream_t stream);
 
+// Launch the mixed prefill + decode kernel on `grid` CTAs: the CTAs below the
+// decode tables' cta_offset run the prefill half, the rest the decode half
+// (head_dim 128 only).  The two halves' merges are launched separately.
+cudaError_t launch_mixed(const PrefillArgs& pa, const DecodeArgs& da, int head_dim, int group, int dtype, bool cap,
+                         int grid, int64_t total_q, int64_t num_pages, cudaStream_t stream);
+
 }  // namespace pkv

@@ -59,14 +59,10 @@ struct pkv_plan {
   cudaEvent_t time_stop = nullptr;
   // Mixed plans: the decode and prefill halves (each a plan of its own kind,
   // sharing this plan's device), where their tables and workspaces sit inside
-  // this plan's workspaces, the last SM split, and the side stream and events
-  // the run call forks the prefill half onto.
+  // this plan's workspaces, and the last SM split.
   pkv_plan* sub_dec = nullptr;
   pkv_plan* sub_pre = nullptr;
   size_t dec_dev_off = 0, pre_dev_off = 0, dec_host_off = 0, pre_host_off = 0;
   int prefill_ctas = 0;
   int decode_ctas = 0;
-  cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr;
-  cudaEvent_t join = nullptr;
 };

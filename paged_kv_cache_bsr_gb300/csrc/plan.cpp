@@ -89,6 +89,7 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
   pkv_status st = check_params(kind, params, limits);
   if (st != PKV_OK) return st;
   if (num_sms <= 0) return PKV_ERR_INVALID_ARG;
+  if (kind == PKV_PLAN_MIXED && num_sms < 2) return PKV_ERR_INVALID_ARG;  // one SM for each half at least
   pkv_plan* pl = new (std::nothrow) pkv_plan();
   if (!pl) return PKV_ERR_INVALID_ARG;
   pl->kind = kind;
@@ -297,14 +298,86 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
   return PKV_OK;
 }
 
+// A query tile of the prefill plan: kPrefillRows packed rows of one request and
+// kv head against keys [0, kv_end) (kv_end already clipped by the causal limit).
+struct QueryTile {
+  int b, kvh, pos0, npos, qo, kv, kv_end;
+};
+
+// The prefill plan's query tiles (independent of the CTA count); returns their
+// key blocks in total, an empty tile counting one.
+int64_t query_tiles(const pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                    const int32_t* kv_last, bool skip_single, std::vector<QueryTile>& tiles) {
+  const int P = pl->p.page_size;
+  const int mp = pkv::kPrefillRows / pl->group;
+  tiles.clear();
+  int64_t total = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int qo = qo_indptr[b + 1] - qo_indptr[b];
+    if (skip_single && qo == 1) continue;
+    const int kv = static_cast<int>(kv_len_of(kv_indptr, kv_last, b, P));
+    for (int h = 0; h < pl->p.num_kv_heads; ++h)
+      for (int pos0 = 0; pos0 < qo; pos0 += mp) {
+        const int npos = std::min(mp, qo - pos0);
+        int kv_end = kv;
+        if (pl->p.causal) kv_end = std::max(0, std::min(kv, pos0 + npos + kv - qo));
+        tiles.push_back({b, static_cast<int>(h), pos0, npos, qo, kv, kv_end});
+        total += std::max<int64_t>(1, ceil_div(kv_end, pkv::kPrefillKeys));
+      }
+  }
+  return total;
+}
+
+// Key blocks per work item when `total` blocks go to C CTAs: a tile longer than
+// this is cut into that many near-equal chunks (each a partial state to merge).
+int64_t key_chunk(int64_t total, int C) { return std::max<int64_t>(ceil_div(total, std::max(C, 1)), 2); }
+
+// The busiest CTA's load (key blocks, plus one per item for its setup and
+// epilogue) when compute_prefill chunks the tiles for C CTAs and assigns them
+// longest first.  Item costs are small integers and the least load of a
+// longest-first schedule never decreases, so the schedule runs on counts: the
+// items per cost, and the CTAs per load (`by_cost`, `by_load` are scratch).
+// Ties change no load, so the result equals compute_prefill's assignment.
+int64_t prefill_makespan(const std::vector<QueryTile>& tiles, int64_t total, int C, std::vector<int64_t>& by_cost,
+                         std::vector<int64_t>& by_load) {
+  if (tiles.empty() || C <= 0) return 0;
+  const int64_t chunk = key_chunk(total, C);
+  by_cost.assign(chunk + 2, 0);
+  int64_t items = 0;
+  auto add = [&](int64_t c) {
+    if (c >= static_cast<int64_t>(by_cost.size())) by_cost.resize(c + 1, 0);
+    ++by_cost[c];
+    ++items;
+  };
+  for (const QueryTile& t : tiles) {
+    const int64_t nb = ceil_div(t.kv_end, pkv::kPrefillKeys);
+    if (nb <= chunk) {
+      add(std::max<int64_t>(nb, 1) + 1);
+    } else {
+      const int64_t parts = ceil_div(nb, chunk);
+      for (int64_t i = 0; i < parts; ++i) add((i + 1) * nb / parts - i * nb / parts + 1);
+    }
+  }
+  const int64_t ctas = std::min<int64_t>(C, items);
+  by_load.assign(1, ctas);
+  int64_t least = 0, worst = 0;
+  for (int64_t c = static_cast<int64_t>(by_cost.size()) - 1; c >= 1; --c)
+    for (int64_t k = 0; k < by_cost[c]; ++k) {
+      while (by_load[least] == 0) ++least;
+      --by_load[least];
+      const int64_t l = least + c;
+      if (l >= static_cast<int64_t>(by_load.size())) by_load.resize(l + 1, 0);
+      ++by_load[l];
+      worst = std::max(worst, l);
+    }
+  return worst;
+}
+
 // Prefill work over `C` CTAs; with skip_single the requests holding one query
 // row are left out (they are the decode half of a mixed batch).
 pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
                            const int32_t* kv_last, uint8_t* host, int C = 0, bool skip_single = false) {
   const int P = pl->p.page_size;
-  const int hkv = pl->p.num_kv_heads;
-  const int G = pl->group;
-  const int mp = pkv::kPrefillRows / G;
   const int BN = pkv::kPrefillKeys;
   if (C <= 0) C = pl->workers;
 
@@ -314,33 +387,17 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   };
   std::vector<Item> items;
   std::vector<PrefillMerge> merges;
-  struct Tile {
-    int b, kvh, pos0, npos, qo, kv, kv_end;
-  };
-  std::vector<Tile> tiles;
-  int64_t total = 0;
   // Request b's custom-mask block starts at bit sum over b' < b of qo_len * kv_len.
   std::vector<int64_t> mask_off(batch + 1, 0);
   for (int b = 0; b < batch; ++b)
     mask_off[b + 1] = mask_off[b] + static_cast<int64_t>(qo_indptr[b + 1] - qo_indptr[b]) *
                                         kv_len_of(kv_indptr, kv_last, b, P);
   pl->mask_bits = mask_off[batch];
-  for (int b = 0; b < batch; ++b) {
-    const int qo = qo_indptr[b + 1] - qo_indptr[b];
-    if (skip_single && qo == 1) continue;
-    const int kv = static_cast<int>(kv_len_of(kv_indptr, kv_last, b, P));
-    for (int h = 0; h < hkv; ++h)
-      for (int pos0 = 0; pos0 < qo; pos0 += mp) {
-        const int npos = std::min(mp, qo - pos0);
-        int kv_end = kv;
-        if (pl->p.causal) kv_end = std::max(0, std::min(kv, pos0 + npos + kv - qo));
-        tiles.push_back({b, h, pos0, npos, qo, kv, kv_end});
-        total += std::max<int64_t>(1, ceil_div(kv_end, BN));
-      }
-  }
-  const int64_t chunk = std::max<int64_t>(ceil_div(total, std::max(C, 1)), 2);
+  std::vector<QueryTile> tiles;
+  const int64_t total = query_tiles(pl, batch, qo_indptr, kv_indptr, kv_last, skip_single, tiles);
+  const int64_t chunk = key_chunk(total, C);
   int n_slot = 0;
-  for (const Tile& t : tiles) {
+  for (const QueryTile& t : tiles) {
     PrefillTile pt{};
     pt.b = t.b;
     pt.kvh = t.kvh;
@@ -440,53 +497,88 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   return PKV_OK;
 }
 
-// Throughputs of the two kernels on a whole GB300, measured on the two halves of
-// a 60-decode + 4-prompt-chunk batch (decode 4.98 TB/s of K/V, prefill 0.84
-// PFLOP/s of unmasked work); only their ratio matters: it turns each half's work
-// into time for the SM split.
-constexpr double kDecodeBytesPerSec = 4.98e12;
-constexpr double kPrefillFlopsPerSec = 0.84e15;
+// Time of each half on n SMs, fitted to the two halves of a 60-decode +
+// 4-prompt-chunk batch (32 q / 8 kv heads, head_dim 128, bf16) run alone on 20
+// to 152 SMs: both follow a fixed part plus their plan's largest per-worker
+// load to within 2 us.  Prefill: 13.8 us + 1.83 us per 128-key block of a
+// 256-row tile on the busiest CTA (one extra block per work item).  Decode:
+// 14.2 us + 1.38 us per 16-row page on the busiest warp.
+constexpr double kPrefillFixedUs = 13.8;
+constexpr double kPrefillBlockUs = 1.827;
+constexpr double kDecodeFixedUs = 14.2;
+constexpr double kDecodePage16Us = 1.384;
 
 // Mixed batch: single-row requests to the decode half, the rest to the prefill
-// half, and the SMs shared in proportion to the estimated time of each half
-// alone on the whole GPU, so both halves end together.
+// half, and the SMs split so that both halves end together: the split that
+// minimises the larger of the two estimated times (each half's time falls as
+// it gains SMs, so the search brackets the crossing and then checks its
+// neighbours, whose chunking can differ).
 pkv_status compute_mixed(pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
                          const int32_t* kv_last, int64_t num_pages, uint8_t* host) {
   const int P = pl->p.page_size;
-  const double elem = 2.0;
-  double dec_bytes = 0.0, pre_flops = 0.0;
-  for (int b = 0; b < batch; ++b) {
-    const int64_t qo = qo_indptr[b + 1] - qo_indptr[b];
-    const int64_t kv = kv_len_of(kv_indptr, kv_last, b, P);
-    if (qo == 1) {
-      dec_bytes += 2.0 * kv * pl->p.num_kv_heads * pl->p.head_dim * elem;
-    } else if (qo > 1) {
-      int64_t pairs = 0;
-      if (pl->p.causal) {
-        const int64_t pre = std::max<int64_t>(kv - qo, 0);
-        const int64_t seen = std::min<int64_t>(qo, kv);  // rows that see at least their prefix
-        pairs = seen * pre + seen * (seen + 1) / 2;
-      } else {
-        pairs = qo * kv;
-      }
-      pre_flops += 4.0 * pairs * pl->p.num_qo_heads * pl->p.head_dim;
-    }
-  }
-  const double t_dec = dec_bytes / kDecodeBytesPerSec, t_pre = pre_flops / kPrefillFlopsPerSec;
   const int S = pl->num_sms;
-  int kp = 0;
+  int64_t dec_pages = 0;  // (request, kv head) pages of the decode half
   bool any_pre = false, any_dec = false;
   for (int b = 0; b < batch; ++b) {
     const int qo = qo_indptr[b + 1] - qo_indptr[b];
     any_dec |= qo == 1;
     any_pre |= qo > 1;
+    if (qo == 1) dec_pages += static_cast<int64_t>(kv_indptr[b + 1] - kv_indptr[b]) * pl->p.num_kv_heads;
   }
+  int kp = 0;
   if (any_pre && !any_dec) {
     kp = S;
   } else if (any_pre && any_dec) {
-    const double share = (t_pre + t_dec) > 0.0 ? t_pre / (t_pre + t_dec) : 0.5;
-    kp = static_cast<int>(std::lround(share * S));
-    kp = std::min(std::max(kp, 1), S - 1);
+    std::vector<QueryTile> tiles;
+    std::vector<int64_t> by_cost, by_load;
+    const int64_t total = query_tiles(pl, batch, qo_indptr, kv_indptr, kv_last, true, tiles);
+    const int64_t min_run = std::max<int64_t>(1, 4 / ceil_div(P, pkv::kDecodeTileRows));
+    const double page_us = kDecodePage16Us * P / 16.0;
+    auto t_pre = [&](int c) { return kPrefillFixedUs + kPrefillBlockUs * prefill_makespan(tiles, total, c, by_cost, by_load); };
+    auto t_dec = [&](int n) {
+      const int64_t run = std::max<int64_t>(ceil_div(dec_pages, (int64_t)n * pkv::kDecodeWarps), min_run);
+      return kDecodeFixedUs + page_us * run;
+    };
+    // Smallest prefill share whose prefill time no longer exceeds the decode time.
+    int lo = 1, hi = S - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) / 2;
+      if (t_pre(mid) <= t_dec(S - mid))
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    const int c0 = std::max(1, lo - 2), c1 = std::min(S - 1, lo + 2);
+    double best = 0.0;
+    kp = c0;
+    for (int c = c0; c <= c1; ++c) {
+      const double t = std::max(t_pre(c), t_dec(S - c));
+      if (c == c0 || t < best) {
+        best = t;
+        kp = c;
+      }
+    }
+    // The prefill load is a step function of the CTA count: take the fewest CTAs
+    // that reach the same prefill time, leaving the decode half more SMs.
+    const double target = t_pre(kp);
+    int a = 1, z = kp;
+    while (a < z) {
+      const int mid = (a + z) / 2;
+      if (t_pre(mid) <= target)
+        z = mid;
+      else
+        a = mid + 1;
+    }
+    kp = a;
+    // An even split: measured on a 60-decode + 4-chunk batch over splits 60 to
+    // 81, odd splits ran up to 15% slower than their even neighbours, which fits
+    // the SMs working in pairs (an odd number of prefill SMs must leave some
+    // pair with one SM of each half).
+    if ((kp & 1) && S >= 4) {
+      const int lo_even = std::max(2, kp - 1), hi_even = std::min(S - 2, kp + 1);
+      kp = std::max(t_pre(lo_even), t_dec(S - lo_even)) <= std::max(t_pre(hi_even), t_dec(S - hi_even)) ? lo_even
+                                                                                                         : hi_even;
+    }
   }
   pl->prefill_ctas = kp;
   pl->decode_ctas = any_dec ? S - kp : 0;
@@ -497,6 +589,8 @@ pkv_status compute_mixed(pkv_plan* pl, int batch, const int32_t* qo_indptr, cons
   if (st != PKV_OK) return st;
   st = compute_prefill(p, batch, qo_indptr, kv_indptr, kv_last, host + pl->pre_host_off, std::max(kp, 1), true);
   if (st != PKV_OK) return st;
+  // The mixed kernel's CTAs below this serve the prefill half, the rest the decode half.
+  reinterpret_cast<PlanHeader*>(host + pl->dec_host_off + d->L.header)->cta_offset = any_dec ? kp : S;
   for (pkv_plan* q : {d, p}) {
     uint8_t* h = host + (q == d ? pl->dec_host_off : pl->pre_host_off);
     reinterpret_cast<PlanHeader*>(h + q->L.header)->num_pages = num_pages;
@@ -536,12 +630,6 @@ pkv_status pkv_plan_create(pkv_plan** out, int kind, const pkv_params* params, c
   cudaGetDevice(&prev);
   cudaSetDevice(device);
   cudaError_t e = cudaEventCreateWithFlags(&(*out)->copy_done, cudaEventDisableTiming);
-  if (e == cudaSuccess && kind == PKV_PLAN_MIXED) {
-    // The run call forks the prefill half onto this stream and joins it back.
-    e = cudaStreamCreateWithFlags(&(*out)->side, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&(*out)->fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&(*out)->join, cudaEventDisableTiming);
-  }
   cudaSetDevice(prev);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -563,10 +651,6 @@ pkv_status pkv_plan_destroy(pkv_plan* plan) {
     if (plan->copy_pending) cudaEventSynchronize(plan->copy_done);
     cudaEventDestroy(plan->copy_done);
   }
-  if (plan->side) {
-    cudaStreamSynchronize(plan->side);
-    cudaStreamDestroy(plan->side);
-  }
   if (plan->copy_stream) {
     cudaStreamSynchronize(plan->copy_stream);
     cudaStreamDestroy(plan->copy_stream);
@@ -575,8 +659,6 @@ pkv_status pkv_plan_destroy(pkv_plan* plan) {
     if (plan->copy_ev[r]) cudaEventDestroy(plan->copy_ev[r]);
     if (plan->free_ev[r]) cudaEventDestroy(plan->free_ev[r]);
   }
-  if (plan->fork) cudaEventDestroy(plan->fork);
-  if (plan->join) cudaEventDestroy(plan->join);
   delete plan->sub_dec;
   delete plan->sub_pre;
   delete plan;

@@ -84,14 +84,14 @@ bool prefill_supported(int head_dim, int group, int dtype, int page_size) {
           page_size == 32 || page_size == 64 || page_size == 128);
 }
 
-cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dtype, bool cap, int grid,
-                           int64_t total_q, int64_t num_pages, cudaStream_t stream) {
-  if (!prefill_supported(head_dim, group, dtype, a.page_size)) return cudaErrorInvalidValue;
+namespace prefill_impl {
+
+cudaError_t make_tensor_maps(const PrefillArgs& a, int group, int dtype, int64_t total_q, int64_t num_pages,
+                             CUtensorMap& tq, CUtensorMap& tkv) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   const CUtensorMapDataType dt = dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const cuuint64_t hq = a.num_qo_heads, hkv = a.num_kv_heads, P = a.page_size;
-  CUtensorMap tq, tkv;
   {
     // q [total_q, Hq, D]: box = 64 columns x the G heads of a group x 128/G positions.
     cuuint64_t dims[3] = {kD, hq, static_cast<cuuint64_t>(total_q > 0 ? total_q : 1)};
@@ -114,6 +114,17 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dt
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  return cudaSuccess;
+}
+
+}  // namespace prefill_impl
+
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dtype, bool cap, int grid,
+                           int64_t total_q, int64_t num_pages, cudaStream_t stream) {
+  if (!prefill_supported(head_dim, group, dtype, a.page_size)) return cudaErrorInvalidValue;
+  CUtensorMap tq, tkv;
+  cudaError_t e = make_tensor_maps(a, group, dtype, total_q, num_pages, tq, tkv);
+  if (e != cudaSuccess) return e;
   const bool masked = a.mask != nullptr, small = a.page_size < 8;
   using L = cudaError_t (*)(const PrefillArgs&, int, bool, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
   L fn;

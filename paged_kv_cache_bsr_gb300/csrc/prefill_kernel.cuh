@@ -140,14 +140,15 @@ __device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uin
 
 // SMALL: pages of fewer than 8 rows, gathered with cp.async (its own instance set,
 // so the tensor-copy path of larger pages carries none of that code).
+// One CTA's share of the work: `cta` indexes the plan's workers, `sm` is the
+// CTA's dynamic shared memory (kSmemBytes, or kSmemBytesSmall for SMALL).  Warps
+// 0-10 take the roles above; any further warp of the CTA only joins the two
+// CTA-wide barriers.
 template <int G, typename T, bool CAP, bool MASK, bool SMALL>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
-                   const __grid_constant__ CUtensorMap tkv) {
+__device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv,
+                                            int cta, uint8_t* sm) {
   constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
   constexpr int MP = kTM / G;  // query positions per UMMA tile
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* sm = smem_raw;
   const uint32_t base = smem_addr(sm);
   if (base & 1023u) {  // never expected; refuse rather than misread swizzled tiles
     if (threadIdx.x == 0) atomicOr(a.err, kErrTmemAlloc);
@@ -182,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const PlanHeader* hdr = a.hdr;
   int t_begin = 0, t_end = 0;
-  if (static_cast<int>(blockIdx.x) < hdr->num_workers) {
-    t_begin = a.worker_ptr[blockIdx.x];
-    t_end = a.worker_ptr[blockIdx.x + 1];
+  if (cta < hdr->num_workers) {
+    t_begin = a.worker_ptr[cta];
+    t_end = a.worker_ptr[cta + 1];
   }
   const int num_pages = static_cast<int>(hdr->num_pages);
   const int P = a.page_size;
@@ -464,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncwarp();
-  } else {
+  } else if (warp < kVWarp) {
     // ------------------------------------------------------------ softmax + epilogue
     const int x = (warp - 2) >> 2;           // UMMA tile of this warp group
     const int quarter = warp & 3;            // TMEM lanes this warp may access
@@ -674,6 +675,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+template <int G, typename T, bool CAP, bool MASK, bool SMALL>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
+                   const __grid_constant__ CUtensorMap tkv) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  prefill_cta<G, T, CAP, MASK, SMALL>(a, tq, tkv, blockIdx.x, smem_raw);
+}
+
 
 // Launch one instance of the kernel (group size and cap chosen at run time).
 template <typename T, bool MASK, bool SMALL>
@@ -695,6 +704,11 @@ cudaError_t launch_kernel(const PrefillArgs& a, int G, bool cap, int grid, const
   kern<<<grid, kThreads, smem, s>>>(a, tq, tkv);
   return cudaGetLastError();
 }
+
+// The tensor maps of q (3D boxes of 64 columns x G heads x 128/G positions) and
+// kv_data (5D boxes of 64 columns x one page's rows) for the prefill tiles.
+cudaError_t make_tensor_maps(const PrefillArgs& a, int group, int dtype, int64_t total_q, int64_t num_pages,
+                             CUtensorMap& tq, CUtensorMap& tkv);
 
 // Each instance set is compiled in its own translation unit.
 extern template cudaError_t launch_kernel<__nv_bfloat16, false, false>(const PrefillArgs&, int, bool, int,

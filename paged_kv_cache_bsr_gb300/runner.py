@@ -107,7 +107,8 @@ def append_kv(db: DeviceBatch, k_new: torch.Tensor, v_new: torch.Tensor, rope_th
 
 def mixed(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """A batch mixing single-row (decode) and multi-row (prefill) requests in one
-    call: the plan routes each request by its row count and splits the SMs."""
+    call: the plan routes each request by its row count and splits the SMs, and one
+    persistent launch runs both halves."""
     b = db.host
     if plan is None:
         plan = make_plan(b, api.PLAN_MIXED)
@@ -122,9 +123,9 @@ def mixed(db: DeviceBatch, plan: Optional[api.Plan] = None, stream=None) -> Tupl
 def levels_mixed(db: DeviceBatch, n_levels: int, plan: Optional[api.Plan] = None, stream=None
                  ) -> Tuple[torch.Tensor, torch.Tensor]:
     """A prefix tree (or a cascade, n_levels = 2) as one mixed launch: ``db`` holds
-    ``workloads.levels_as_mixed(levels)``.  Multi-row nodes run on the prefill kernel
-    and single-row nodes on the decode kernel side by side; merge_state then folds
-    every level's rows into the last level's."""
+    ``workloads.levels_as_mixed(levels)``.  Multi-row nodes run on the prefill half
+    of the mixed kernel and single-row nodes on its decode half; merge_state then
+    folds every level's rows into the last level's."""
     o, lse = mixed(db, plan, stream)
     R = db.q.shape[0] // n_levels
     o_out, l_out = o[(n_levels - 1) * R:], lse[(n_levels - 1) * R:]

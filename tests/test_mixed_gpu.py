@@ -1,6 +1,6 @@
 """GPU parity of mixed batches (single-row decode requests and multi-row prefill
-requests in one call, routed by the plan to the CUDA-core decode kernel and the
-tcgen05 prefill kernel running side by side) against the fp64 oracle."""
+requests in one call: one persistent launch whose first CTAs run the tcgen05
+prefill half and the rest the CUDA-core decode workers) against the fp64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -49,6 +49,48 @@ def test_small_mixed_batches(group, dtype):
     assert info.prefill_ctas >= 1 and info.decode_ctas >= 1
 
 
+@pytest.mark.parametrize("page_size,group,cap", [(1, 4, 0.0), (4, 2, 30.0), (2, 8, 0.0), (64, 1, 30.0)])
+def test_mixed_page_sizes_and_cap(page_size, group, cap):
+    """Pages of 1, 2 and 4 rows take the cp.async-gather instances of the mixed kernel;
+    64-row pages and the soft-capped instances the others."""
+    b = W.mixed_batch(seed=30 + page_size, n_decode=9, n_prefill=3, decode_lo=1, decode_hi=500, qo_lo=2,
+                      qo_hi=260, prefix_lo=0, prefix_hi=150, num_qo_heads=2 * group, num_kv_heads=2,
+                      page_size=page_size, poison=True)
+    b = W.PagedBatch(**{**b.__dict__, "logits_cap": cap})
+    plan = mixed_vs_oracle(b, f"mixed page {page_size} g{group} cap {cap}")
+    info = plan.info()
+    assert info.prefill_ctas >= 1 and info.decode_ctas >= 1
+
+
+def test_mixed_is_one_attention_launch(tmp_path):
+    """The run call launches the mixed kernel once, then the two merges; neither the
+    standalone decode nor the standalone prefill kernel runs."""
+    import json
+    from torch.profiler import ProfilerActivity, profile
+    b = small_mixed(40)
+    db = runner.DeviceBatch.from_host(b)
+    plan = runner.make_plan(b, api.PLAN_MIXED)
+    runner.plan_batch(plan, b)
+    runner.mixed(db, plan)
+    marker = torch.ones(1, device="cuda")
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
+        marker.add_(1)  # a torch kernel: shows that kernel records reached the trace
+        runner.mixed(db, plan)
+        torch.cuda.synchronize()
+    # The exported trace lists every kernel record, also those no torch op launched.
+    path = tmp_path / "trace.json"
+    prof.export_chrome_trace(str(path))
+    names = [e.get("name", "") for e in json.loads(path.read_text()).get("traceEvents", [])
+             if e.get("cat") == "kernel"]
+    if not names:
+        pytest.skip("the profiler recorded no kernels on this machine")
+    ours = [n for n in names if "pkv" in n]
+    assert sum("mixed_kernel" in n for n in ours) == 1, ours
+    assert not any("decode_kernel" in n or "prefill_kernel" in n for n in ours), ours
+    assert sum("merge_kernel" in n for n in ours) == 2, ours
+
+
 @pytest.mark.parametrize("n_decode,n_prefill", [(7, 0), (0, 4)])
 def test_mixed_batch_with_one_half(n_decode, n_prefill):
     mixed_vs_oracle(small_mixed(11, n_decode=n_decode, n_prefill=n_prefill), f"{n_decode}+{n_prefill}")
@@ -75,8 +117,9 @@ def test_mixed_full_size():
 
 
 def test_mixed_graph_replay_after_replanning():
-    """Capture the mixed run (fork onto the plan's side stream, join back) once;
-    re-plan a batch with another decode/prefill mix of the same total rows; replay."""
+    """Capture the mixed run once; re-plan a batch with another decode/prefill mix of
+    the same total rows (so another SM split, read by the kernel from the device
+    tables); replay."""
     a = small_mixed(20, n_decode=10, n_prefill=2)
     total = a.total_q
     bb = W.mixed_batch(seed=21, n_decode=total - 2 * 50, n_prefill=2, decode_lo=1, decode_hi=700, qo_lo=50,
