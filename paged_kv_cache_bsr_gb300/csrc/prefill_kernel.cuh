@@ -239,14 +239,25 @@ __device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensor
     const uint32_t dst_c = dst + (c >> 3) * kHalf;
     const int cc = c & 7;
     const T* kvp = static_cast<const T*>(a.kv);
-    for (int i = 0; i < kBN / 2; ++i) {
-      const int r = 2 * i + (lane >> 4);
-      const int id = ids[r >> lp];
-      const bool valid = id >= 0 && key0 + r < t.kv_len;
-      const T* src = kvp;
-      if (valid)
-        src = kvp + ((((int64_t)id * 2 + kv_sel) * a.num_kv_heads + t.kvh) * P + (r & (P - 1))) * kD + c * 8;
-      cp_async_16(dst_c + r * 128 + ((cc ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+    // Eight rows at a time: their page ids first (independent shared loads), then
+    // their copies; a copy is ordered after everything before it, so one id load
+    // between two copies would expose its whole latency.
+    constexpr int kBatch = 8;
+#pragma unroll 1
+    for (int i0 = 0; i0 < kBN / 2; i0 += kBatch) {
+      int idb[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) idb[u] = ids[(2 * (i0 + u) + (lane >> 4)) >> lp];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int r = 2 * (i0 + u) + (lane >> 4);
+        const int id = idb[u];
+        const bool valid = id >= 0 && key0 + r < t.kv_len;
+        const T* src = kvp;
+        if (valid)
+          src = kvp + ((((int64_t)id * 2 + kv_sel) * a.num_kv_heads + t.kvh) * P + (r & (P - 1))) * kD + c * 8;
+        cp_async_16(dst_c + r * 128 + ((cc ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+      }
     }
     cp_async_commit();
     next();
