@@ -234,29 +234,39 @@ __device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensor
     for (int m = 0; m < 4; ++m)
       if (lane + 32 * m < ppt) ids[lane + 32 * m] = idr[m];
     __syncwarp();
-    const int lp = __ffs(P) - 1;     // P is a power of two
+    const int lp = __ffs(P) - 1;     // P is a power of two (1, 2 or 4 here)
     const int c = lane & 15;         // 16-byte chunk of the 256-byte row
-    const uint32_t dst_c = dst + (c >> 3) * kHalf;
-    const int cc = c & 7;
+    const int hr = lane >> 4;        // this half-warp takes rows 2i + hr
     const T* kvp = static_cast<const T*>(a.kv);
+    // Per lane and block: the chunk's address in page 0 of this (K|V, kv head), the
+    // distance from one page to the next, and for the eight rows of a batch their
+    // swizzled shared-memory offset and slot offset inside the page (a batch
+    // starts at a multiple of 16 rows, so both repeat from batch to batch).
+    const T* base_c = kvp + (static_cast<int64_t>(kv_sel) * a.num_kv_heads + t.kvh) * P * kD + c * 8;
+    const int64_t page_stride = 2ll * a.num_kv_heads * P * kD;
+    constexpr int kBatch = 8;
+    uint32_t dst_u[kBatch];
+    int slot_u[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int r = 2 * u + hr;
+      dst_u[u] = dst + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+      slot_u[u] = (r & (P - 1)) * kD;
+    }
+    const int rows_left = t.kv_len - key0 - hr;  // row 2i + hr exists while 2i < rows_left
     // Eight rows at a time: their page ids first (independent shared loads), then
     // their copies; a copy is ordered after everything before it, so one id load
     // between two copies would expose its whole latency.
-    constexpr int kBatch = 8;
 #pragma unroll 1
     for (int i0 = 0; i0 < kBN / 2; i0 += kBatch) {
       int idb[kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) idb[u] = ids[(2 * (i0 + u) + (lane >> 4)) >> lp];
+      for (int u = 0; u < kBatch; ++u) idb[u] = ids[(2 * (i0 + u) + hr) >> lp];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const int r = 2 * (i0 + u) + (lane >> 4);
-        const int id = idb[u];
-        const bool valid = id >= 0 && key0 + r < t.kv_len;
-        const T* src = kvp;
-        if (valid)
-          src = kvp + ((((int64_t)id * 2 + kv_sel) * a.num_kv_heads + t.kvh) * P + (r & (P - 1))) * kD + c * 8;
-        cp_async_16(dst_c + r * 128 + ((cc ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+        const bool valid = idb[u] >= 0 && 2 * (i0 + u) < rows_left;
+        const T* src = valid ? base_c + idb[u] * page_stride + slot_u[u] : kvp;
+        cp_async_16(dst_u[u] + i0 * 256, src, valid ? 16u : 0u);
       }
     }
     cp_async_commit();
