@@ -25,7 +25,7 @@
 //               coordinate, which TMA fills with zeros; V rows past
 //               kv_last_page_len of the last page are zeroed before the MMA
 //               may read them.  Pages of 1, 2 or 4 rows (column-vector BSR)
-//               are gathered instead with 16-byte cp.async, half a warp per
+//               are gathered instead with 16-byte cp.async, four lanes per
 //               256-byte row, into the same swizzled layout, zero-filled past
 //               the request; each lane waits for its own copies, fences them
 //               for the tensor cores and arrives on the block's barrier, while
@@ -207,7 +207,7 @@ __device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensor
   // Pages smaller than 8 rows.  gather_ids loads the page ids of block j of tile t
   // (up to 128, four per lane; -1 past the request); gather_block copies that
   // block's K (kv_sel 0) or V (1) rows into the swizzled stage at `dst` with
-  // cp.async, 16 bytes a lane and half a warp per 256-byte row, zero-filling rows
+  // cp.async, 16 bytes a copy and four lanes per 256-byte row, zero-filling rows
   // past the request, waits for this lane's copies, fences them for the tensor
   // cores and arrives on `full_bar`.  The caller loads the next block's ids in
   // between (`next`), so their latency hides behind the copies.
@@ -235,38 +235,43 @@ __device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensor
       if (lane + 32 * m < ppt) ids[lane + 32 * m] = idr[m];
     __syncwarp();
     const int lp = __ffs(P) - 1;     // P is a power of two (1, 2 or 4 here)
-    const int c = lane & 15;         // 16-byte chunk of the 256-byte row
-    const int hr = lane >> 4;        // this half-warp takes rows 2i + hr
+    // Four lanes per row: lane group g = lane / 4 takes rows 8q + g (q = 0 .. 15),
+    // lane cl = lane % 4 the 16-byte chunks cl and cl + 4 of both 128-byte halves
+    // of the row.  Every row's id lookup and address arithmetic then serve four
+    // copies, and every copy instruction still reads whole 64-byte pieces of eight
+    // rows.  (16 lanes per row issued four times the instructions: 31 % of peak on
+    // 1-token pages against 42 %; 8 lanes per row gave 41 %.)
+    const int g = lane >> 2, cl = lane & 3;
     const T* kvp = static_cast<const T*>(a.kv);
-    // Per lane and block: the chunk's address in page 0 of this (K|V, kv head), the
-    // distance from one page to the next, and for the eight rows of a batch their
-    // swizzled shared-memory offset and slot offset inside the page (a batch
-    // starts at a multiple of 16 rows, so both repeat from batch to batch).
-    const T* base_c = kvp + (static_cast<int64_t>(kv_sel) * a.num_kv_heads + t.kvh) * P * kD + c * 8;
-    const int64_t page_stride = 2ll * a.num_kv_heads * P * kD;
-    constexpr int kBatch = 8;
-    uint32_t dst_u[kBatch];
-    int slot_u[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int r = 2 * u + hr;
-      dst_u[u] = dst + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-      slot_u[u] = (r & (P - 1)) * kD;
-    }
-    const int rows_left = t.kv_len - key0 - hr;  // row 2i + hr exists while 2i < rows_left
+    // The chunk's address in page 0 of this (K|V, kv head) plus the row's slot in
+    // its page (the same for every row of this lane: 8q is a multiple of P), and
+    // the distance from one page to the next.
+    const T* base_c =
+        kvp + (static_cast<int64_t>(kv_sel) * a.num_kv_heads + t.kvh) * P * kD + (g & (P - 1)) * kD + cl * 8;
+    const int page_stride = 2 * a.num_kv_heads * P * kD;
+    // Swizzled shared-memory offsets of chunks cl and cl + 4 (first half): every row
+    // of this lane has row % 8 = g.
+    const uint32_t d0 = dst + g * 128 + ((cl ^ g) << 4), d1 = dst + g * 128 + (((cl + 4) ^ g) << 4);
+    const int rows_left = t.kv_len - key0 - g;  // row 8q + g exists while 8q < rows_left
     // Eight rows at a time: their page ids first (independent shared loads), then
     // their copies; a copy is ordered after everything before it, so one id load
     // between two copies would expose its whole latency.
+    constexpr int kBatch = 8;
 #pragma unroll 1
-    for (int i0 = 0; i0 < kBN / 2; i0 += kBatch) {
+    for (int q0 = 0; q0 < kBN / 8; q0 += kBatch) {
       int idb[kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) idb[u] = ids[(2 * (i0 + u) + hr) >> lp];
+      for (int u = 0; u < kBatch; ++u) idb[u] = ids[(8 * (q0 + u) + g) >> lp];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const bool valid = idb[u] >= 0 && 2 * (i0 + u) < rows_left;
-        const T* src = valid ? base_c + idb[u] * page_stride + slot_u[u] : kvp;
-        cp_async_16(dst_u[u] + i0 * 256, src, valid ? 16u : 0u);
+        const bool valid = idb[u] >= 0 && 8 * (q0 + u) < rows_left;
+        const T* src = base_c + static_cast<int64_t>(valid ? idb[u] : 0) * page_stride;
+        const uint32_t ro = (q0 + u) * 1024;  // row 8q + g is 1024 q bytes past row g
+        const uint32_t nb = valid ? 16u : 0u;
+        cp_async_16(d0 + ro, src, nb);
+        cp_async_16(d1 + ro, src + 32, nb);
+        cp_async_16(d0 + ro + kHalf, src + 64, nb);
+        cp_async_16(d1 + ro + kHalf, src + 96, nb);
       }
     }
     cp_async_commit();
