@@ -171,7 +171,8 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
   auto s = static_cast<cudaStream_t>(stream);
   cudaError_t e = wait_tables(plan, s);
   if (plan->time_start && e == cudaSuccess) cudaEventRecord(plan->time_start, s);
-  if (e == cudaSuccess) e = pkv::launch_decode(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, s);
+  if (e == cudaSuccess)
+    e = pkv::launch_decode(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, plan->num_pages, s);
   if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
   if (e == cudaSuccess) e = pkv::launch_decode_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
   if (e == cudaSuccess) e = release_tables(plan, s);

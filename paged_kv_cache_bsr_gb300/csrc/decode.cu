@@ -1,25 +1,23 @@
-// decode.cu -- batch decode over a paged KV cache: the decode kernel (one CTA
-// of kDecodeWarps independent workers per SM; the worker is in
-// decode_kernel.cuh), the n-way merge of split sequences, and their launches.
+// decode.cu -- batch decode over a paged KV cache: the decode kernel instances
+// that read pages with bulk copies (the kernel, one CTA of kDecodeWarps
+// independent workers per SM, is in decode_kernel.cuh), the n-way merge of split
+// sequences, and their launches.
 #include <cuda_runtime.h>
 #include <math.h>
 
 #include "decode_kernel.cuh"
 
 namespace pkv {
+namespace decode_impl {
+
+template cudaError_t launch_decode_kernel<__nv_bfloat16, false>(const DecodeArgs&, int, int, bool, int, cudaStream_t);
+template cudaError_t launch_decode_kernel<__half, false>(const DecodeArgs&, int, int, bool, int, cudaStream_t);
+
+}  // namespace decode_impl
+
 namespace {
 
 using namespace decode_impl;
-
-template <int D, int G, int LPT, typename T, bool CAP>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
-  constexpr int S = DecodeShape<D, T>::kStages;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kDecodeWarps][S];
-  const int warp = threadIdx.x >> 5;
-  decode_worker<D, G, LPT, T, CAP>(a, blockIdx.x * kDecodeWarps + warp, smem + warp * kDecodeWarpSmem,
-                                   smem_addr(&bars[warp][0]));
-}
 
 // n-way merge of the partial states of split (request, kv head) sequences:
 // one warp per (item, head of the group), lanes over head_dim, the slot loop
@@ -95,37 +93,6 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __gri
   }
 }
 
-template <int D, int G, int LPT, typename T>
-cudaError_t launch_decode_t(const DecodeArgs& a, bool cap, int grid, cudaStream_t stream) {
-  const int smem = kDecodeWarps * kDecodeWarpSmem;
-  static_assert(kDecodeWarps * kDecodeWarpSmem <= 200 * 1024, "decode ring exceeds shared memory");
-  auto kern = cap ? decode_kernel<D, G, LPT, T, true> : decode_kernel<D, G, LPT, T, false>;
-  cudaError_t e = ensure_smem_limit(kern, smem);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kDecodeWarps * 32, smem, stream>>>(a);
-  return cudaGetLastError();
-}
-
-template <typename T>
-cudaError_t dispatch_decode(const DecodeArgs& a, int D, int G, bool cap, int grid, cudaStream_t s) {
-  if (D == 128) {
-    switch (G) {
-      case 1: return launch_decode_t<128, 1, 8, T>(a, cap, grid, s);
-      case 2: return launch_decode_t<128, 2, 8, T>(a, cap, grid, s);
-      case 4: return launch_decode_t<128, 4, 8, T>(a, cap, grid, s);
-      case 8: return launch_decode_t<128, 8, 16, T>(a, cap, grid, s);
-    }
-  } else if (D == 64) {
-    switch (G) {
-      case 1: return launch_decode_t<64, 1, 8, T>(a, cap, grid, s);
-      case 2: return launch_decode_t<64, 2, 8, T>(a, cap, grid, s);
-      case 4: return launch_decode_t<64, 4, 8, T>(a, cap, grid, s);
-      case 8: return launch_decode_t<64, 8, 8, T>(a, cap, grid, s);
-    }
-  }
-  return cudaErrorInvalidValue;
-}
-
 template <typename T>
 cudaError_t dispatch_merge(const DecodeArgs& a, int D, int G, int grid, cudaStream_t s) {
 // The merge kernel is a programmatic dependent of the decode kernel just
@@ -159,11 +126,18 @@ bool decode_supported(int head_dim, int group, int dtype) {
          (dtype == PKV_F16 || dtype == PKV_BF16);
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, int head_dim, int group, int dtype, bool cap, int grid,
-                          cudaStream_t stream) {
-  if (dtype == PKV_BF16) return dispatch_decode<__nv_bfloat16>(a, head_dim, group, cap, grid, stream);
-  if (dtype == PKV_F16) return dispatch_decode<__half>(a, head_dim, group, cap, grid, stream);
-  return cudaErrorInvalidValue;
+cudaError_t launch_decode(const DecodeArgs& a0, int head_dim, int group, int dtype, bool cap, int grid,
+                          int64_t num_pages, cudaStream_t stream) {
+  if (!decode_supported(head_dim, group, dtype)) return cudaErrorInvalidValue;
+  if (a0.page_size > kDecodeGatherMaxRows) {
+    return dtype == PKV_BF16 ? launch_decode_kernel<__nv_bfloat16, false>(a0, head_dim, group, cap, grid, stream)
+                             : launch_decode_kernel<__half, false>(a0, head_dim, group, cap, grid, stream);
+  }
+  DecodeArgs a = a0;
+  cudaError_t e = set_kv_rows_map(a, head_dim, dtype, num_pages);
+  if (e != cudaSuccess) return e;
+  return dtype == PKV_BF16 ? launch_decode_kernel<__nv_bfloat16, true>(a, head_dim, group, cap, grid, stream)
+                           : launch_decode_kernel<__half, true>(a, head_dim, group, cap, grid, stream);
 }
 
 cudaError_t launch_decode_merge(const DecodeArgs& a, int head_dim, int group, int dtype, int grid,

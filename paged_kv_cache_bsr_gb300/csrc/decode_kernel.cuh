@@ -18,6 +18,8 @@
 // tiles in shared memory (24 KB) that its lane 0 fills with TMA bulk copies
 // (cp.async.bulk, completion on an mbarrier): one copy for the tile's K rows
 // and one for its V rows, each a contiguous 16-row x head_dim block of a page.
+// With one-row pages the tile's rows come instead as four-row tensor gathers
+// (tile::gather4) over kv_data viewed as a 2-D tensor of rows.
 // The copies run ahead of the compute by the depth of the ring, so every SM
 // keeps up to 192 KB of reads in flight.  A warp works through the list of
 // (request, kv head, page range) segments the plan gave it, back to back, so
@@ -96,7 +98,10 @@ __device__ __forceinline__ void producer_enter(Producer& p, const DecodeArgs& a,
 }
 
 // Issue the next tile of the warp's stream into its stage; false when done.
-template <int D, typename T>
+// GATHER (one-row pages): the tile's rows come as four-row tensor gathers, four
+// for K (lanes 0-3) and four for V (lanes 4-7), instead of one 256-byte bulk copy
+// per page and K|V.
+template <int D, typename T, bool GATHER>
 __device__ __forceinline__ bool producer_issue(Producer& p, const DecodeArgs& a, uint8_t* ring,
                                                uint32_t bar0, int lane, int64_t num_pages,
                                                uint64_t policy) {
@@ -114,6 +119,34 @@ __device__ __forceinline__ bool producer_issue(Producer& p, const DecodeArgs& a,
       const int stage = p.issued % Shape::kStages;
       const uint32_t dst = smem_addr(ring + stage * Shape::kStageBytes);
       const uint32_t bar = bar0 + 8 * stage;
+      if constexpr (GATHER) {
+        // Every gather writes four whole rows (rows past the segment, or of a bad
+        // page id, as zeros from past the tensor), so the stage always gets a full tile.
+        if (lane == 0) mbar_arrive_expect_tx(bar, 2u * kDecodeTileRows * D * sizeof(T));
+        __syncwarp();
+        const int q4 = lane & 3, sel = (lane >> 2) & 1;  // four tokens' rows of K (sel 0) or V (1)
+        int rowi[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 4 * q4 + i;
+          const int tok = p.tok + r;
+          const int k = tok / P;
+          const int page_id = __shfl_sync(kFull, p.win, min(max(k - p.win_base, 0), 31));
+          rowi[i] = a.kv_rows_n;
+          if (r < rows) {
+            if (page_id >= 0 && page_id < num_pages)
+              rowi[i] = ((page_id * 2 + sel) * a.num_kv_heads + p.kvh) * P + (tok - k * P);
+            else if (lane < 8)
+              atomicOr(a.err, kErrPageIndex);
+          }
+        }
+        if (lane < 8)
+          tma_gather4(dst + sel * Shape::kTileBytes + q4 * 4 * D * static_cast<int>(sizeof(T)), &a.kv_rows, 0,
+                      rowi[0], rowi[1], rowi[2], rowi[3], bar);
+        ++p.issued;
+        p.tok += rows;
+        return true;
+      }
       if (lane == 0) mbar_arrive_expect_tx(bar, 2u * rows * D * sizeof(T));
       __syncwarp();
       const int k = pa + lane;  // this lane's page
@@ -300,7 +333,7 @@ __device__ __forceinline__ void tile_step(const DecodeArgs& a, const T* ks, cons
 // (shared-memory address) and streams the segments the plan gave `worker`
 // through its ring of S stages of K and V tiles at `ring`.  Warps are
 // independent: nothing here synchronises beyond the calling warp.
-template <int D, int G, int LPT, typename T, bool CAP>
+template <int D, int G, int LPT, typename T, bool CAP, bool GATHER>
 __device__ __forceinline__ void decode_worker(const DecodeArgs& a, int worker, uint8_t* ring, uint32_t bar0) {
   using Shape = DecodeShape<D, T>;
   constexpr int S = Shape::kStages;
@@ -336,7 +369,7 @@ __device__ __forceinline__ void decode_worker(const DecodeArgs& a, int worker, u
   prod.issued = 0;
   producer_enter<D, T>(prod, a, lane);
   for (int s = 0; s < S; ++s)
-    if (!producer_issue<D, T>(prod, a, ring, bar0, lane, num_pages, policy)) break;
+    if (!producer_issue<D, T, GATHER>(prod, a, ring, bar0, lane, num_pages, policy)) break;
 
   int consumed = 0;
   bool ok = true;
@@ -390,7 +423,7 @@ __device__ __forceinline__ void decode_worker(const DecodeArgs& a, int worker, u
         tile_step<D, G, LPT, T, CAP, false>(a, ks, vs, rows, sub, grp, my_head, qf, m, m_own, l_own, acc);
       ++consumed;
       __syncwarp();
-      producer_issue<D, T>(prod, a, ring, bar0, lane, num_pages, policy);
+      producer_issue<D, T, GATHER>(prod, a, ring, bar0, lane, num_pages, policy);
     }
     if (!ok) break;
 
@@ -452,6 +485,45 @@ __device__ __forceinline__ void decode_worker(const DecodeArgs& a, int worker, u
       if (!mbar_wait(bar0 + 8 * (t % S), (t / S) & 1, a.err)) break;
   }
 }
+
+template <int D, int G, int LPT, typename T, bool CAP, bool GATHER>
+__global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
+  constexpr int S = DecodeShape<D, T>::kStages;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kDecodeWarps][S];
+  const int warp = threadIdx.x >> 5;
+  decode_worker<D, G, LPT, T, CAP, GATHER>(a, blockIdx.x * kDecodeWarps + warp, smem + warp * kDecodeWarpSmem,
+                                           smem_addr(&bars[warp][0]));
+}
+
+// Launch one decode instance (head_dim, group size and cap chosen at run time).
+// Lanes per token: 8, or 16 for a group of 8 at head_dim 128.
+template <typename T, bool GATHER>
+cudaError_t launch_decode_kernel(const DecodeArgs& a, int D, int G, bool cap, int grid, cudaStream_t s) {
+  void (*kern)(DecodeArgs) = nullptr;
+#define PKV_DEC_CASE(DD, GG, LL)                                                                                 \
+  if (D == DD && G == GG)                                                                                       \
+    kern = cap ? decode_kernel<DD, GG, LL, T, true, GATHER> : decode_kernel<DD, GG, LL, T, false, GATHER>;
+  PKV_DEC_CASE(128, 1, 8) PKV_DEC_CASE(128, 2, 8) PKV_DEC_CASE(128, 4, 8) PKV_DEC_CASE(128, 8, 16)
+  PKV_DEC_CASE(64, 1, 8) PKV_DEC_CASE(64, 2, 8) PKV_DEC_CASE(64, 4, 8) PKV_DEC_CASE(64, 8, 8)
+#undef PKV_DEC_CASE
+  if (!kern) return cudaErrorInvalidValue;
+  const int smem = kDecodeWarps * kDecodeWarpSmem;
+  static_assert(kDecodeWarps * kDecodeWarpSmem <= 200 * 1024, "decode ring exceeds shared memory");
+  cudaError_t e = ensure_smem_limit(kern, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kDecodeWarps * 32, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+// Each instance set is compiled in its own translation unit (decode.cu: bulk
+// copies; decode_gather.cu: tensor gathers for one-row pages).
+extern template cudaError_t launch_decode_kernel<__nv_bfloat16, false>(const DecodeArgs&, int, int, bool, int,
+                                                                       cudaStream_t);
+extern template cudaError_t launch_decode_kernel<__half, false>(const DecodeArgs&, int, int, bool, int, cudaStream_t);
+extern template cudaError_t launch_decode_kernel<__nv_bfloat16, true>(const DecodeArgs&, int, int, bool, int,
+                                                                      cudaStream_t);
+extern template cudaError_t launch_decode_kernel<__half, true>(const DecodeArgs&, int, int, bool, int, cudaStream_t);
 
 }  // namespace decode_impl
 }  // namespace pkv

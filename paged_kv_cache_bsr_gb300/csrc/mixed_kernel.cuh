@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kDecodeRegs));
   using M = MixedSmem<G, T>;
-  decode_impl::decode_worker<128, G, MixedLpt<G>::value, T, CAP>(
+  decode_impl::decode_worker<128, G, MixedLpt<G>::value, T, CAP, false>(
       da, (cta - split) * kDecodeWarps + warp, smem + warp * kDecodeWarpSmem,
       smem_addr(smem + M::kDecBarOff) + 8u * M::kDecStages * warp);
 }

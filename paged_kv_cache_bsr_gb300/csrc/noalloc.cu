@@ -103,7 +103,7 @@ extern "C" pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const
   a.page_size = p.page_size;
   a.q_scale = cap ? p.sm_scale : p.sm_scale * pkv::kLog2e;
   a.cap = cap ? p.logits_cap : 0.f;
-  cudaError_t e = pkv::launch_decode(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, s);
+  cudaError_t e = pkv::launch_decode(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, plan->num_pages, s);
   if (e == cudaSuccess) e = pkv::launch_decode_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -2,6 +2,7 @@
 // kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,6 +30,11 @@ struct DecodeArgs {
   int page_size;
   float q_scale;               // multiplies q: sm_scale * log2(e) without a cap, sm_scale with one
   float cap;                   // logits cap (> 0 only in the capped instantiation)
+  // One-row pages (the gather instances): kv_data as a 2-D tensor of
+  // head_dim-element rows, row ((page * 2 + K|V) * Hkv + kv head) * page_size +
+  // slot, with kv_rows_n rows; set by the launch, unused otherwise.
+  int32_t kv_rows_n;
+  CUtensorMap kv_rows;
 };
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device): the
@@ -45,12 +51,20 @@ constexpr int kDecodeWarps = 8;
 // Shared memory each decode warp uses for its ring of page tiles.
 constexpr int kDecodeWarpSmem = 24 * 1024;
 constexpr int kDecodeTileRows = 16;
+// Pages of one row (column-vector BSR) reach decode tiles as four-row tensor
+// gathers; pages of two rows or more as one bulk copy per page (measured: one-row
+// pages 4.31 vs 3.92 TB/s, two-row pages 4.47 vs 4.86 TB/s with gathers vs copies).
+constexpr int kDecodeGatherMaxRows = 1;
 constexpr int kMergeThreads = 256;
 
-// Launch the decode kernel for (head_dim, group, dtype, cap); returns
-// cudaErrorInvalidValue for a combination that was not built.
+// Launch the decode kernel for (head_dim, group, dtype, cap) over a pool of
+// num_pages pages; returns cudaErrorInvalidValue for a combination that was not
+// built.
 cudaError_t launch_decode(const DecodeArgs& a, int head_dim, int group, int dtype, bool cap,
-                          int grid, cudaStream_t stream);
+                          int grid, int64_t num_pages, cudaStream_t stream);
+// Fill a.kv_rows / a.kv_rows_n for the gather instances: kv_data as rows of
+// head_dim elements, one-row boxes.
+cudaError_t set_kv_rows_map(DecodeArgs& a, int head_dim, int dtype, int64_t num_pages);
 // Launch the n-way merge of split decode sequences (fixed grid).
 cudaError_t launch_decode_merge(const DecodeArgs& a, int head_dim, int group, int dtype, int grid,
                                 cudaStream_t stream);

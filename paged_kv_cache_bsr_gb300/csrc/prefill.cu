@@ -119,6 +119,24 @@ cudaError_t make_tensor_maps(const PrefillArgs& a, int group, int dtype, int64_t
 
 }  // namespace prefill_impl
 
+cudaError_t set_kv_rows_map(DecodeArgs& a, int head_dim, int dtype, int64_t num_pages) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  const int64_t rows = (num_pages > 0 ? num_pages : 1) * 2 * a.num_kv_heads * a.page_size;
+  if (rows >= INT32_MAX) return cudaErrorInvalidValue;  // row coordinates are 32-bit
+  const CUtensorMapDataType dt = dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(head_dim), 1};
+  cuuint32_t es[2] = {1, 1};
+  if (encode(&a.kv_rows, dt, 2, const_cast<void*>(a.kv), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  a.kv_rows_n = static_cast<int32_t>(rows);
+  return cudaSuccess;
+}
+
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dtype, bool cap, int grid,
                            int64_t total_q, int64_t num_pages, cudaStream_t stream) {
   if (!prefill_supported(head_dim, group, dtype, a.page_size)) return cudaErrorInvalidValue;

@@ -94,6 +94,43 @@ def test_page_sizes(page_size):
     decode_vs_oracle(b, f"page {page_size}")
 
 
+@pytest.mark.parametrize("group,head_dim,cap", [(1, 64, 0.0), (2, 128, 0.0), (4, 128, 30.0), (8, 128, 0.0),
+                                                (8, 64, 30.0)])
+def test_one_row_pages_take_tensor_gathers(group, head_dim, cap):
+    """One-row pages (column-vector BSR) reach the tiles as four-row tensor gathers;
+    lengths end inside a gather (1, 3), inside a tile (17) and at none (0)."""
+    b = W.make_paged_batch(qo_lens=[1] * 6, kv_lens=[1, 3, 17, 0, 250, 1031], num_qo_heads=2 * group,
+                           num_kv_heads=2, head_dim=head_dim, page_size=1, dtype=torch.bfloat16,
+                           seed=group * 10 + head_dim, logits_cap=cap, poison=True)
+    decode_vs_oracle(b, f"one-row pages g{group} d{head_dim} cap{cap}")
+
+
+def test_one_row_pages_full_size():
+    """The Llama-3-8B decode batch on one-row pages, split and merged."""
+    decode_vs_oracle(W.llama3_decode(page_size=1, poison=True), "llama3 one-row pages")
+
+
+@pytest.mark.parametrize("page_size", [16, 1])
+def test_page_id_outside_the_pool_sets_the_error_bit(page_size):
+    """A device page table that holds an id outside [0, num_pages) (the plan checked a
+    host copy): the kernel reads no memory for it (bulk copies fall back to page 0,
+    gathers to a row past the tensor), records the page-index error bit, and every
+    request without the bad entry still gets its exact result."""
+    b = W.make_paged_batch(qo_lens=[1] * 4, kv_lens=[40, 300, 77, 129], num_qo_heads=8, num_kv_heads=2,
+                           head_dim=128, page_size=page_size, dtype=torch.bfloat16, seed=31 + page_size, poison=True)
+    db = runner.DeviceBatch.from_host(b)
+    plan = runner.make_plan(b, api.PLAN_DECODE)
+    runner.plan_batch(plan, b)
+    bad = int(b.kv_indptr[1])  # the first page of request 1
+    db.kv_indices[bad] = b.num_pages + 7
+    o, lse = runner.decode(db, plan)
+    torch.cuda.synchronize()
+    assert plan.device_error() & 1
+    keep = [0, 2, 3]
+    ref_o, ref_lse = oracle.attention_of(b)
+    assert_matches_oracle(o[keep], lse[keep], ref_o[keep], ref_lse[keep], b.dtype, "other requests")
+
+
 def test_long_single_request_is_split_and_merged():
     b = W.make_paged_batch(qo_lens=[1], kv_lens=[60000], num_qo_heads=8, num_kv_heads=2, head_dim=128,
                            page_size=16, dtype=torch.bfloat16, seed=5, poison=True)

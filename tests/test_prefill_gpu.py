@@ -114,6 +114,27 @@ def test_cascade_softcap_full_size_equals_full_attention():
     assert_matches_oracle(o, lse, ref_o, ref_lse, torch.bfloat16, "cascade")
 
 
+@pytest.mark.parametrize("page_size", [16, 1])
+def test_prefill_page_id_outside_the_pool_sets_the_error_bit(page_size):
+    """A device page table with an id outside the pool: tensor loads use a page
+    coordinate past the pool and the row gather zero-fills, so nothing outside
+    kv_data is read; the page-index error bit is set, and the requests without the
+    bad entry keep their exact results."""
+    b = batch([40, 130, 77], [20, 300, 0], P=page_size, seed=41 + page_size)
+    db = runner.DeviceBatch.from_host(b)
+    plan = runner.make_plan(b, api.PLAN_PREFILL)
+    runner.plan_batch(plan, b)
+    bad = int(b.kv_indptr[1])  # the first page of request 1
+    db.kv_indices[bad] = -3
+    o, lse = runner.prefill(db, plan)
+    torch.cuda.synchronize()
+    assert plan.device_error() & 1
+    rows = [i for r in (0, 2) for i in range(int(b.qo_indptr[r]), int(b.qo_indptr[r + 1]))]
+    ref_o, ref_lse = oracle.attention_of(b, rows=rows)
+    idx = torch.as_tensor(rows, dtype=torch.long, device=o.device)
+    assert_matches_oracle(o[idx], lse[idx], ref_o, ref_lse, b.dtype, "other requests")
+
+
 def test_prefill_page_permutation_is_bit_exact():
     b = batch([300, 45], [60, 200], seed=8)
     db = runner.DeviceBatch.from_host(b)
