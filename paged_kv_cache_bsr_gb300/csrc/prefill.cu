@@ -22,6 +22,9 @@ namespace {
 // lanes over head_dim, log-sum-exp merge of the chunks' fp32 partial states.
 template <typename T>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constant__ PrefillArgs a) {
+  // Launched as a programmatic dependent of the kernel before it: wait until that
+  // grid has finished and its partial states are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int warp_id = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int n_warps = gridDim.x * 8;
@@ -158,13 +161,20 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dt
 cudaError_t launch_prefill_merge(const PrefillArgs& a, int head_dim, int group, int dtype, int grid,
                                  cudaStream_t stream) {
   if (head_dim != kD || group <= 0) return cudaErrorInvalidValue;
-  if (dtype == PKV_BF16)
-    prefill_merge_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a);
-  else if (dtype == PKV_F16)
-    prefill_merge_kernel<__half><<<grid, 256, 0, stream>>>(a);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  // A programmatic dependent of the prefill (or mixed) kernel before it: its CTAs
+  // start as that grid's CTAs leave, and wait for the whole grid before reading.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dtype == PKV_BF16) return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<__nv_bfloat16>, a);
+  if (dtype == PKV_F16) return cudaLaunchKernelEx(&cfg, prefill_merge_kernel<__half>, a);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv
