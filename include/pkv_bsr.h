@@ -339,7 +339,9 @@ pkv_status pkv_batch_mixed_paged(const pkv_plan* plan, const void* q, const int3
  * Both lse = -inf gives o = 0, lse = -inf; a state with lse = -inf adds nothing.
  * o_* : [n_rows, num_heads, head_dim] of `dtype` (PKV_F16, PKV_BF16 or PKV_F32;
  * inputs and output share it); lse_*: [n_rows, num_heads] fp32.  o_out and
- * lse_out may alias o_a and lse_a.  lse_out may be NULL.
+ * lse_out may alias o_a and lse_a.  lse_out may be NULL.  The kernel is
+ * launched as a programmatic dependent of the work before it on `stream`: its
+ * CTAs may start early but read nothing before that work has completed.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  */
 pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,

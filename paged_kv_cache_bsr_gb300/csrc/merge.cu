@@ -50,6 +50,9 @@ __global__ void __launch_bounds__(256) merge_state_kernel(const uint8_t* o_a, co
                                                           uint8_t* o_out, float* lse_out, int64_t rows,
                                                           int chunks) {
   using C = Chunk<T>;
+  // Launched as a programmatic dependent of whatever kernel precedes it on the
+  // stream: wait until that grid has finished and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int per_warp = 32 / chunks;  // (row, head) pairs per warp
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -111,13 +114,24 @@ cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* 
   auto a = static_cast<const uint8_t*>(o_a);
   auto b = static_cast<const uint8_t*>(o_b);
   auto o = static_cast<uint8_t*>(o_out);
+  // Its CTAs may start while the producing kernel's last CTAs finish (they wait
+  // for the whole grid before reading).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (dtype) {
-    case PKV_F32: merge_state_kernel<float><<<grid, 256, 0, stream>>>(a, lse_a, b, lse_b, o, lse_out, rows, chunks); break;
-    case PKV_BF16: merge_state_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a, lse_a, b, lse_b, o, lse_out, rows, chunks); break;
-    case PKV_F16: merge_state_kernel<__half><<<grid, 256, 0, stream>>>(a, lse_a, b, lse_b, o, lse_out, rows, chunks); break;
+    case PKV_F32: return cudaLaunchKernelEx(&cfg, merge_state_kernel<float>, a, lse_a, b, lse_b, o, lse_out, rows, chunks);
+    case PKV_BF16:
+      return cudaLaunchKernelEx(&cfg, merge_state_kernel<__nv_bfloat16>, a, lse_a, b, lse_b, o, lse_out, rows, chunks);
+    case PKV_F16: return cudaLaunchKernelEx(&cfg, merge_state_kernel<__half>, a, lse_a, b, lse_b, o, lse_out, rows, chunks);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace pkv
