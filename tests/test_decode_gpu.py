@@ -131,6 +131,26 @@ def test_page_id_outside_the_pool_sets_the_error_bit(page_size):
     assert_matches_oracle(o[keep], lse[keep], ref_o[keep], ref_lse[keep], b.dtype, "other requests")
 
 
+def test_request_split_by_key_range_merges_to_the_whole():
+    """One long request split by key range as over three ranks (run here one after the
+    other on one GPU): the decode kernel's partial states of the pieces, stacked as the
+    all-gather would stack them, folded by merge_state on the device, equal the whole
+    request's attention."""
+    from paged_kv_cache_bsr_gb300 import shard
+    b = W.make_paged_batch(qo_lens=[1], kv_lens=[30011], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                           page_size=16, dtype=torch.bfloat16, seed=13, logits_cap=30.0, poison=True)
+    kv = b.kv_data.cuda()
+    os_, ls = [], []
+    for piece in shard.split_sequence(b, 0, 3):
+        o, lse = runner.decode(runner.DeviceBatch.from_host(piece, kv_data=kv))
+        os_.append(o)
+        ls.append(lse)
+    o, lse = shard.merge_gathered(torch.stack(os_), torch.stack(ls))
+    torch.cuda.synchronize()
+    ref_o, ref_lse = oracle.attention_of(b)
+    assert_matches_oracle(o, lse, ref_o, ref_lse, b.dtype, "key-range split merged")
+
+
 def test_long_single_request_is_split_and_merged():
     b = W.make_paged_batch(qo_lens=[1], kv_lens=[60000], num_qo_heads=8, num_kv_heads=2, head_dim=128,
                            page_size=16, dtype=torch.bfloat16, seed=5, poison=True)
