@@ -218,6 +218,11 @@ pkv_status pkv_plan_set_pipelined(pkv_plan* plan, int on);
  * plan (a mismatch sets the device error word and skips the work).
  * Long sequences are split into chunks whose fp32 partial states go to dev_ws
  * and are merged by log-sum-exp in a second fixed-grid kernel.  Graph-capturable.
+ * Pages of one row (column-vector BSR) reach the kernel through a TMA tensor
+ * map over kv_data built at launch from kv_data and num_pages of the current
+ * plan: with page_size 1 a captured graph can be replayed after re-planning a
+ * batch over the same kv_data buffer and pool size (page_size 1 with more than
+ * 2^31 (page, K|V, kv head) rows in the pool is refused with PKV_ERR_UNSUPPORTED).
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  */
 pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const void* kv_data,
