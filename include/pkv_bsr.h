@@ -323,7 +323,10 @@ pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const void* host
  * fdeinterviews summary, "Customizable attention": a query tile size from 1 to
  * 128 picked per batch; greptalks, "Future Directions and Features": mixed
  * prefill and decode phases in one batch).  The split is read from the device
- * tables, so a captured graph stays valid across re-planning within the limits.
+ * tables and the prefill half's tensor maps are built at launch as for
+ * pkv_batch_prefill_paged, so a captured graph stays valid across re-planning
+ * within the limits with the same q and kv_data buffers, total query rows and
+ * pool size.
  * Arguments and layouts as for pkv_batch_prefill_paged (qo_indptr_d covers
  * every request; causal per params->causal applies to the prefill half, and a
  * single-row request sees all its keys either way).
