@@ -31,7 +31,8 @@
 //               for the tensor cores and arrives on the block's barrier, while
 //               the next block's page ids load.
 //   warp 1      one thread issues the tcgen05 MMAs, alternating the tiles:
-//               P_A V -> O_A, S_A(next) = Q_A K^T, P_B V -> O_B, S_B(next).
+//               P_A V -> O_A, S_A(next) = Q_A K^T, P_B V -> O_B, S_B(next)
+//               (tile A only when the work tile's positions fit in it).
 //               S, P and O stay in tensor memory: S_A, S_B, O_A, O_B take the
 //               512 columns, and each P (bf16/fp16) overwrites the first 64
 //               columns of its S, the A operand of its P V MMA.
@@ -440,6 +441,9 @@ __device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensor
       for (int ti = t_begin, tn = 0; ti < t_end && ok; ++ti, ++tn) {
         const PrefillTile t = a.tiles[ti];
         const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
+        // Tile B holds positions MP .. 2 MP - 1; a work tile of at most MP
+        // positions (a request's short last tile, a decode row) runs tile A only.
+        const int nx = t.n_pos > MP ? 2 : 1;
         if (!(ok = wait(bar(Q_FULL), tn & 1))) break;
         tc_fence_after();
         if (n == 0) {
@@ -449,36 +453,45 @@ __device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensor
         if (!(ok = wait(bar(K_FULL + kvc % kKStages), (kvc / kKStages) & 1))) break;
         tc_fence_after();
         mma_s(0, kvc);
-        mma_s(1, kvc);
+        if (nx == 2) mma_s(1, kvc);
         umma_commit(bar(K_EMPTY + kvc % kKStages));
         if (n == 1) umma_commit(bar(Q_EMPTY));
-        for (int j = 0; j < n && ok; ++j) {
-          const int c = kvc + j;
-          for (int x = 0; x < 2 && ok; ++x) {
-            if (!(ok = wait(bar(P_FULL + x), pc[x] & 1))) break;
-            ++pc[x];
-            if (j == 0 && o_used[x]) {  // the previous tile's epilogue has read O_x
-              if (!(ok = wait(bar(O_FREE + x), ofree[x] & 1))) break;
-              ++ofree[x];
-            }
-            if (x == 0 && !(ok = wait(bar(V_FULL + c % kVStages), (c / kVStages) & 1))) break;
-            tc_fence_after();
-            mma_pv(x, c, j > 0, j == n - 1);
-            o_used[x] = true;
-            if (x == 1) umma_commit(bar(V_EMPTY + c % kVStages));  // both P V of block c issued
-            if (j + 1 < n) {
-              if (x == 0) {
-                if (!(ok = wait(bar(K_FULL + (c + 1) % kKStages), ((c + 1) / kKStages) & 1))) break;
-                tc_fence_after();
+        // The key blocks of the tile, compiled once for each number of UMMA tiles
+        // (NX = 2 is the loop of a full work tile, with nothing tested per tile).
+        auto blocks = [&](auto nx_c) {
+          constexpr int NX = decltype(nx_c)::value;
+          for (int j = 0; j < n && ok; ++j) {
+            const int c = kvc + j;
+            for (int x = 0; x < NX && ok; ++x) {
+              if (!(ok = wait(bar(P_FULL + x), pc[x] & 1))) break;
+              ++pc[x];
+              if (j == 0 && o_used[x]) {  // the previous tile's epilogue has read O_x
+                if (!(ok = wait(bar(O_FREE + x), ofree[x] & 1))) break;
+                ++ofree[x];
               }
-              mma_s(x, c + 1);
-              if (x == 1) {
-                umma_commit(bar(K_EMPTY + (c + 1) % kKStages));  // both S of block c + 1 issued
-                if (j + 1 == n - 1) umma_commit(bar(Q_EMPTY));
+              if (x == 0 && !(ok = wait(bar(V_FULL + c % kVStages), (c / kVStages) & 1))) break;
+              tc_fence_after();
+              mma_pv(x, c, j > 0, j == n - 1);
+              o_used[x] = true;
+              if (x == NX - 1) umma_commit(bar(V_EMPTY + c % kVStages));  // every P V of block c issued
+              if (j + 1 < n) {
+                if (x == 0) {
+                  if (!(ok = wait(bar(K_FULL + (c + 1) % kKStages), ((c + 1) / kKStages) & 1))) break;
+                  tc_fence_after();
+                }
+                mma_s(x, c + 1);
+                if (x == NX - 1) {
+                  umma_commit(bar(K_EMPTY + (c + 1) % kKStages));  // every S of block c + 1 issued
+                  if (j + 1 == n - 1) umma_commit(bar(Q_EMPTY));
+                }
               }
             }
           }
-        }
+        };
+        if (nx == 2)
+          blocks(std::integral_constant<int, 2>{});
+        else
+          blocks(std::integral_constant<int, 1>{});
         kvc += n;
       }
       // Every MMA issued so far must finish before tensor memory is released.
@@ -504,6 +517,10 @@ __device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensor
     bool ok = true;
     for (int ti = t_begin; ti < t_end && ok; ++ti) {
       const PrefillTile t = a.tiles[ti];
+      // A work tile of at most MP positions has no rows in tile B: the MMA thread
+      // issues nothing for it, and its group skips the tile (its rows are past
+      // n_pos, written nowhere and not read by the merge of a split key range).
+      if (x == 1 && t.n_pos <= MP) continue;
       const int n = ceil_div_i(t.kv_end - t.kv_begin, kBN);
       const int rpos = x * MP + r / G;     // position of this row within the work tile
       const bool row_valid = rpos < t.n_pos;
