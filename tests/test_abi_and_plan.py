@@ -346,6 +346,27 @@ def test_mixed_plan_routes_requests_by_row_count(lib):
     assert info2.prefill_ctas > info.prefill_ctas
 
 
+@pytest.mark.parametrize("num_sms", [152, 10, 4, 2])
+def test_mixed_split_gives_each_half_sms_and_is_even(lib, num_sms):
+    """Both halves get SMs and together all of them; the prefill share is even when the
+    GPU has room for it (an odd share would leave an SM pair with one CTA of each half)."""
+    for seed, n_prefill in ((1007, 4), (1007, 12), (3, 1)):
+        b = W.mixed_batch(seed=seed, n_prefill=n_prefill)
+        h, ws = host_plan(b, api.PLAN_MIXED, num_sms=num_sms)
+        compute(h, ws, b)
+        info = check_mixed_plan(h, b, num_sms=num_sms)
+        assert info.prefill_ctas >= 1 and info.decode_ctas >= 1
+        assert info.prefill_ctas + info.decode_ctas == num_sms
+        if num_sms >= 4:
+            assert info.prefill_ctas % 2 == 0
+
+
+def test_mixed_plan_needs_two_sms(lib):
+    b = W.mixed_batch(seed=2, n_decode=2, n_prefill=1)
+    with pytest.raises(api.PkvError):
+        host_plan(b, api.PLAN_MIXED, num_sms=1)
+
+
 @pytest.mark.parametrize("n_decode,n_prefill", [(0, 3), (5, 0), (0, 0)])
 def test_mixed_plan_with_one_half_empty(lib, n_decode, n_prefill):
     b = W.mixed_batch(seed=5, n_decode=n_decode, n_prefill=n_prefill, qo_lo=20, qo_hi=300, decode_lo=1,
