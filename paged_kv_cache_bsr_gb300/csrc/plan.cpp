@@ -88,7 +88,7 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
   *out = nullptr;
   pkv_status st = check_params(kind, params, limits);
   if (st != PKV_OK) return st;
-  if (num_sms <= 0) return PKV_ERR_INVALID_ARG;
+  if (num_sms <= 0 || num_sms >= (1 << 20)) return PKV_ERR_INVALID_ARG;  // CTA ids fit the plan's heap keys
   if (kind == PKV_PLAN_MIXED && num_sms < 2) return PKV_ERR_INVALID_ARG;  // one SM for each half at least
   pkv_plan* pl = new (std::nothrow) pkv_plan();
   if (!pl) return PKV_ERR_INVALID_ARG;
@@ -396,6 +396,8 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   std::vector<QueryTile> tiles;
   const int64_t total = query_tiles(pl, batch, qo_indptr, kv_indptr, kv_last, skip_single, tiles);
   const int64_t chunk = key_chunk(total, C);
+  items.reserve(tiles.size() + static_cast<size_t>(std::min<int64_t>(total / std::max<int64_t>(chunk, 1) + 1,
+                                                                        pl->max_work)));
   int n_slot = 0;
   for (const QueryTile& t : tiles) {
     PrefillTile pt{};
@@ -437,23 +439,41 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   if ((int64_t)items.size() > pl->max_work || n_slot > pl->max_slots || (int)merges.size() > pl->max_merge)
     return PKV_ERR_WORKSPACE;
 
-  // Longest processing time first onto the least-loaded CTA.
-  std::vector<int> order(items.size());
-  for (size_t i = 0; i < order.size(); ++i) order[i] = static_cast<int>(i);
-  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return items[a].cost > items[b].cost; });
-  const int ctas = static_cast<int>(std::min<int64_t>(C, (int64_t)items.size()));
-  std::vector<std::vector<int>> per(ctas);
+  // Longest processing time first onto the least-loaded CTA (ties: the lower
+  // item, then the lower CTA).  Costs are small integers, so the items are
+  // ordered by a stable counting sort on descending cost, and each CTA's list
+  // is gathered afterwards by a stable counting pass over the assignment.
+  const int n_items = static_cast<int>(items.size());
+  int64_t max_c = 0;
+  for (const Item& it : items) max_c = std::max(max_c, it.cost);
+  std::vector<int> start(static_cast<size_t>(max_c) + 2, 0);
+  for (const Item& it : items) ++start[static_cast<size_t>(max_c - it.cost) + 1];
+  for (size_t k = 1; k < start.size(); ++k) start[k] += start[k - 1];
+  std::vector<int> order(n_items);
+  for (int i = 0; i < n_items; ++i) order[start[static_cast<size_t>(max_c - items[i].cost)]++] = i;
+  const int ctas = static_cast<int>(std::min<int64_t>(C, (int64_t)n_items));
   std::vector<int64_t> load(ctas, 0);
-  using Slot = std::pair<int64_t, int>;
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int c = 0; c < ctas; ++c) heap.push({0, c});
+  std::vector<int> cta_of(n_items);
+  std::vector<int> per_cta(static_cast<size_t>(ctas) + 1, 0);
+  // Heap keys (load << 20) | cta: one integer comparison orders them as the
+  // (load, cta) pairs (CTA counts stay below 2^20, loads below 2^43).
+  constexpr int kCtaBits = 20;
+  std::priority_queue<uint64_t, std::vector<uint64_t>, std::greater<uint64_t>> heap;
+  for (int c = 0; c < ctas; ++c) heap.push(static_cast<uint64_t>(c));
   for (int i : order) {
-    Slot s = heap.top();
+    const uint64_t key = heap.top();
     heap.pop();
-    per[s.second].push_back(i);
-    s.first += items[i].cost;
-    load[s.second] = s.first;
-    heap.push(s);
+    const int c = static_cast<int>(key & ((1u << kCtaBits) - 1));
+    cta_of[i] = c;
+    ++per_cta[static_cast<size_t>(c) + 1];
+    load[c] += items[i].cost;
+    heap.push((static_cast<uint64_t>(load[c]) << kCtaBits) | static_cast<uint64_t>(c));
+  }
+  for (int c = 0; c < ctas; ++c) per_cta[static_cast<size_t>(c) + 1] += per_cta[c];
+  std::vector<int> by_cta(n_items);  // each CTA's items in the order they were assigned
+  {
+    std::vector<int> fill(per_cta.begin(), per_cta.end() - 1);
+    for (int i : order) by_cta[fill[cta_of[i]]++] = i;
   }
 
   auto* hdr = reinterpret_cast<PlanHeader*>(host + pl->L.header);
@@ -465,7 +485,8 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   pl->max_cost = 0;
   for (int c = 0; c < ctas; ++c) {
     wptr[c] = n;
-    for (int i : per[c]) {
+    for (int k = per_cta[c]; k < per_cta[c + 1]; ++k) {
+      const int i = by_cta[k];
       work[n] = items[i].t;
       int32_t* r = &pl->work_rows[(size_t)n * 8];
       const PrefillTile& t = items[i].t;
