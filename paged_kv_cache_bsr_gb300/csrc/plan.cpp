@@ -334,42 +334,50 @@ int64_t key_chunk(int64_t total, int C) { return std::max<int64_t>(ceil_div(tota
 
 // The busiest CTA's load (key blocks, plus one per item for its setup and
 // epilogue) when compute_prefill chunks the tiles for C CTAs and assigns them
-// longest first.  Item costs are small integers and the least load of a
-// longest-first schedule never decreases, so the schedule runs on counts: the
-// items per cost, and the CTAs per load (`by_cost`, `by_load` are scratch).
+// longest first.  `nb_tiles[k]` counts the tiles of k key blocks: an item's cost
+// depends on nothing else.  The costs are small integers and the least load of a
+// longest-first schedule never decreases, so the schedule runs on counts (`by_cost`
+// items per cost, `by_load` CTAs per load; both scratch), and a run of items of
+// equal cost moves the least-loaded CTAs together, exactly as one at a time would.
 // Ties change no load, so the result equals compute_prefill's assignment.
-int64_t prefill_makespan(const std::vector<QueryTile>& tiles, int64_t total, int C, std::vector<int64_t>& by_cost,
+int64_t prefill_makespan(const std::vector<int64_t>& nb_tiles, int64_t total, int C, std::vector<int64_t>& by_cost,
                          std::vector<int64_t>& by_load) {
-  if (tiles.empty() || C <= 0) return 0;
+  if (C <= 0) return 0;
   const int64_t chunk = key_chunk(total, C);
   by_cost.assign(chunk + 2, 0);
   int64_t items = 0;
-  auto add = [&](int64_t c) {
+  auto add = [&](int64_t c, int64_t m) {
     if (c >= static_cast<int64_t>(by_cost.size())) by_cost.resize(c + 1, 0);
-    ++by_cost[c];
-    ++items;
+    by_cost[c] += m;
+    items += m;
   };
-  for (const QueryTile& t : tiles) {
-    const int64_t nb = ceil_div(t.kv_end, pkv::kPrefillKeys);
+  for (int64_t nb = 0; nb < static_cast<int64_t>(nb_tiles.size()); ++nb) {
+    const int64_t m = nb_tiles[nb];
+    if (m == 0) continue;
     if (nb <= chunk) {
-      add(std::max<int64_t>(nb, 1) + 1);
+      add(std::max<int64_t>(nb, 1) + 1, m);
     } else {
       const int64_t parts = ceil_div(nb, chunk);
-      for (int64_t i = 0; i < parts; ++i) add((i + 1) * nb / parts - i * nb / parts + 1);
+      for (int64_t i = 0; i < parts; ++i) add((i + 1) * nb / parts - i * nb / parts + 1, m);
     }
   }
+  if (items == 0) return 0;
   const int64_t ctas = std::min<int64_t>(C, items);
   by_load.assign(1, ctas);
   int64_t least = 0, worst = 0;
-  for (int64_t c = static_cast<int64_t>(by_cost.size()) - 1; c >= 1; --c)
-    for (int64_t k = 0; k < by_cost[c]; ++k) {
+  for (int64_t c = static_cast<int64_t>(by_cost.size()) - 1; c >= 1; --c) {
+    int64_t k = by_cost[c];
+    while (k > 0) {
       while (by_load[least] == 0) ++least;
-      --by_load[least];
+      const int64_t take = std::min(k, by_load[least]);
+      by_load[least] -= take;
       const int64_t l = least + c;
       if (l >= static_cast<int64_t>(by_load.size())) by_load.resize(l + 1, 0);
-      ++by_load[l];
+      by_load[l] += take;
       worst = std::max(worst, l);
+      k -= take;
     }
+  }
   return worst;
 }
 
@@ -553,9 +561,15 @@ pkv_status compute_mixed(pkv_plan* pl, int batch, const int32_t* qo_indptr, cons
     std::vector<QueryTile> tiles;
     std::vector<int64_t> by_cost, by_load;
     const int64_t total = query_tiles(pl, batch, qo_indptr, kv_indptr, kv_last, true, tiles);
+    std::vector<int64_t> nb_tiles;  // tiles per count of key blocks
+    for (const QueryTile& t : tiles) {
+      const int64_t nb = ceil_div(t.kv_end, pkv::kPrefillKeys);
+      if (nb >= static_cast<int64_t>(nb_tiles.size())) nb_tiles.resize(nb + 1, 0);
+      ++nb_tiles[nb];
+    }
     const int64_t min_run = std::max<int64_t>(1, 4 / ceil_div(P, pkv::kDecodeTileRows));
     const double page_us = kDecodePage16Us * P / 16.0;
-    auto t_pre = [&](int c) { return kPrefillFixedUs + kPrefillBlockUs * prefill_makespan(tiles, total, c, by_cost, by_load); };
+    auto t_pre = [&](int c) { return kPrefillFixedUs + kPrefillBlockUs * prefill_makespan(nb_tiles, total, c, by_cost, by_load); };
     auto t_dec = [&](int n) {
       const int64_t run = std::max<int64_t>(ceil_div(dec_pages, (int64_t)n * pkv::kDecodeWarps), min_run);
       return kDecodeFixedUs + page_us * run;
