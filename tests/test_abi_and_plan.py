@@ -252,6 +252,65 @@ def check_prefill_plan(h, b, num_sms=152, rows_per_tile=256):
     return info, work
 
 
+def longest_first_prefill(b, C, rows_per_tile=256, keys=128):
+    """The prefill plan's schedule restated plainly: query tiles per (request, kv head,
+    rows_per_tile / G positions), their key ranges cut into near-equal chunks when longer
+    than total / C blocks, item cost = blocks + 1, items longest first (ties: lower item)
+    onto the least-loaded CTA (ties: lower CTA).  Returns the work rows in the plan's
+    order (CTA by CTA, each CTA's items in the order assigned)."""
+    import heapq
+    g = b.num_qo_heads // b.num_kv_heads
+    mp_ = rows_per_tile // g
+    tiles, total = [], 0
+    for bb in range(b.batch):
+        qo, kv = b.qo_lens[bb], b.kv_lens[bb]
+        for kvh in range(b.num_kv_heads):
+            for pos0 in range(0, qo, mp_):
+                npos = min(mp_, qo - pos0)
+                end = max(0, min(kv, pos0 + npos + kv - qo)) if b.causal else kv
+                tiles.append((bb, kvh, pos0, npos, end))
+                total += max(1, -(-end // keys))
+    chunk = max(-(-total // max(C, 1)), 2)
+    items, slot = [], 0
+    for bb, kvh, pos0, npos, end in tiles:
+        nb = -(-end // keys)
+        if nb <= chunk:
+            items.append(((bb, kvh, pos0, npos, 0, end, -1), max(nb, 1) + 1))
+        else:
+            parts = -(-nb // chunk)
+            for i in range(parts):
+                lo, hi = i * nb // parts, (i + 1) * nb // parts
+                items.append(((bb, kvh, pos0, npos, lo * keys, min(hi * keys, end), slot), hi - lo + 1))
+                slot += 1
+    order = sorted(range(len(items)), key=lambda i: -items[i][1])  # stable: ties keep item order
+    ctas = min(C, len(items))
+    heap = [(0, c) for c in range(ctas)]
+    per = [[] for _ in range(ctas)]
+    for i in order:
+        load, c = heapq.heappop(heap)
+        per[c].append(i)
+        heapq.heappush(heap, (load + items[i][1], c))
+    return [[c, *items[i][0]] for c in range(ctas) for i in per[c]]
+
+
+@pytest.mark.parametrize("seed,batch,C,causal,page", [(1003, 16, 152, True, 16), (7, 5, 8, True, 16),
+                                                      (9, 3, 152, False, 16), (11, 6, 20, True, 1),
+                                                      (13, 1, 152, False, 16)])
+def test_prefill_plan_is_the_longest_first_schedule(lib, seed, batch, C, causal, page):
+    """The plan's work rows equal the plainly restated schedule, item by item and CTA by
+    CTA (a faster implementation of the plan must not change what the GPU runs)."""
+    b = W.ragged_prefill(seed=seed, batch=batch, page_size=page)
+    if not causal:
+        b = W.PagedBatch(**{**b.__dict__, "causal": False})
+    if batch == 1:  # one long request: its key range is cut into chunks over the CTAs
+        b = W.make_paged_batch(qo_lens=[300], kv_lens=[40000], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                               page_size=16, dtype=torch.bfloat16, seed=seed)
+    h, ws = host_plan(b, api.PLAN_PREFILL, num_sms=C)
+    compute(h, ws, b)
+    work = api.plan_get_work(h).tolist()
+    assert work == longest_first_prefill(b, C)
+
+
 def test_prefill_plan_ragged_causal(lib):
     b = W.ragged_prefill(seed=1003)
     h, ws = host_plan(b, api.PLAN_PREFILL)
