@@ -389,11 +389,10 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   const int BN = pkv::kPrefillKeys;
   if (C <= 0) C = pl->workers;
 
-  struct Item {
-    PrefillTile t;
-    int64_t cost;
-  };
-  std::vector<Item> items;
+  // Work items: their tiles and costs in separate arrays (a PrefillTile is 64-byte
+  // aligned, so a tile and its cost in one struct would take 128 bytes).
+  std::vector<PrefillTile> item_tile;
+  std::vector<int64_t> item_cost;
   std::vector<PrefillMerge> merges;
   // Request b's custom-mask block starts at bit sum over b' < b of qo_len * kv_len.
   std::vector<int64_t> mask_off(batch + 1, 0);
@@ -404,8 +403,10 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   std::vector<QueryTile> tiles;
   const int64_t total = query_tiles(pl, batch, qo_indptr, kv_indptr, kv_last, skip_single, tiles);
   const int64_t chunk = key_chunk(total, C);
-  items.reserve(tiles.size() + static_cast<size_t>(std::min<int64_t>(total / std::max<int64_t>(chunk, 1) + 1,
-                                                                        pl->max_work)));
+  const size_t expect = tiles.size() + static_cast<size_t>(std::min<int64_t>(total / std::max<int64_t>(chunk, 1) + 1,
+                                                                                pl->max_work));
+  item_tile.reserve(expect);
+  item_cost.reserve(expect);
   int n_slot = 0;
   for (const QueryTile& t : tiles) {
     PrefillTile pt{};
@@ -424,7 +425,8 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
       pt.kv_begin = 0;
       pt.kv_end = t.kv_end;
       pt.slot = -1;
-      items.push_back({pt, std::max<int64_t>(nb, 1) + 1});
+      item_tile.push_back(pt);
+      item_cost.push_back(std::max<int64_t>(nb, 1) + 1);
     } else {
       const int64_t parts = ceil_div(nb, chunk);
       PrefillMerge m{};
@@ -440,25 +442,26 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
         pt.kv_begin = static_cast<int32_t>(blo * BN);
         pt.kv_end = static_cast<int32_t>(std::min<int64_t>(bhi * BN, t.kv_end));
         pt.slot = n_slot++;
-        items.push_back({pt, (bhi - blo) + 1});
+        item_tile.push_back(pt);
+        item_cost.push_back((bhi - blo) + 1);
       }
     }
   }
-  if ((int64_t)items.size() > pl->max_work || n_slot > pl->max_slots || (int)merges.size() > pl->max_merge)
+  if ((int64_t)item_tile.size() > pl->max_work || n_slot > pl->max_slots || (int)merges.size() > pl->max_merge)
     return PKV_ERR_WORKSPACE;
 
   // Longest processing time first onto the least-loaded CTA (ties: the lower
   // item, then the lower CTA).  Costs are small integers, so the items are
   // ordered by a stable counting sort on descending cost, and each CTA's list
   // is gathered afterwards by a stable counting pass over the assignment.
-  const int n_items = static_cast<int>(items.size());
+  const int n_items = static_cast<int>(item_tile.size());
   int64_t max_c = 0;
-  for (const Item& it : items) max_c = std::max(max_c, it.cost);
+  for (int64_t c : item_cost) max_c = std::max(max_c, c);
   std::vector<int> start(static_cast<size_t>(max_c) + 2, 0);
-  for (const Item& it : items) ++start[static_cast<size_t>(max_c - it.cost) + 1];
+  for (int64_t c : item_cost) ++start[static_cast<size_t>(max_c - c) + 1];
   for (size_t k = 1; k < start.size(); ++k) start[k] += start[k - 1];
   std::vector<int> order(n_items);
-  for (int i = 0; i < n_items; ++i) order[start[static_cast<size_t>(max_c - items[i].cost)]++] = i;
+  for (int i = 0; i < n_items; ++i) order[start[static_cast<size_t>(max_c - item_cost[i])]++] = i;
   const int ctas = static_cast<int>(std::min<int64_t>(C, (int64_t)n_items));
   std::vector<int64_t> load(ctas, 0);
   std::vector<int> cta_of(n_items);
@@ -474,7 +477,7 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
     const int c = static_cast<int>(key & ((1u << kCtaBits) - 1));
     cta_of[i] = c;
     ++per_cta[static_cast<size_t>(c) + 1];
-    load[c] += items[i].cost;
+    load[c] += item_cost[i];
     heap.push((static_cast<uint64_t>(load[c]) << kCtaBits) | static_cast<uint64_t>(c));
   }
   for (int c = 0; c < ctas; ++c) per_cta[static_cast<size_t>(c) + 1] += per_cta[c];
@@ -489,15 +492,15 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   auto* mrec = reinterpret_cast<PrefillMerge*>(host + pl->L.merge);
   auto* work = reinterpret_cast<PrefillTile*>(host + pl->L.segs);
   int n = 0;
-  pl->work_rows.assign(items.size() * 8, 0);
+  pl->work_rows.assign(static_cast<size_t>(n_items) * 8, 0);
   pl->max_cost = 0;
   for (int c = 0; c < ctas; ++c) {
     wptr[c] = n;
     for (int k = per_cta[c]; k < per_cta[c + 1]; ++k) {
       const int i = by_cta[k];
-      work[n] = items[i].t;
+      const PrefillTile& t = item_tile[i];
+      work[n] = t;
       int32_t* r = &pl->work_rows[(size_t)n * 8];
-      const PrefillTile& t = items[i].t;
       r[0] = c; r[1] = t.b; r[2] = t.kvh; r[3] = t.q_pos0; r[4] = t.n_pos;
       r[5] = t.kv_begin; r[6] = t.kv_end; r[7] = t.slot;
       ++n;
