@@ -311,6 +311,49 @@ def test_prefill_plan_is_the_longest_first_schedule(lib, seed, batch, C, causal,
     assert work == longest_first_prefill(b, C)
 
 
+def equal_runs_decode(b, W, tile_rows=16):
+    """The decode plan restated plainly: the (request, kv head) page lists concatenated in
+    order and cut into runs of max(ceil(total / W), min_run) pages, one run per worker; a
+    list that crosses a run boundary is split there, each piece a partial-state slot.
+    Returns the work rows [worker, request, kv head, first page, pages, last rows, slot, 0]."""
+    P = b.page_size
+    pages_per_tile = -(-P // tile_rows)
+    min_run = max(1, 4 // pages_per_tile)
+    lens = [int(b.kv_indptr[r + 1] - b.kv_indptr[r]) for r in range(b.batch)]
+    total = sum(lens) * b.num_kv_heads
+    run = max(-(-total // W), min_run) if total else 1
+    active = -(-total // run) if total else (1 if b.batch else 0)
+    rows, x, slot = [], 0, 0
+    for r in range(b.batch):
+        n = lens[r]
+        last = int(b.kv_last_page_len[r])
+        for h in range(b.num_kv_heads):
+            if n == 0:
+                rows.append([min(x // run, active - 1), r, h, 0, 0, 0, -1, 0])
+                continue
+            w0, w1 = x // run, (x + n - 1) // run
+            if w0 == w1:
+                rows.append([w0, r, h, 0, n, last, -1, 0])
+            else:
+                for w in range(w0, w1 + 1):
+                    lo, hi = max(x, w * run) - x, min(x + n, (w + 1) * run) - x
+                    rows.append([w, r, h, lo, hi - lo, last if hi == n else P, slot, 0])
+                    slot += 1
+            x += n
+    return rows
+
+
+@pytest.mark.parametrize("seed,batch,workers,page", [(1001, 64, 1216, 16), (3, 9, 40, 16), (5, 7, 1216, 1),
+                                                       (8, 3, 8, 64)])
+def test_decode_plan_is_the_equal_run_split(lib, seed, batch, workers, page):
+    """The decode plan's work rows equal the plainly restated equal-run split, worker by
+    worker (8 workers per SM)."""
+    b = W.llama3_decode(seed=seed, batch=batch, page_size=page)
+    h, ws = host_plan(b, api.PLAN_DECODE, num_sms=workers // 8)
+    compute(h, ws, b)
+    assert api.plan_get_work(h).tolist() == equal_runs_decode(b, workers)
+
+
 def test_prefill_plan_ragged_causal(lib):
     b = W.ragged_prefill(seed=1003)
     h, ws = host_plan(b, api.PLAN_PREFILL)
