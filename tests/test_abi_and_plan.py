@@ -47,6 +47,26 @@ def test_status_strings(lib):
     assert api.status_string(-99) == "unknown status"
 
 
+def test_public_header_is_plain_c(tmp_path):
+    """include/pkv_bsr.h compiles as strict C99 and as C++ (a C ABI, no C++ types)."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("no gcc")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "t.c"
+    src.write_text('#include "pkv_bsr.h"\nint main(void) { pkv_params p; (void)p; '
+                   'return (int)sizeof(pkv_plan_info) > 0 ? 0 : 1; }\n')
+    inc = ["-I", os.path.join(root, "include")]
+    cuda_inc = "/usr/local/cuda/include"
+    if os.path.isdir(cuda_inc):
+        inc += ["-I", cuda_inc]
+    for cmd in (["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror"],
+                ["g++", "-std=c++17", "-Wall", "-Werror", "-x", "c++"]):
+        r = subprocess.run(cmd + inc + ["-c", str(src), "-o", os.devnull], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 # --------------------------------------------------------------------------- helpers
 def host_plan(b, kind, num_sms=152, **lim):
     params = api.make_params(b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.dtype, b.sm_scale,
