@@ -35,7 +35,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_ranks_combine_to_whole_job_figures():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
     r0, r1 = out[0], out[1]
     assert r0[0] == r1[0] == pytest.approx(0.2)               # max over ranks

@@ -73,7 +73,7 @@ def _split_rank(rank, world, port, out):
 
 def test_two_ranks_split_one_long_request_and_merge():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_split_rank, args=(world, _free_port(), out), nprocs=world, join=True)
     for rank in range(world):
         do, dl, shape = out[rank]
@@ -98,7 +98,7 @@ def _partition_rank(rank, world, port, out):
 
 def test_two_ranks_partition_requests_without_exchange():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_partition_rank, args=(world, _free_port(), out), nprocs=world, join=True)
     assert sorted(out[0][0] + out[1][0]) == list(range(6))
     for rank in range(world):
