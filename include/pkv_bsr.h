@@ -151,6 +151,8 @@ pkv_status pkv_plan_run(pkv_plan* plan, int batch, const int32_t* qo_indptr_h,
  * The host half of pkv_plan_run: validate the host index arrays and write
  * the plan tables into `host_ws` (ordinary or pinned host memory), with no
  * CUDA call.  pkv_plan_run is this step followed by one asynchronous copy.
+ * Prefill and mixed plans keep their working arrays in the plan object and
+ * reuse them from call to call (they grow with the largest batch planned).
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_BAD_INDEX, PKV_ERR_WORKSPACE.
  */
 pkv_status pkv_plan_compute(pkv_plan* plan, int batch, const int32_t* qo_indptr_h,

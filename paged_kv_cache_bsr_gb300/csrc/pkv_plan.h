@@ -9,6 +9,29 @@
 #include "pkv_bsr.h"
 #include "pkv_internal.h"
 
+namespace pkv {
+
+// A prefill work item before it has its place: the query tile of request b, kv
+// head kvh and positions from pos0, against keys [kv_begin, kv_end), with its
+// partial slot or -1.
+struct PlanItem {
+  int32_t b, kvh, pos0, kv_begin, kv_end, slot;
+};
+
+// Working arrays of the prefill and mixed plan steps.  They live in the plan and
+// keep their capacity from call to call, so re-planning a batch no larger than
+// one planned before allocates nothing.
+struct PlanScratch {
+  std::vector<PlanItem> items;
+  std::vector<PrefillMerge> merges;
+  std::vector<int32_t> item_cost;
+  std::vector<int64_t> mask_off, load, nb_tiles, by_cost, by_load;
+  std::vector<int> start, order, cta_of, per_cta, by_cta, fill;
+  std::vector<uint64_t> buckets;
+};
+
+}  // namespace pkv
+
 struct pkv_plan {
   int kind = 0;
   pkv_params p{};
@@ -40,6 +63,7 @@ struct pkv_plan {
   int64_t total_cost = 0;
   size_t used_bytes = 0;
   std::vector<int32_t> work_rows;  // 8 int32 per work entry, for pkv_plan_get_work
+  pkv::PlanScratch scratch;
   // The copy of the tables out of the pinned buffer.
   cudaEvent_t copy_done = nullptr;
   bool copy_pending = false;

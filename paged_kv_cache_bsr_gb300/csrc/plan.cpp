@@ -23,9 +23,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
-#include <functional>
 #include <new>
-#include <queue>
 #include <utility>
 #include <vector>
 
@@ -37,6 +35,7 @@
 using pkv::DecodeSeg;
 using pkv::MergeItem;
 using pkv::PlanHeader;
+using pkv::PlanScratch;
 using pkv::PrefillMerge;
 using pkv::PrefillTile;
 
@@ -298,32 +297,38 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
   return PKV_OK;
 }
 
-// A query tile of the prefill plan: kPrefillRows packed rows of one request and
-// kv head against keys [0, kv_end) (kv_end already clipped by the causal limit).
-struct QueryTile {
-  int b, kvh, pos0, npos, qo, kv, kv_end;
-};
+// Key end of the query tile of positions [pos0, pos0 + npos) of a request with
+// qo rows and kv keys: every key, or under the causal mask the limit of its last
+// row, clipped to [0, kv].
+int tile_kv_end(bool causal, int qo, int kv, int pos0, int npos) {
+  return causal ? std::max(0, std::min(kv, pos0 + npos + kv - qo)) : kv;
+}
 
-// The prefill plan's query tiles (independent of the CTA count); returns their
-// key blocks in total, an empty tile counting one.
-int64_t query_tiles(const pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
-                    const int32_t* kv_last, bool skip_single, std::vector<QueryTile>& tiles) {
+// The prefill plan's query tiles are one per (request, kv head, block of
+// kPrefillRows / group query positions), each against keys [0, kv_end).  Returns
+// their key blocks in total, an empty tile counting one (independent of the CTA
+// count); with nb_tiles, also the number of tiles of each count of key blocks.
+// The kv heads of a request repeat its tiles, so they count once per block.
+int64_t query_tile_blocks(const pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                          const int32_t* kv_last, bool skip_single, std::vector<int64_t>* nb_tiles) {
   const int P = pl->p.page_size;
   const int mp = pkv::kPrefillRows / pl->group;
-  tiles.clear();
+  const int64_t hkv = pl->p.num_kv_heads;
+  if (nb_tiles) nb_tiles->clear();
   int64_t total = 0;
   for (int b = 0; b < batch; ++b) {
     const int qo = qo_indptr[b + 1] - qo_indptr[b];
     if (skip_single && qo == 1) continue;
     const int kv = static_cast<int>(kv_len_of(kv_indptr, kv_last, b, P));
-    for (int h = 0; h < pl->p.num_kv_heads; ++h)
-      for (int pos0 = 0; pos0 < qo; pos0 += mp) {
-        const int npos = std::min(mp, qo - pos0);
-        int kv_end = kv;
-        if (pl->p.causal) kv_end = std::max(0, std::min(kv, pos0 + npos + kv - qo));
-        tiles.push_back({b, static_cast<int>(h), pos0, npos, qo, kv, kv_end});
-        total += std::max<int64_t>(1, ceil_div(kv_end, pkv::kPrefillKeys));
+    for (int pos0 = 0; pos0 < qo; pos0 += mp) {
+      const int64_t nb = ceil_div(tile_kv_end(pl->p.causal, qo, kv, pos0, std::min(mp, qo - pos0)),
+                                  pkv::kPrefillKeys);
+      total += hkv * std::max<int64_t>(1, nb);
+      if (nb_tiles) {
+        if (nb >= static_cast<int64_t>(nb_tiles->size())) nb_tiles->resize(nb + 1, 0);
+        (*nb_tiles)[nb] += hkv;
       }
+    }
   }
   return total;
 }
@@ -389,101 +394,122 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   const int BN = pkv::kPrefillKeys;
   if (C <= 0) C = pl->workers;
 
-  // Work items: their tiles and costs in separate arrays (a PrefillTile is 64-byte
-  // aligned, so a tile and its cost in one struct would take 128 bytes).
-  std::vector<PrefillTile> item_tile;
-  std::vector<int64_t> item_cost;
-  std::vector<PrefillMerge> merges;
+  PlanScratch& sc = pl->scratch;
+  const int mp = pkv::kPrefillRows / pl->group;
+  // Work items: one key chunk of one query tile each; the full table entry is
+  // written only once the item has its place.
+  std::vector<pkv::PlanItem>& items = sc.items;
+  std::vector<int32_t>& item_cost = sc.item_cost;
+  std::vector<PrefillMerge>& merges = sc.merges;
+  items.clear();
+  item_cost.clear();
+  merges.clear();
   // Request b's custom-mask block starts at bit sum over b' < b of qo_len * kv_len.
-  std::vector<int64_t> mask_off(batch + 1, 0);
+  std::vector<int64_t>& mask_off = sc.mask_off;
+  mask_off.assign(static_cast<size_t>(batch) + 1, 0);
   for (int b = 0; b < batch; ++b)
     mask_off[b + 1] = mask_off[b] + static_cast<int64_t>(qo_indptr[b + 1] - qo_indptr[b]) *
                                         kv_len_of(kv_indptr, kv_last, b, P);
   pl->mask_bits = mask_off[batch];
-  std::vector<QueryTile> tiles;
-  const int64_t total = query_tiles(pl, batch, qo_indptr, kv_indptr, kv_last, skip_single, tiles);
+  const int64_t total = query_tile_blocks(pl, batch, qo_indptr, kv_indptr, kv_last, skip_single, nullptr);
   const int64_t chunk = key_chunk(total, C);
-  const size_t expect = tiles.size() + static_cast<size_t>(std::min<int64_t>(total / std::max<int64_t>(chunk, 1) + 1,
-                                                                                pl->max_work));
-  item_tile.reserve(expect);
-  item_cost.reserve(expect);
+  // Each tile gives at most as many items as it counts blocks (chunk >= 2).
+  items.reserve(static_cast<size_t>(std::min<int64_t>(total, pl->max_work) + 1));
+  item_cost.reserve(items.capacity());
   int n_slot = 0;
-  for (const QueryTile& t : tiles) {
-    PrefillTile pt{};
-    pt.b = t.b;
-    pt.kvh = t.kvh;
-    pt.q_row0 = qo_indptr[t.b] + t.pos0;
-    pt.q_pos0 = t.pos0;
-    pt.n_pos = t.npos;
-    pt.qo_len = t.qo;
-    pt.kv_len = t.kv;
-    pt.idx_base = kv_indptr[t.b];
-    pt.last_rows = kv_last[t.b];
-    pt.mask_off = mask_off[t.b];
-    const int64_t nb = ceil_div(t.kv_end, BN);
-    if (nb <= chunk) {
-      pt.kv_begin = 0;
-      pt.kv_end = t.kv_end;
-      pt.slot = -1;
-      item_tile.push_back(pt);
-      item_cost.push_back(std::max<int64_t>(nb, 1) + 1);
-    } else {
-      const int64_t parts = ceil_div(nb, chunk);
-      PrefillMerge m{};
-      m.b = t.b;
-      m.kvh = t.kvh;
-      m.q_row0 = pt.q_row0;
-      m.n_pos = t.npos;
-      m.slot_begin = n_slot;
-      m.n_slots = static_cast<int32_t>(parts);
-      merges.push_back(m);
-      for (int64_t i = 0; i < parts; ++i) {
-        const int64_t blo = i * nb / parts, bhi = (i + 1) * nb / parts;
-        pt.kv_begin = static_cast<int32_t>(blo * BN);
-        pt.kv_end = static_cast<int32_t>(std::min<int64_t>(bhi * BN, t.kv_end));
-        pt.slot = n_slot++;
-        item_tile.push_back(pt);
-        item_cost.push_back((bhi - blo) + 1);
+  for (int b = 0; b < batch; ++b) {
+    const int qo = qo_indptr[b + 1] - qo_indptr[b];
+    if (skip_single && qo == 1) continue;
+    const int kv = static_cast<int>(kv_len_of(kv_indptr, kv_last, b, P));
+    for (int h = 0; h < pl->p.num_kv_heads; ++h)
+      for (int pos0 = 0; pos0 < qo; pos0 += mp) {
+        const int npos = std::min(mp, qo - pos0);
+        const int kv_end = tile_kv_end(pl->p.causal, qo, kv, pos0, npos);
+        const int64_t nb = ceil_div(kv_end, BN);
+        if (nb <= chunk) {
+          items.push_back({b, h, pos0, 0, kv_end, -1});
+          item_cost.push_back(static_cast<int32_t>(std::max<int64_t>(nb, 1) + 1));
+          continue;
+        }
+        const int64_t parts = ceil_div(nb, chunk);
+        PrefillMerge m{};
+        m.b = b;
+        m.kvh = h;
+        m.q_row0 = qo_indptr[b] + pos0;
+        m.n_pos = npos;
+        m.slot_begin = n_slot;
+        m.n_slots = static_cast<int32_t>(parts);
+        merges.push_back(m);
+        for (int64_t i = 0; i < parts; ++i) {
+          const int64_t blo = i * nb / parts, bhi = (i + 1) * nb / parts;
+          items.push_back({b, h, pos0, static_cast<int32_t>(blo * BN),
+                           static_cast<int32_t>(std::min<int64_t>(bhi * BN, kv_end)), n_slot++});
+          item_cost.push_back(static_cast<int32_t>(bhi - blo + 1));
+        }
       }
-    }
   }
-  if ((int64_t)item_tile.size() > pl->max_work || n_slot > pl->max_slots || (int)merges.size() > pl->max_merge)
+  if ((int64_t)items.size() > pl->max_work || n_slot > pl->max_slots || (int)merges.size() > pl->max_merge)
     return PKV_ERR_WORKSPACE;
 
   // Longest processing time first onto the least-loaded CTA (ties: the lower
   // item, then the lower CTA).  Costs are small integers, so the items are
   // ordered by a stable counting sort on descending cost, and each CTA's list
   // is gathered afterwards by a stable counting pass over the assignment.
-  const int n_items = static_cast<int>(item_tile.size());
+  const int n_items = static_cast<int>(items.size());
   int64_t max_c = 0;
-  for (int64_t c : item_cost) max_c = std::max(max_c, c);
-  std::vector<int> start(static_cast<size_t>(max_c) + 2, 0);
-  for (int64_t c : item_cost) ++start[static_cast<size_t>(max_c - c) + 1];
+  for (int32_t c : item_cost) max_c = std::max<int64_t>(max_c, c);
+  std::vector<int>& start = sc.start;
+  start.assign(static_cast<size_t>(max_c) + 2, 0);
+  for (int32_t c : item_cost) ++start[static_cast<size_t>(max_c - c) + 1];
   for (size_t k = 1; k < start.size(); ++k) start[k] += start[k - 1];
-  std::vector<int> order(n_items);
+  std::vector<int>& order = sc.order;
+  order.resize(n_items);
   for (int i = 0; i < n_items; ++i) order[start[static_cast<size_t>(max_c - item_cost[i])]++] = i;
   const int ctas = static_cast<int>(std::min<int64_t>(C, (int64_t)n_items));
-  std::vector<int64_t> load(ctas, 0);
-  std::vector<int> cta_of(n_items);
-  std::vector<int> per_cta(static_cast<size_t>(ctas) + 1, 0);
-  // Heap keys (load << 20) | cta: one integer comparison orders them as the
-  // (load, cta) pairs (CTA counts stay below 2^20, loads below 2^43).
-  constexpr int kCtaBits = 20;
-  std::priority_queue<uint64_t, std::vector<uint64_t>, std::greater<uint64_t>> heap;
-  for (int c = 0; c < ctas; ++c) heap.push(static_cast<uint64_t>(c));
+  std::vector<int64_t>& load = sc.load;
+  load.assign(ctas, 0);
+  std::vector<int>& cta_of = sc.cta_of;
+  cta_of.resize(n_items);
+  std::vector<int>& per_cta = sc.per_cta;
+  per_cta.assign(static_cast<size_t>(ctas) + 1, 0);
+  // The least-loaded CTA, ties to the lower index, without a heap: loads only
+  // grow, the least load never falls, and every load lies within max_c of the
+  // least one, so the CTAs sit in a ring of at least max_c + 1 buckets by load
+  // (a power of two, indexed by the load's low bits), each a bitset over the
+  // CTAs.  The lowest bit of the least non-empty bucket is the CTA a (load, cta)
+  // min-heap would pop.
+  const int words = (ctas + 63) / 64;
+  int64_t ring = 1;
+  while (ring < max_c + 1) ring <<= 1;
+  std::vector<uint64_t>& buckets = sc.buckets;
+  buckets.assign(static_cast<size_t>(ring * words), 0);
+  for (int c = 0; c < ctas; ++c) buckets[c >> 6] |= uint64_t{1} << (c & 63);
+  auto bucket = [&](int64_t l) { return &buckets[static_cast<size_t>((l & (ring - 1)) * words)]; };
+  int64_t least = 0;
   for (int i : order) {
-    const uint64_t key = heap.top();
-    heap.pop();
-    const int c = static_cast<int>(key & ((1u << kCtaBits) - 1));
+    uint64_t* bk = bucket(least);
+    int w = 0;
+    while (bk[w] == 0) ++w;
+    const int c = w * 64 + __builtin_ctzll(bk[w]);
+    bk[w] &= bk[w] - 1;
     cta_of[i] = c;
     ++per_cta[static_cast<size_t>(c) + 1];
     load[c] += item_cost[i];
-    heap.push((static_cast<uint64_t>(load[c]) << kCtaBits) | static_cast<uint64_t>(c));
+    bucket(load[c])[c >> 6] |= uint64_t{1} << (c & 63);
+    for (;;) {  // the next non-empty bucket (one exists: every CTA is in one)
+      const uint64_t* b = bucket(least);
+      bool any = false;
+      for (int k = 0; k < words && !any; ++k) any = b[k] != 0;
+      if (any) break;
+      ++least;
+    }
   }
   for (int c = 0; c < ctas; ++c) per_cta[static_cast<size_t>(c) + 1] += per_cta[c];
-  std::vector<int> by_cta(n_items);  // each CTA's items in the order they were assigned
+  std::vector<int>& by_cta = sc.by_cta;  // each CTA's items in the order they were assigned
+  by_cta.resize(n_items);
   {
-    std::vector<int> fill(per_cta.begin(), per_cta.end() - 1);
+    std::vector<int>& fill = sc.fill;
+    fill.assign(per_cta.begin(), per_cta.end() - 1);
     for (int i : order) by_cta[fill[cta_of[i]]++] = i;
   }
 
@@ -497,8 +523,22 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   for (int c = 0; c < ctas; ++c) {
     wptr[c] = n;
     for (int k = per_cta[c]; k < per_cta[c + 1]; ++k) {
-      const int i = by_cta[k];
-      const PrefillTile& t = item_tile[i];
+      const pkv::PlanItem& it = items[by_cta[k]];
+      const int qo = qo_indptr[it.b + 1] - qo_indptr[it.b];
+      PrefillTile t{};
+      t.b = it.b;
+      t.kvh = it.kvh;
+      t.q_row0 = qo_indptr[it.b] + it.pos0;
+      t.q_pos0 = it.pos0;
+      t.n_pos = std::min(mp, qo - it.pos0);
+      t.qo_len = qo;
+      t.kv_len = static_cast<int32_t>(kv_len_of(kv_indptr, kv_last, it.b, P));
+      t.kv_begin = it.kv_begin;
+      t.kv_end = it.kv_end;
+      t.idx_base = kv_indptr[it.b];
+      t.last_rows = kv_last[it.b];
+      t.slot = it.slot;
+      t.mask_off = mask_off[it.b];
       work[n] = t;
       int32_t* r = &pl->work_rows[(size_t)n * 8];
       r[0] = c; r[1] = t.b; r[2] = t.kvh; r[3] = t.q_pos0; r[4] = t.n_pos;
@@ -561,15 +601,11 @@ pkv_status compute_mixed(pkv_plan* pl, int batch, const int32_t* qo_indptr, cons
   if (any_pre && !any_dec) {
     kp = S;
   } else if (any_pre && any_dec) {
-    std::vector<QueryTile> tiles;
-    std::vector<int64_t> by_cost, by_load;
-    const int64_t total = query_tiles(pl, batch, qo_indptr, kv_indptr, kv_last, true, tiles);
-    std::vector<int64_t> nb_tiles;  // tiles per count of key blocks
-    for (const QueryTile& t : tiles) {
-      const int64_t nb = ceil_div(t.kv_end, pkv::kPrefillKeys);
-      if (nb >= static_cast<int64_t>(nb_tiles.size())) nb_tiles.resize(nb + 1, 0);
-      ++nb_tiles[nb];
-    }
+    PlanScratch& sc = pl->scratch;
+    std::vector<int64_t>& by_cost = sc.by_cost;
+    std::vector<int64_t>& by_load = sc.by_load;
+    std::vector<int64_t>& nb_tiles = sc.nb_tiles;  // tiles per count of key blocks
+    const int64_t total = query_tile_blocks(pl, batch, qo_indptr, kv_indptr, kv_last, true, &nb_tiles);
     const int64_t min_run = std::max<int64_t>(1, 4 / ceil_div(P, pkv::kDecodeTileRows));
     const double page_us = kDecodePage16Us * P / 16.0;
     auto t_pre = [&](int c) { return kPrefillFixedUs + kPrefillBlockUs * prefill_makespan(nb_tiles, total, c, by_cost, by_load); };

@@ -505,3 +505,30 @@ def test_mixed_plan_needs_qo_indptr(lib):
     h, ws = host_plan(b, api.PLAN_MIXED)
     with pytest.raises(api.PkvError):
         compute(h, ws, b, qo=None)
+
+
+@pytest.mark.parametrize("kind", [api.PLAN_PREFILL, api.PLAN_MIXED])
+def test_replanning_after_other_batches_gives_a_fresh_plans_tables(lib, kind):
+    """A plan keeps its working arrays from call to call: re-planning one plan object
+    small -> big -> small gives each time the work and figures of a fresh plan of
+    that batch (nothing left over from the previous call)."""
+    big = W.mixed_batch(seed=1007, n_prefill=32)
+    small = W.mixed_batch(seed=3, n_decode=5, n_prefill=3)
+    lim = dict(max_batch=big.batch, max_total_q=big.total_q, max_kv_pages=int(big.kv_indptr[-1]))
+
+    def fresh(b):
+        h, ws = host_plan(b, kind, **lim)
+        compute(h, ws, b)
+        return api.plan_get_work(h), _info_tuple(api.plan_get_info(h))
+
+    want = {id(b): fresh(b) for b in (small, big)}
+    h, ws = host_plan(big, kind, **lim)
+    for b in (small, big, small, big):
+        compute(h, ws, b)
+        work, info = api.plan_get_work(h), _info_tuple(api.plan_get_info(h))
+        assert torch.equal(work, want[id(b)][0])
+        assert info == want[id(b)][1]
+
+
+def _info_tuple(info):
+    return tuple(getattr(info, f) for f, _ in info._fields_)
