@@ -164,9 +164,14 @@ pkv_status validate(const pkv_plan* pl, int batch, const int32_t* qo_indptr, con
   const int64_t nnz = kv_indptr[batch];
   if (nnz > pl->lim.max_kv_pages) return PKV_ERR_WORKSPACE;
   if (nnz > 0 && num_pages == 0) return PKV_ERR_BAD_INDEX;
-  if (kv_indices)
-    for (int64_t j = 0; j < nnz; ++j)
-      if (kv_indices[j] < 0 || kv_indices[j] >= num_pages) return PKV_ERR_BAD_INDEX;
+  if (kv_indices) {
+    // One pass with no early exit, so that it vectorises: taken as unsigned, a
+    // negative id wraps above every num_pages (at most INT32_MAX).
+    const uint32_t np = static_cast<uint32_t>(num_pages);
+    uint32_t bad = 0;
+    for (int64_t j = 0; j < nnz; ++j) bad |= static_cast<uint32_t>(kv_indices[j]) >= np;
+    if (bad) return PKV_ERR_BAD_INDEX;
+  }
   if (qo_indptr) {
     if (qo_indptr[0] != 0) return PKV_ERR_BAD_INDEX;
     for (int b = 0; b < batch; ++b)
