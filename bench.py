@@ -226,8 +226,9 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- own arm
-def cpu_baseline(b, seconds=10.0):
-    """The oracle as it stands on the host cores over the whole batch, repeated ~10 s."""
+def cpu_baseline(b, seconds=10.0, single_core_seconds=3.0):
+    """The oracle as it stands on the host cores over the whole batch, repeated ~10 s;
+    then on one core over requests taken in turn, ~3 s."""
     import oracle
     oracle.build()
     reps, t0 = 0, time.perf_counter()
@@ -237,8 +238,20 @@ def cpu_baseline(b, seconds=10.0):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
+    per_req = [n * 2 * b.num_kv_heads * b.head_dim * 2 for n in b.kv_lens]
+    done, nbytes, t1 = 0, 0, time.perf_counter()
+    while True:
+        r = done % b.batch
+        oracle.attention_of(b, rows=[r], threads=1)
+        nbytes += per_req[r]
+        done += 1
+        if time.perf_counter() - t1 >= single_core_seconds:
+            break
+    dt1 = time.perf_counter() - t1
     return {"value": round(b.kv_bytes() * reps / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": f"the full {WORKLOAD} batch (64 requests), {reps} passes, {dt:.1f} s"}
+            "kind": "oracle", "sample": f"the full {WORKLOAD} batch (64 requests), {reps} passes, {dt:.1f} s",
+            "single_core": {"value": round(nbytes / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                            "sample": f"{done} requests of the same batch in turn, {dt1:.1f} s"}}
 
 
 def time_steps(fn, steps, warmup, stream, kernel_events=None, sync_each=False):
