@@ -11,9 +11,9 @@ HBM; the KV read per step (~0.63 GB) is larger than L2, so no flush is needed
 between steps.
 
 The JSON line also carries the prefill (ragged causal, tensor cores), skewed
-long-context decode, cascade, multi-level cascade, append + RoPE, tree
-verification, mixed batch and column-vector prefill measurements under
-"secondary".
+long-context decode (with and without the split), cascade, multi-level cascade,
+append + RoPE, tree verification, mixed batch and column-vector prefill
+measurements under "secondary".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -275,14 +275,15 @@ def time_steps(fn, steps, warmup, stream, kernel_events=None, sync_each=False):
     return total, kern
 
 
-def decode_measure(b, steps, warmup, peaks, profile_name=None):
-    """Step time and main-kernel time of plan + decode + merge on one workload."""
+def decode_measure(b, steps, warmup, peaks, profile_name=None, split_kv=True):
+    """Step time and main-kernel time of plan + decode + merge on one workload
+    (split_kv False: each page list whole on one worker, nothing to merge)."""
     import torch
     from paged_kv_cache_bsr_gb300 import runner, api
     db = runner.DeviceBatch.from_host(b)
     # A step loop re-plans every call: the pipelined plan copies each step's tables
     # while the previous step's kernels run.
-    plan = runner.make_plan(b, api.PLAN_DECODE, pipelined=True)
+    plan = runner.make_plan(b, api.PLAN_DECODE, pipelined=True, split_kv=split_kv)
     o = torch.empty_like(db.q)
     lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device=db.q.device)
     stream = torch.cuda.current_stream()
@@ -699,8 +700,12 @@ def run_only(args):
         res = {"tree": tree_measure(peaks, steps=args.steps, warmup=args.warmup),
                "page_size_1": prefill_measure(peaks, steps=args.steps, warmup=args.warmup, page_size=1)}
     else:
-        r = decode_measure(W.skewed_decode(seed=1002), args.steps, args.warmup, peaks)
-        res = {"value": round(r["value"], 1), "unit": "GB/s", "roofline": r["roofline"]}
+        sk = W.skewed_decode(seed=1002)
+        r = decode_measure(sk, args.steps, args.warmup, peaks)
+        r0 = decode_measure(sk, args.steps, args.warmup, peaks, split_kv=False)
+        res = {"value": round(r["value"], 1), "unit": "GB/s", "roofline": r["roofline"],
+               "split_off": {"value": round(r0["value"], 1), "ms_per_step": round(r0["ms_per_step"], 4),
+                             "split_speedup": round(r0["ms_per_step"] / r["ms_per_step"], 2)}}
     print(json.dumps({"only": args.only, **res}), flush=True)
 
 
@@ -749,6 +754,16 @@ def run_own(args):
             secondary["skewed_decode"] = {"value": round(r3["value"], 1), "unit": "GB/s",
                                           "ms_per_step": round(r3["ms_per_step"], 4),
                                           "roofline": r3["roofline"], "slots": r3["info"].num_slots}
+            # The same batch with the split turned off: each page list whole on one
+            # warp, so the 131072-token request sets the step time.
+            try:
+                r4 = decode_measure(sk, max(20, args.steps // 10), 5, peaks, split_kv=False)
+                secondary["skewed_decode"]["split_off"] = {
+                    "value": round(r4["value"], 1), "unit": "GB/s", "ms_per_step": round(r4["ms_per_step"], 4),
+                    "kernel_ms": round(r4["kernel_ms"], 4),
+                    "split_speedup": round(r4["ms_per_step"] / r3["ms_per_step"], 2)}
+            except Exception as e:  # recorded, so that the lines after it still run
+                secondary["skewed_decode"]["split_off"] = {"error": f"{type(e).__name__}: {e}"[:300]}
             del sk
             ident = W.llama3_decode(seed=1001, identity_pages=True)
             r_id = decode_measure(ident, max(20, args.steps // 10), 5, peaks)

@@ -212,6 +212,19 @@ pkv_status pkv_plan_set_timing_events(pkv_plan* plan, void* start, void* stop);
 pkv_status pkv_plan_set_pipelined(pkv_plan* plan, int on);
 
 /*
+ * Split-KV on or off for a decode plan (default on).  On, the plan step cuts
+ * the (request, kv head) page lists into equal runs over the workers and merges
+ * the partial states ("FlashInfer" guide, section 3 "FlashDecoding"; fdeinterviews
+ * summary, "Load balancing that survives CUDA graphs").  Off, each page list goes
+ * whole to one worker, longest first onto the least-loaded worker (ties to the
+ * earlier list, then the lower worker), with no partial states and no merge:
+ * the baseline the split is measured against, in which one long request rests
+ * on one worker.  Takes effect at the next plan step; the run call is unchanged.
+ * Errors: PKV_ERR_INVALID_ARG (NULL, or not a plan of kind DECODE).
+ */
+pkv_status pkv_plan_set_split_kv(pkv_plan* plan, int on);
+
+/*
  * Batch decode over the paged KV cache ("The Interface", step 3; guide
  * section 3 "FlashDecoding"): one query row per request, all query heads.
  * q and o: [batch, Hq, d]; lse: [batch, Hq] fp32 (may be NULL).

@@ -59,6 +59,7 @@ EXPORTS = [
     "pkv_batch_decode_paged", "pkv_batch_prefill_paged", "pkv_merge_state", "pkv_get_device_error",
     "pkv_plan_set_timing_events", "pkv_batch_decode_paged_noalloc", "pkv_append_paged_kv",
     "pkv_batch_prefill_paged_masked", "pkv_batch_mixed_paged", "pkv_plan_set_pipelined",
+    "pkv_plan_set_split_kv",
 ]
 
 
@@ -97,6 +98,7 @@ def load(path: Optional[str] = None):
             "pkv_batch_prefill_paged_masked": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp]),
             "pkv_batch_mixed_paged": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_plan_set_pipelined": (i32, [vp, i32]),
+            "pkv_plan_set_split_kv": (i32, [vp, i32]),
             "pkv_append_paged_kv": (i32, [ctypes.POINTER(Params), i32, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
                                           vp, ctypes.c_double, vp, vp]),
         }
@@ -195,6 +197,11 @@ def plan_run(h, batch: int, qo_indptr_h, kv_indptr_h, kv_indices_h, kv_last_page
     _check(load().pkv_plan_run(h, int(batch), _ptr(qo), _ptr(ip), _ptr(ix), _ptr(la), int(num_pages),
                                _ptr(dev_ws), dev_ws.numel() * dev_ws.element_size(), _ptr(host_ws),
                                host_ws.numel() * host_ws.element_size(), _stream(stream)), "pkv_plan_run")
+
+
+def plan_set_split_kv(h, on: bool) -> None:
+    """Decode plans: split-KV on (default) or off (each page list whole on one worker)."""
+    _check(load().pkv_plan_set_split_kv(h, int(bool(on))), "pkv_plan_set_split_kv")
 
 
 def plan_get_info(h) -> PlanInfo:
@@ -310,7 +317,7 @@ class Plan:
     def __init__(self, kind: int, *, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                  dtype: torch.dtype, sm_scale: float, logits_cap: float = 0.0, causal: bool = False,
                  max_batch: int, max_total_q: Optional[int] = None, max_kv_pages: int,
-                 device: Optional[int] = None, pipelined: bool = False):
+                 device: Optional[int] = None, pipelined: bool = False, split_kv: bool = True):
         self.kind = kind
         self.device = torch.cuda.current_device() if device is None else int(device)
         self.params = make_params(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, sm_scale, logits_cap,
@@ -324,6 +331,8 @@ class Plan:
         self.num_pages = 0
         if pipelined:
             _check(load().pkv_plan_set_pipelined(self.handle, 1), "pkv_plan_set_pipelined")
+        if not split_kv:
+            plan_set_split_kv(self.handle, False)
 
     def __del__(self):
         h = getattr(self, "handle", None)

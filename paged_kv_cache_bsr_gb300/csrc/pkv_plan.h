@@ -47,6 +47,7 @@ struct pkv_plan {
   int max_slots = 0;
   int rows_per_slot = 0;
   int merge_grid = 0;
+  bool split_kv = true;     // decode: cut page lists into equal runs (pkv_plan_set_split_kv)
   pkv::WorkspaceLayout L{};
   size_t host_bytes = 0;
   // Last computed plan.

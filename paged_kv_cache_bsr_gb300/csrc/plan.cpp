@@ -24,6 +24,8 @@
 #include <cmath>
 #include <cstring>
 #include <new>
+#include <numeric>
+#include <queue>
 #include <utility>
 #include <vector>
 
@@ -87,7 +89,8 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
   *out = nullptr;
   pkv_status st = check_params(kind, params, limits);
   if (st != PKV_OK) return st;
-  if (num_sms <= 0 || num_sms >= (1 << 20)) return PKV_ERR_INVALID_ARG;  // CTA ids fit the plan's heap keys
+  // Worker ids (num_sms x kDecodeWarps) fit the 24-bit field of the whole-list decode plan's heap keys.
+  if (num_sms <= 0 || num_sms >= (1 << 20)) return PKV_ERR_INVALID_ARG;
   if (kind == PKV_PLAN_MIXED && num_sms < 2) return PKV_ERR_INVALID_ARG;  // one SM for each half at least
   pkv_plan* pl = new (std::nothrow) pkv_plan();
   if (!pl) return PKV_ERR_INVALID_ARG;
@@ -188,6 +191,91 @@ int64_t kv_len_of(const int32_t* kv_indptr, const int32_t* kv_last, int b, int P
   return n > 0 ? (n - 1) * P + kv_last[b] : 0;
 }
 
+// Decode work with the split turned off (pkv_plan_set_split_kv): every
+// (request, kv head) page list whole on one of `W` workers, longest first onto
+// the least-loaded worker (ties: the earlier list, then the lower worker).  No
+// list is cut, so there are no partial slots and nothing to merge.
+pkv_status compute_decode_whole(pkv_plan* pl, int batch, const int32_t* kv_indptr, const int32_t* kv_last,
+                                uint8_t* host, int W) {
+  const int hkv = pl->p.num_kv_heads;
+  const int lists = batch * hkv;  // list i is request i / hkv, kv head i % hkv
+  if (lists > pl->max_work) return PKV_ERR_WORKSPACE;
+  auto pages = [&](int i) { return kv_indptr[i / hkv + 1] - kv_indptr[i / hkv]; };
+  PlanScratch& sc = pl->scratch;
+  std::vector<int>& order = sc.order;
+  order.resize(lists);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return pages(x) > pages(y); });
+  const int active = std::min(W, lists);
+  std::vector<int64_t>& load = sc.load;
+  load.assign(active, 0);
+  std::vector<int>& owner = sc.cta_of;
+  owner.resize(lists);
+  std::vector<int>& per_worker = sc.per_cta;
+  per_worker.assign(static_cast<size_t>(active) + 1, 0);
+  // Keys (load << 24) | worker order (load, worker) pairs by one integer comparison.
+  constexpr int kWorkerBits = 24;
+  std::priority_queue<uint64_t, std::vector<uint64_t>, std::greater<uint64_t>> heap;
+  for (int w = 0; w < active; ++w) heap.push(static_cast<uint64_t>(w));
+  for (int i : order) {
+    const int w = static_cast<int>(heap.top() & ((uint64_t{1} << kWorkerBits) - 1));
+    heap.pop();
+    owner[i] = w;
+    ++per_worker[static_cast<size_t>(w) + 1];
+    load[w] += pages(i);
+    heap.push((static_cast<uint64_t>(load[w]) << kWorkerBits) | static_cast<uint64_t>(w));
+  }
+  for (int w = 0; w < active; ++w) per_worker[static_cast<size_t>(w) + 1] += per_worker[w];
+
+  auto* hdr = reinterpret_cast<PlanHeader*>(host + pl->L.header);
+  auto* wptr = reinterpret_cast<int32_t*>(host + pl->L.worker_ptr);
+  auto* segs = reinterpret_cast<DecodeSeg*>(host + pl->L.segs);
+  std::vector<int>& fill = sc.fill;  // each worker's lists in the order they were assigned
+  fill.assign(per_worker.begin(), per_worker.end() - 1);
+  for (int i : order) {
+    const int b = i / hkv;
+    const int32_t n = pages(i);
+    DecodeSeg s{};
+    s.b = b;
+    s.kvh = i % hkv;
+    s.q_row = b;
+    s.idx_begin = kv_indptr[b];
+    s.n_pages = n;
+    s.last_rows = n > 0 ? kv_last[b] : 0;
+    s.page_begin = 0;
+    s.slot = -1;
+    segs[fill[owner[i]]++] = s;
+  }
+  for (int w = 0; w <= active; ++w) wptr[w] = per_worker[w];
+
+  std::memset(hdr, 0, sizeof(PlanHeader));
+  hdr->kind = PKV_PLAN_DECODE;
+  hdr->batch = batch;
+  hdr->num_workers = active;
+  hdr->num_segments = lists;
+
+  pl->active_workers = active;
+  pl->num_work = lists;
+  pl->num_merge = 0;
+  pl->num_slots = 0;
+  int64_t total = 0, most = 0;
+  for (int64_t v : load) {
+    total += v;
+    most = std::max(most, v);
+  }
+  pl->total_cost = total;
+  pl->max_cost = most;
+  pl->work_rows.assign(static_cast<size_t>(lists) * 8, 0);
+  for (int w = 0; w < active; ++w)
+    for (int k = wptr[w]; k < wptr[w + 1]; ++k) {
+      const DecodeSeg& s = segs[k];
+      int32_t* r = &pl->work_rows[static_cast<size_t>(k) * 8];
+      r[0] = w; r[1] = s.b; r[2] = s.kvh; r[3] = 0; r[4] = s.n_pages; r[5] = s.last_rows; r[6] = -1; r[7] = 0;
+    }
+  pl->used_bytes = pl->L.segs + sizeof(DecodeSeg) * static_cast<size_t>(lists);
+  return PKV_OK;
+}
+
 // Decode work over `W` warp workers.  With qo_indptr (a mixed batch) only the
 // requests holding exactly one query row take part, and each reads and writes
 // its row qo_indptr[b]; without it every request is one row, row b.
@@ -196,6 +284,7 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
   const int P = pl->p.page_size;
   const int hkv = pl->p.num_kv_heads;
   if (W <= 0) W = pl->workers;
+  if (!pl->split_kv && !qo_indptr) return compute_decode_whole(pl, batch, kv_indptr, kv_last, host, W);
   auto takes_part = [&](int b) { return !qo_indptr || qo_indptr[b + 1] - qo_indptr[b] == 1; };
   const int64_t pages_per_chunk = ceil_div(P, pkv::kDecodeTileRows);
   // Runs of at least 4 tiles: shorter ones no longer help small batches (measured).
@@ -859,6 +948,12 @@ pkv_status pkv_plan_set_pipelined(pkv_plan* plan, int on) {
   }
   plan->pipelined = true;
   plan->cur = 1;  // the first plan_run fills image 0
+  return PKV_OK;
+}
+
+pkv_status pkv_plan_set_split_kv(pkv_plan* plan, int on) {
+  if (!plan || plan->kind != PKV_PLAN_DECODE) return PKV_ERR_INVALID_ARG;
+  plan->split_kv = on != 0;
   return PKV_OK;
 }
 

@@ -38,11 +38,11 @@ def _limits_of(b, max_batch=None, max_total_q=None, max_kv_pages=None):
                 max_kv_pages=max_kv_pages or max(int(b.kv_indptr[-1]), 1))
 
 
-def make_plan(b, kind: int, pipelined: bool = False, **limits) -> api.Plan:
+def make_plan(b, kind: int, pipelined: bool = False, split_kv: bool = True, **limits) -> api.Plan:
     lim = _limits_of(b, **limits)
     return api.Plan(kind, num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads, head_dim=b.head_dim,
                     page_size=b.page_size, dtype=b.dtype, sm_scale=b.sm_scale, logits_cap=b.logits_cap,
-                    causal=b.causal, pipelined=pipelined, **lim)
+                    causal=b.causal, pipelined=pipelined, split_kv=split_kv, **lim)
 
 
 def plan_batch(plan: api.Plan, b, stream=None) -> None:

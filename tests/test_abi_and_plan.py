@@ -8,6 +8,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
 
@@ -532,3 +533,70 @@ def test_replanning_after_other_batches_gives_a_fresh_plans_tables(lib, kind):
 
 def _info_tuple(info):
     return tuple(getattr(info, f) for f, _ in info._fields_)
+
+
+# --------------------------------------------------------------------------- decode plan, split-KV off
+def check_whole_list_plan(h, b, workers):
+    """Every (request, kv head) page list whole on one worker, placed longest first on
+    the least-loaded worker (a plain restatement of that schedule), no slots, no merges."""
+    info = api.plan_get_info(h)
+    rows = api.plan_get_work(h).tolist()
+    hkv = b.num_kv_heads
+    counts = (b.kv_indptr[1:] - b.kv_indptr[:-1]).tolist()
+    n_lists = b.batch * hkv
+    order = sorted(range(n_lists), key=lambda i: -counts[i // hkv])  # stable: ties keep list order
+    loads = [0] * min(workers, n_lists)
+    owner, seq = {}, {w: [] for w in range(len(loads))}
+    for i in order:
+        w = min(range(len(loads)), key=lambda j: (loads[j], j))
+        owner[(i // hkv, i % hkv)] = w
+        seq[w].append((i // hkv, i % hkv))
+        loads[w] += counts[i // hkv]
+    got = {}
+    for w, bb, kvh, p0, n, last, slot, _ in rows:
+        assert (bb, kvh) not in got
+        got[(bb, kvh)] = w
+        assert p0 == 0 and n == counts[bb] and slot == -1
+        assert last == (int(b.kv_last_page_len[bb]) if n else 0)
+    assert got == owner
+    assert [r[0] for r in rows] == sorted(r[0] for r in rows)                 # grouped by worker
+    assert [(r[1], r[2]) for r in rows] == [x for w in sorted(seq) for x in seq[w]]
+    assert info.num_merge == 0 and info.num_slots == 0 and info.num_work == n_lists
+    assert info.active_workers == len(loads)
+    assert info.max_cost == max(loads, default=0) and info.total_cost == sum(counts) * hkv
+
+
+def test_decode_plan_without_split_keeps_each_list_whole(lib):
+    # the skewed long-context batch: 31 requests of 1024 tokens and one of 131072
+    b = table_batch([1024] * 31 + [131072])
+    h, ws = host_plan(b, api.PLAN_DECODE)
+    api.plan_set_split_kv(h, False)
+    compute(h, ws, b)
+    check_whole_list_plan(h, b, 152 * 8)
+    assert api.plan_get_info(h).max_cost == 8192          # the long request on one worker
+    api.plan_set_split_kv(h, True)                        # back on: the split plan again
+    compute(h, ws, b)
+    check_decode_plan(h, b)
+    assert api.plan_get_info(h).num_slots > 0
+    api.plan_destroy(h)
+
+
+def test_decode_plan_without_split_more_lists_than_workers(lib):
+    rng = np.random.default_rng(7)
+    kv = [int(x) for x in rng.integers(0, 900, size=11)] + [0, 5]   # an empty request, a short one
+    b = table_batch(kv)
+    h, ws = host_plan(b, api.PLAN_DECODE, num_sms=2)      # 16 workers for 13 x 8 lists
+    api.plan_set_split_kv(h, False)
+    compute(h, ws, b)
+    check_whole_list_plan(h, b, 2 * 8)
+    api.plan_destroy(h)
+
+
+@pytest.mark.parametrize("kind", [api.PLAN_PREFILL, api.PLAN_MIXED])
+def test_split_kv_switch_is_for_decode_plans(lib, kind):
+    b = W.mixed_batch(seed=6, n_decode=3, n_prefill=1)
+    h, ws = host_plan(b, kind)
+    with pytest.raises(api.PkvError) as e:
+        api.plan_set_split_kv(h, False)
+    assert e.value.status == -1
+    api.plan_destroy(h)
