@@ -66,28 +66,6 @@ def test_cascade_full_view_decode_softcap():
 
 
 # --------------------------------------------------------------------------- edge cases
-def test_tiny_and_edge_decode_with_split_off():
-    """Split-KV off: every (request, kv head) page list whole on one worker, with no
-    partial states, gives the oracle's results (empty and one-token requests too)."""
-    for b, what in ((W.tiny_decode(seed=1000, poison=True), "tiny, split off"),
-                    (W.make_paged_batch(qo_lens=[1] * 5, kv_lens=[33, 0, 257, 1000, 1], num_qo_heads=8,
-                                        num_kv_heads=2, head_dim=128, page_size=16, dtype=torch.bfloat16,
-                                        seed=77, poison=True, pool_pages=90), "edge, split off")):
-        plan, _, _ = decode_vs_oracle(b, what, plan_limits={"split_kv": False})
-        info = plan.info()
-        assert info.num_merge == 0 and info.num_slots == 0 and info.num_work == b.batch * b.num_kv_heads
-
-
-@pytest.mark.slow
-def test_skewed_decode_full_size_with_split_off():
-    """The skewed batch with split-KV off: the 131072-token request streams through
-    one warp per kv head; results as the oracle's."""
-    plan, _, _ = decode_vs_oracle(W.skewed_decode(seed=1002, poison=True), "skewed, split off",
-                                  plan_limits={"split_kv": False})
-    info = plan.info()
-    assert info.num_merge == 0 and info.num_slots == 0 and info.max_cost == 131072 // 16
-
-
 @pytest.mark.parametrize("kv_lens", [[1, 15, 16, 17], [0, 3, 0], [1], [16], [33, 0, 257, 1000]])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 def test_edge_lengths(kv_lens, dtype):

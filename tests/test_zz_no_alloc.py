@@ -9,7 +9,7 @@ returns what pkv_batch_decode_paged returns on the same inputs, on two calls
 in a row with different batches (the static array keeps the previous call's
 contents), and that a plan too large for the array is refused.
 
-This file is named to be collected last.
+This file is named to be collected after the main GPU tests.
 """
 import pytest
 import torch
