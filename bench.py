@@ -754,17 +754,6 @@ def run_own(args):
             secondary["skewed_decode"] = {"value": round(r3["value"], 1), "unit": "GB/s",
                                           "ms_per_step": round(r3["ms_per_step"], 4),
                                           "roofline": r3["roofline"], "slots": r3["info"].num_slots}
-            # The same batch with the split turned off: each page list whole on one
-            # warp, so the 131072-token request sets the step time.
-            try:
-                r4 = decode_measure(sk, max(20, args.steps // 10), 5, peaks, split_kv=False)
-                secondary["skewed_decode"]["split_off"] = {
-                    "value": round(r4["value"], 1), "unit": "GB/s", "ms_per_step": round(r4["ms_per_step"], 4),
-                    "kernel_ms": round(r4["kernel_ms"], 4),
-                    "split_speedup": round(r4["ms_per_step"] / r3["ms_per_step"], 2)}
-            except Exception as e:  # recorded, so that the lines after it still run
-                secondary["skewed_decode"]["split_off"] = {"error": f"{type(e).__name__}: {e}"[:300]}
-            del sk
             ident = W.llama3_decode(seed=1001, identity_pages=True)
             r_id = decode_measure(ident, max(20, args.steps // 10), 5, peaks)
             secondary["page_permutation_overhead"] = {
@@ -783,6 +772,18 @@ def run_own(args):
             secondary["tree_verify"] = tree_measure(peaks)
             secondary["mixed_batch"] = mixed_measure()
             secondary["prefill_page_size_1"] = prefill_measure(peaks, page_size=1)
+            # The skewed batch again with the split turned off: each page list whole on
+            # one warp, so the 131072-token request sets the step time.  Last, and any
+            # error recorded in place: nothing after it uses the GPU.
+            try:
+                r4 = decode_measure(sk, max(20, args.steps // 10), 5, peaks, split_kv=False)
+                secondary["skewed_decode"]["split_off"] = {
+                    "value": round(r4["value"], 1), "unit": "GB/s", "ms_per_step": round(r4["ms_per_step"], 4),
+                    "kernel_ms": round(r4["kernel_ms"], 4),
+                    "split_speedup": round(r4["ms_per_step"] / r3["ms_per_step"], 2)}
+            except Exception as e:
+                secondary["skewed_decode"]["split_off"] = {"error": f"{type(e).__name__}: {e}"[:300]}
+            del sk
     clocks.stop()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
