@@ -275,6 +275,37 @@ def time_steps(fn, steps, warmup, stream, kernel_events=None, sync_each=False):
     return total, kern
 
 
+def host_plan_us(b, kind, reps=200):
+    """Median host time of one plan step for batch b: pkv_plan_compute alone
+    (validation and tables, no copy), on a host-only plan for this GPU's SM count."""
+    import torch
+    from paged_kv_cache_bsr_gb300 import api
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    params = api.make_params(b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.dtype, b.sm_scale,
+                             b.logits_cap, b.causal)
+    limits = api.Limits(max(b.batch, 1), max(b.total_q, 1), max(int(b.kv_indptr[-1]), 1))
+    h = api.plan_create_host(kind, params, limits, sms)
+    try:
+        _, nbytes = api.plan_workspace_bytes(h)
+        raw = torch.empty(nbytes + 64, dtype=torch.uint8)
+        off = (-raw.data_ptr()) % 64
+        ws = raw[off:off + nbytes]
+        qo = b.qo_indptr if kind != api.PLAN_DECODE else None
+        arrays = [api._host_i32(x) for x in (qo, b.kv_indptr, b.kv_indices, b.kv_last_page_len)]
+        args = [api._ptr(x) for x in arrays] + [int(b.num_pages), api._ptr(ws), nbytes]
+        lib = api.load()
+        times = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            st = lib.pkv_plan_compute(h, b.batch, *args)
+            times.append(time.perf_counter() - t0)
+            if st != api.PKV_OK:
+                raise api.PkvError(st, "pkv_plan_compute")
+        return round(sorted(times)[len(times) // 2] * 1e6, 1)
+    finally:
+        api.plan_destroy(h)
+
+
 def decode_measure(b, steps, warmup, peaks, profile_name=None, split_kv=True):
     """Step time and main-kernel time of plan + decode + merge on one workload
     (split_kv False: each page list whole on one worker, nothing to merge)."""
@@ -386,6 +417,7 @@ def prefill_measure(peaks, steps=20, warmup=3, page_size=16):
     return {"workload": "ragged_causal_prefill", "page_size": page_size,
             "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "kernel_ms": round(kern_ms, 4), "flops": flops,
+            "host_plan_us": host_plan_us(b, api.PLAN_PREFILL),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
                          "peak_source": peaks["source"], "kernel": "prefill_kernel"}}
@@ -670,6 +702,7 @@ def mixed_measure(steps=50, warmup=5):
     info = pm.info()
     out["prefill_ctas"], out["decode_ctas"] = info.prefill_ctas, info.decode_ctas
     out["speedup_vs_sequential"] = round(out["sequential_us"] / out["mixed_us"], 3)
+    out["host_plan_us"] = host_plan_us(b, api.PLAN_MIXED)
     err = pm.device_error()
     if err:
         out["error"] = f"device error word {err}"
@@ -796,6 +829,9 @@ def run_own(args):
                    "active_workers": info.active_workers, "split_sequences": info.num_merge},
         "hbm_frac_of_step": round(value / world / peaks["hbm_gbs"], 4),
         "roofline": res["roofline"],
+        "host_plan": {"us": host_plan_us(b, api.PLAN_DECODE),
+                      "what": "pkv_plan_compute alone (validation + tables), median of 200 on the host; "
+                              "the timed step's pipelined plan overlaps it with the GPU"},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
     }
