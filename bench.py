@@ -306,6 +306,17 @@ def host_plan_us(b, kind, reps=200):
         api.plan_destroy(h)
 
 
+def host_plan_entry(b):
+    """The bench line's host plan figure for the decode batch (an error is recorded in place)."""
+    from paged_kv_cache_bsr_gb300 import api
+    what = ("pkv_plan_compute alone (validation + tables), median of 200 on the host; "
+            "the timed step's pipelined plan overlaps it with the GPU")
+    try:
+        return {"us": host_plan_us(b, api.PLAN_DECODE), "what": what}
+    except Exception as e:
+        return {"error": f"{type(e).__name__}: {e}"[:300], "what": what}
+
+
 def decode_measure(b, steps, warmup, peaks, profile_name=None, split_kv=True):
     """Step time and main-kernel time of plan + decode + merge on one workload
     (split_kv False: each page list whole on one worker, nothing to merge)."""
@@ -829,9 +840,7 @@ def run_own(args):
                    "active_workers": info.active_workers, "split_sequences": info.num_merge},
         "hbm_frac_of_step": round(value / world / peaks["hbm_gbs"], 4),
         "roofline": res["roofline"],
-        "host_plan": {"us": host_plan_us(b, api.PLAN_DECODE),
-                      "what": "pkv_plan_compute alone (validation + tables), median of 200 on the host; "
-                              "the timed step's pipelined plan overlaps it with the GPU"},
+        "host_plan": host_plan_entry(b),
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
     }
