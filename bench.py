@@ -306,15 +306,20 @@ def host_plan_us(b, kind, reps=200):
         api.plan_destroy(h)
 
 
-def host_plan_entry(b):
-    """The bench line's host plan figure for the decode batch (an error is recorded in place)."""
-    from paged_kv_cache_bsr_gb300 import api
-    what = ("pkv_plan_compute alone (validation + tables), median of 200 on the host; "
-            "the timed step's pipelined plan overlaps it with the GPU")
+def host_plan_or_error(b, kind):
+    """host_plan_us, or the error it raised as text (recorded in place)."""
     try:
-        return {"us": host_plan_us(b, api.PLAN_DECODE), "what": what}
+        return host_plan_us(b, kind)
     except Exception as e:
-        return {"error": f"{type(e).__name__}: {e}"[:300], "what": what}
+        return f"{type(e).__name__}: {e}"[:300]
+
+
+def host_plan_entry(b):
+    """The bench line's host plan figure for the decode batch."""
+    from paged_kv_cache_bsr_gb300 import api
+    return {"us": host_plan_or_error(b, api.PLAN_DECODE),
+            "what": "pkv_plan_compute alone (validation + tables), median of 200 on the host; "
+                    "the timed step's pipelined plan overlaps it with the GPU"}
 
 
 def decode_measure(b, steps, warmup, peaks, profile_name=None, split_kv=True):
@@ -428,7 +433,7 @@ def prefill_measure(peaks, steps=20, warmup=3, page_size=16):
     return {"workload": "ragged_causal_prefill", "page_size": page_size,
             "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "kernel_ms": round(kern_ms, 4), "flops": flops,
-            "host_plan_us": host_plan_us(b, api.PLAN_PREFILL),
+            "host_plan_us": host_plan_or_error(b, api.PLAN_PREFILL),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
                          "peak_source": peaks["source"], "kernel": "prefill_kernel"}}
@@ -713,7 +718,7 @@ def mixed_measure(steps=50, warmup=5):
     info = pm.info()
     out["prefill_ctas"], out["decode_ctas"] = info.prefill_ctas, info.decode_ctas
     out["speedup_vs_sequential"] = round(out["sequential_us"] / out["mixed_us"], 3)
-    out["host_plan_us"] = host_plan_us(b, api.PLAN_MIXED)
+    out["host_plan_us"] = host_plan_or_error(b, api.PLAN_MIXED)
     err = pm.device_error()
     if err:
         out["error"] = f"device error word {err}"
