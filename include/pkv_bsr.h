@@ -216,10 +216,12 @@ pkv_status pkv_plan_set_pipelined(pkv_plan* plan, int on);
  * the (request, kv head) page lists into equal runs over the workers and merges
  * the partial states ("FlashInfer" guide, section 3 "FlashDecoding"; fdeinterviews
  * summary, "Load balancing that survives CUDA graphs").  Off, each page list goes
- * whole to one worker, longest first onto the least-loaded worker (ties to the
- * earlier list, then the lower worker), with no partial states and no merge:
- * the baseline the split is measured against, in which one long request rests
- * on one worker.  Takes effect at the next plan step; the run call is unchanged.
+ * whole to one worker (one warp), longest first onto the least-loaded worker,
+ * with no partial states and no merge: the baseline the split is measured
+ * against, in which one long request rests on one warp per kv head.  Ties go to
+ * the earlier list, then to the worker of lower rank, rank r being warp r / C of
+ * CTA r % C over the plan's C CTAs (equal loads spread over the SMs first).
+ * Takes effect at the next plan step; the run call is unchanged.
  * Errors: PKV_ERR_INVALID_ARG (NULL, or not a plan of kind DECODE).
  */
 pkv_status pkv_plan_set_split_kv(pkv_plan* plan, int on);

@@ -192,40 +192,48 @@ int64_t kv_len_of(const int32_t* kv_indptr, const int32_t* kv_last, int b, int P
 }
 
 // Decode work with the split turned off (pkv_plan_set_split_kv): every
-// (request, kv head) page list whole on one of `W` workers, longest first onto
-// the least-loaded worker (ties: the earlier list, then the lower worker).  No
-// list is cut, so there are no partial slots and nothing to merge.
+// (request, kv head) page list whole on one of `W` workers (warps of W / 8
+// CTAs), longest first onto the least-loaded worker.  Ties go to the earlier
+// list, and between workers to the lower rank, rank r being warp r / C of CTA
+// r % C over C CTAs: so equal loads fill one warp on every SM before a second
+// warp on any, and the longest lists land on different SMs.  No list is cut,
+// so there are no partial slots and nothing to merge.
 pkv_status compute_decode_whole(pkv_plan* pl, int batch, const int32_t* kv_indptr, const int32_t* kv_last,
                                 uint8_t* host, int W) {
   const int hkv = pl->p.num_kv_heads;
   const int lists = batch * hkv;  // list i is request i / hkv, kv head i % hkv
   if (lists > pl->max_work) return PKV_ERR_WORKSPACE;
+  const int ctas = std::max(1, W / pkv::kDecodeWarps);
+  auto worker_of_rank = [&](int r) { return (r % ctas) * pkv::kDecodeWarps + r / ctas; };
   auto pages = [&](int i) { return kv_indptr[i / hkv + 1] - kv_indptr[i / hkv]; };
   PlanScratch& sc = pl->scratch;
   std::vector<int>& order = sc.order;
   order.resize(lists);
   std::iota(order.begin(), order.end(), 0);
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return pages(x) > pages(y); });
-  const int active = std::min(W, lists);
-  std::vector<int64_t>& load = sc.load;
-  load.assign(active, 0);
-  std::vector<int>& owner = sc.cta_of;
+  const int ranks = std::min(W, lists);
+  int n_workers = 0;  // highest worker used + 1
+  for (int r = 0; r < ranks; ++r) n_workers = std::max(n_workers, worker_of_rank(r) + 1);
+  std::vector<int64_t>& load = sc.load;  // by rank
+  load.assign(ranks, 0);
+  std::vector<int>& owner = sc.cta_of;   // worker of each list
   owner.resize(lists);
   std::vector<int>& per_worker = sc.per_cta;
-  per_worker.assign(static_cast<size_t>(active) + 1, 0);
-  // Keys (load << 24) | worker order (load, worker) pairs by one integer comparison.
-  constexpr int kWorkerBits = 24;
+  per_worker.assign(static_cast<size_t>(n_workers) + 1, 0);
+  // Keys (load << 24) | rank order (load, rank) pairs by one integer comparison.
+  constexpr int kRankBits = 24;
   std::priority_queue<uint64_t, std::vector<uint64_t>, std::greater<uint64_t>> heap;
-  for (int w = 0; w < active; ++w) heap.push(static_cast<uint64_t>(w));
+  for (int r = 0; r < ranks; ++r) heap.push(static_cast<uint64_t>(r));
   for (int i : order) {
-    const int w = static_cast<int>(heap.top() & ((uint64_t{1} << kWorkerBits) - 1));
+    const int r = static_cast<int>(heap.top() & ((uint64_t{1} << kRankBits) - 1));
     heap.pop();
+    const int w = worker_of_rank(r);
     owner[i] = w;
     ++per_worker[static_cast<size_t>(w) + 1];
-    load[w] += pages(i);
-    heap.push((static_cast<uint64_t>(load[w]) << kWorkerBits) | static_cast<uint64_t>(w));
+    load[r] += pages(i);
+    heap.push((static_cast<uint64_t>(load[r]) << kRankBits) | static_cast<uint64_t>(r));
   }
-  for (int w = 0; w < active; ++w) per_worker[static_cast<size_t>(w) + 1] += per_worker[w];
+  for (int w = 0; w < n_workers; ++w) per_worker[static_cast<size_t>(w) + 1] += per_worker[w];
 
   auto* hdr = reinterpret_cast<PlanHeader*>(host + pl->L.header);
   auto* wptr = reinterpret_cast<int32_t*>(host + pl->L.worker_ptr);
@@ -246,15 +254,15 @@ pkv_status compute_decode_whole(pkv_plan* pl, int batch, const int32_t* kv_indpt
     s.slot = -1;
     segs[fill[owner[i]]++] = s;
   }
-  for (int w = 0; w <= active; ++w) wptr[w] = per_worker[w];
+  for (int w = 0; w <= n_workers; ++w) wptr[w] = per_worker[w];
 
   std::memset(hdr, 0, sizeof(PlanHeader));
   hdr->kind = PKV_PLAN_DECODE;
   hdr->batch = batch;
-  hdr->num_workers = active;
+  hdr->num_workers = n_workers;  // workers below this with no list return at once
   hdr->num_segments = lists;
 
-  pl->active_workers = active;
+  pl->active_workers = ranks;
   pl->num_work = lists;
   pl->num_merge = 0;
   pl->num_slots = 0;
@@ -266,7 +274,7 @@ pkv_status compute_decode_whole(pkv_plan* pl, int batch, const int32_t* kv_indpt
   pl->total_cost = total;
   pl->max_cost = most;
   pl->work_rows.assign(static_cast<size_t>(lists) * 8, 0);
-  for (int w = 0; w < active; ++w)
+  for (int w = 0; w < n_workers; ++w)
     for (int k = wptr[w]; k < wptr[w + 1]; ++k) {
       const DecodeSeg& s = segs[k];
       int32_t* r = &pl->work_rows[static_cast<size_t>(k) * 8];

@@ -538,20 +538,23 @@ def _info_tuple(info):
 # --------------------------------------------------------------------------- decode plan, split-KV off
 def check_whole_list_plan(h, b, workers):
     """Every (request, kv head) page list whole on one worker, placed longest first on
-    the least-loaded worker (a plain restatement of that schedule), no slots, no merges."""
+    the least-loaded worker, ties to the lower rank (rank r = warp r // C of CTA r % C)
+    (a plain restatement of that schedule); no slots, no merges."""
     info = api.plan_get_info(h)
     rows = api.plan_get_work(h).tolist()
     hkv = b.num_kv_heads
     counts = (b.kv_indptr[1:] - b.kv_indptr[:-1]).tolist()
     n_lists = b.batch * hkv
+    ctas = workers // 8
     order = sorted(range(n_lists), key=lambda i: -counts[i // hkv])  # stable: ties keep list order
-    loads = [0] * min(workers, n_lists)
-    owner, seq = {}, {w: [] for w in range(len(loads))}
+    loads = [0] * min(workers, n_lists)                               # by rank
+    owner, seq = {}, {}
     for i in order:
-        w = min(range(len(loads)), key=lambda j: (loads[j], j))
+        r = min(range(len(loads)), key=lambda j: (loads[j], j))
+        w = (r % ctas) * 8 + r // ctas
         owner[(i // hkv, i % hkv)] = w
-        seq[w].append((i // hkv, i % hkv))
-        loads[w] += counts[i // hkv]
+        seq.setdefault(w, []).append((i // hkv, i % hkv))
+        loads[r] += counts[i // hkv]
     got = {}
     for w, bb, kvh, p0, n, last, slot, _ in rows:
         assert (bb, kvh) not in got
@@ -573,7 +576,9 @@ def test_decode_plan_without_split_keeps_each_list_whole(lib):
     api.plan_set_split_kv(h, False)
     compute(h, ws, b)
     check_whole_list_plan(h, b, 152 * 8)
-    assert api.plan_get_info(h).max_cost == 8192          # the long request on one worker
+    assert api.plan_get_info(h).max_cost == 8192          # the long request on one worker per kv head
+    long_workers = [r[0] for r in api.plan_get_work(h).tolist() if r[1] == 31]
+    assert len({w // 8 for w in long_workers}) == 8       # ... its 8 kv heads on 8 CTAs
     api.plan_set_split_kv(h, True)                        # back on: the split plan again
     compute(h, ws, b)
     check_decode_plan(h, b)
