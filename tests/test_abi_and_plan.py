@@ -316,7 +316,10 @@ def longest_first_prefill(b, C, rows_per_tile=256, keys=128):
 
 @pytest.mark.parametrize("seed,batch,C,causal,page", [(1003, 16, 152, True, 16), (7, 5, 8, True, 16),
                                                       (9, 3, 152, False, 16), (11, 6, 20, True, 1),
-                                                      (13, 1, 152, False, 16)])
+                                                      (13, 1, 152, False, 16),
+                                                      # CTA counts at the edges of 64-bit CTA sets
+                                                      (21, 8, 64, True, 16), (23, 8, 65, True, 16),
+                                                      (25, 4, 1, True, 16), (27, 10, 130, False, 8)])
 def test_prefill_plan_is_the_longest_first_schedule(lib, seed, batch, C, causal, page):
     """The plan's work rows equal the plainly restated schedule, item by item and CTA by
     CTA (a faster implementation of the plan must not change what the GPU runs)."""
