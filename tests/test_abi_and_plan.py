@@ -608,3 +608,62 @@ def test_split_kv_switch_is_for_decode_plans(lib, kind):
         api.plan_set_split_kv(h, False)
     assert e.value.status == -1
     api.plan_destroy(h)
+
+
+# --------------------------------------------------------------------------- argument checks of the run calls
+def test_run_calls_refuse_bad_arguments_before_any_cuda_call(lib):
+    """Each case fails a host-side check that comes before the first CUDA call (so no
+    case can reach a kernel with these host pointers): the status the header states."""
+    L = api.load()
+    buf = torch.zeros(4096, dtype=torch.uint8)
+    base = buf.data_ptr() + (-buf.data_ptr()) % 256
+    p16, odd = ctypes.c_void_p(base), ctypes.c_void_p(base + 2)   # 256-aligned, and 2 bytes off
+    INVALID, UNSUPPORTED = -1, -3
+    # merge_state: sizes, dtype, pointers, alignment
+    ms = L.pkv_merge_state
+    assert ms(p16, p16, p16, p16, p16, p16, -1, 4, 64, api.PKV_BF16, None) == INVALID
+    assert ms(p16, p16, p16, p16, p16, p16, 8, 0, 64, api.PKV_BF16, None) == INVALID
+    assert ms(p16, p16, p16, p16, p16, p16, 8, 4, 0, api.PKV_BF16, None) == INVALID
+    assert ms(p16, p16, p16, p16, p16, p16, 8, 4, 64, 7, None) == UNSUPPORTED
+    assert ms(None, None, None, None, None, None, 0, 4, 64, api.PKV_BF16, None) == api.PKV_OK   # nothing to do
+    assert ms(None, p16, p16, p16, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID
+    assert ms(odd, p16, p16, p16, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID
+    assert ms(p16, odd, p16, p16, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID
+    # append: params, theta, head_dim, dtype, counts, pointers, alignment
+    ap = L.pkv_append_paged_kv
+    good = api.make_params(8, 2, 128, 16, torch.bfloat16, 0.1)
+
+    def append(params, batch=2, nnz=5, theta=0.0, k=p16, q_in=None, q_out=None):
+        return ap(ctypes.byref(params) if params is not None else None, batch, nnz, 10, p16, p16, p16, p16, k, p16,
+                  p16, q_in, q_out, theta, None, None)
+    assert append(None) == INVALID
+    for theta in (-1.0, float("nan"), float("inf")):
+        assert append(good, theta=theta) == INVALID
+    assert append(api.make_params(8, 2, 96, 16, torch.bfloat16, 0.1)) == UNSUPPORTED
+    assert append(api.make_params(8, 2, 128, 16, api.PKV_F32, 0.1)) == UNSUPPORTED
+    assert append(good, nnz=0) == api.PKV_OK                                   # nothing to append
+    assert append(good, batch=0) == INVALID                                    # tokens but no requests
+    assert append(good, q_in=p16) == INVALID                                   # q_in without q_out
+    assert append(good, k=odd) == INVALID
+    # run calls: a plan of another kind, and a host-only plan of the right kind
+    b = W.mixed_batch(seed=6, n_decode=3, n_prefill=1)
+    plans = {k: host_plan(b, k) for k in (api.PLAN_DECODE, api.PLAN_PREFILL, api.PLAN_MIXED)}
+    for k, (h, ws) in plans.items():
+        compute(h, ws, b)
+    ptrs = [p16] * 9
+    dec = lambda h: L.pkv_batch_decode_paged(h, *ptrs[:7], p16, None)
+    pre = lambda h: L.pkv_batch_prefill_paged(h, *ptrs[:8], p16, None)
+    mix = lambda h: L.pkv_batch_mixed_paged(h, *ptrs[:8], p16, None)
+    masked_no_mask = lambda h: L.pkv_batch_prefill_paged_masked(h, *ptrs[:6], None, 64, p16, p16, p16, None)
+    for run, kind in ((dec, api.PLAN_DECODE), (pre, api.PLAN_PREFILL), (mix, api.PLAN_MIXED)):
+        for k, (h, _) in plans.items():
+            assert run(h) == INVALID, (kind, k)                    # other kinds, and host-only plans
+    assert masked_no_mask(plans[api.PLAN_PREFILL][0]) == INVALID
+    # setters and the error read-back
+    h = plans[api.PLAN_DECODE][0]
+    assert L.pkv_plan_set_timing_events(h, p16, None) == INVALID      # start without stop
+    assert L.pkv_plan_set_pipelined(h, 1) == INVALID                  # host-only plan
+    code = ctypes.c_int(0)
+    assert L.pkv_get_device_error(None, p16, ctypes.byref(code), 0, None) == INVALID
+    for h, _ in plans.values():
+        api.plan_destroy(h)
