@@ -103,7 +103,10 @@ int pkv_version(void);
  * Create a plan for `kind` on CUDA device `device`.  Validates params and
  * limits, queries the device's SM count, and fixes the worker grid.
  * Allocates only host memory (freed by pkv_plan_destroy).
- * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ * Errors: PKV_ERR_INVALID_ARG (also limits whose tables would need more than
+ * 2^31 - 1 work entries: decode max_batch * num_kv_heads, prefill about
+ * (max_total_q * group / 256 + max_batch) * num_kv_heads), PKV_ERR_UNSUPPORTED,
+ * PKV_ERR_CUDA.
  */
 pkv_status pkv_plan_create(pkv_plan** out, int kind, const pkv_params* params,
                            const pkv_limits* limits, int device);
@@ -114,6 +117,7 @@ pkv_status pkv_plan_destroy(pkv_plan* plan);
  * Create a plan for a device with `num_sms` SMs without any CUDA call, so that
  * the plan's decisions can be inspected on a machine without a GPU.  Such a
  * plan computes tables (pkv_plan_compute) but cannot run (PKV_ERR_INVALID_ARG).
+ * Errors: as pkv_plan_create, less PKV_ERR_CUDA.
  */
 pkv_status pkv_plan_create_host(pkv_plan** out, int kind, const pkv_params* params,
                                 const pkv_limits* limits, int num_sms);

@@ -128,7 +128,12 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
     pl->workers = num_sms * pkv::kDecodeWarps;
     // Each worker's run cuts at most two page lists, and every list adds at
     // most one uncut entry; see the decode branch of compute_decode.
-    pl->max_work = static_cast<int>(pl->workers + (int64_t)limits->max_batch * hkv + 1);
+    const int64_t max_work = pl->workers + static_cast<int64_t>(limits->max_batch) * hkv + 1;
+    if (max_work > INT32_MAX) {  // table entries are counted in int32
+      delete pl;
+      return PKV_ERR_INVALID_ARG;
+    }
+    pl->max_work = static_cast<int>(max_work);
     pl->max_merge = static_cast<int>(std::min<int64_t>((int64_t)limits->max_batch * hkv, pl->workers) + 1);
     pl->max_slots = 2 * pl->workers;
     pl->rows_per_slot = pl->group;
@@ -140,7 +145,12 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
     const int64_t tiles = (ceil_div(limits->max_total_q, mp) + limits->max_batch) * hkv;
     // Splitting only touches tiles costing more than total / CTAs (fewer than
     // CTAs of them), and adds at most CTAs chunks in total.
-    pl->max_work = static_cast<int>(tiles + 2 * (int64_t)num_sms + 1);
+    const int64_t max_work = tiles + 2 * static_cast<int64_t>(num_sms) + 1;
+    if (max_work > INT32_MAX) {  // table entries are counted in int32
+      delete pl;
+      return PKV_ERR_INVALID_ARG;
+    }
+    pl->max_work = static_cast<int>(max_work);
     pl->max_merge = num_sms + 1;
     pl->max_slots = 2 * num_sms + 2;
     pl->rows_per_slot = pkv::kPrefillRows;

@@ -227,6 +227,27 @@ def test_plan_create_rejects_bad_params(lib):
         assert e.value.status == st
 
 
+def test_plan_create_refuses_limits_past_int32_tables(lib):
+    """Table entries are counted in int32: limits that would need more are refused at
+    create time (rather than wrapping the table sizes)."""
+    big = (1 << 31) - 1
+    dec = api.make_params(32, 8, 128, 16, torch.bfloat16, 0.1)
+    with pytest.raises(api.PkvError) as e:                       # 300M requests x 8 kv heads
+        api.plan_create_host(api.PLAN_DECODE, dec, api.Limits(300_000_000, 300_000_000, 1000), 152)
+    assert e.value.status == -1
+    wide = api.make_params(256, 256, 128, 16, torch.bfloat16, 0.1)
+    for kind in (api.PLAN_PREFILL, api.PLAN_MIXED):              # 2^31 rows / 256 per tile x 256 kv heads
+        with pytest.raises(api.PkvError) as e:
+            api.plan_create_host(kind, wide, api.Limits(1, big, 1000), 152)
+        assert e.value.status == -1
+    # the largest row count with 8 kv heads still fits: 8.6 GB of tables, sized without wrapping
+    h = api.plan_create_host(api.PLAN_PREFILL, api.make_params(8, 8, 128, 16, torch.bfloat16, 0.1),
+                             api.Limits(1, big, 1000), 152)
+    dev, host = api.plan_workspace_bytes(h)
+    assert host >= 2 * 64 * 8 * (big // 256) and dev > host // 2
+    api.plan_destroy(h)
+
+
 def test_run_calls_refuse_host_only_plans(lib):
     b = table_batch([40])
     h, ws = host_plan(b, api.PLAN_DECODE)
