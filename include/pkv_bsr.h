@@ -144,7 +144,8 @@ pkv_status pkv_plan_workspace_bytes(const pkv_plan* plan, size_t* dev_bytes, siz
  * A later plan_run on the same plan first waits for the previous copy out of
  * host_ws to finish.  Run calls must be enqueued after this call on the same
  * stream (or ordered after it).
- * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_BAD_INDEX, PKV_ERR_WORKSPACE, PKV_ERR_CUDA.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_BAD_INDEX, PKV_ERR_WORKSPACE (also a
+ * request of 2^31 keys or more), PKV_ERR_CUDA.
  */
 pkv_status pkv_plan_run(pkv_plan* plan, int batch, const int32_t* qo_indptr_h,
                         const int32_t* kv_indptr_h, const int32_t* kv_indices_h,

@@ -174,6 +174,8 @@ pkv_status validate(const pkv_plan* pl, int batch, const int32_t* qo_indptr, con
     const int32_t n = kv_indptr[b + 1] - kv_indptr[b];
     if (n < 0) return PKV_ERR_BAD_INDEX;
     if (n > 0 && (kv_last[b] < 1 || kv_last[b] > pl->p.page_size)) return PKV_ERR_BAD_INDEX;
+    // Keys of one request are counted in int32 (a page id may be listed many times).
+    if (n > 0 && static_cast<int64_t>(n - 1) * pl->p.page_size + kv_last[b] > INT32_MAX) return PKV_ERR_WORKSPACE;
   }
   const int64_t nnz = kv_indptr[batch];
   if (nnz > pl->lim.max_kv_pages) return PKV_ERR_WORKSPACE;

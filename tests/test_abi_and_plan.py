@@ -212,6 +212,20 @@ def test_plan_rejects_malformed_index_arrays(lib):
     api.plan_destroy(h)
 
 
+def test_plan_refuses_a_request_of_2_31_keys(lib):
+    """Keys of one request are counted in int32: 2^27 page entries of 16 rows (a page id
+    may repeat) make 2^31 keys, refused; one key fewer is planned."""
+    b = table_batch([40])
+    h, ws = host_plan(b, api.PLAN_DECODE, max_kv_pages=1 << 27)
+    ip = torch.tensor([0, 1 << 27], dtype=torch.int32)
+    with pytest.raises(api.PkvError) as e:
+        api.plan_compute(h, 1, None, ip, None, torch.tensor([16], dtype=torch.int32), 10, ws)
+    assert e.value.status == -4
+    api.plan_compute(h, 1, None, ip, None, torch.tensor([15], dtype=torch.int32), 10, ws)
+    assert api.plan_get_info(h).total_cost == (1 << 27) * b.num_kv_heads
+    api.plan_destroy(h)
+
+
 def test_plan_create_rejects_bad_params(lib):
     lim = api.Limits(4, 4, 100)
     for params, st in [
