@@ -702,3 +702,14 @@ def test_run_calls_refuse_bad_arguments_before_any_cuda_call(lib):
     assert L.pkv_get_device_error(None, p16, ctypes.byref(code), 0, None) == INVALID
     for h, _ in plans.values():
         api.plan_destroy(h)
+
+
+def test_bench_mixed_batch_takes_the_measured_split(lib):
+    """The bench's mixed batch (60 decodes + 4 prompt chunks) splits 68 prefill / 84 decode
+    SMs of 152: the split its one-launch timings and profile were taken at."""
+    b = W.mixed_batch(seed=1007)
+    h, ws = host_plan(b, api.PLAN_MIXED)
+    compute(h, ws, b)
+    info = api.plan_get_info(h)
+    assert (info.prefill_ctas, info.decode_ctas) == (68, 84)
+    api.plan_destroy(h)
