@@ -236,6 +236,15 @@ def _uniform_ints(lo: int, hi: int, n: int, gen: torch.Generator) -> List[int]:
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
 
 
+def zipf_lengths(n: int, s: float, lo: int, hi: int, seed: int) -> List[int]:
+    """n lengths from a Zipf law on [lo, hi], P(len = k) proportional to k^-s: the
+    heavy-tailed request mix the runtime scheduler is built to balance (greptalks
+    summary, "Runtime Scheduler for Dynamic Problem Shapes")."""
+    gen = _gen(seed)
+    w = torch.arange(lo, hi + 1, dtype=torch.float64).pow(-float(s))
+    return [lo + int(i) for i in torch.multinomial(w, n, replacement=True, generator=gen)]
+
+
 def tiny_decode(seed: int = 1000, poison: bool = False) -> PagedBatch:
     """Tiny paged decode: batch 4, 8 q / 2 kv heads, head_dim 64, page 16, fp16,
     kv_len ~ U[1, 256], pages drawn from a randomly permuted 64-page pool."""

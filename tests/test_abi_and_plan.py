@@ -713,3 +713,33 @@ def test_bench_mixed_batch_takes_the_measured_split(lib):
     info = api.plan_get_info(h)
     assert (info.prefill_ctas, info.decode_ctas) == (68, 84)
     api.plan_destroy(h)
+
+
+# --------------------------------------------------------------------------- Zipf-distributed lengths
+@pytest.mark.parametrize("s", [1.1, 1.5])
+def test_decode_plan_balances_zipf_request_lengths(lib, s):
+    """Request lengths from a Zipf law (the skew the pages' scheduler is built for):
+    every worker still streams at most ceil(total pages / workers) pages."""
+    kv = W.zipf_lengths(128, s, 16, 131072, seed=11)
+    assert max(kv) > 20 * sorted(kv)[len(kv) // 2]                 # heavy-tailed
+    b = table_batch(kv)
+    h, ws = host_plan(b, api.PLAN_DECODE)
+    compute(h, ws, b)
+    info, _ = check_decode_plan(h, b)
+    total = sum((n + 15) // 16 for n in kv) * b.num_kv_heads
+    assert info.max_cost <= max(-(-total // info.workers), 8)
+    api.plan_destroy(h)
+
+
+@pytest.mark.parametrize("s", [1.1, 1.5])
+def test_prefill_plan_balances_zipf_prompt_lengths(lib, s):
+    """Prompt lengths from a Zipf law: the busiest CTA carries at most the average load
+    plus one work item (the list-scheduling bound), long tiles being cut into chunks."""
+    qo = W.zipf_lengths(24, s, 16, 8192, seed=12)
+    b = table_batch(qo, qo_lens=qo, causal=True)
+    h, ws = host_plan(b, api.PLAN_PREFILL)
+    compute(h, ws, b)
+    info, work = check_prefill_plan(h, b)
+    biggest = max(max(1, -(-(ke - kb) // 128)) + 1 for _, _, _, _, _, kb, ke, _ in work)
+    assert info.max_cost <= -(-info.total_cost // info.active_workers) + biggest
+    api.plan_destroy(h)
