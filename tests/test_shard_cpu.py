@@ -27,13 +27,15 @@ def _free_port():
 
 def test_partition_covers_every_request_once_and_balances():
     rng = np.random.default_rng(3)
-    costs = [int(c) for c in rng.integers(1, 500, size=37)]
-    for world in (1, 2, 3, 8):
-        parts = shard.partition_requests(costs, world)
-        assert sorted(r for p in parts for r in p) == list(range(len(costs)))
-        loads = [sum(costs[r] for r in p) for p in parts]
-        # longest first: no rank ends more than one request's cost above another
-        assert max(loads) - min(loads) <= max(costs)
+    uniform = [int(c) for c in rng.integers(1, 500, size=37)]
+    zipf = W.zipf_lengths(200, 1.1, 16, 131072, seed=5)       # a heavy-tailed request mix
+    for costs in (uniform, zipf):
+        for world in (1, 2, 3, 8):
+            parts = shard.partition_requests(costs, world)
+            assert sorted(r for p in parts for r in p) == list(range(len(costs)))
+            loads = [sum(costs[r] for r in p) for p in parts]
+            # longest first: no rank ends more than one request's cost above another
+            assert max(loads) - min(loads) <= max(costs)
     # longest first: 5 -> rank 0, 4 -> rank 1, 2 -> rank 1 (4 < 5), 1 -> rank 0: loads 6 and 6
     assert shard.partition_requests([5, 1, 4, 2], 2) == [[0, 1], [2, 3]]
     with pytest.raises(ValueError):
