@@ -171,11 +171,13 @@ pkv_status validate(const pkv_plan* pl, int batch, const int32_t* qo_indptr, con
   if (num_pages < 0 || num_pages > INT32_MAX) return PKV_ERR_INVALID_ARG;
   if (kv_indptr[0] != 0) return PKV_ERR_BAD_INDEX;
   for (int b = 0; b < batch; ++b) {
-    const int32_t n = kv_indptr[b + 1] - kv_indptr[b];
-    if (n < 0) return PKV_ERR_BAD_INDEX;
+    // Compared before any subtraction: an int32 difference of a non-monotone
+    // pair could wrap around to a positive page count.
+    if (kv_indptr[b + 1] < kv_indptr[b]) return PKV_ERR_BAD_INDEX;
+    const int64_t n = static_cast<int64_t>(kv_indptr[b + 1]) - kv_indptr[b];
     if (n > 0 && (kv_last[b] < 1 || kv_last[b] > pl->p.page_size)) return PKV_ERR_BAD_INDEX;
     // Keys of one request are counted in int32 (a page id may be listed many times).
-    if (n > 0 && static_cast<int64_t>(n - 1) * pl->p.page_size + kv_last[b] > INT32_MAX) return PKV_ERR_WORKSPACE;
+    if (n > 0 && (n - 1) * pl->p.page_size + kv_last[b] > INT32_MAX) return PKV_ERR_WORKSPACE;
   }
   const int64_t nnz = kv_indptr[batch];
   if (nnz > pl->lim.max_kv_pages) return PKV_ERR_WORKSPACE;
@@ -200,7 +202,7 @@ pkv_status validate(const pkv_plan* pl, int batch, const int32_t* qo_indptr, con
 }
 
 int64_t kv_len_of(const int32_t* kv_indptr, const int32_t* kv_last, int b, int P) {
-  const int64_t n = kv_indptr[b + 1] - kv_indptr[b];
+  const int64_t n = static_cast<int64_t>(kv_indptr[b + 1]) - kv_indptr[b];
   return n > 0 ? (n - 1) * P + kv_last[b] : 0;
 }
 

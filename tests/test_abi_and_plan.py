@@ -212,6 +212,21 @@ def test_plan_rejects_malformed_index_arrays(lib):
     api.plan_destroy(h)
 
 
+def test_plan_rejects_an_indptr_whose_int32_difference_wraps(lib):
+    """indptr [0, 2^31 - 1, -2^31] is not monotone, but its second difference taken in
+    int32 wraps to +1: the plan must compare the entries, not their difference."""
+    for kind in (api.PLAN_DECODE, api.PLAN_PREFILL):
+        b = table_batch([1, 1], page_size=1)
+        h, ws = host_plan(b, kind, max_kv_pages=4)
+        ip = torch.tensor([0, (1 << 31) - 1, -(1 << 31)], dtype=torch.int32)
+        qo = torch.tensor([0, 1, 2], dtype=torch.int32) if kind != api.PLAN_DECODE else None
+        for ix in (torch.zeros(1, dtype=torch.int32), None):
+            with pytest.raises(api.PkvError) as e:
+                api.plan_compute(h, 2, qo, ip, ix, torch.tensor([1, 1], dtype=torch.int32), 1, ws)
+            assert e.value.status == -2
+        api.plan_destroy(h)
+
+
 def test_plan_refuses_a_request_of_2_31_keys(lib):
     """Keys of one request are counted in int32: 2^27 page entries of 16 rows (a page id
     may repeat) make 2^31 keys, refused; one key fewer is planned."""
