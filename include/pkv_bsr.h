@@ -322,7 +322,9 @@ pkv_status pkv_batch_prefill_paged_masked(const pkv_plan* plan, const void* q, c
  *    its kernels read them).  Calls whose work overlaps on the GPU (on other
  *    streams, or from several host threads) race on the array: serialise them.
  *  - The first call on each device looks up the array's device address with
- *    that device current; make that first call before any stream capture.
+ *    that device current, and so does the first call after the device's
+ *    context was made anew (after cudaDeviceReset, say); make such a call
+ *    before any stream capture.
  *  - The device error word lives in the static array and is not reported.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_WORKSPACE, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  */

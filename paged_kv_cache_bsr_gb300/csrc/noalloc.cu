@@ -9,7 +9,9 @@
 // pkv_batch_decode_paged_noalloc serves them: its scratch is the file-scope
 // array below, which exists on every device that loads this library until
 // the process exits, so the call itself allocates nothing.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -29,19 +31,60 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_noalloc_scratch, looked up once per device.  In host
-// code the symbol names a host-side stand-in, so kernels must receive the
-// address that cudaGetSymbolAddress returns with the device current.
+// Driver calls that name the current context and its process-unique id.
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+
+const CtxFns* ctx_fns() {
+  static std::once_flag once;
+  static CtxFns f;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  return (f.get_current && f.get_id) ? &f : nullptr;
+}
+
+// Device address of g_noalloc_scratch in the current context of `device`.
+// In host code the symbol names a host-side stand-in, so kernels must receive
+// the address that cudaGetSymbolAddress returns with the device current.  The
+// lookup is the set-up step: done once per device, and again only when the
+// device's context has changed (a context made after cudaDeviceReset holds a
+// fresh copy of the array, possibly at another address), which the context's
+// process-unique id tells.
 cudaError_t scratch_address(int device, void** out) {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {nullptr};
+  static unsigned long long ctx_of[kMaxDevices] = {0};
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  const CtxFns* f = ctx_fns();
+  if (!f) return cudaErrorNotSupported;
+  // The id of the current context; 0 while the runtime has made none current on
+  // this thread yet (cudaGetSymbolAddress below makes the device's one current).
+  auto current_id = [&](unsigned long long* id) {
+    CUcontext ctx = nullptr;
+    *id = 0;
+    if (f->get_current(&ctx) != CUDA_SUCCESS) return false;
+    return !ctx || f->get_id(ctx, id) == CUDA_SUCCESS;
+  };
+  unsigned long long id = 0;
+  if (!current_id(&id)) return cudaErrorInvalidContext;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[device]) {
+  if (id == 0 || !addr[device] || ctx_of[device] != id) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
+    if (!current_id(&id) || id == 0) return cudaErrorInvalidContext;
     addr[device] = p;
+    ctx_of[device] = id;
   }
   *out = addr[device];
   return cudaSuccess;
@@ -58,7 +101,7 @@ extern "C" pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const
                                                      void* stream) {
   if (!plan || plan->kind != PKV_PLAN_DECODE || !plan->planned || plan->device < 0 || plan->pipelined)
     return PKV_ERR_INVALID_ARG;
-  if (!host_tables || host_tables_bytes < plan->used_bytes) return PKV_ERR_INVALID_ARG;
+  if (!host_tables || host_tables_bytes < plan->host_bytes) return PKV_ERR_INVALID_ARG;
   if (!q || !kv_data || !kv_indices_d || !kv_indptr_d || !kv_last_page_len_d || !o) return PKV_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_data, 16) || !aligned(o, 16) || !aligned(kv_indices_d, 4) ||
       !aligned(kv_indptr_d, 4) || (lse && !aligned(lse, 4)))

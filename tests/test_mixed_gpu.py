@@ -1,7 +1,6 @@
 """GPU parity of mixed batches (single-row decode requests and multi-row prefill
 requests in one call: one persistent launch whose first CTAs run the tcgen05
 prefill half and the rest the CUDA-core decode workers) against the fp64 oracle."""
-import numpy as np
 import pytest
 import torch
 
@@ -62,33 +61,78 @@ def test_mixed_page_sizes_and_cap(page_size, group, cap):
     assert info.prefill_ctas >= 1 and info.decode_ctas >= 1
 
 
-def test_mixed_is_one_attention_launch(tmp_path):
-    """The run call launches the mixed kernel once, then the two merges; neither the
-    standalone decode nor the standalone prefill kernel runs."""
-    import json
-    from torch.profiler import ProfilerActivity, profile
+def _kernel_nodes(fn, stream):
+    """Capture fn's launches on `stream` into a CUDA graph through the driver API (the
+    kernels come from this library's own runtime, so no profiler is involved) and
+    return (grid, block) of every kernel node."""
+    import ctypes
+    cu = ctypes.CDLL("libcuda.so.1")
+    vp = ctypes.c_void_p
+    h, graph = vp(stream.cuda_stream), vp()
+    assert cu.cuStreamBeginCapture_v2(h, 2) == 0  # CU_STREAM_CAPTURE_MODE_RELAXED
+    try:
+        fn()
+    finally:
+        assert cu.cuStreamEndCapture(h, ctypes.byref(graph)) == 0
+    try:
+        n = ctypes.c_size_t(0)
+        assert cu.cuGraphGetNodes(graph, None, ctypes.byref(n)) == 0
+        nodes = (vp * max(n.value, 1))()
+        assert cu.cuGraphGetNodes(graph, nodes, ctypes.byref(n)) == 0
+        out = []
+        for i in range(n.value):
+            t = ctypes.c_int(-1)
+            assert cu.cuGraphNodeGetType(vp(nodes[i]), ctypes.byref(t)) == 0
+            if t.value == 0:  # CU_GRAPH_NODE_TYPE_KERNEL
+                par = (ctypes.c_uint32 * 32)()  # CUDA_KERNEL_NODE_PARAMS_v2: func, then grid and block
+                assert cu.cuGraphKernelNodeGetParams_v2(vp(nodes[i]), par) == 0
+                out.append((tuple(par[2:5]), tuple(par[5:8])))
+        return out
+    finally:
+        cu.cuGraphDestroy(graph)
+
+
+def test_mixed_is_one_attention_launch():
+    """The run call launches the mixed kernel once (every SM, 384 threads), then the two
+    halves' merges; neither the decode kernel (256 threads) nor the prefill kernel (352)
+    runs.  The two halves run as their own plans give the four launches that the mixed
+    kernel replaces, which shows the count sees every kernel."""
     b = small_mixed(40)
-    db = runner.DeviceBatch.from_host(b)
-    plan = runner.make_plan(b, api.PLAN_MIXED)
-    runner.plan_batch(plan, b)
-    runner.mixed(db, plan)
-    marker = torch.ones(1, device="cuda")
-    torch.cuda.synchronize()
-    with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
-        marker.add_(1)  # a torch kernel: shows that kernel records reached the trace
-        runner.mixed(db, plan)
-        torch.cuda.synchronize()
-    # The exported trace lists every kernel record, also those no torch op launched.
-    path = tmp_path / "trace.json"
-    prof.export_chrome_trace(str(path))
-    names = [e.get("name", "") for e in json.loads(path.read_text()).get("traceEvents", [])
-             if e.get("cat") == "kernel"]
-    if not names:
-        pytest.skip("the profiler recorded no kernels on this machine")
-    ours = [n for n in names if "pkv" in n]
-    assert sum("mixed_kernel" in n for n in ours) == 1, ours
-    assert not any("decode_kernel" in n or "prefill_kernel" in n for n in ours), ours
-    assert sum("merge_kernel" in n for n in ours) == 2, ours
+    dec = [r for r in range(b.batch) if b.qo_lens[r] == 1]
+    pre = [r for r in range(b.batch) if b.qo_lens[r] > 1]
+    bd, bp = W.sub_batch(b, dec), W.sub_batch(b, pre)
+    kv = b.kv_data.cuda()
+    db, dd, dp = (runner.DeviceBatch.from_host(x, kv_data=kv) for x in (b, bd, bp))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    s = torch.cuda.Stream()
+    plans, outs = [], []
+    with torch.cuda.stream(s):
+        for x, kind in ((b, api.PLAN_MIXED), (bd, api.PLAN_DECODE), (bp, api.PLAN_PREFILL)):
+            p = runner.make_plan(x, kind)
+            runner.plan_batch(p, x, stream=s)
+            plans.append(p)
+        for x in (db, dd, dp):
+            outs.append((torch.empty_like(x.q), torch.empty(x.q.shape[:2], dtype=torch.float32, device="cuda")))
+    s.synchronize()
+
+    def run(i, x):
+        plans[i].run(x.q, kv, x.kv_indices, x.kv_indptr, x.kv_last_page_len, *outs[i], qo_indptr=x.qo_indptr,
+                     stream=s)
+
+    nodes = _kernel_nodes(lambda: run(0, db), s)
+    assert len(nodes) == 3, nodes
+    assert [n for n in nodes if n[1] == (384, 1, 1)] == [((sms, 1, 1), (384, 1, 1))], nodes
+    assert not any(n[1][0] in (352,) for n in nodes), nodes
+    halves = _kernel_nodes(lambda: (run(1, dd), run(2, dp)), s)
+    assert len(halves) == 4, halves
+    assert sum(n[1] == (352, 1, 1) for n in halves) == 1, halves
+    assert not any(n[1] == (384, 1, 1) for n in halves), halves
+    # the captured mixed launch still gives the oracle's result when run
+    run(0, db)
+    s.synchronize()
+    assert plans[0].device_error() == 0
+    ref_o, ref_lse = oracle.attention_of(b)
+    assert_matches_oracle(outs[0][0], outs[0][1], ref_o, ref_lse, b.dtype, "mixed after capture")
 
 
 @pytest.mark.parametrize("n_decode,n_prefill", [(7, 0), (0, 4)])
@@ -106,14 +150,8 @@ def test_mixed_with_softcap_and_split_decode():
 
 def test_mixed_full_size():
     """60 decode requests (kv U[512, 4096]) and 4 prompt chunks (qo U[256, 2048] after
-    a prefix U[0, 1024]), 32 q / 8 kv heads: every decode row and 2000 prefill rows."""
-    b = W.mixed_batch(seed=1007, poison=True)
-    dec_rows = [int(b.qo_indptr[r]) for r in range(b.batch) if b.qo_lens[r] == 1]
-    pre_rows = [i for r in range(b.batch) if b.qo_lens[r] > 1
-                for i in range(int(b.qo_indptr[r]), int(b.qo_indptr[r + 1]))]
-    rng = np.random.default_rng(0)
-    rows = np.sort(np.concatenate([dec_rows, rng.choice(pre_rows, size=2000, replace=False)]))
-    mixed_vs_oracle(b, "mixed full size", rows=rows)
+    a prefix U[0, 1024]), 32 q / 8 kv heads: every row of both halves."""
+    mixed_vs_oracle(W.mixed_batch(seed=1007, poison=True), "mixed full size")
 
 
 def test_mixed_graph_replay_after_replanning():
