@@ -76,13 +76,13 @@ cudaError_t scratch_address(int device, void** out) {
     return !ctx || f->get_id(ctx, id) == CUDA_SUCCESS;
   };
   unsigned long long id = 0;
-  if (!current_id(&id)) return cudaErrorInvalidContext;
+  if (!current_id(&id)) return cudaErrorDeviceUninitialized;
   std::lock_guard<std::mutex> lock(mu);
   if (id == 0 || !addr[device] || ctx_of[device] != id) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (!current_id(&id) || id == 0) return cudaErrorInvalidContext;
+    if (!current_id(&id) || id == 0) return cudaErrorDeviceUninitialized;
     addr[device] = p;
     ctx_of[device] = id;
   }
