@@ -323,7 +323,7 @@ def host_plan_entry(b):
                     "the timed step's pipelined plan overlaps it with the GPU"}
 
 
-def decode_measure(b, steps, warmup, peaks, profile_name=None, split_kv=True):
+def decode_measure(b, steps, warmup, peaks, profile_name=None, split_kv=True, kernel="decode_kernel"):
     """Step time and main-kernel time of plan + decode + merge on one workload
     (split_kv False: each page list whole on one worker, nothing to merge)."""
     import torch
@@ -356,7 +356,7 @@ def decode_measure(b, steps, warmup, peaks, profile_name=None, split_kv=True):
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     res["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                       "peak_source": peaks["source"], "kernel": "decode_kernel"}
+                       "peak_source": peaks["source"], "kernel": kernel}
     del db, o, lse
     return res
 
@@ -873,6 +873,13 @@ def run_own(args):
             secondary["decode_page_size_1"] = {"value": round(r1["value"], 1), "unit": "GB/s",
                                                "ms_per_step": round(r1["ms_per_step"], 4), "roofline": r1["roofline"]}
             del col
+            g8 = W.group8_decode(seed=1008)
+            r8 = decode_measure(g8, max(20, args.steps // 10), 5, peaks,
+                                kernel="prefill_kernel (group-8 decode on the tensor cores)")
+            secondary["decode_group8"] = {"value": round(r8["value"], 1), "unit": "GB/s",
+                                          "ms_per_step": round(r8["ms_per_step"], 4), "roofline": r8["roofline"],
+                                          "workload": "64 q / 8 kv heads, head_dim 128, Llama-3-8B lengths"}
+            del g8
             secondary["tiny_decode"] = tiny_measure(peaks)
             secondary["prefill"] = prefill_measure(peaks)
             secondary["cascade"] = cascade_measure(peaks)

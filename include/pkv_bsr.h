@@ -226,8 +226,11 @@ pkv_status pkv_plan_set_pipelined(pkv_plan* plan, int on);
  * against, in which one long request rests on one warp per kv head.  Ties go to
  * the earlier list, then to the worker of lower rank, rank r being warp r / C of
  * CTA r % C over the plan's C CTAs (equal loads spread over the SMs first).
- * Takes effect at the next plan step; the run call is unchanged.
- * Errors: PKV_ERR_INVALID_ARG (NULL, or not a plan of kind DECODE).
+ * Takes effect at the next plan step; the run call is unchanged.  The switch is
+ * the CUDA-core decode schedule's: a decode plan on the tensor-core path (see
+ * pkv_batch_decode_paged) refuses on = 0.
+ * Errors: PKV_ERR_INVALID_ARG (NULL, or not a plan of kind DECODE),
+ * PKV_ERR_UNSUPPORTED (on = 0 for a tensor-core decode plan).
  */
 pkv_status pkv_plan_set_split_kv(pkv_plan* plan, int on);
 
@@ -245,6 +248,15 @@ pkv_status pkv_plan_set_split_kv(pkv_plan* plan, int on);
  * plan: with page_size 1 a captured graph can be replayed after re-planning a
  * batch over the same kv_data buffer and pool size (page_size 1 with more than
  * 2^31 (page, K|V, kv head) rows in the pool is refused with PKV_ERR_UNSUPPORTED).
+ * Tensor-core path: with 8 query heads per kv head, head_dim 128 and pages of 8
+ * rows or more, the plan makes prefill work tiles of one query row per request
+ * (greptalks summary, "Head Group Packing": the 8 heads of a group form the
+ * rows of one 128-row tile; fdeinterviews summary, "Customizable attention": a
+ * query tile size matched to the batch) and this call runs the tcgen05 prefill
+ * kernel and its merge on them, causal mask off.  There a group-8 decode worker
+ * on the CUDA cores is compute-bound.  The device kv_indptr is not re-checked
+ * on that path, and dev_ws is sized for prefill tables and 128-row partial
+ * states (pkv_plan_workspace_bytes reports it).
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  */
 pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const void* kv_data,
@@ -326,6 +338,9 @@ pkv_status pkv_batch_prefill_paged_masked(const pkv_plan* plan, const void* q, c
  *    context was made anew (after cudaDeviceReset, say); make such a call
  *    before any stream capture.
  *  - The device error word lives in the static array and is not reported.
+ *  - Decode plans on the tensor-core path (8 query heads per kv head at
+ *    head_dim 128, see pkv_batch_decode_paged) are refused with
+ *    PKV_ERR_UNSUPPORTED: their prefill-sized partial states do not fit.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_WORKSPACE, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  */
 pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const void* host_tables,
@@ -340,7 +355,9 @@ pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const void* host
  * PKV_PLAN_MIXED.  The plan routes each request by its query-tile size: one
  * row to the CUDA-core decode path (split-KV over warp workers), several rows
  * to the tcgen05 prefill path (128-row tiles), and splits the SMs between the
- * two halves in proportion to their estimated times.  The run call makes one
+ * two halves in proportion to their estimated times.  Where single rows run on
+ * the tensor cores (8 query heads per kv head, head_dim 128, pages of 8 rows or
+ * more; see pkv_batch_decode_paged) every request goes to the prefill half.  The run call makes one
  * persistent launch on every SM: the CTAs below the split run the prefill
  * half, the others the decode workers; then each half's merge of split
  * sequences follows on `stream` ("FlashInfer" guide, "Prefill-Decode Mixing";

@@ -134,6 +134,22 @@ pkv_status launch_status(cudaError_t e) {
   return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
 }
 
+// The prefill kernel and its merge over a plan's prefill tables (a prefill plan,
+// or a decode plan whose work runs on the tensor cores).
+cudaError_t launch_prefill_tables(const pkv_plan* plan, const pkv::PrefillArgs& a, cudaStream_t s) {
+  const pkv_params& p = plan->p;
+  const bool cap = p.logits_cap > 0.f;
+  cudaError_t e = wait_tables(plan, s);
+  if (plan->time_start && e == cudaSuccess) cudaEventRecord(plan->time_start, s);
+  if (e == cudaSuccess)
+    e = pkv::launch_prefill(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, plan->total_q,
+                            plan->num_pages, s);
+  if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
+  if (e == cudaSuccess) e = pkv::launch_prefill_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
+  if (e == cudaSuccess) e = release_tables(plan, s);
+  return e;
+}
+
 }  // namespace
 
 extern "C" {
@@ -165,10 +181,13 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
     return PKV_ERR_INVALID_ARG;
   pkv_status st = check_device(plan);
   if (st != PKV_OK) return st;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (plan->exec_prefill)  // one query row per request on the tensor cores
+    return launch_status(launch_prefill_tables(
+        plan, prefill_args(plan, dev_ws, q, kv_data, kv_indices_d, nullptr, 0, o, lse), s));
   const pkv_params& p = plan->p;
   const bool cap = p.logits_cap > 0.f;
   const pkv::DecodeArgs a = decode_args(plan, dev_ws, q, kv_data, kv_indices_d, kv_indptr_d, o, lse);
-  auto s = static_cast<cudaStream_t>(stream);
   cudaError_t e = wait_tables(plan, s);
   if (plan->time_start && e == cudaSuccess) cudaEventRecord(plan->time_start, s);
   if (e == cudaSuccess)
@@ -196,20 +215,8 @@ static pkv_status prefill_run(const pkv_plan* plan, const void* q, const int32_t
     return PKV_ERR_INVALID_ARG;
   pkv_status st = check_device(plan);
   if (st != PKV_OK) return st;
-  const pkv_params& p = plan->p;
-  const bool cap = p.logits_cap > 0.f;
   const pkv::PrefillArgs a = prefill_args(plan, dev_ws, q, kv_data, kv_indices_d, mask, mask_bytes, o, lse);
-  auto s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = wait_tables(plan, s);
-  if (plan->time_start && e == cudaSuccess) cudaEventRecord(plan->time_start, s);
-  if (e == cudaSuccess)
-    e = pkv::launch_prefill(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, plan->total_q,
-                            plan->num_pages, s);
-  if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
-  if (e == cudaSuccess)
-    e = pkv::launch_prefill_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
-  if (e == cudaSuccess) e = release_tables(plan, s);
-  return launch_status(e);
+  return launch_status(launch_prefill_tables(plan, a, static_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,

@@ -101,6 +101,9 @@ extern "C" pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const
                                                      void* stream) {
   if (!plan || plan->kind != PKV_PLAN_DECODE || !plan->planned || plan->device < 0 || plan->pipelined)
     return PKV_ERR_INVALID_ARG;
+  // Tensor-core decode plans keep prefill tables and 128-row partial states, far
+  // more than the static array holds.
+  if (plan->exec_prefill) return PKV_ERR_UNSUPPORTED;
   if (!host_tables || host_tables_bytes < plan->host_bytes) return PKV_ERR_INVALID_ARG;
   if (!q || !kv_data || !kv_indices_d || !kv_indptr_d || !kv_last_page_len_d || !o) return PKV_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv_data, 16) || !aligned(o, 16) || !aligned(kv_indices_d, 4) ||

@@ -48,6 +48,11 @@ struct pkv_plan {
   int rows_per_slot = 0;
   int merge_grid = 0;
   bool split_kv = true;     // decode: cut page lists into equal runs (pkv_plan_set_split_kv)
+  // Decode plan whose batches run on the tcgen05 prefill kernel, one query row per
+  // request (group 8 at head_dim 128, pages of 8 rows or more): its tables are
+  // prefill tables, planned over row_indptr = 0, 1, ..., batch.
+  bool exec_prefill = false;
+  std::vector<int32_t> row_indptr;
   pkv::WorkspaceLayout L{};
   size_t host_bytes = 0;
   // Last computed plan.

@@ -50,6 +50,18 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 bool is_pow2_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
+// Single-row (decode) work that runs on the tcgen05 prefill kernel instead of the
+// CUDA-core decode kernel.  With a group of 8 query heads per kv head the decode
+// worker does 8 dot products and 8 P V accumulations per key on the CUDA cores
+// and turns compute-bound (3.7 TB/s on the Llama-3-8B lengths, head_dim 128); the
+// tensor cores take one request's 8 rows as a 128-row tile (4.95 TB/s).  Pages of
+// fewer than 8 rows keep the decode kernel's tensor gathers.
+bool decode_on_tensor_cores(const pkv_params* p) {
+  const int g = p->num_qo_heads / p->num_kv_heads;
+  return g == 8 && p->head_dim == 128 && p->page_size >= 8 &&
+         pkv::prefill_supported(p->head_dim, g, p->dtype, p->page_size);
+}
+
 pkv_status check_params(int kind, const pkv_params* p, const pkv_limits* lim) {
   if (!p || !lim) return PKV_ERR_INVALID_ARG;
   if (kind != PKV_PLAN_DECODE && kind != PKV_PLAN_PREFILL && kind != PKV_PLAN_MIXED) return PKV_ERR_INVALID_ARG;
@@ -70,7 +82,7 @@ pkv_status check_params(int kind, const pkv_params* p, const pkv_limits* lim) {
 
 void set_layout(pkv_plan* pl) {
   pkv::WorkspaceLayout& L = pl->L;
-  const bool dec = pl->kind == PKV_PLAN_DECODE;
+  const bool dec = pl->kind == PKV_PLAN_DECODE && !pl->exec_prefill;
   const size_t work_bytes = dec ? sizeof(DecodeSeg) : sizeof(PrefillTile);
   const size_t merge_bytes = dec ? sizeof(MergeItem) : sizeof(PrefillMerge);
   L.header = 0;
@@ -84,8 +96,11 @@ void set_layout(pkv_plan* pl) {
   L.total = L.alt + L.tables_end;
 }
 
+// route_decode: a decode plan may run on the tensor cores (decode_on_tensor_cores);
+// the decode half of a mixed plan never does (the mixed kernel's decode CTAs read
+// decode tables).
 pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const pkv_limits* limits,
-                     int device, int num_sms) {
+                     int device, int num_sms, bool route_decode = true) {
   if (!out) return PKV_ERR_INVALID_ARG;
   *out = nullptr;
   pkv_status st = check_params(kind, params, limits);
@@ -104,7 +119,7 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
   const int64_t hkv = params->num_kv_heads;
   if (kind == PKV_PLAN_MIXED) {
     // Two plans of the same problem and limits; their workspaces are laid end to end.
-    pkv_status s1 = make_plan(&pl->sub_dec, PKV_PLAN_DECODE, params, limits, device, num_sms);
+    pkv_status s1 = make_plan(&pl->sub_dec, PKV_PLAN_DECODE, params, limits, device, num_sms, false);
     pkv_status s2 = s1 == PKV_OK ? make_plan(&pl->sub_pre, PKV_PLAN_PREFILL, params, limits, device, num_sms) : s1;
     if (s2 != PKV_OK) {
       delete pl->sub_dec;
@@ -123,7 +138,8 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
     *out = pl;
     return PKV_OK;
   }
-  if (kind == PKV_PLAN_DECODE) {
+  pl->exec_prefill = kind == PKV_PLAN_DECODE && route_decode && decode_on_tensor_cores(params);
+  if (kind == PKV_PLAN_DECODE && !pl->exec_prefill) {
     pl->grid_ctas = num_sms;
     pl->workers = num_sms * pkv::kDecodeWarps;
     // Each worker's run cuts at most two page lists, and every list adds at
@@ -142,7 +158,9 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
     const int mp = pkv::kPrefillRows / pl->group;  // query positions per tile
     pl->grid_ctas = num_sms;
     pl->workers = num_sms;
-    const int64_t tiles = (ceil_div(limits->max_total_q, mp) + limits->max_batch) * hkv;
+    // A decode plan on the tensor cores has one query row per request.
+    const int64_t max_rows = pl->exec_prefill ? limits->max_batch : limits->max_total_q;
+    const int64_t tiles = (ceil_div(max_rows, mp) + limits->max_batch) * hkv;
     // Splitting only touches tiles costing more than total / CTAs (fewer than
     // CTAs of them), and adds at most CTAs chunks in total.
     const int64_t max_work = tiles + 2 * static_cast<int64_t>(num_sms) + 1;
@@ -706,13 +724,17 @@ pkv_status compute_mixed(pkv_plan* pl, int batch, const int32_t* qo_indptr, cons
                          const int32_t* kv_last, int64_t num_pages, uint8_t* host) {
   const int P = pl->p.page_size;
   const int S = pl->num_sms;
+  // Where single-row work runs on the tensor cores, every request goes to the
+  // prefill half and the decode half is empty.
+  const bool rows_to_prefill = decode_on_tensor_cores(&pl->p);
   int64_t dec_pages = 0;  // (request, kv head) pages of the decode half
   bool any_pre = false, any_dec = false;
   for (int b = 0; b < batch; ++b) {
     const int qo = qo_indptr[b + 1] - qo_indptr[b];
-    any_dec |= qo == 1;
-    any_pre |= qo > 1;
-    if (qo == 1) dec_pages += static_cast<int64_t>(kv_indptr[b + 1] - kv_indptr[b]) * pl->p.num_kv_heads;
+    const bool single = qo == 1 && !rows_to_prefill;
+    any_dec |= single;
+    any_pre |= qo >= 1 && !single;
+    if (single) dec_pages += static_cast<int64_t>(kv_indptr[b + 1] - kv_indptr[b]) * pl->p.num_kv_heads;
   }
   int kp = 0;
   if (any_pre && !any_dec) {
@@ -775,10 +797,11 @@ pkv_status compute_mixed(pkv_plan* pl, int batch, const int32_t* qo_indptr, cons
   pl->decode_ctas = any_dec ? S - kp : 0;
   pkv_plan* d = pl->sub_dec;
   pkv_plan* p = pl->sub_pre;
-  pkv_status st = compute_decode(d, batch, kv_indptr, kv_last, host + pl->dec_host_off, qo_indptr,
-                                 std::max(pl->decode_ctas, 1) * pkv::kDecodeWarps);
+  pkv_status st = compute_decode(d, rows_to_prefill ? 0 : batch, kv_indptr, kv_last, host + pl->dec_host_off,
+                                 qo_indptr, std::max(pl->decode_ctas, 1) * pkv::kDecodeWarps);
   if (st != PKV_OK) return st;
-  st = compute_prefill(p, batch, qo_indptr, kv_indptr, kv_last, host + pl->pre_host_off, std::max(kp, 1), true);
+  st = compute_prefill(p, batch, qo_indptr, kv_indptr, kv_last, host + pl->pre_host_off, std::max(kp, 1),
+                       !rows_to_prefill);
   if (st != PKV_OK) return st;
   // The mixed kernel's CTAs below this serve the prefill half, the rest the decode half.
   reinterpret_cast<PlanHeader*>(host + pl->dec_host_off + d->L.header)->cta_offset = any_dec ? kp : S;
@@ -887,6 +910,15 @@ pkv_status pkv_plan_compute(pkv_plan* plan, int batch, const int32_t* qo_indptr_
   }
   if (plan->kind == PKV_PLAN_MIXED) {
     st = compute_mixed(plan, batch, qo_indptr_h, kv_indptr_h, kv_last_page_len_h, num_pages, host);
+  } else if (plan->kind == PKV_PLAN_DECODE && plan->exec_prefill) {
+    // One query row per request: qo_indptr = 0, 1, ..., batch.
+    std::vector<int32_t>& rows = plan->row_indptr;
+    if (rows.size() < static_cast<size_t>(batch) + 1) {
+      const size_t from = rows.size();
+      rows.resize(static_cast<size_t>(batch) + 1);
+      for (size_t i = from; i < rows.size(); ++i) rows[i] = static_cast<int32_t>(i);
+    }
+    st = compute_prefill(plan, batch, rows.data(), kv_indptr_h, kv_last_page_len_h, host);
   } else if (plan->kind == PKV_PLAN_DECODE) {
     st = compute_decode(plan, batch, kv_indptr_h, kv_last_page_len_h, host);
   } else {
@@ -976,6 +1008,7 @@ pkv_status pkv_plan_set_pipelined(pkv_plan* plan, int on) {
 
 pkv_status pkv_plan_set_split_kv(pkv_plan* plan, int on) {
   if (!plan || plan->kind != PKV_PLAN_DECODE) return PKV_ERR_INVALID_ARG;
+  if (plan->exec_prefill && !on) return PKV_ERR_UNSUPPORTED;  // the switch is the CUDA-core decode schedule's
   plan->split_kv = on != 0;
   return PKV_OK;
 }

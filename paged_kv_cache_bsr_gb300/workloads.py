@@ -33,6 +33,7 @@ __all__ = [
     "make_paged_batch",
     "tiny_decode",
     "llama3_decode",
+    "group8_decode",
     "skewed_decode",
     "ragged_prefill",
     "cascade_decode",
@@ -264,6 +265,17 @@ def llama3_decode(seed: int = 1001, batch: int = 64, poison: bool = False,
     return make_paged_batch(qo_lens=[1] * batch, kv_lens=kv_lens, num_qo_heads=32, num_kv_heads=8,
                             head_dim=128, page_size=page_size, dtype=torch.bfloat16, seed=seed + 1,
                             poison=poison, identity_pages=identity_pages, name="llama3_8b_decode")
+
+
+def group8_decode(seed: int = 1008, batch: int = 64, poison: bool = False) -> PagedBatch:
+    """Batch decode with a group of 8: 64 q / 8 kv heads (the GQA shape of 70B-class
+    models), head_dim 128, page 16, bf16, kv_len ~ U[512, 4096] as in the
+    Llama-3-8B-shaped batch, pool = exactly the pages used, randomly permuted."""
+    gen = _gen(seed)
+    kv_lens = _uniform_ints(512, 4096, batch, gen)
+    return make_paged_batch(qo_lens=[1] * batch, kv_lens=kv_lens, num_qo_heads=64, num_kv_heads=8,
+                            head_dim=128, page_size=16, dtype=torch.bfloat16, seed=seed + 1,
+                            poison=poison, name="group8_decode")
 
 
 def skewed_decode(seed: int = 1002, long_len: int = 131072, short_len: int = 1024,

@@ -758,3 +758,52 @@ def test_prefill_plan_balances_zipf_prompt_lengths(lib, s):
     biggest = max(max(1, -(-(ke - kb) // 128)) + 1 for _, _, _, _, _, kb, ke, _ in work)
     assert info.max_cost <= -(-info.total_cost // info.active_workers) + biggest
     api.plan_destroy(h)
+
+
+# --------------------------------------------------------------------------- group-8 decode on the tensor cores
+def test_group8_decode_plans_hold_prefill_tiles_of_one_row(lib):
+    """A decode plan with 8 query heads per kv head at head_dim 128 (pages of 8 rows or
+    more) plans its batch as prefill tiles of one query row per request: every
+    (request, kv head) key range is covered exactly once, on at most one CTA each
+    unless the plan cut it into chunks (then with partial slots)."""
+    rng = np.random.default_rng(11)
+    kv = [int(x) for x in rng.integers(512, 4097, size=64)]
+    b = table_batch(kv, hq=64, hkv=8)
+    h, ws = host_plan(b, api.PLAN_DECODE)
+    compute(h, ws, b)
+    rows = api.plan_get_work(h).tolist()
+    cover = {}
+    for cta, req, kvh, pos0, npos, k0, k1, slot in rows:
+        assert 0 <= cta < 152 and npos == 1 and pos0 == 0
+        cover.setdefault((req, kvh), []).append((k0, k1, slot))
+    assert sorted(cover) == [(r, k) for r in range(64) for k in range(8)]
+    for (req, kvh), ranges in cover.items():
+        ranges.sort()
+        assert ranges[0][0] == 0 and ranges[-1][1] == kv[req]
+        assert all(a[1] == c[0] for a, c in zip(ranges, ranges[1:]))
+        assert (len(ranges) == 1) == (ranges[0][2] == -1)
+    with pytest.raises(api.PkvError) as e:                 # the split switch is the CUDA-core schedule's
+        api.plan_set_split_kv(h, False)
+    assert e.value.status == -3
+    api.plan_destroy(h)
+
+
+@pytest.mark.parametrize("hd,P", [(64, 16), (128, 1), (128, 4)])
+def test_group8_decode_keeps_the_decode_kernel_elsewhere(lib, hd, P):
+    """head_dim 64 (the prefill kernel is head_dim 128 only) and pages of fewer than 8
+    rows keep decode segments: one row per (worker, request, kv head, page run)."""
+    b = table_batch([300, 17, 900], hq=64, hkv=8, d=hd, page_size=P)
+    h, ws = host_plan(b, api.PLAN_DECODE)
+    compute(h, ws, b)
+    check_decode_plan(h, b)
+    api.plan_set_split_kv(h, False)
+    api.plan_destroy(h)
+
+
+def test_group8_mixed_plan_sends_single_rows_to_the_prefill_half(lib):
+    b = W.mixed_batch(seed=5, n_decode=9, n_prefill=2, num_qo_heads=64, num_kv_heads=8)
+    h, ws = host_plan(b, api.PLAN_MIXED)
+    compute(h, ws, b)
+    info = api.plan_get_info(h)
+    assert info.prefill_ctas == 152 and info.decode_ctas == 0
+    api.plan_destroy(h)

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from paged_kv_cache_bsr_gb300 import api, runner, workloads as W
-from gpu_util import LSE_TOL, TOL, assert_matches_oracle
+from gpu_util import LSE_TOL, TOL, assert_matches_oracle, kernel_nodes
 
 pytestmark = pytest.mark.gpu
 
@@ -240,6 +240,50 @@ def test_cuda_graph_replay_after_replanning():
         ref_o, ref_lse = oracle.attention_of(b)
         assert_matches_oracle(o_buf, lse_buf, ref_o, ref_lse, torch.bfloat16, "graph replay")
     assert plan.device_error() == 0
+
+
+# --------------------------------------------------------------------------- group 8 on the tensor cores
+@pytest.mark.parametrize("dtype,cap", [(torch.bfloat16, 0.0), (torch.float16, 30.0)])
+def test_group8_decode_runs_on_the_tensor_cores(dtype, cap):
+    """64 q / 8 kv heads at head_dim 128: the decode plan's run launches the tcgen05
+    prefill kernel with one query row per request (and its merge), not the CUDA-core
+    decode kernel.  A 60000-token request is cut into key chunks whose partial states
+    are merged; an empty request gives 0 and -inf; soft-capped and not."""
+    b = W.make_paged_batch(qo_lens=[1] * 6, kv_lens=[60000, 1, 17, 0, 700, 4100], num_qo_heads=64,
+                           num_kv_heads=8, head_dim=128, page_size=16, dtype=dtype, seed=88 + int(cap),
+                           logits_cap=cap, poison=True)
+    db = runner.DeviceBatch.from_host(b)
+    plan = runner.make_plan(b, api.PLAN_DECODE)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        runner.plan_batch(plan, b, stream=s)
+        o = torch.empty_like(db.q)
+        lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device="cuda")
+    s.synchronize()
+
+    def run():
+        plan.run(db.q, db.kv_data, db.kv_indices, db.kv_indptr, db.kv_last_page_len, o, lse, stream=s)
+
+    names = [n for n, _, _ in kernel_nodes(run, s)]
+    assert len(names) == 2 and "prefill_kernel" in names[0] + names[1] and \
+        any("prefill_merge" in n for n in names), names
+    assert not any("decode_kernel" in n for n in names), names
+    run()
+    s.synchronize()
+    assert plan.device_error() == 0
+    assert plan.info().num_merge > 0  # the long request was cut into chunks
+    ref_o, ref_lse = oracle.attention_of(b)
+    assert_matches_oracle(o, lse, ref_o, ref_lse, dtype, f"group 8 cap {cap}")
+
+
+@pytest.mark.slow
+def test_group8_llama3_lengths_full_size():
+    """64 q / 8 kv heads on the Llama-3-8B lengths (batch 64, kv ~ U[512, 4096]),
+    through the tensor-core decode path: every output element."""
+    ref = W.llama3_decode(seed=1001)
+    b = W.make_paged_batch(qo_lens=[1] * 64, kv_lens=list(ref.kv_lens), num_qo_heads=64, num_kv_heads=8,
+                           head_dim=128, page_size=16, dtype=torch.bfloat16, seed=1011, poison=True)
+    decode_vs_oracle(b, "group 8 llama3 lengths")
 
 
 # --------------------------------------------------------------------------- device-side checks

@@ -93,3 +93,14 @@ def test_soft_capped_cascade():
     assert full.num_pages == 128 + len(sfx)          # the pool holds the prefix once
     assert full.kv_data.data_ptr() == prefix.kv_data.data_ptr() == suffix.kv_data.data_ptr()
     check_page_table(suffix, pool_pages=full.num_pages)
+
+
+def test_group8_decode():
+    """64 q / 8 kv heads on the Llama-3-8B decode lengths (the tensor-core decode bench)."""
+    b = W.group8_decode(seed=1008)
+    assert (b.batch, b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size) == (64, 64, 8, 128, 16)
+    assert b.dtype == torch.bfloat16 and b.is_decode
+    assert min(b.kv_lens) >= 512 and max(b.kv_lens) <= 4096
+    assert b.num_pages == int(b.kv_indptr[-1])
+    assert sorted(b.kv_indices.tolist()) == list(range(b.num_pages))
+
