@@ -65,9 +65,9 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
 
 
 def test_noalloc_refuses_plans_larger_than_its_scratch():
-    b = W.make_paged_batch(qo_lens=[1] * 2, kv_lens=[100, 200], num_qo_heads=64, num_kv_heads=8, head_dim=128,
+    b = W.make_paged_batch(qo_lens=[1] * 2, kv_lens=[100, 200], num_qo_heads=32, num_kv_heads=8, head_dim=128,
                            page_size=16, dtype=torch.bfloat16, seed=3)
-    plan = runner.make_plan(b, api.PLAN_DECODE, max_batch=4096, max_kv_pages=1 << 20)
+    plan = runner.make_plan(b, api.PLAN_DECODE, max_batch=65536, max_kv_pages=1 << 20)
     dev_bytes, _ = api.plan_workspace_bytes(plan.handle)
     assert dev_bytes > (8 << 20)
     host_tables = torch.empty_like(plan.host_ws)
@@ -79,3 +79,20 @@ def test_noalloc_refuses_plans_larger_than_its_scratch():
         api.batch_decode_paged_noalloc(plan.handle, host_tables, db.q, db.kv_data, db.kv_indices, db.kv_indptr,
                                        db.kv_last_page_len, o, None)
     assert e.value.status == -4
+
+
+def test_noalloc_refuses_tensor_core_decode_plans():
+    """8 query heads per kv head at head_dim 128 decode on the tensor cores, whose
+    prefill-sized partial states the static array cannot hold."""
+    b = W.make_paged_batch(qo_lens=[1] * 2, kv_lens=[100, 200], num_qo_heads=64, num_kv_heads=8, head_dim=128,
+                           page_size=16, dtype=torch.bfloat16, seed=3)
+    plan = runner.make_plan(b, api.PLAN_DECODE)
+    host_tables = torch.empty_like(plan.host_ws)
+    api.plan_compute(plan.handle, b.batch, None, b.kv_indptr, b.kv_indices, b.kv_last_page_len, b.num_pages,
+                     host_tables)
+    db = runner.DeviceBatch.from_host(b)
+    o = torch.empty_like(db.q)
+    with pytest.raises(api.PkvError) as e:
+        api.batch_decode_paged_noalloc(plan.handle, host_tables, db.q, db.kv_data, db.kv_indices, db.kv_indptr,
+                                       db.kv_last_page_len, o, None)
+    assert e.value.status == -3
