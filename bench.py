@@ -52,7 +52,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--only", choices=["prefill", "prefill1", "cascade", "multilevel", "mixed", "append", "tree", "skewed",
-                                      "tiny"], default=None,
+                                      "tiny", "oracle"], default=None,
                    help="time one secondary measurement alone (for profiling) and print it")
     return p.parse_args()
 
@@ -783,7 +783,60 @@ def mixed_measure(steps=50, warmup=5):
     return out
 
 
+def oracle_configs(seconds_per_config=8.0):
+    """The fp64 CPU oracle as it stands on each of the five workloads, on the host
+    cores: whole workloads (repeated until the time budget) where one pass is short,
+    else the ragged prefill's query rows taken in order until the budget; each rate in
+    the workload's own unit."""
+    import oracle
+    from paged_kv_cache_bsr_gb300 import workloads as W
+    oracle.build()
+    out = {"cores": oracle.num_threads()}
+
+    def kv_rate(b):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.attention_of(b)
+            reps += 1
+            if time.perf_counter() - t0 >= seconds_per_config:
+                break
+        dt = time.perf_counter() - t0
+        return {"GBps": round(b.kv_bytes() * reps / dt / 1e9, 4), "passes": reps, "s": round(dt, 2)}
+
+    t = W.tiny_decode(seed=1000)
+    t0 = time.perf_counter()
+    oracle.attention_of(t)
+    out["tiny_decode"] = {"us_per_call": round((time.perf_counter() - t0) * 1e6, 1)}
+    for name, b in (("llama3_8b_decode", W.llama3_decode(seed=1001)), ("skewed_decode", W.skewed_decode(seed=1002))):
+        out[name] = kv_rate(b)
+    p = W.ragged_prefill(seed=1003)
+    pairs_row = []
+    for qo, kv in zip(p.qo_lens, p.kv_lens):
+        pre = kv - qo
+        pairs_row += [pre + i + 1 for i in range(qo)]
+    done, t0 = 0, time.perf_counter()
+    step = 256
+    while time.perf_counter() - t0 < seconds_per_config and done < p.total_q:
+        rows = list(range(done, min(done + step, p.total_q)))
+        oracle.attention_of(p, rows=rows)
+        done = rows[-1] + 1
+    dt = time.perf_counter() - t0
+    flops = sum(pairs_row[:done]) * p.num_qo_heads * 4 * p.head_dim
+    out["ragged_causal_prefill"] = {"TFLOPs": round(flops / dt / 1e12, 5), "rows": done, "of": p.total_q,
+                                    "s": round(dt, 2)}
+    cb = W.cascade_decode(seed=1004)
+    t0 = time.perf_counter()
+    oracle.attention_of(cb.full)
+    dt = time.perf_counter() - t0
+    out["cascade_softcap_decode"] = {"us_per_call": round(dt * 1e6, 1),
+                                     "what": "non-cascade attention over every request's full page list"}
+    return out
+
+
 def run_only(args):
+    if args.only == "oracle":  # host cores only
+        print(json.dumps({"only": "oracle", **oracle_configs()}), flush=True)
+        return
     import torch
     from paged_kv_cache_bsr_gb300 import build, api, workloads as W
     torch.cuda.set_device(0)
