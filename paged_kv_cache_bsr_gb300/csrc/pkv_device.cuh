@@ -359,29 +359,6 @@ __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[12
       : "r"(taddr)
       : "memory");
 }
-// 64 consecutive fp32 columns of this thread's TMEM lane into r, without waiting:
-// the values are valid only after tmem_wait_ld64 on the same array.
-__device__ __forceinline__ void tmem_ld64_async(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "{\n\t.reg .b32 a1;\n\tadd.u32 a1, %64, 32;\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
-      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [a1];\n\t}"
-      : PKV_R32(r), PKV_R32((r + 32))
-      : "r"(taddr)
-      : "memory");
-}
-#define PKV_RW32(r) "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), \
-    "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),     \
-    "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]),  \
-    "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),  \
-    "+r"(r[31])
-// Wait for this thread's tensor-memory loads; r is named as read and written here so
-// that no use of the loaded values moves above the wait.
-__device__ __forceinline__ void tmem_wait_ld64(uint32_t* r) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : PKV_RW32(r), PKV_RW32((r + 32)) : : "memory");
-}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a 128B-swizzled operand tile whose
