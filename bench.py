@@ -668,9 +668,8 @@ def multilevel_measure(steps=50, warmup=5):
     def one_launch():
         mplan.run(dm.q, kv, dm.kv_indices, dm.kv_indptr, dm.kv_last_page_len, o_m, l_m, qo_indptr=dm.qo_indptr,
                   stream=s)
-        oo, ll = o_m[(nl - 1) * R:], l_m[(nl - 1) * R:]
-        for lvl in range(nl - 1):
-            api.merge_state(oo, ll, o_m[lvl * R:(lvl + 1) * R], l_m[lvl * R:(lvl + 1) * R], oo, ll, stream=s)
+        # every level's states in one n-state merge, into the last level's rows
+        api.merge_states(o_m, l_m, nl, o_m[(nl - 1) * R:], l_m[(nl - 1) * R:], stream=s)
 
     out = {"workload": "parallel_generation_3_level"}
     for name, fn in (("levels_serial", serial), ("levels_concurrent", concurrent), ("levels_one_mixed_launch",

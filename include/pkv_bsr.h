@@ -398,6 +398,26 @@ pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b,
                            int dtype, void* stream);
 
 /*
+ * merge_state over n states at once (the same composition as pkv_merge_state,
+ * applied to any number of states over disjoint key sets: FlashDecoding's
+ * partial outputs, or the levels of a shared-prefix tree, guide section 3):
+ * for each of n_rows * num_heads rows, m = max_k lse_k, w_k = exp(lse_k - m),
+ * o = sum_k w_k o_k / sum_k w_k, lse = m + ln(sum_k w_k); every lse_k = -inf
+ * gives o = 0, lse = -inf, and a state with lse = -inf adds nothing.
+ * State k of row r is row k * state_stride_rows + r of o_states ([rows,
+ * num_heads, head_dim] of `dtype`) and lse_states ([rows, num_heads] fp32), so
+ * n states of n_rows rows laid out one after another have state_stride_rows =
+ * n_rows.  o_out / lse_out ([n_rows, num_heads, ...]) may be the rows of one of
+ * the states (in place); lse_out may be NULL.  Launched as a programmatic
+ * dependent of the work before it on `stream`, like pkv_merge_state.
+ * Errors: PKV_ERR_INVALID_ARG (num_states < 1, state_stride_rows < n_rows, a
+ * null or misaligned pointer), PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+pkv_status pkv_merge_states(const void* o_states, const float* lse_states, int num_states,
+                            int64_t state_stride_rows, void* o_out, float* lse_out, int64_t n_rows,
+                            int num_heads, int head_dim, int dtype, void* stream);
+
+/*
  * Append new tokens' K and V into their pages, with the rotary position
  * embedding (RoPE) of the keys and of the queries fused into the same pass.
  * Serving appends each step's new tokens to the KV cache (greptalks MLSys

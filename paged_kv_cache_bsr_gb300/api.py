@@ -56,7 +56,8 @@ _lock = threading.Lock()
 EXPORTS = [
     "pkv_status_string", "pkv_version", "pkv_plan_create", "pkv_plan_create_host", "pkv_plan_destroy",
     "pkv_plan_workspace_bytes", "pkv_plan_compute", "pkv_plan_run", "pkv_plan_get_info", "pkv_plan_get_work",
-    "pkv_batch_decode_paged", "pkv_batch_prefill_paged", "pkv_merge_state", "pkv_get_device_error",
+    "pkv_batch_decode_paged", "pkv_batch_prefill_paged", "pkv_merge_state", "pkv_merge_states",
+    "pkv_get_device_error",
     "pkv_plan_set_timing_events", "pkv_batch_decode_paged_noalloc", "pkv_append_paged_kv",
     "pkv_batch_prefill_paged_masked", "pkv_batch_mixed_paged", "pkv_plan_set_pipelined",
     "pkv_plan_set_split_kv",
@@ -92,6 +93,7 @@ def load(path: Optional[str] = None):
             "pkv_batch_decode_paged": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_batch_prefill_paged": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "pkv_merge_state": (i32, [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp]),
+            "pkv_merge_states": (i32, [vp, vp, i32, i64, vp, vp, i64, i32, i32, i32, vp]),
             "pkv_get_device_error": (i32, [vp, vp, ctypes.POINTER(i32), i32, vp]),
             "pkv_plan_set_timing_events": (i32, [vp, vp, vp]),
             "pkv_batch_decode_paged_noalloc": (i32, [vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]),
@@ -270,6 +272,19 @@ def merge_state(o_a, lse_a, o_b, lse_b, o_out, lse_out=None, stream=None) -> Non
     n, hh, d = o_a.shape
     _check(load().pkv_merge_state(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o_out), _ptr(lse_out),
                                   n, hh, d, dtype_code(o_a.dtype), _stream(stream)), "pkv_merge_state")
+
+
+def merge_states(o_states, lse_states, num_states: int, o_out, lse_out=None, stream=None) -> None:
+    """merge_state over ``num_states`` states laid out one after another: o_states is
+    [num_states * n_rows, num_heads, head_dim] (fp16/bf16/fp32) and lse_states
+    [num_states * n_rows, num_heads]; o_out [n_rows, num_heads, head_dim] may be the
+    rows of one of the states."""
+    if o_states.dim() != 3 or o_states.shape[0] % num_states:
+        raise ValueError("o_states must be [num_states * n_rows, num_heads, head_dim]")
+    rows, hh, d = o_states.shape
+    n = rows // num_states
+    _check(load().pkv_merge_states(_ptr(o_states), _ptr(lse_states), int(num_states), n, _ptr(o_out), _ptr(lse_out),
+                                   n, hh, d, dtype_code(o_states.dtype), _stream(stream)), "pkv_merge_states")
 
 
 def append_paged_kv(params: Params, append_indptr, kv_indptr, kv_indices, kv_last_page_len, k_new, v_new,

@@ -8,6 +8,7 @@
 // and replayed after plan_run has written a new plan into the same workspace.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdint.h>
 
 #include <mutex>
 #include <vector>
@@ -282,6 +283,28 @@ pkv_status pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b,
     return PKV_ERR_INVALID_ARG;
   cudaError_t e = pkv::launch_merge_state(o_a, lse_a, o_b, lse_b, o_out, lse_out, n_rows * num_heads, head_dim,
                                           dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_merge_states(const void* o_states, const float* lse_states, int num_states, int64_t state_stride_rows,
+                            void* o_out, float* lse_out, int64_t n_rows, int num_heads, int head_dim, int dtype,
+                            void* stream) {
+  if (n_rows < 0 || num_heads <= 0 || head_dim <= 0 || num_states < 1 || state_stride_rows < n_rows)
+    return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F16 && dtype != PKV_BF16 && dtype != PKV_F32) return PKV_ERR_UNSUPPORTED;
+  if (n_rows == 0) return PKV_OK;
+  if (!o_states || !lse_states || !o_out) return PKV_ERR_INVALID_ARG;
+  if (!aligned(o_states, 16) || !aligned(o_out, 16) || !aligned(lse_states, 4) || (lse_out && !aligned(lse_out, 4)))
+    return PKV_ERR_INVALID_ARG;
+  // Flat (row, head) indices and state offsets stay within int64.
+  if (state_stride_rows > INT64_MAX / num_heads / num_states) return PKV_ERR_INVALID_ARG;
+  cudaError_t e = pkv::launch_merge_states(o_states, lse_states, num_states, state_stride_rows * num_heads, o_out,
+                                           lse_out, n_rows * num_heads, head_dim, dtype,
+                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorInvalidValue ? PKV_ERR_UNSUPPORTED : PKV_ERR_CUDA;

@@ -1,4 +1,5 @@
-// merge.cu -- merge_state: log-sum-exp composition of two attention states.
+// merge.cu -- merge_state: log-sum-exp composition of two attention states, and
+// of n states laid out one after another (merge_states).
 //
 // Two states (o_a, lse_a), (o_b, lse_b) over disjoint key sets combine into
 // the state over their union ("FlashInfer" guide, section 3: cascade
@@ -93,6 +94,55 @@ __global__ void __launch_bounds__(256) merge_state_kernel(const uint8_t* o_a, co
   }
 }
 
+// n states of each (row, head), state k at rows k * stride + r: m = max_k lse_k,
+// w_k = exp(lse_k - m), o = sum_k w_k o_k / sum_k w_k, lse = m + ln(sum_k w_k).
+// Each lane reads its chunk of every state before writing it, and every lane of a
+// (row, head) reads the lse values before any lane writes one, so the output may
+// be one of the states (in place).
+template <typename T>
+__global__ void __launch_bounds__(256) merge_states_kernel(const uint8_t* o_in, const float* lse_in, int n_states,
+                                                           int64_t stride, uint8_t* o_out, float* lse_out,
+                                                           int64_t rows, int chunks) {
+  using C = Chunk<T>;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int per_warp = 32 / chunks;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int chunk = lane % chunks;
+  for (int64_t base = warp_id * per_warp; base < rows; base += n_warps * per_warp) {
+    const int64_t r = base + lane / chunks;
+    const bool valid = r < rows;
+    float m = -INFINITY;
+    if (valid)
+      for (int k = 0; k < n_states; ++k) m = fmaxf(m, lse_in[k * stride + r]);
+    float out[C::N];
+#pragma unroll
+    for (int i = 0; i < C::N; ++i) out[i] = 0.f;
+    float s = 0.f;
+    if (valid && m != -INFINITY) {
+      for (int k = 0; k < n_states; ++k) {
+        const float w = expf(lse_in[k * stride + r] - m);
+        if (w > 0.f) {  // an empty state adds nothing (its o is not read)
+          float f[C::N];
+          C::load(o_in + ((k * stride + r) * chunks + chunk) * 16, f);
+#pragma unroll
+          for (int i = 0; i < C::N; ++i) out[i] = fmaf(w, f[i], out[i]);
+          s += w;
+        }
+      }
+    }
+    __syncwarp();  // every lane has read the states' lse values
+    if (valid) {
+      const float inv = s > 0.f ? 1.f / s : 0.f;
+#pragma unroll
+      for (int i = 0; i < C::N; ++i) out[i] *= inv;
+      C::store(o_out + (r * chunks + chunk) * 16, out);
+      if (chunk == 0 && lse_out) lse_out[r] = s > 0.f ? m + logf(s) : -INFINITY;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
@@ -130,6 +180,45 @@ cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* 
     case PKV_BF16:
       return cudaLaunchKernelEx(&cfg, merge_state_kernel<__nv_bfloat16>, a, lse_a, b, lse_b, o, lse_out, rows, chunks);
     case PKV_F16: return cudaLaunchKernelEx(&cfg, merge_state_kernel<__half>, a, lse_a, b, lse_b, o, lse_out, rows, chunks);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_merge_states(const void* o_in, const float* lse_in, int n_states, int64_t stride, void* o_out,
+                                float* lse_out, int64_t rows, int head_dim, int dtype, cudaStream_t stream) {
+  const int elem = dtype == PKV_F32 ? 4 : 2;
+  const int bytes = head_dim * elem;
+  if (bytes % 16) return cudaErrorInvalidValue;
+  const int chunks = bytes / 16;
+  if (chunks > 32 || (chunks & (chunks - 1))) return cudaErrorInvalidValue;
+  if (rows == 0) return cudaSuccess;
+  const int per_warp = 32 / chunks;
+  const int64_t warps = (rows + per_warp - 1) / per_warp;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (warps + 7) / 8;
+  const int grid = static_cast<int>(want < sms * 8 ? want : sms * 8);
+  auto in = static_cast<const uint8_t*>(o_in);
+  auto o = static_cast<uint8_t*>(o_out);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  switch (dtype) {
+    case PKV_F32:
+      return cudaLaunchKernelEx(&cfg, merge_states_kernel<float>, in, lse_in, n_states, stride, o, lse_out, rows, chunks);
+    case PKV_BF16:
+      return cudaLaunchKernelEx(&cfg, merge_states_kernel<__nv_bfloat16>, in, lse_in, n_states, stride, o, lse_out,
+                                rows, chunks);
+    case PKV_F16:
+      return cudaLaunchKernelEx(&cfg, merge_states_kernel<__half>, in, lse_in, n_states, stride, o, lse_out, rows,
+                                chunks);
     default: return cudaErrorInvalidValue;
   }
 }

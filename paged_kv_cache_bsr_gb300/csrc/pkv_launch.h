@@ -73,6 +73,10 @@ cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* 
                                const float* lse_b, void* o_out, float* lse_out, int64_t rows,
                                int head_dim, int dtype, cudaStream_t stream);
 
+// n-state merge_state: state k of flat row r at rows k * stride + r of o_in / lse_in.
+cudaError_t launch_merge_states(const void* o_in, const float* lse_in, int n_states, int64_t stride, void* o_out,
+                                float* lse_out, int64_t rows, int head_dim, int dtype, cudaStream_t stream);
+
 bool decode_supported(int head_dim, int group, int dtype);
 
 // Prefill work tile: kPrefillRows packed query rows (two 128-row UMMA tiles),

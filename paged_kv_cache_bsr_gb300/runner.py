@@ -124,14 +124,13 @@ def levels_mixed(db: DeviceBatch, n_levels: int, plan: Optional[api.Plan] = None
                  ) -> Tuple[torch.Tensor, torch.Tensor]:
     """A prefix tree (or a cascade, n_levels = 2) as one mixed launch: ``db`` holds
     ``workloads.levels_as_mixed(levels)``.  Multi-row nodes run on the prefill half
-    of the mixed kernel and single-row nodes on its decode half; merge_state then
-    folds every level's rows into the last level's."""
+    of the mixed kernel and single-row nodes on its decode half; one n-state
+    merge_state then folds every level's rows into the last level's."""
     o, lse = mixed(db, plan, stream)
     R = db.q.shape[0] // n_levels
     o_out, l_out = o[(n_levels - 1) * R:], lse[(n_levels - 1) * R:]
-    for lvl in range(n_levels - 1):
-        api.merge_state(o_out, l_out, o[lvl * R:(lvl + 1) * R], lse[lvl * R:(lvl + 1) * R], o_out, l_out,
-                        stream=stream)
+    # every level's states at once, into the last level's rows
+    api.merge_states(o, lse, n_levels, o_out, l_out, stream=stream)
     return o_out, l_out
 
 

@@ -679,6 +679,18 @@ def test_run_calls_refuse_bad_arguments_before_any_cuda_call(lib):
     assert ms(None, p16, p16, p16, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID
     assert ms(odd, p16, p16, p16, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID
     assert ms(p16, odd, p16, p16, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID
+    # merge_states: counts, stride, sizes, dtype, pointers, alignment
+    mn = L.pkv_merge_states
+    assert mn(p16, p16, 0, 8, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID      # no state
+    assert mn(p16, p16, 3, 7, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID      # states overlap
+    assert mn(p16, p16, 3, 8, p16, p16, -1, 4, 64, api.PKV_BF16, None) == INVALID
+    assert mn(p16, p16, 3, 8, p16, p16, 8, 0, 64, api.PKV_BF16, None) == INVALID
+    assert mn(p16, p16, 3, 8, p16, p16, 8, 4, 64, 7, None) == UNSUPPORTED
+    assert mn(None, None, 3, 0, None, None, 0, 4, 64, api.PKV_BF16, None) == api.PKV_OK  # nothing to do
+    assert mn(None, p16, 3, 8, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID
+    assert mn(odd, p16, 3, 8, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID
+    assert mn(p16, p16, 3, 8, odd, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID
+    assert mn(p16, p16, 3, 1 << 62, p16, p16, 8, 4, 64, api.PKV_BF16, None) == INVALID  # offsets past int64
     # append: params, theta, head_dim, dtype, counts, pointers, alignment
     ap = L.pkv_append_paged_kv
     good = api.make_params(8, 2, 128, 16, torch.bfloat16, 0.1)

@@ -336,6 +336,38 @@ def test_merge_state_matches_oracle(dtype, head_dim):
     assert torch.equal(oa, o_out) and torch.equal(la, l_out)
 
 
+@pytest.mark.parametrize("dtype,head_dim", [(torch.bfloat16, 128), (torch.float16, 64), (torch.float32, 128)])
+@pytest.mark.parametrize("n_states", [1, 2, 3, 5])
+def test_merge_states_matches_oracle(dtype, head_dim, n_states):
+    """n states laid out one after another, merged in one call, against the oracle's
+    n-way merge: rows where some states are empty (their o holds NaN and is not
+    read), rows where every state is empty (0, -inf), and the merge written in place
+    over the last state."""
+    n, h = 257, 8
+    gen = torch.Generator().manual_seed(head_dim + 10 * n_states)
+    o = torch.randn(n_states * n, h, head_dim, generator=gen).to(dtype)
+    lse = (torch.randn(n_states * n, h, generator=gen) * 4).float()
+    lse[0, :] = -math.inf                # state 0 of row 0 empty
+    o[0, :] = float("nan")
+    for k in range(n_states):            # row 1 empty in every state
+        lse[k * n + 1, :] = -math.inf
+    if n_states > 2:
+        lse[n + 2, 3] = -math.inf        # state 1 of row 2, head 3 empty
+        o[n + 2, 3] = float("nan")
+    ref_o, ref_l = oracle.merge_states([o[k * n:(k + 1) * n].double().numpy() for k in range(n_states)],
+                                       [lse[k * n:(k + 1) * n].double().numpy() for k in range(n_states)])
+    od, ld = o.cuda(), lse.cuda()
+    o_out = torch.empty(n, h, head_dim, dtype=dtype, device="cuda")
+    l_out = torch.empty(n, h, dtype=torch.float32, device="cuda")
+    api.merge_states(od, ld, n_states, o_out, l_out)
+    torch.cuda.synchronize()
+    assert_matches_oracle(o_out, l_out, ref_o, ref_l, dtype, f"merge_states n={n_states}")
+    last = slice((n_states - 1) * n, n_states * n)
+    api.merge_states(od, ld, n_states, od[last], ld[last])  # in place over the last state
+    torch.cuda.synchronize()
+    assert torch.equal(od[last], o_out) and torch.equal(ld[last], l_out)
+
+
 def test_split_decode_merged_with_merge_state_equals_unsplit():
     """FlashDecoding with the public merge: two halves of every page list, merged."""
     b = W.llama3_decode(seed=5, batch=6)
