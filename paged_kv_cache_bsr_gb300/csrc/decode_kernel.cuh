@@ -79,6 +79,7 @@ struct Producer {
   int tok, n_tok;
   int idx_begin, kvh;
   int win_base, win;
+  int win_next;  // one-row pages: the window after `win`, loaded a window ahead
   int issued;
 };
 
@@ -86,7 +87,7 @@ __device__ __forceinline__ int seg_tokens(int n_pages, int last_rows, int P) {
   return n_pages > 0 ? (n_pages - 1) * P + last_rows : 0;
 }
 
-template <int D, typename T>
+template <int D, typename T, bool GATHER>
 __device__ __forceinline__ void producer_enter(Producer& p, const DecodeArgs& a, int lane) {
   const SegInfo s = load_seg(a.segs, p.seg, lane);
   p.idx_begin = s.idx_begin;
@@ -95,6 +96,9 @@ __device__ __forceinline__ void producer_enter(Producer& p, const DecodeArgs& a,
   p.tok = 0;
   p.win_base = 0;
   p.win = lane < s.n_pages ? __ldg(a.kv_indices + p.idx_begin + lane) : 0;
+  // One-row pages also hold the next window, loaded a window ahead (the gather
+  // path's tiles are 16 pages each, so a window lasts only two of them).
+  if constexpr (GATHER) p.win_next = 32 + lane < s.n_pages ? __ldg(a.kv_indices + p.idx_begin + 32 + lane) : 0;
 }
 
 // Issue the next tile of the warp's stream into its stage; false when done.
@@ -108,34 +112,35 @@ __device__ __forceinline__ bool producer_issue(Producer& p, const DecodeArgs& a,
   using Shape = DecodeShape<D, T>;
   while (p.seg < p.seg_end) {
     if (p.tok < p.n_tok) {
-      const int P = a.page_size;
       const int rows = min(kDecodeTileRows, p.n_tok - p.tok);
-      const int pa = p.tok / P, pb = (p.tok + rows - 1) / P;  // pages the tile overlaps
-      if (pb - p.win_base >= 32) {
-        p.win_base = pa;
-        const int n_pages = (p.n_tok + P - 1) / P;
-        p.win = (pa + lane < n_pages) ? __ldg(a.kv_indices + p.idx_begin + pa + lane) : 0;
-      }
       const int stage = p.issued % Shape::kStages;
       const uint32_t dst = smem_addr(ring + stage * Shape::kStageBytes);
       const uint32_t bar = bar0 + 8 * stage;
       if constexpr (GATHER) {
+        static_assert(kDecodeGatherMaxRows == 1, "the gather path takes one-row pages only");
+        // One-row pages: token = page.  A tile of 16 tokens never straddles two
+        // 32-id windows, and the next window was loaded one window earlier, so
+        // the id load's latency hides behind two tiles of work.
+        if (p.tok - p.win_base >= 32) {
+          p.win_base += 32;
+          p.win = p.win_next;
+          const int k = p.win_base + 32 + lane;
+          p.win_next = k < p.n_tok ? __ldg(a.kv_indices + p.idx_begin + k) : 0;
+        }
         // Every gather writes four whole rows (rows past the segment, or of a bad
         // page id, as zeros from past the tensor), so the stage always gets a full tile.
         if (lane == 0) mbar_arrive_expect_tx(bar, 2u * kDecodeTileRows * D * sizeof(T));
         __syncwarp();
         const int q4 = lane & 3, sel = (lane >> 2) & 1;  // four tokens' rows of K (sel 0) or V (1)
+        const int w0 = p.tok - p.win_base + 4 * q4;      // window slot of this lane's first token
         int rowi[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int r = 4 * q4 + i;
-          const int tok = p.tok + r;
-          const int k = tok / P;
-          const int page_id = __shfl_sync(kFull, p.win, min(max(k - p.win_base, 0), 31));
+          const int page_id = __shfl_sync(kFull, p.win, (w0 + i) & 31);
           rowi[i] = a.kv_rows_n;
-          if (r < rows) {
+          if (4 * q4 + i < rows) {
             if (page_id >= 0 && page_id < num_pages)
-              rowi[i] = ((page_id * 2 + sel) * a.num_kv_heads + p.kvh) * P + (tok - k * P);
+              rowi[i] = (page_id * 2 + sel) * a.num_kv_heads + p.kvh;
             else if (lane < 8)
               atomicOr(a.err, kErrPageIndex);
           }
@@ -146,6 +151,13 @@ __device__ __forceinline__ bool producer_issue(Producer& p, const DecodeArgs& a,
         ++p.issued;
         p.tok += rows;
         return true;
+      }
+      const int P = a.page_size;
+      const int pa = p.tok / P, pb = (p.tok + rows - 1) / P;  // pages the tile overlaps
+      if (pb - p.win_base >= 32) {
+        p.win_base = pa;
+        const int n_pages = (p.n_tok + P - 1) / P;
+        p.win = (pa + lane < n_pages) ? __ldg(a.kv_indices + p.idx_begin + pa + lane) : 0;
       }
       if (lane == 0) mbar_arrive_expect_tx(bar, 2u * rows * D * sizeof(T));
       __syncwarp();
@@ -173,7 +185,7 @@ __device__ __forceinline__ bool producer_issue(Producer& p, const DecodeArgs& a,
       return true;
     }
     ++p.seg;
-    if (p.seg < p.seg_end) producer_enter<D, T>(p, a, lane);
+    if (p.seg < p.seg_end) producer_enter<D, T, GATHER>(p, a, lane);
   }
   return false;
 }
@@ -367,7 +379,7 @@ __device__ __forceinline__ void decode_worker(const DecodeArgs& a, int worker, u
   prod.seg = seg_begin;
   prod.seg_end = seg_end;
   prod.issued = 0;
-  producer_enter<D, T>(prod, a, lane);
+  producer_enter<D, T, GATHER>(prod, a, lane);
   for (int s = 0; s < S; ++s)
     if (!producer_issue<D, T, GATHER>(prod, a, ring, bar0, lane, num_pages, policy)) break;
 
