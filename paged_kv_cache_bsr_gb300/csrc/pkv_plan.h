@@ -28,6 +28,8 @@ struct PlanScratch {
   std::vector<int64_t> mask_off, load, nb_tiles, by_cost, by_load;
   std::vector<int> start, order, cta_of, per_cta, by_cta, fill;
   std::vector<uint64_t> buckets;
+  std::vector<DecodeSeg> dsegs;
+  std::vector<int32_t> run_ptr;
 };
 
 }  // namespace pkv

@@ -388,8 +388,10 @@ def test_prefill_plan_is_the_longest_first_schedule(lib, seed, batch, C, causal,
 def equal_runs_decode(b, W, tile_rows=16):
     """The decode plan restated plainly: the (request, kv head) page lists concatenated in
     order and cut into runs of max(ceil(total / W), min_run) pages, one run per worker; a
-    list that crosses a run boundary is split there, each piece a partial-state slot.
-    Returns the work rows [worker, request, kv head, first page, pages, last rows, slot, 0]."""
+    list that crosses a run boundary is split there, each piece a partial-state slot.  Run r
+    goes to warp r // C of CTA r % C (C = W // 8 CTAs of 8 warps), worker 8 * CTA + warp.
+    Returns the work rows [worker, request, kv head, first page, pages, last rows, slot, 0]
+    in worker order."""
     P = b.page_size
     pages_per_tile = -(-P // tile_rows)
     min_run = max(1, 4 // pages_per_tile)
@@ -414,7 +416,10 @@ def equal_runs_decode(b, W, tile_rows=16):
                     rows.append([w, r, h, lo, hi - lo, last if hi == n else P, slot, 0])
                     slot += 1
             x += n
-    return rows
+    C = W // 8
+    for row in rows:
+        row[0] = (row[0] % C) * 8 + row[0] // C
+    return sorted(rows, key=lambda row: row[0])  # stable: a run keeps its order
 
 
 @pytest.mark.parametrize("seed,batch,workers,page", [(1001, 64, 1216, 16), (3, 9, 40, 16), (5, 7, 1216, 1),
@@ -425,7 +430,36 @@ def test_decode_plan_is_the_equal_run_split(lib, seed, batch, workers, page):
     b = W.llama3_decode(seed=seed, batch=batch, page_size=page)
     h, ws = host_plan(b, api.PLAN_DECODE, num_sms=workers // 8)
     compute(h, ws, b)
-    assert api.plan_get_work(h).tolist() == equal_runs_decode(b, workers)
+    if fits_in_one_run(b, workers):
+        check_whole_list_plan(h, b, workers)
+    else:
+        assert api.plan_get_work(h).tolist() == equal_runs_decode(b, workers)
+
+
+def fits_in_one_run(b, W, tile_rows=16):
+    """No (request, kv head) list longer than a run, and a worker for every list: the
+    split plan then keeps each list whole, one per worker (the whole-list schedule)."""
+    lens = [int(b.kv_indptr[r + 1] - b.kv_indptr[r]) for r in range(b.batch)]
+    total = sum(lens) * b.num_kv_heads
+    min_run = max(1, 4 // -(-b.page_size // tile_rows))
+    run = max(-(-total // W), min_run) if total else 1
+    return b.batch * b.num_kv_heads <= W and max(lens, default=0) <= run
+
+
+@pytest.mark.parametrize("kv_lens,sms,whole", [([16] * 64, 152, True), ([64] * 64, 152, True),
+                                               ([128] * 64, 152, False), ([16] * 64, 4, False)])
+def test_decode_plan_keeps_short_lists_whole_when_workers_allow(lib, kv_lens, sms, whole):
+    """64 x 8 lists of 1, 4 or 8 pages on 152 SMs (1216 workers), and of one page on 4 SMs
+    (32 workers, fewer than the lists): whole lists exactly when none exceeds a run."""
+    b = table_batch(kv_lens)
+    assert fits_in_one_run(b, sms * 8) == whole
+    h, ws = host_plan(b, api.PLAN_DECODE, num_sms=sms)
+    compute(h, ws, b)
+    if whole:
+        check_whole_list_plan(h, b, sms * 8)
+    else:
+        assert api.plan_get_work(h).tolist() == equal_runs_decode(b, sms * 8)
+    api.plan_destroy(h)
 
 
 def test_prefill_plan_ragged_causal(lib):
