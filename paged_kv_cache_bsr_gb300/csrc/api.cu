@@ -262,13 +262,13 @@ pkv_status pkv_batch_mixed_paged(const pkv_plan* plan, const void* q, const int3
   const pkv::PrefillArgs pa = prefill_args(pp, base + plan->pre_dev_off, q, kv_data, kv_indices_d, nullptr, 0, o, lse);
   auto s = static_cast<cudaStream_t>(stream);
   // One persistent launch serves both halves (the CTA split is in the decode
-  // tables); then each half's merge of split sequences.
+  // tables); then one launch merges both halves' split sequences.
   cudaError_t e = cudaSuccess;
   if (plan->time_start) cudaEventRecord(plan->time_start, s);
   e = pkv::launch_mixed(pa, da, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, pp->total_q, pp->num_pages, s);
   if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
-  if (e == cudaSuccess) e = pkv::launch_prefill_merge(pa, p.head_dim, plan->group, p.dtype, pp->merge_grid, s);
-  if (e == cudaSuccess) e = pkv::launch_decode_merge(da, p.head_dim, plan->group, p.dtype, dp->merge_grid, s);
+  if (e == cudaSuccess)
+    e = pkv::launch_mixed_merge(pa, da, plan->group, p.dtype, std::max(pp->merge_grid, dp->merge_grid), s);
   return launch_status(e);
 }
 

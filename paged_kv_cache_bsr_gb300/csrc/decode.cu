@@ -19,13 +19,10 @@ namespace {
 
 using namespace decode_impl;
 
-// n-way merge of the partial states of split (request, kv head) sequences:
-// one warp per (item, head of the group), lanes over head_dim, the slot loop
-// unrolled so that several partial rows are in flight per lane.
+// n-way merge of the partial states of split (request, kv head) sequences
+// (decode_merge_pair in decode_kernel.cuh): one warp per (item, head of the group).
 template <int D, int G, typename T>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
-  constexpr int PER = D / 32;  // dims per lane
-  constexpr int U = 8;         // slots in flight per lane
   const int lane = threadIdx.x & 31;
   const int warp_id = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
   const int n_warps = gridDim.x * (kMergeThreads / 32);
@@ -33,64 +30,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __gri
   // grid has finished and its partial states are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int pairs = a.hdr->num_merge * G;
-  for (int pair = warp_id; pair < pairs; pair += n_warps) {
-    const MergeItem it = a.merge[pair / G];
-    const int g = pair % G;
-    const float* lse_p = a.part_lse + static_cast<int64_t>(it.slot_begin) * G + g;
-    float mx = -INFINITY;
-    for (int i = lane; i < it.n_slots; i += 32) mx = fmaxf(mx, lse_p[static_cast<int64_t>(i) * G]);
-    mx = warp_max(mx);
-    float acc[PER];
-#pragma unroll
-    for (int v = 0; v < PER; ++v) acc[v] = 0.f;
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-      const float* o_p = a.part_o + (static_cast<int64_t>(it.slot_begin) * G + g) * D + lane * PER;
-      for (int i0 = 0; i0 < it.n_slots; i0 += 32) {
-        // lane j holds the weight of slot i0 + j
-        const float w_lane = (i0 + lane < it.n_slots)
-                                 ? fast_exp2((lse_p[static_cast<int64_t>(i0 + lane) * G] - mx) * kLog2e)
-                                 : 0.f;
-        const int cnt = min(32, it.n_slots - i0);
-        for (int j0 = 0; j0 < cnt; j0 += U) {
-          float vals[U][PER];
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int i = i0 + j0 + u;
-            if (j0 + u < cnt) {
-              const float* src = o_p + static_cast<int64_t>(i) * G * D;
-              if constexpr (PER == 4) {
-                const float4 t = *reinterpret_cast<const float4*>(src);
-                vals[u][0] = t.x; vals[u][1] = t.y; vals[u][2] = t.z; vals[u][3] = t.w;
-              } else {
-                const float2 t = *reinterpret_cast<const float2*>(src);
-                vals[u][0] = t.x; vals[u][1] = t.y;
-              }
-            } else {
-#pragma unroll
-              for (int v = 0; v < PER; ++v) vals[u][v] = 0.f;
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const float w = __shfl_sync(kFull, w_lane, (j0 + u) & 31);
-            if (j0 + u < cnt) {
-#pragma unroll
-              for (int v = 0; v < PER; ++v) acc[v] = fmaf(w, vals[u][v], acc[v]);
-              wsum += w;
-            }
-          }
-        }
-      }
-    }
-    const int hq = it.kvh * G + g;
-    T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(it.row) * a.num_qo_heads + hq) * D;
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-    for (int v = 0; v < PER; ++v) orow[lane * PER + v] = from_float<T>(acc[v] * inv);
-    if (lane == 0 && a.lse)
-      a.lse[static_cast<int64_t>(it.row) * a.num_qo_heads + hq] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
-  }
+  for (int pair = warp_id; pair < pairs; pair += n_warps) decode_merge_pair<D, G, T>(a, pair, lane);
 }
 
 template <typename T>

@@ -118,8 +118,12 @@ cudaError_t launch_prefill_merge(const PrefillArgs& a, int head_dim, int group, 
 
 // Launch the mixed prefill + decode kernel on `grid` CTAs: the CTAs below the
 // decode tables' cta_offset run the prefill half, the rest the decode half
-// (head_dim 128 only).  The two halves' merges are launched separately.
+// (head_dim 128 only).  Both halves' merges follow in one launch (launch_mixed_merge).
 cudaError_t launch_mixed(const PrefillArgs& pa, const DecodeArgs& da, int head_dim, int group, int dtype, bool cap,
                          int grid, int64_t total_q, int64_t num_pages, cudaStream_t stream);
+// The merges of both halves of a mixed batch (split decode sequences and split
+// prefill tiles) in one launch, a programmatic dependent of the mixed kernel.
+cudaError_t launch_mixed_merge(const PrefillArgs& pa, const DecodeArgs& da, int group, int dtype, int grid,
+                               cudaStream_t stream);
 
 }  // namespace pkv

@@ -18,8 +18,8 @@ using namespace prefill_impl;
 
 namespace {
 
-// Rows of query tiles whose key range the plan split: one warp per packed row,
-// lanes over head_dim, log-sum-exp merge of the chunks' fp32 partial states.
+// Rows of query tiles whose key range the plan split (prefill_merge_row in
+// prefill_kernel.cuh): one warp per packed row.
 template <typename T>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constant__ PrefillArgs a) {
   // Launched as a programmatic dependent of the kernel before it: wait until that
@@ -30,37 +30,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constan
   const int n_warps = gridDim.x * 8;
   const int G = a.num_qo_heads / a.num_kv_heads;
   const int pairs = a.hdr->num_merge * kWR;
-  for (int pair = warp_id; pair < pairs; pair += n_warps) {
-    const PrefillMerge it = a.merge[pair / kWR];
-    const int r = pair % kWR;
-    if (r / G >= it.n_pos) continue;
-    float mx = -INFINITY;
-    for (int i = lane; i < it.n_slots; i += 32)
-      mx = fmaxf(mx, a.part_lse[static_cast<int64_t>(it.slot_begin + i) * kWR + r]);
-    mx = warp_max(mx);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-      for (int i = 0; i < it.n_slots; ++i) {
-        const int64_t row = static_cast<int64_t>(it.slot_begin + i) * kWR + r;
-        const float w = fast_exp2((a.part_lse[row] - mx) * kLog2e);
-        if (w > 0.f) {
-          const float4 v = reinterpret_cast<const float4*>(a.part_o + row * kD)[lane];
-          acc[0] = fmaf(w, v.x, acc[0]);
-          acc[1] = fmaf(w, v.y, acc[1]);
-          acc[2] = fmaf(w, v.z, acc[2]);
-          acc[3] = fmaf(w, v.w, acc[3]);
-          wsum += w;
-        }
-      }
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int64_t orow = static_cast<int64_t>(it.q_row0 + r / G) * a.num_qo_heads + it.kvh * G + (r % G);
-    T* dst = static_cast<T*>(a.o) + orow * kD + lane * 4;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) dst[v] = from_float<T>(acc[v] * inv);
-    if (lane == 0 && a.lse) a.lse[orow] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
-  }
+  for (int pair = warp_id; pair < pairs; pair += n_warps) prefill_merge_row<T>(a, pair, lane, G);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

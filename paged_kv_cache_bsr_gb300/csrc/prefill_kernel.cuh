@@ -718,6 +718,43 @@ __device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensor
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Log-sum-exp merge of the chunks' fp32 partial states of one packed row of a
+// query tile whose key range the plan split (pair = item * 256 + row), by the
+// calling warp, lanes over head_dim.  Shared by the prefill merge kernel and the
+// mixed batch's merge kernel.
+template <typename T>
+__device__ __forceinline__ void prefill_merge_row(const PrefillArgs& a, int pair, int lane, int G) {
+  const PrefillMerge it = a.merge[pair / kWR];
+  const int r = pair % kWR;
+  if (r / G >= it.n_pos) return;
+  float mx = -INFINITY;
+  for (int i = lane; i < it.n_slots; i += 32)
+    mx = fmaxf(mx, a.part_lse[static_cast<int64_t>(it.slot_begin + i) * kWR + r]);
+  mx = warp_max(mx);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int i = 0; i < it.n_slots; ++i) {
+      const int64_t row = static_cast<int64_t>(it.slot_begin + i) * kWR + r;
+      const float w = fast_exp2((a.part_lse[row] - mx) * kLog2e);
+      if (w > 0.f) {
+        const float4 v = reinterpret_cast<const float4*>(a.part_o + row * kD)[lane];
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]);
+        acc[3] = fmaf(w, v.w, acc[3]);
+        wsum += w;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int64_t orow = static_cast<int64_t>(it.q_row0 + r / G) * a.num_qo_heads + it.kvh * G + (r % G);
+  T* dst = static_cast<T*>(a.o) + orow * kD + lane * 4;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) dst[v] = from_float<T>(acc[v] * inv);
+  if (lane == 0 && a.lse) a.lse[orow] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
 template <int G, typename T, bool CAP, bool MASK, bool SMALL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,

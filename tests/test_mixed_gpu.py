@@ -65,10 +65,10 @@ def test_mixed_page_sizes_and_cap(page_size, group, cap):
 
 
 def test_mixed_is_one_attention_launch():
-    """The run call launches the mixed kernel once (a CTA on every SM), then the two
-    halves' merges; neither the decode kernel nor the prefill kernel runs.  The two
-    halves run as their own plans give the four launches that the mixed kernel
-    replaces, which shows the count sees every kernel."""
+    """The run call launches the mixed kernel once (a CTA on every SM), then one merge
+    kernel for both halves; neither the decode kernel nor the prefill kernel runs.  The
+    two halves run as their own plans give the four launches that these two replace,
+    which shows the count sees every kernel."""
     b = small_mixed(40)
     dec = [r for r in range(b.batch) if b.qo_lens[r] == 1]
     pre = [r for r in range(b.batch) if b.qo_lens[r] > 1]
@@ -92,11 +92,12 @@ def test_mixed_is_one_attention_launch():
                      stream=s)
 
     def kinds(nodes):
-        return sorted(next((k for k in ("mixed_kernel", "prefill_merge", "decode_merge", "prefill_kernel",
-                                        "decode_kernel") if k in name), name) for name, _, _ in nodes)
+        return sorted(next((k for k in ("mixed_merge", "mixed_kernel", "prefill_merge", "decode_merge",
+                                        "prefill_kernel", "decode_kernel") if k in name), name)
+                      for name, _, _ in nodes)
 
     nodes = kernel_nodes(lambda: run(0, db), s)
-    assert kinds(nodes) == ["decode_merge", "mixed_kernel", "prefill_merge"], nodes
+    assert kinds(nodes) == ["mixed_kernel", "mixed_merge"], nodes  # both halves' merges in one launch
     assert [g for name, g, _ in nodes if "mixed_kernel" in name] == [(sms, 1, 1)], nodes
     halves = kernel_nodes(lambda: (run(1, dd), run(2, dp)), s)
     assert kinds(halves) == ["decode_kernel", "decode_merge", "prefill_kernel", "prefill_merge"], halves
