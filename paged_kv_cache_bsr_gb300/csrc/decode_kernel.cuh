@@ -153,7 +153,17 @@ __device__ __forceinline__ bool producer_issue(Producer& p, const DecodeArgs& a,
         return true;
       }
       const int P = a.page_size;
-      const int pa = p.tok / P, pb = (p.tok + rows - 1) / P;  // pages the tile overlaps
+      // Pages the tile overlaps: a shift for power-of-two page sizes (a division by a
+      // run-time divisor costs the warp about twenty instructions per tile).
+      int pa, pb;
+      if ((P & (P - 1)) == 0) {
+        const int lp = __ffs(P) - 1;
+        pa = p.tok >> lp;
+        pb = (p.tok + rows - 1) >> lp;
+      } else {
+        pa = p.tok / P;
+        pb = (p.tok + rows - 1) / P;
+      }
       if (pb - p.win_base >= 32) {
         p.win_base = pa;
         const int n_pages = (p.n_tok + P - 1) / P;
