@@ -359,8 +359,8 @@ pkv_status pkv_batch_decode_paged_noalloc(const pkv_plan* plan, const void* host
  * the tensor cores (8 query heads per kv head, head_dim 128, pages of 8 rows or
  * more; see pkv_batch_decode_paged) every request goes to the prefill half.  The run call makes one
  * persistent launch on every SM: the CTAs below the split run the prefill
- * half, the others the decode workers; then each half's merge of split
- * sequences follows on `stream` ("FlashInfer" guide, "Prefill-Decode Mixing";
+ * half, the others the decode workers; then one merge launch folds both
+ * halves' split sequences, on `stream` ("FlashInfer" guide, "Prefill-Decode Mixing";
  * fdeinterviews summary, "Customizable attention": a query tile size from 1 to
  * 128 picked per batch; greptalks, "Future Directions and Features": mixed
  * prefill and decode phases in one batch).  The split is read from the device
