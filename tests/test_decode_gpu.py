@@ -65,6 +65,25 @@ def test_cascade_full_view_decode_softcap():
     decode_vs_oracle(cb.full, "cascade-full")
 
 
+@pytest.mark.parametrize("kv_len,whole", [(16, True), (64, True), (128, False), (200, False)])
+def test_plan_placements_of_short_lists(kv_len, whole):
+    """64 requests x 8 kv heads of equal short lists: one and four pages are kept whole, one list
+    per worker; eight and thirteen pages are split into runs spread over the CTAs and merged.
+    Both placements give the oracle's result (poisoned pool, soft-cap on)."""
+    b = W.make_paged_batch(qo_lens=[1] * 64, kv_lens=[kv_len] * 64, num_qo_heads=32, num_kv_heads=8,
+                           head_dim=128, page_size=16, dtype=torch.bfloat16, seed=40 + kv_len, poison=True,
+                           logits_cap=30.0)
+    plan, _, _ = decode_vs_oracle(b, f"64 x {kv_len}")
+    info = plan.info()
+    assert (info.num_merge == 0) == whole
+    if whole:
+        assert info.active_workers == 64 * 8
+    else:
+        # the runs are spread one warp per CTA first: every CTA of the grid gets work
+        ctas = {w // 8 for w in plan.work()[:, 0].tolist()}
+        assert info.active_workers >= info.grid_ctas and len(ctas) == info.grid_ctas
+
+
 # --------------------------------------------------------------------------- edge cases
 @pytest.mark.parametrize("kv_lens", [[1, 15, 16, 17], [0, 3, 0], [1], [16], [33, 0, 257, 1000]])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
