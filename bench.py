@@ -429,7 +429,11 @@ def prefill_measure(peaks, steps=20, warmup=3, page_size=16):
     flops = pairs * b.num_qo_heads * 4 * b.head_dim
     ms = total_ms / steps
     achieved = flops / (kern_ms * 1e-3) / 1e12
-    traffic = recorded_traffic("prefill_kernel_ragged_causal_prefill.txt", source_hash("prefill_kernel.cuh"))
+    # Pages of fewer than 8 rows: the timed span is the packing copy and the kernel
+    # over it (the recorded ncu traffic is for 16-row pages only).
+    packed = page_size < 8
+    traffic = None if packed else recorded_traffic("prefill_kernel_ragged_causal_prefill.txt",
+                                                   source_hash("prefill_kernel.cuh"))
     traffic = traffic if page_size == 16 else None
     return {"workload": "ragged_causal_prefill", "page_size": page_size,
             "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
@@ -437,7 +441,8 @@ def prefill_measure(peaks, steps=20, warmup=3, page_size=16):
             "host_plan_us": host_plan_or_error(b, api.PLAN_PREFILL),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
-                         "peak_source": peaks["source"], "kernel": "prefill_kernel"}}
+                         "peak_source": peaks["source"],
+                         "kernel": "pack_pages_kernel + prefill_kernel" if packed else "prefill_kernel"}}
 
 
 def tree_measure(peaks, steps=20, warmup=3):

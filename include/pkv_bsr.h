@@ -124,7 +124,9 @@ pkv_status pkv_plan_create_host(pkv_plan** out, int kind, const pkv_params* para
 
 /*
  * Bytes of caller-provided memory the plan needs:
- *  - dev_bytes: device workspace (plan tables, fp32 partial states, error word);
+ *  - dev_bytes: device workspace (plan tables, fp32 partial states, error word;
+ *    for a prefill plan on pages of fewer than 8 rows also the 16-row-page copy
+ *    of up to limits->max_kv_pages pages' keys);
  *  - host_bytes: pinned host staging buffer for the plan tables.
  * Both depend only on params and limits.
  */
@@ -269,8 +271,10 @@ pkv_status pkv_batch_decode_paged(const pkv_plan* plan, const void* q, const voi
  * query rows given by qo_indptr_d, causal per params->causal, computed with
  * tcgen05 tensor-core MMAs (bf16 and fp16) and fp32 TMEM accumulators.
  * Built for head_dim 128, groups 1/2/4/8 and page sizes 1, 2, 4, 8, 16, 32,
- * 64 and 128 (pages of 1-4 rows, the column-vector BSR of sparse patterns,
- * are gathered row by row; larger pages by one tensor copy per page).
+ * 64 and 128.  Pages of 1-4 rows (the column-vector BSR of sparse patterns)
+ * are first copied, row by row, into 16-row pages of the device workspace (each
+ * request's keys in order, ceil(kv_len / 16) pages), and the tensor-core kernel
+ * runs over that copy; larger pages are read in place, one tensor copy per page.
  * q and o: [total_q, Hq, d]; lse: [total_q, Hq] fp32 (may be NULL).
  * With causal = 0 and one request whose rows are many requests' queries, this
  * is the shared-prefix half of cascade attention.  The kernel's TMA tensor maps

@@ -136,15 +136,18 @@ pkv_status launch_status(cudaError_t e) {
 }
 
 // The prefill kernel and its merge over a plan's prefill tables (a prefill plan,
-// or a decode plan whose work runs on the tensor cores).
-cudaError_t launch_prefill_tables(const pkv_plan* plan, const pkv::PrefillArgs& a, cudaStream_t s) {
+// or a decode plan whose work runs on the tensor cores); a packed plan's copy of
+// small pages (`pack`) is made first, inside the timed span.
+cudaError_t launch_prefill_tables(const pkv_plan* plan, const pkv::PrefillArgs& a, cudaStream_t s,
+                                  const pkv::PackArgs* pack = nullptr) {
   const pkv_params& p = plan->p;
   const bool cap = p.logits_cap > 0.f;
   cudaError_t e = wait_tables(plan, s);
   if (plan->time_start && e == cudaSuccess) cudaEventRecord(plan->time_start, s);
+  if (pack && e == cudaSuccess) e = pkv::launch_pack_pages(*pack, p.head_dim, plan->num_sms * 8, s);
   if (e == cudaSuccess)
     e = pkv::launch_prefill(a, p.head_dim, plan->group, p.dtype, cap, plan->grid_ctas, plan->total_q,
-                            plan->num_pages, s);
+                            plan->packed ? plan->max_packed : plan->num_pages, s);
   if (plan->time_stop && e == cudaSuccess) cudaEventRecord(plan->time_stop, s);
   if (e == cudaSuccess) e = pkv::launch_prefill_merge(a, p.head_dim, plan->group, p.dtype, plan->merge_grid, s);
   if (e == cudaSuccess) e = release_tables(plan, s);
@@ -216,8 +219,26 @@ static pkv_status prefill_run(const pkv_plan* plan, const void* q, const int32_t
     return PKV_ERR_INVALID_ARG;
   pkv_status st = check_device(plan);
   if (st != PKV_OK) return st;
-  const pkv::PrefillArgs a = prefill_args(plan, dev_ws, q, kv_data, kv_indices_d, mask, mask_bytes, o, lse);
-  return launch_status(launch_prefill_tables(plan, a, static_cast<cudaStream_t>(stream)));
+  pkv::PrefillArgs a = prefill_args(plan, dev_ws, q, kv_data, kv_indices_d, mask, mask_bytes, o, lse);
+  if (!plan->packed) return launch_status(launch_prefill_tables(plan, a, static_cast<cudaStream_t>(stream)));
+  // Pages of fewer than 8 rows: the kernel reads the packed copy, in 16-row pages
+  // whose ids are the plan's own table.
+  auto* base = static_cast<uint8_t*>(dev_ws);
+  auto* tb = base + table_off(plan);
+  pkv::PackArgs pk{};
+  pk.kv = kv_data;
+  pk.kv_indices = kv_indices_d;
+  pk.src = reinterpret_cast<const pkv::PackedSrc*>(tb + plan->L.pk_src);
+  pk.hdr = a.hdr;
+  pk.packed = base + plan->L.pk_kv;
+  pk.err = a.err;
+  pk.num_kv_heads = plan->p.num_kv_heads;
+  pk.page_size = plan->p.page_size;
+  pk.num_pages = plan->num_pages;
+  a.kv = pk.packed;
+  a.kv_indices = reinterpret_cast<const int32_t*>(tb + plan->L.pk_ids);
+  a.page_size = 16;
+  return launch_status(launch_prefill_tables(plan, a, static_cast<cudaStream_t>(stream), &pk));
 }
 
 pkv_status pkv_batch_prefill_paged(const pkv_plan* plan, const void* q, const int32_t* qo_indptr_d,

@@ -33,7 +33,9 @@ struct alignas(64) PlanHeader {
   int32_t error;         // device error word; cleared by every plan_run
   int32_t cta_offset;    // mixed plans, decode half: the first CTA of the mixed launch
                          // that serves it (CTAs below it serve the prefill half); 0 otherwise
-  int32_t pad[4];
+  int32_t num_packed;    // prefill plans on pages of fewer than 8 rows: 16-row pages in the
+                         // packed copy of the requests' K/V (0 otherwise)
+  int32_t pad[3];
 };
 static_assert(sizeof(PlanHeader) == 64, "PlanHeader layout");
 
@@ -98,14 +100,26 @@ struct alignas(32) PrefillMerge {
 static_assert(sizeof(PrefillMerge) == 32, "PrefillMerge layout");
 
 // Byte offsets of the regions inside the device workspace.
+// Packed prefill plans: where the 16 rows of packed page p come from, the
+// request's keys tok0 .. tok0 + ntok - 1 counted from its first kv_indices entry
+// times the page size (so token u is row u % P of page kv_indices[u / P]).
+struct PackedSrc {
+  int32_t tok0;
+  int32_t ntok;        // 1 .. 16
+};
+static_assert(sizeof(PackedSrc) == 8, "PackedSrc layout");
+
 struct WorkspaceLayout {
   size_t header;       // PlanHeader
   size_t worker_ptr;   // int32 [max_workers + 1]
   size_t merge;        // MergeItem / PrefillMerge [max_merge]
+  size_t pk_ids;       // packed prefill plans: int32 [max_packed], page p's id p
+  size_t pk_src;       // packed prefill plans: PackedSrc [max_packed]
   size_t segs;         // DecodeSeg [max_segments]  or PrefillTile [max_tiles]
   size_t tables_end;   // everything above is copied from the pinned host buffer
   size_t part_o;       // fp32 [max_slots][rows_per_slot][head_dim]
   size_t part_lse;     // fp32 [max_slots][rows_per_slot]
+  size_t pk_kv;        // packed prefill plans: [max_packed, 2, Hkv, 16, D] copy of the K/V rows
   size_t alt;          // a second copy of the tables [0, tables_end), for pipelined plans
   size_t total;
 };

@@ -113,6 +113,21 @@ struct PrefillArgs {
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dtype, bool cap, int grid,
                            int64_t total_q, int64_t num_pages, cudaStream_t stream);
+
+// Packed prefill plans: copy the requests' K/V rows from pages of fewer than 8
+// rows into 16-row pages of the workspace, page p from the keys src[p] names.
+struct PackArgs {
+  const void* kv;              // [num_pages, 2, Hkv, P, D], the caller's pool
+  const int32_t* kv_indices;
+  const PackedSrc* src;        // [num_packed]
+  const PlanHeader* hdr;       // num_packed
+  void* packed;                // [max_packed, 2, Hkv, 16, D]
+  int32_t* err;
+  int num_kv_heads;
+  int page_size;               // 1, 2 or 4
+  int64_t num_pages;
+};
+cudaError_t launch_pack_pages(const PackArgs& a, int head_dim, int grid, cudaStream_t stream);
 cudaError_t launch_prefill_merge(const PrefillArgs& a, int head_dim, int group, int dtype, int grid,
                                  cudaStream_t stream);
 

@@ -30,6 +30,7 @@ struct PlanScratch {
   std::vector<uint64_t> buckets;
   std::vector<DecodeSeg> dsegs;
   std::vector<int32_t> run_ptr;
+  std::vector<int32_t> pk_indptr, pk_last;
 };
 
 }  // namespace pkv
@@ -55,6 +56,11 @@ struct pkv_plan {
   // prefill tables, planned over row_indptr = 0, 1, ..., batch.
   bool exec_prefill = false;
   std::vector<int32_t> row_indptr;
+  // Prefill plan on pages of fewer than 8 rows: each run first copies the
+  // requests' K/V rows into 16-row pages of its workspace (pack_pages_kernel),
+  // and the tables describe the prefill over that copy.
+  bool packed = false;
+  int64_t max_packed = 0;
   pkv::WorkspaceLayout L{};
   size_t host_bytes = 0;
   // Last computed plan.

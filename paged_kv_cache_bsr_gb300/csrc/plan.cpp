@@ -88,11 +88,19 @@ void set_layout(pkv_plan* pl) {
   L.header = 0;
   L.worker_ptr = align_up(sizeof(PlanHeader), 256);
   L.merge = align_up(L.worker_ptr + sizeof(int32_t) * (pl->workers + 1), 256);
-  L.segs = align_up(L.merge + merge_bytes * std::max(pl->max_merge, 1), 256);
+  // Packed prefill plans: the packed pages' ids and sources sit before the
+  // tiles, so the table copy (up to the last tile in use) carries them.
+  const size_t n_pk = pl->packed ? static_cast<size_t>(pl->max_packed) : 0;
+  L.pk_ids = align_up(L.merge + merge_bytes * std::max(pl->max_merge, 1), 256);
+  L.pk_src = align_up(L.pk_ids + sizeof(int32_t) * n_pk, 256);
+  L.segs = align_up(L.pk_src + sizeof(pkv::PackedSrc) * n_pk, 256);
   L.tables_end = align_up(L.segs + work_bytes * std::max(pl->max_work, 1), 256);
   L.part_o = L.tables_end;
   L.part_lse = align_up(L.part_o + sizeof(float) * (size_t)pl->max_slots * pl->rows_per_slot * pl->p.head_dim, 256);
-  L.alt = align_up(L.part_lse + sizeof(float) * (size_t)pl->max_slots * pl->rows_per_slot, 256);
+  L.pk_kv = align_up(L.part_lse + sizeof(float) * (size_t)pl->max_slots * pl->rows_per_slot, 256);
+  // 2 bytes per element (fp16 / bf16), 16 rows per packed page.
+  const size_t pk_bytes = n_pk * 2 * static_cast<size_t>(pl->p.num_kv_heads) * 16 * pl->p.head_dim * 2;
+  L.alt = align_up(L.pk_kv + pk_bytes, 256);
   L.total = L.alt + L.tables_end;
 }
 
@@ -100,7 +108,7 @@ void set_layout(pkv_plan* pl) {
 // the decode half of a mixed plan never does (the mixed kernel's decode CTAs read
 // decode tables).
 pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const pkv_limits* limits,
-                     int device, int num_sms, bool route_decode = true) {
+                     int device, int num_sms, bool route_decode = true, bool allow_pack = true) {
   if (!out) return PKV_ERR_INVALID_ARG;
   *out = nullptr;
   pkv_status st = check_params(kind, params, limits);
@@ -120,7 +128,10 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
   if (kind == PKV_PLAN_MIXED) {
     // Two plans of the same problem and limits; their workspaces are laid end to end.
     pkv_status s1 = make_plan(&pl->sub_dec, PKV_PLAN_DECODE, params, limits, device, num_sms, false);
-    pkv_status s2 = s1 == PKV_OK ? make_plan(&pl->sub_pre, PKV_PLAN_PREFILL, params, limits, device, num_sms) : s1;
+    // The mixed kernel's prefill CTAs read the caller's pages (its own gather
+    // instances for small pages): no packed copy.
+    pkv_status s2 =
+        s1 == PKV_OK ? make_plan(&pl->sub_pre, PKV_PLAN_PREFILL, params, limits, device, num_sms, true, false) : s1;
     if (s2 != PKV_OK) {
       delete pl->sub_dec;
       delete pl->sub_pre;
@@ -173,6 +184,17 @@ pkv_status make_plan(pkv_plan** out, int kind, const pkv_params* params, const p
     pl->max_slots = 2 * num_sms + 2;
     pl->rows_per_slot = pkv::kPrefillRows;
     pl->merge_grid = num_sms * 4;
+    // Pages of fewer than 8 rows: the tensor-core prefill runs over a packed copy
+    // in 16-row pages (a request of L keys fills ceil(L / 16) of them).
+    pl->packed = kind == PKV_PLAN_PREFILL && allow_pack && params->page_size < 8;
+    if (pl->packed) {
+      pl->max_packed = ceil_div(static_cast<int64_t>(limits->max_kv_pages) * params->page_size, 16) + limits->max_batch;
+      // Packed page ids and the packed copy's row coordinates are 32-bit.
+      if (pl->max_packed * 2 * hkv * 16 >= INT32_MAX) {
+        delete pl;
+        return PKV_ERR_INVALID_ARG;
+      }
+    }
   }
   set_layout(pl);
   pl->host_bytes = 2 * pl->L.tables_end;  // two table images: see pkv_plan_set_pipelined
@@ -477,8 +499,9 @@ int tile_kv_end(bool causal, int qo, int kv, int pos0, int npos) {
 // count); with nb_tiles, also the number of tiles of each count of key blocks.
 // The kv heads of a request repeat its tiles, so they count once per block.
 int64_t query_tile_blocks(const pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
-                          const int32_t* kv_last, bool skip_single, std::vector<int64_t>* nb_tiles) {
-  const int P = pl->p.page_size;
+                          const int32_t* kv_last, bool skip_single, std::vector<int64_t>* nb_tiles,
+                          int page_size = 0) {
+  const int P = page_size > 0 ? page_size : pl->p.page_size;
   const int mp = pkv::kPrefillRows / pl->group;
   const int64_t hkv = pl->p.num_kv_heads;
   if (nb_tiles) nb_tiles->clear();
@@ -556,8 +579,9 @@ int64_t prefill_makespan(const std::vector<int64_t>& nb_tiles, int64_t total, in
 // Prefill work over `C` CTAs; with skip_single the requests holding one query
 // row are left out (they are the decode half of a mixed batch).
 pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
-                           const int32_t* kv_last, uint8_t* host, int C = 0, bool skip_single = false) {
-  const int P = pl->p.page_size;
+                           const int32_t* kv_last, uint8_t* host, int C = 0, bool skip_single = false,
+                           int page_size = 0) {
+  const int P = page_size > 0 ? page_size : pl->p.page_size;
   const int BN = pkv::kPrefillKeys;
   if (C <= 0) C = pl->workers;
 
@@ -578,7 +602,7 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
     mask_off[b + 1] = mask_off[b] + static_cast<int64_t>(qo_indptr[b + 1] - qo_indptr[b]) *
                                         kv_len_of(kv_indptr, kv_last, b, P);
   pl->mask_bits = mask_off[batch];
-  const int64_t total = query_tile_blocks(pl, batch, qo_indptr, kv_indptr, kv_last, skip_single, nullptr);
+  const int64_t total = query_tile_blocks(pl, batch, qo_indptr, kv_indptr, kv_last, skip_single, nullptr, P);
   const int64_t chunk = key_chunk(total, C);
   // Each tile gives at most as many items as it counts blocks (chunk >= 2).
   items.reserve(static_cast<size_t>(std::min<int64_t>(total, pl->max_work) + 1));
@@ -733,6 +757,41 @@ pkv_status compute_prefill(pkv_plan* pl, int batch, const int32_t* qo_indptr, co
   for (int64_t v : load) tot += v;
   pl->total_cost = tot;
   pl->used_bytes = pl->L.segs + sizeof(PrefillTile) * (size_t)n;
+  return PKV_OK;
+}
+
+// A prefill plan on pages of fewer than 8 rows: request b's L keys become
+// ceil(L / 16) pages of 16 rows in the workspace's packed copy (page ids 0, 1, ...
+// in request order), each with its source run of keys; the prefill tables are then
+// planned over the packed page table as for 16-row pages.
+pkv_status compute_packed(pkv_plan* pl, int batch, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                          const int32_t* kv_last, uint8_t* host) {
+  const int P = pl->p.page_size;
+  PlanScratch& sc = pl->scratch;
+  sc.pk_indptr.assign(static_cast<size_t>(batch) + 1, 0);
+  sc.pk_last.assign(static_cast<size_t>(batch), 0);
+  auto* ids = reinterpret_cast<int32_t*>(host + pl->L.pk_ids);
+  auto* src = reinterpret_cast<pkv::PackedSrc*>(host + pl->L.pk_src);
+  int64_t n = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t L = kv_len_of(kv_indptr, kv_last, b, P);
+    const int64_t np = ceil_div(L, 16);
+    if (n + np > pl->max_packed) return PKV_ERR_WORKSPACE;
+    sc.pk_indptr[b] = static_cast<int32_t>(n);
+    sc.pk_last[b] = np > 0 ? static_cast<int32_t>(L - 16 * (np - 1)) : 0;
+    // tok0 + L <= max_kv_pages * P (validate() bounds the listed pages), which the
+    // size check at plan creation keeps far below 2^31.
+    const int64_t tok0 = static_cast<int64_t>(kv_indptr[b]) * P;
+    for (int64_t j = 0; j < np; ++j, ++n) {
+      ids[n] = static_cast<int32_t>(n);
+      src[n].tok0 = static_cast<int32_t>(tok0 + 16 * j);
+      src[n].ntok = static_cast<int32_t>(std::min<int64_t>(16, L - 16 * j));
+    }
+  }
+  sc.pk_indptr[batch] = static_cast<int32_t>(n);
+  pkv_status st = compute_prefill(pl, batch, qo_indptr, sc.pk_indptr.data(), sc.pk_last.data(), host, 0, false, 16);
+  if (st != PKV_OK) return st;
+  reinterpret_cast<PlanHeader*>(host + pl->L.header)->num_packed = static_cast<int32_t>(n);
   return PKV_OK;
 }
 
@@ -953,11 +1012,16 @@ pkv_status pkv_plan_compute(pkv_plan* plan, int batch, const int32_t* qo_indptr_
     st = compute_prefill(plan, batch, rows.data(), kv_indptr_h, kv_last_page_len_h, host);
   } else if (plan->kind == PKV_PLAN_DECODE) {
     st = compute_decode(plan, batch, kv_indptr_h, kv_last_page_len_h, host);
+  } else if (plan->packed) {
+    st = compute_packed(plan, batch, qo_indptr_h, kv_indptr_h, kv_last_page_len_h, host);
   } else {
     st = compute_prefill(plan, batch, qo_indptr_h, kv_indptr_h, kv_last_page_len_h, host);
   }
   if (st != PKV_OK) return st;
-  if (plan->kind != PKV_PLAN_MIXED) reinterpret_cast<PlanHeader*>(host + plan->L.header)->num_pages = num_pages;
+  // A packed plan's kernel reads the packed copy: its page-id check and its tensor
+  // map span the copy's capacity (and an id of max_packed, past it, reads zeros).
+  if (plan->kind != PKV_PLAN_MIXED)
+    reinterpret_cast<PlanHeader*>(host + plan->L.header)->num_pages = plan->packed ? plan->max_packed : num_pages;
   plan->batch = batch;
   plan->num_pages = num_pages;
   plan->total_q = plan->kind == PKV_PLAN_DECODE ? batch : (batch > 0 ? qo_indptr_h[batch] : 0);

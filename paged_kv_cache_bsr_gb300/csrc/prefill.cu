@@ -33,6 +33,42 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constan
   for (int pair = warp_id; pair < pairs; pair += n_warps) prefill_merge_row<T>(a, pair, lane, G);
 }
 
+// Packed copy of small pages: one CTA of 256 threads per packed page at a time.
+// Thread t owns row t / 16 of the page and its 16-byte piece t % 16 (16 pieces to
+// a 256-byte row: head_dim 128, 16-bit values) in every (K|V, head) block hs, so
+// it looks its source page up once and then issues the 2 Hkv loads of its piece
+// back to back.  The copy's layout [2, Hkv, 16, D] puts piece t of block hs at
+// hs * 256 + t; rows past the page's keys are zeros.
+constexpr int kPackThreads = 256;
+__global__ void __launch_bounds__(kPackThreads) pack_pages_kernel(const __grid_constant__ PackArgs a) {
+  constexpr int kPieces = kD * 2 / 16;  // 16-byte pieces per row
+  static_assert(kPackThreads == 16 * kPieces, "a thread per (row, piece) of a 16-row page");
+  const int nblk = 2 * a.num_kv_heads;   // (K|V, head) blocks of a page
+  const int n_packed = a.hdr->num_packed;
+  const int lp = __ffs(a.page_size) - 1;  // P is a power of two here
+  const int64_t row_elems = static_cast<int64_t>(a.page_size) * kD;  // one (page, K|V, head)
+  const int t = threadIdx.x, r = t / kPieces, piece = t % kPieces;
+  const uint4* kv = static_cast<const uint4*>(a.kv);
+  uint4* out = static_cast<uint4*>(a.packed);
+  for (int p = blockIdx.x; p < n_packed; p += gridDim.x) {
+    const PackedSrc sp = a.src[p];
+    int64_t e0 = -1;  // element offset of this thread's piece in block 0 of its source page
+    if (r < sp.ntok) {
+      const int u = sp.tok0 + r;
+      const int page = __ldg(a.kv_indices + (u >> lp));
+      if (page >= 0 && page < a.num_pages)
+        e0 = static_cast<int64_t>(page) * nblk * row_elems + static_cast<int64_t>(u & (a.page_size - 1)) * kD +
+             piece * 8;
+      else
+        atomicOr(a.err, kErrPageIndex);
+    }
+    uint4* dst = out + static_cast<int64_t>(p) * nblk * kPackThreads + t;
+#pragma unroll 16
+    for (int hs = 0; hs < nblk; ++hs)
+      dst[hs * kPackThreads] = e0 >= 0 ? ld_nc_v4(kv + (e0 + hs * row_elems) / 8) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::mutex mu;
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -126,6 +162,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int dt
     fn = masked ? (small ? launch_kernel<__half, true, true> : launch_kernel<__half, true, false>)
                 : (small ? launch_kernel<__half, false, true> : launch_kernel<__half, false, false>);
   return fn(a, group, cap, grid, tq, tkv, stream);
+}
+
+cudaError_t launch_pack_pages(const PackArgs& a, int head_dim, int grid, cudaStream_t stream) {
+  if (head_dim != kD || !(a.page_size == 1 || a.page_size == 2 || a.page_size == 4)) return cudaErrorInvalidValue;
+  pack_pages_kernel<<<grid, kPackThreads, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_merge(const PrefillArgs& a, int head_dim, int group, int dtype, int grid,
