@@ -369,7 +369,10 @@ def longest_first_prefill(b, C, rows_per_tile=256, keys=128):
                                                       (13, 1, 152, False, 16),
                                                       # CTA counts at the edges of 64-bit CTA sets
                                                       (21, 8, 64, True, 16), (23, 8, 65, True, 16),
-                                                      (25, 4, 1, True, 16), (27, 10, 130, False, 8)])
+                                                      (25, 4, 1, True, 16), (27, 10, 130, False, 8),
+                                                      # pages of 1 and 4 rows: planned over the packed
+                                                      # copy in 16-row pages, the same key ranges
+                                                      (29, 6, 37, True, 1), (31, 5, 152, True, 4)])
 def test_prefill_plan_is_the_longest_first_schedule(lib, seed, batch, C, causal, page):
     """The plan's work rows equal the plainly restated schedule, item by item and CTA by
     CTA (a faster implementation of the plan must not change what the GPU runs)."""
