@@ -148,11 +148,14 @@ def test_prefill_page_permutation_is_bit_exact():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_prefill_cuda_graph_replay_after_replanning():
+@pytest.mark.parametrize("P", [16, 1])
+def test_prefill_cuda_graph_replay_after_replanning(P):
     """Capture the prefill run calls once; re-plan another batch (same total query rows,
-    same pool) into the same workspace and buffers; replay gives that batch's result."""
-    hq, hkv, d, P = 8, 2, 128, 16
-    pool = 160
+    same pool) into the same workspace and buffers; replay gives that batch's result.
+    With one-row pages the captured calls include the packing copy, whose page count
+    the replay reads from the re-planned tables."""
+    hq, hkv, d = 8, 2, 128
+    pool = 2560 // P
     gen = torch.Generator().manual_seed(21)
     kv = torch.randn(pool, 2, hkv, P, d, generator=gen).to(torch.bfloat16)
 
