@@ -64,11 +64,14 @@ def test_page_sizes(page_size):
     prefill_vs_oracle(batch([90, 257], [33, 5], P=page_size, seed=page_size), f"page {page_size}")
 
 
-def test_rows_that_see_no_key_and_empty_requests():
-    # causal with more rows than keys: the first qo - kv rows see nothing (o = 0, lse = -inf)
-    b = W.make_paged_batch(qo_lens=[10, 0, 3, 40], kv_lens=[5, 9, 3, 1], num_qo_heads=8, num_kv_heads=2,
-                           head_dim=128, page_size=16, dtype=torch.bfloat16, seed=4, causal=True, poison=True)
-    prefill_vs_oracle(b, "no keys")
+@pytest.mark.parametrize("page_size", [16, 1])
+def test_rows_that_see_no_key_and_empty_requests(page_size):
+    # causal with more rows than keys: the first qo - kv rows see nothing (o = 0, lse = -inf);
+    # a request with no keys at all (no packed page either, with one-row pages)
+    b = W.make_paged_batch(qo_lens=[10, 0, 3, 40, 6], kv_lens=[5, 9, 3, 1, 0], num_qo_heads=8, num_kv_heads=2,
+                           head_dim=128, page_size=page_size, dtype=torch.bfloat16, seed=4, causal=True,
+                           poison=True)
+    prefill_vs_oracle(b, f"no keys, page {page_size}")
 
 
 def test_softcap_prefill():
