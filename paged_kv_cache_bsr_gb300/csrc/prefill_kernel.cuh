@@ -560,10 +560,22 @@ __device__ __forceinline__ void prefill_cta(const PrefillArgs& a, const CUtensor
         float mul = scale;
         if constexpr (CAP) {
           // cap * tanh(s * scale / cap), already in log2 units
+          // in pairs: cap * tanh(y) = k_out - 2 k_out / (e^(2y) + 1), e^(2y) = 2^(s * k_in)
           const float k_in = scale * 2.f * kLog2e / a.cap, k_out = a.cap * kLog2e;
+          const float2 kin2 = make_float2(k_in, k_in), one2 = make_float2(1.f, 1.f);
+          const float2 m2k = make_float2(-2.f * k_out, -2.f * k_out), kout2 = make_float2(k_out, k_out);
 #pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            sr[i] = __float_as_uint(k_out * tanh_from_log2(__uint_as_float(sr[i]) * k_in));
+          for (int i = 0; i < kBN; i += 2) {
+            float2 e = fmul2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), kin2);
+            e.x = fast_exp2(e.x);
+            e.y = fast_exp2(e.y);
+            float2 d = fadd2(e, one2);
+            d.x = fast_rcp(d.x);
+            d.y = fast_rcp(d.y);
+            const float2 x = ffma2(d, m2k, kout2);
+            sr[i] = __float_as_uint(x.x);
+            sr[i + 1] = __float_as_uint(x.y);
+          }
           mul = 1.f;
         }
         if (!full) {
