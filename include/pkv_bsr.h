@@ -196,9 +196,10 @@ pkv_status pkv_plan_get_work(const pkv_plan* plan, int32_t* out, int64_t capacit
 
 /*
  * Profiling hook.  While set, every run call on this plan records `start` on
- * its stream just before the main kernel (decode or prefill) and `stop` just
- * after it, before the merge kernel, so the caller can time the main kernel
- * alone with cudaEventElapsedTime.  The events (cudaEvent_t) stay the
+ * its stream just before the main kernel (decode or prefill; for a prefill
+ * plan on pages of fewer than 8 rows, before the copy into 16-row pages that
+ * precedes it) and `stop` just after it, before the merge kernel, so the caller
+ * can time the main kernel alone with cudaEventElapsedTime.  The events (cudaEvent_t) stay the
  * caller's; pass NULL for both to clear.
  * Errors: PKV_ERR_INVALID_ARG.
  */
