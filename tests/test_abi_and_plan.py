@@ -856,3 +856,38 @@ def test_group8_mixed_plan_sends_single_rows_to_the_prefill_half(lib):
     info = api.plan_get_info(h)
     assert info.prefill_ctas == 152 and info.decode_ctas == 0
     api.plan_destroy(h)
+
+
+# --------------------------------------------------------------------------- prefill on small pages: the packed copy
+@pytest.mark.parametrize("P", [1, 2, 4])
+def test_packed_prefill_workspace_holds_the_copy(lib, P):
+    """A prefill plan on pages of fewer than 8 rows reserves, in its device workspace, a copy of
+    its limits' keys in 16-row pages: ceil(max_kv_pages * P / 16) + max_batch pages of
+    2 x Hkv x 16 x head_dim 16-bit values beyond what the same plan on 16-row pages needs."""
+    hq, hkv, d = 32, 8, 128
+    max_b, max_q, max_pages = 7, 4000, 3000
+    def dev_bytes(page_size, kind=api.PLAN_PREFILL):
+        params = api.make_params(hq, hkv, d, page_size, torch.bfloat16, d ** -0.5, 0.0, True)
+        h = api.plan_create_host(kind, params, api.Limits(max_b, max_q, max_pages), 152)
+        dev, _ = api.plan_workspace_bytes(h)
+        api.plan_destroy(h)
+        return dev
+    packed_pages = -(-max_pages * P // 16) + max_b
+    copy_bytes = packed_pages * 2 * hkv * 16 * d * 2
+    assert dev_bytes(P) - dev_bytes(16) >= copy_bytes
+    # decode plans and mixed plans read the caller's pages directly: no copy
+    assert dev_bytes(P, api.PLAN_DECODE) == dev_bytes(16, api.PLAN_DECODE)
+    assert dev_bytes(P, api.PLAN_MIXED) < dev_bytes(P) + dev_bytes(P, api.PLAN_DECODE)
+
+
+def test_packed_prefill_refuses_limits_past_32_bit_rows(lib):
+    """The packed copy's rows are counted in 32 bits: limits whose copy would pass 2^31 rows are
+    refused at plan creation (PKV_ERR_INVALID_ARG), the same limits on 16-row pages are not."""
+    params1 = api.make_params(32, 8, 128, 1, torch.bfloat16, 128 ** -0.5, 0.0, True)
+    params16 = api.make_params(32, 8, 128, 16, torch.bfloat16, 128 ** -0.5, 0.0, True)
+    lim = api.Limits(4, 1 << 20, 150_000_000)  # 150 M one-row pages: 9.4 M packed pages x 256 rows
+    with pytest.raises(api.PkvError) as e:
+        api.plan_create_host(api.PLAN_PREFILL, params1, lim, 152)
+    assert e.value.status == -1
+    h = api.plan_create_host(api.PLAN_PREFILL, params16, api.Limits(4, 1 << 20, 150_000_000 // 16), 152)
+    api.plan_destroy(h)
