@@ -349,9 +349,10 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
   if (W <= 0) W = pl->workers;
   if (!pl->split_kv && !qo_indptr) return compute_decode_whole(pl, batch, kv_indptr, kv_last, host, W);
   auto takes_part = [&](int b) { return !qo_indptr || qo_indptr[b + 1] - qo_indptr[b] == 1; };
-  const int64_t pages_per_chunk = ceil_div(P, pkv::kDecodeTileRows);
-  // Runs of at least 4 tiles: shorter ones no longer help small batches (measured).
-  const int64_t min_run = std::max<int64_t>(1, 4 / pages_per_chunk);
+  // Runs as short as one page: on the tiny fp16 batch (4 requests x 2 kv heads of
+  // 5-13 pages) runs of one page took a run call from 10.1 us to 6.3 us against
+  // a 4-tile minimum, and no batch measured slower (64 x 8 lists of 1-128 pages,
+  // the Llama-3-8B lengths, the prefix tree, the mixed batch).
   int64_t total = 0;
   int parts = 0;
   for (int b = 0; b < batch; ++b)
@@ -359,7 +360,7 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
       total += (int64_t)(kv_indptr[b + 1] - kv_indptr[b]) * hkv;
       ++parts;
     }
-  const int64_t run = total > 0 ? std::max<int64_t>(ceil_div(total, W), min_run) : 1;
+  const int64_t run = total > 0 ? ceil_div(total, W) : 1;
   const int active = total > 0 ? static_cast<int>(ceil_div(total, run)) : (parts > 0 ? 1 : 0);
   if (!qo_indptr && static_cast<int64_t>(batch) * hkv <= W) {
     // When no list is longer than a run there is nothing to split, and the run
@@ -836,11 +837,10 @@ pkv_status compute_mixed(pkv_plan* pl, int batch, const int32_t* qo_indptr, cons
     std::vector<int64_t>& by_load = sc.by_load;
     std::vector<int64_t>& nb_tiles = sc.nb_tiles;  // tiles per count of key blocks
     const int64_t total = query_tile_blocks(pl, batch, qo_indptr, kv_indptr, kv_last, true, &nb_tiles);
-    const int64_t min_run = std::max<int64_t>(1, 4 / ceil_div(P, pkv::kDecodeTileRows));
     const double page_us = kDecodePage16Us * P / 16.0;
     auto t_pre = [&](int c) { return kPrefillFixedUs + kPrefillBlockUs * prefill_makespan(nb_tiles, total, c, by_cost, by_load); };
     auto t_dec = [&](int n) {
-      const int64_t run = std::max<int64_t>(ceil_div(dec_pages, (int64_t)n * pkv::kDecodeWarps), min_run);
+      const int64_t run = ceil_div(dec_pages, (int64_t)n * pkv::kDecodeWarps);
       return kDecodeFixedUs + page_us * run;
     };
     // Smallest prefill share whose prefill time no longer exceeds the decode time.

@@ -390,17 +390,15 @@ def test_prefill_plan_is_the_longest_first_schedule(lib, seed, batch, C, causal,
 
 def equal_runs_decode(b, W, tile_rows=16):
     """The decode plan restated plainly: the (request, kv head) page lists concatenated in
-    order and cut into runs of max(ceil(total / W), min_run) pages, one run per worker; a
+    order and cut into runs of ceil(total / W) pages, one run per worker; a
     list that crosses a run boundary is split there, each piece a partial-state slot.  Run r
     goes to warp r // C of CTA r % C (C = W // 8 CTAs of 8 warps), worker 8 * CTA + warp.
     Returns the work rows [worker, request, kv head, first page, pages, last rows, slot, 0]
     in worker order."""
     P = b.page_size
-    pages_per_tile = -(-P // tile_rows)
-    min_run = max(1, 4 // pages_per_tile)
     lens = [int(b.kv_indptr[r + 1] - b.kv_indptr[r]) for r in range(b.batch)]
     total = sum(lens) * b.num_kv_heads
-    run = max(-(-total // W), min_run) if total else 1
+    run = -(-total // W) if total else 1
     active = -(-total // run) if total else (1 if b.batch else 0)
     rows, x, slot = [], 0, 0
     for r in range(b.batch):
@@ -444,16 +442,17 @@ def fits_in_one_run(b, W, tile_rows=16):
     split plan then keeps each list whole, one per worker (the whole-list schedule)."""
     lens = [int(b.kv_indptr[r + 1] - b.kv_indptr[r]) for r in range(b.batch)]
     total = sum(lens) * b.num_kv_heads
-    min_run = max(1, 4 // -(-b.page_size // tile_rows))
-    run = max(-(-total // W), min_run) if total else 1
+    run = -(-total // W) if total else 1
     return b.batch * b.num_kv_heads <= W and max(lens, default=0) <= run
 
 
-@pytest.mark.parametrize("kv_lens,sms,whole", [([16] * 64, 152, True), ([64] * 64, 152, True),
-                                               ([128] * 64, 152, False), ([16] * 64, 4, False)])
+@pytest.mark.parametrize("kv_lens,sms,whole", [([16] * 64, 152, True), ([64] * 64, 152, False),
+                                               ([128] * 64, 152, False), ([16] * 64, 4, False),
+                                               ([16] * 100, 152, True)])
 def test_decode_plan_keeps_short_lists_whole_when_workers_allow(lib, kv_lens, sms, whole):
-    """64 x 8 lists of 1, 4 or 8 pages on 152 SMs (1216 workers), and of one page on 4 SMs
-    (32 workers, fewer than the lists): whole lists exactly when none exceeds a run."""
+    """64 x 8 lists of 1, 4 or 8 pages on 152 SMs (1216 workers: runs of 1, 2 and 4 pages), one
+    page on 4 SMs (32 workers, fewer than the lists) and 100 x 8 one-page lists: whole lists
+    exactly when none exceeds a run and every list has a worker."""
     b = table_batch(kv_lens)
     assert fits_in_one_run(b, sms * 8) == whole
     h, ws = host_plan(b, api.PLAN_DECODE, num_sms=sms)

@@ -65,10 +65,10 @@ def test_cascade_full_view_decode_softcap():
     decode_vs_oracle(cb.full, "cascade-full")
 
 
-@pytest.mark.parametrize("kv_len,whole", [(16, True), (64, True), (128, False), (200, False)])
+@pytest.mark.parametrize("kv_len,whole", [(16, True), (64, False), (128, False), (200, False)])
 def test_plan_placements_of_short_lists(kv_len, whole):
-    """64 requests x 8 kv heads of equal short lists: one and four pages are kept whole, one list
-    per worker; eight and thirteen pages are split into runs spread over the CTAs and merged.
+    """64 requests x 8 kv heads of equal short lists: one-page lists are kept whole, one list
+    per worker; four, eight and thirteen pages are split into runs spread over the CTAs and merged.
     Both placements give the oracle's result (poisoned pool, soft-cap on)."""
     b = W.make_paged_batch(qo_lens=[1] * 64, kv_lens=[kv_len] * 64, num_qo_heads=32, num_kv_heads=8,
                            head_dim=128, page_size=16, dtype=torch.bfloat16, seed=40 + kv_len, poison=True,
