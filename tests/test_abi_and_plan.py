@@ -341,7 +341,7 @@ def longest_first_prefill(b, C, rows_per_tile=256, keys=128):
                 end = max(0, min(kv, pos0 + npos + kv - qo)) if b.causal else kv
                 tiles.append((bb, kvh, pos0, npos, end))
                 total += max(1, -(-end // keys))
-    chunk = max(-(-total // max(C, 1)), 2)
+    chunk = max(-(-total // max(C, 1)), 1)
     items, slot = [], 0
     for bb, kvh, pos0, npos, end in tiles:
         nb = -(-end // keys)
