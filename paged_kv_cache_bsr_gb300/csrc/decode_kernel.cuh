@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
 template <int D, int G, typename T>
 __device__ __forceinline__ void decode_merge_pair(const DecodeArgs& a, int pair, int lane) {
   constexpr int PER = D / 32;  // dims per lane
-  constexpr int U = 32;        // slots in flight per lane (8: the skewed batch's 180-slot merges ran 3 % slower)
+  constexpr int U = 8;         // slots in flight per lane
   {
     const MergeItem it = a.merge[pair / G];
     const int g = pair % G;
