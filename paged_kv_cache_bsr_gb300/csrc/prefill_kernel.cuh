@@ -746,33 +746,16 @@ __device__ __forceinline__ void prefill_merge_row(const PrefillArgs& a, int pair
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;
   if (mx != -INFINITY) {
-    // Lane j holds the weight of slot i0 + j; the partial rows of up to 8 slots are
-    // loaded before any is used, so their latencies overlap.
-    constexpr int U = 8;
-    for (int i0 = 0; i0 < it.n_slots; i0 += 32) {
-      const float w_lane =
-          i0 + lane < it.n_slots
-              ? fast_exp2((a.part_lse[static_cast<int64_t>(it.slot_begin + i0 + lane) * kWR + r] - mx) * kLog2e)
-              : 0.f;
-      const int cnt = min(32, it.n_slots - i0);
-      for (int j0 = 0; j0 < cnt; j0 += U) {
-        float4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          v[u] = j0 + u < cnt ? reinterpret_cast<const float4*>(
-                                    a.part_o + (static_cast<int64_t>(it.slot_begin + i0 + j0 + u) * kWR + r) * kD)[lane]
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const float w = __shfl_sync(kFull, w_lane, (j0 + u) & 31);
-          if (j0 + u < cnt && w > 0.f) {  // a chunk with no key (w = 0) adds nothing
-            acc[0] = fmaf(w, v[u].x, acc[0]);
-            acc[1] = fmaf(w, v[u].y, acc[1]);
-            acc[2] = fmaf(w, v[u].z, acc[2]);
-            acc[3] = fmaf(w, v[u].w, acc[3]);
-            wsum += w;
-          }
-        }
+    for (int i = 0; i < it.n_slots; ++i) {
+      const int64_t row = static_cast<int64_t>(it.slot_begin + i) * kWR + r;
+      const float w = fast_exp2((a.part_lse[row] - mx) * kLog2e);
+      if (w > 0.f) {
+        const float4 v = reinterpret_cast<const float4*>(a.part_o + row * kD)[lane];
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]);
+        acc[3] = fmaf(w, v.w, acc[3]);
+        wsum += w;
       }
     }
   }
