@@ -326,7 +326,7 @@ def check_prefill_plan(h, b, num_sms=152, rows_per_tile=256):
 def longest_first_prefill(b, C, rows_per_tile=256, keys=128):
     """The prefill plan's schedule restated plainly: query tiles per (request, kv head,
     rows_per_tile / G positions), their key ranges cut into near-equal chunks when longer
-    than total / C blocks, item cost = blocks + 1, items longest first (ties: lower item)
+    than total / C blocks, item cost = blocks + 2, items longest first (ties: lower item)
     onto the least-loaded CTA (ties: lower CTA).  Returns the work rows in the plan's
     order (CTA by CTA, each CTA's items in the order assigned)."""
     import heapq
@@ -346,12 +346,12 @@ def longest_first_prefill(b, C, rows_per_tile=256, keys=128):
     for bb, kvh, pos0, npos, end in tiles:
         nb = -(-end // keys)
         if nb <= chunk:
-            items.append(((bb, kvh, pos0, npos, 0, end, -1), max(nb, 1) + 1))
+            items.append(((bb, kvh, pos0, npos, 0, end, -1), max(nb, 1) + 2))
         else:
             parts = -(-nb // chunk)
             for i in range(parts):
                 lo, hi = i * nb // parts, (i + 1) * nb // parts
-                items.append(((bb, kvh, pos0, npos, lo * keys, min(hi * keys, end), slot), hi - lo + 1))
+                items.append(((bb, kvh, pos0, npos, lo * keys, min(hi * keys, end), slot), hi - lo + 2))
                 slot += 1
     order = sorted(range(len(items)), key=lambda i: -items[i][1])  # stable: ties keep item order
     ctas = min(C, len(items))
@@ -471,8 +471,8 @@ def test_prefill_plan_ragged_causal(lib):
     info, work = check_prefill_plan(h, b)
     costs = {}
     for w, bb, kvh, pos0, npos, kb, ke, slot in work:
-        costs[w] = costs.get(w, 0) + -(-(ke - kb) // 128) + 1
-    biggest = max(-(-(ke - kb) // 128) + 1 for _, _, _, _, _, kb, ke, _ in work)
+        costs[w] = costs.get(w, 0) + -(-(ke - kb) // 128) + 2
+    biggest = max(-(-(ke - kb) // 128) + 2 for _, _, _, _, _, kb, ke, _ in work)
     assert max(costs.values()) - min(costs.values()) <= biggest
     assert info.num_merge == 0  # thousands of tiles: no key range needs splitting
     api.plan_destroy(h)
@@ -768,13 +768,13 @@ def test_run_calls_refuse_bad_arguments_before_any_cuda_call(lib):
 
 
 def test_bench_mixed_batch_takes_the_measured_split(lib):
-    """The bench's mixed batch (60 decodes + 4 prompt chunks) splits 68 prefill / 84 decode
+    """The bench's mixed batch (60 decodes + 4 prompt chunks) splits 72 prefill / 80 decode
     SMs of 152: the split its one-launch timings and profile were taken at."""
     b = W.mixed_batch(seed=1007)
     h, ws = host_plan(b, api.PLAN_MIXED)
     compute(h, ws, b)
     info = api.plan_get_info(h)
-    assert (info.prefill_ctas, info.decode_ctas) == (68, 84)
+    assert (info.prefill_ctas, info.decode_ctas) == (72, 80)
     api.plan_destroy(h)
 
 
@@ -803,7 +803,7 @@ def test_prefill_plan_balances_zipf_prompt_lengths(lib, s):
     h, ws = host_plan(b, api.PLAN_PREFILL)
     compute(h, ws, b)
     info, work = check_prefill_plan(h, b)
-    biggest = max(max(1, -(-(ke - kb) // 128)) + 1 for _, _, _, _, _, kb, ke, _ in work)
+    biggest = max(max(1, -(-(ke - kb) // 128)) + 2 for _, _, _, _, _, kb, ke, _ in work)
     assert info.max_cost <= -(-info.total_cost // info.active_workers) + biggest
     api.plan_destroy(h)
 
