@@ -36,6 +36,7 @@
 #include "pkv_bsr.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_launch.h"
 
 namespace pkv {
 namespace {
@@ -120,6 +121,9 @@ template <int D, typename T, bool ROT>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const __grid_constant__ AppendArgs a) {
   constexpr int LPH = D / 16;  // lanes per head row
   __shared__ int32_t s_indptr[kIndptrSmem];
+  // Launched as a programmatic dependent of the kernel before it on the stream:
+  // nothing global is touched before that grid has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const bool staged = a.batch < kIndptrSmem;
   if (staged)
     for (int i = threadIdx.x; i <= a.batch; i += blockDim.x) s_indptr[i] = a.append_indptr[i];
@@ -201,11 +205,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const __gri
 
 template <int D, typename T>
 cudaError_t launch_t(const AppendArgs& a, int grid, cudaStream_t s) {
-  if (a.rope)
-    append_rope_kernel<D, T, true><<<grid, kAppendThreads, 0, s>>>(a);
-  else
-    append_rope_kernel<D, T, false><<<grid, kAppendThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return a.rope ? launch_dependent(append_rope_kernel<D, T, true>, grid, kAppendThreads, 0, s, a)
+                : launch_dependent(append_rope_kernel<D, T, false>, grid, kAppendThreads, 0, s, a);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

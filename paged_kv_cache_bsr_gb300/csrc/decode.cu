@@ -40,19 +40,8 @@ cudaError_t dispatch_merge(const DecodeArgs& a, int D, int G, int grid, cudaStre
 // kernel triggers no earlier, so waiting merge CTAs never hold SMs that work on
 // another stream needs), and it waits (griddepcontrol.wait) for the whole
 // grid before reading partial states.
-#define PKV_MERGE_CASE(DD, GG)                                                              \
-  if (D == DD && G == GG) {                                                                 \
-    cudaLaunchConfig_t cfg = {};                                                            \
-    cfg.gridDim = dim3(grid);                                                               \
-    cfg.blockDim = dim3(kMergeThreads);                                                     \
-    cfg.stream = s;                                                                         \
-    cudaLaunchAttribute attr[1];                                                            \
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                        \
-    attr[0].val.programmaticStreamSerializationAllowed = 1;                                 \
-    cfg.attrs = attr;                                                                       \
-    cfg.numAttrs = 1;                                                                       \
-    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<DD, GG, T>, a);                     \
-  }
+#define PKV_MERGE_CASE(DD, GG) \
+  if (D == DD && G == GG) return launch_dependent(decode_merge_kernel<DD, GG, T>, grid, kMergeThreads, 0, s, a);
   PKV_MERGE_CASE(128, 1) PKV_MERGE_CASE(128, 2) PKV_MERGE_CASE(128, 4) PKV_MERGE_CASE(128, 8)
   PKV_MERGE_CASE(64, 1) PKV_MERGE_CASE(64, 2) PKV_MERGE_CASE(64, 4) PKV_MERGE_CASE(64, 8)
 #undef PKV_MERGE_CASE

@@ -513,6 +513,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_kernel(const __gr
   constexpr int S = DecodeShape<D, T>::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kDecodeWarps][S];
+  // Launched as a programmatic dependent of the kernel before it on the stream:
+  // nothing global is touched before that grid has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   decode_worker<D, G, LPT, T, CAP, GATHER>(a, blockIdx.x * kDecodeWarps + warp, smem + warp * kDecodeWarpSmem,
                                            smem_addr(&bars[warp][0]));
@@ -602,8 +605,7 @@ cudaError_t launch_decode_kernel(const DecodeArgs& a, int D, int G, bool cap, in
   static_assert(kDecodeWarps * kDecodeWarpSmem <= 200 * 1024, "decode ring exceeds shared memory");
   cudaError_t e = ensure_smem_limit(kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kDecodeWarps * 32, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, kDecodeWarps * 32, smem, s, a);
 }
 
 // Each instance set is compiled in its own translation unit (decode.cu: bulk

@@ -164,22 +164,18 @@ cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* 
   auto a = static_cast<const uint8_t*>(o_a);
   auto b = static_cast<const uint8_t*>(o_b);
   auto o = static_cast<uint8_t*>(o_out);
-  // Its CTAs may start while the producing kernel's last CTAs finish (they wait
-  // for the whole grid before reading).
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // A programmatic dependent of the kernel that produced the states: its CTAs
+  // are placed as that grid's CTAs exit and wait for the whole grid before reading.
   switch (dtype) {
-    case PKV_F32: return cudaLaunchKernelEx(&cfg, merge_state_kernel<float>, a, lse_a, b, lse_b, o, lse_out, rows, chunks);
+    case PKV_F32:
+      return launch_dependent(merge_state_kernel<float>, grid, 256, 0, stream, a, lse_a, b, lse_b, o, lse_out, rows,
+                              chunks);
     case PKV_BF16:
-      return cudaLaunchKernelEx(&cfg, merge_state_kernel<__nv_bfloat16>, a, lse_a, b, lse_b, o, lse_out, rows, chunks);
-    case PKV_F16: return cudaLaunchKernelEx(&cfg, merge_state_kernel<__half>, a, lse_a, b, lse_b, o, lse_out, rows, chunks);
+      return launch_dependent(merge_state_kernel<__nv_bfloat16>, grid, 256, 0, stream, a, lse_a, b, lse_b, o, lse_out,
+                              rows, chunks);
+    case PKV_F16:
+      return launch_dependent(merge_state_kernel<__half>, grid, 256, 0, stream, a, lse_a, b, lse_b, o, lse_out, rows,
+                              chunks);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -201,24 +197,16 @@ cudaError_t launch_merge_states(const void* o_in, const float* lse_in, int n_sta
   const int grid = static_cast<int>(want < sms * 8 ? want : sms * 8);
   auto in = static_cast<const uint8_t*>(o_in);
   auto o = static_cast<uint8_t*>(o_out);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   switch (dtype) {
     case PKV_F32:
-      return cudaLaunchKernelEx(&cfg, merge_states_kernel<float>, in, lse_in, n_states, stride, o, lse_out, rows, chunks);
+      return launch_dependent(merge_states_kernel<float>, grid, 256, 0, stream, in, lse_in, n_states, stride, o,
+                              lse_out, rows, chunks);
     case PKV_BF16:
-      return cudaLaunchKernelEx(&cfg, merge_states_kernel<__nv_bfloat16>, in, lse_in, n_states, stride, o, lse_out,
-                                rows, chunks);
+      return launch_dependent(merge_states_kernel<__nv_bfloat16>, grid, 256, 0, stream, in, lse_in, n_states, stride,
+                              o, lse_out, rows, chunks);
     case PKV_F16:
-      return cudaLaunchKernelEx(&cfg, merge_states_kernel<__half>, in, lse_in, n_states, stride, o, lse_out, rows,
-                                chunks);
+      return launch_dependent(merge_states_kernel<__half>, grid, 256, 0, stream, in, lse_in, n_states, stride, o,
+                              lse_out, rows, chunks);
     default: return cudaErrorInvalidValue;
   }
 }

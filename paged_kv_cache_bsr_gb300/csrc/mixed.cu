@@ -43,16 +43,7 @@ cudaError_t launch_mixed_merge(const PrefillArgs& pa, const DecodeArgs& da, int 
   PKV_MM_CASE(1) PKV_MM_CASE(2) PKV_MM_CASE(4) PKV_MM_CASE(8)
 #undef PKV_MM_CASE
   if (!kern) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kMergeThreads);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, pa, da);
+  return launch_dependent(kern, grid, kMergeThreads, 0, stream, pa, da);
 }
 
 cudaError_t launch_mixed(const PrefillArgs& pa, const DecodeArgs& da, int head_dim, int group, int dtype, bool cap,

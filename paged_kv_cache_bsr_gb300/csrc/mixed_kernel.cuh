@@ -62,6 +62,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mixed_kernel(const __grid_constant__ PrefillArgs pa, const __grid_constant__ DecodeArgs da,
                  const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  // Launched as a programmatic dependent of the kernel before it on the stream:
+  // nothing global is touched before that grid has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int split = da.hdr->cta_offset;
   const int cta = static_cast<int>(blockIdx.x);
   if (cta < split) {
@@ -114,8 +117,7 @@ cudaError_t launch_mixed_kernel(const PrefillArgs& pa, const DecodeArgs& da, int
   const int smem = pre_bytes > dec_bytes ? pre_bytes : dec_bytes;
   cudaError_t e = ensure_smem_limit(kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, s>>>(pa, da, tq, tkv);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, kThreads, smem, s, pa, da, tq, tkv);
 }
 
 extern template cudaError_t launch_mixed_kernel<__nv_bfloat16, false>(const PrefillArgs&, const DecodeArgs&, int,

@@ -46,6 +46,29 @@ inline cudaError_t ensure_smem_limit(Kernel kern, int bytes) {
   return ensure_smem_limit_ptr(reinterpret_cast<const void*>(kern), bytes);
 }
 
+// Launch a kernel as a programmatic dependent of the kernel before it on the
+// stream.  No kernel of this library triggers its dependents early, so the new
+// grid's CTAs are placed as the previous grid's CTAs exit, which hides the gap
+// between the two launches.  The launched kernel executes griddepcontrol.wait
+// before its first global-memory access; the wait returns once the previous
+// grid has finished and its writes are visible.  After a copy, a memset or an
+// event on the stream it is an ordinary launch.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(Params...), int grid, int block, int smem, cudaStream_t s,
+                                   const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Warps per decode CTA; each warp streams its own pages (one CTA per SM).
 constexpr int kDecodeWarps = 8;
 // Shared memory each decode warp uses for its ring of page tiles.
