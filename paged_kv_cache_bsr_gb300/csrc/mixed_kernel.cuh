@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int split = da.hdr->cta_offset;
   const int cta = static_cast<int>(blockIdx.x);
   if (cta < split) {
-    prefill_impl::prefill_cta<G, T, CAP, false, SMALL>(pa, tq, tkv, cta, smem);
+    prefill_impl::prefill_cta<G, T, CAP, false, SMALL, true>(pa, tq, tkv, cta, smem);
     return;
   }
   const int warp = threadIdx.x >> 5;
