@@ -38,7 +38,11 @@
  *  - Causal prefill: row i of a request with qo_len rows and kv_len keys sees
  *    keys j <= i + kv_len - qo_len.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Run calls
- *    enqueue work and return; they never synchronise the host.
+ *    enqueue work and return; they never synchronise the host.  Their kernels
+ *    (all but the standalone prefill kernel) are launched as programmatic
+ *    dependents of the kernel before them on `stream`: their blocks may be
+ *    placed as that kernel's blocks exit, but read and write nothing before
+ *    it has completed and its writes are visible, so stream order holds.
  *  - Errors are returned as pkv_status; nothing is thrown and nothing is
  *    printed.  A failed call enqueues no kernel.
  */

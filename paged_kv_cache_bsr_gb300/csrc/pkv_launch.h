@@ -51,8 +51,11 @@ inline cudaError_t ensure_smem_limit(Kernel kern, int bytes) {
 // grid's CTAs are placed as the previous grid's CTAs exit, which hides the gap
 // between the two launches.  The launched kernel executes griddepcontrol.wait
 // before its first global-memory access; the wait returns once the previous
-// grid has finished and its writes are visible.  After a copy, a memset or an
-// event on the stream it is an ordinary launch.
+// grid has finished and its writes are visible.  Every thread waits before it
+// can return, so no grid launched this way finishes before the grid it depends
+// on, and a chain of such launches stays ordered after every earlier kernel on
+// the stream.  After a copy, a memset or an event on the stream it is an
+// ordinary launch.
 template <typename... Params, typename... Args>
 inline cudaError_t launch_dependent(void (*kern)(Params...), int grid, int block, int smem, cudaStream_t s,
                                    const Args&... args) {
