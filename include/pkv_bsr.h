@@ -140,8 +140,9 @@ pkv_status pkv_plan_workspace_bytes(const pkv_plan* plan, size_t* dev_bytes, siz
  * The plan step (fdeinterviews "Load balancing"; greptalks "Runtime
  * Scheduler").  Reads HOST copies of the index arrays, validates them
  * (monotone indptr, page ids in [0, num_pages), last_page_len in range,
- * sizes within the limits), splits the KV work into equal chunks over the
- * fixed worker grid, records where every partial state goes, and enqueues one
+ * sizes within the limits), splits the KV work into chunks of equal cost over
+ * the fixed worker grid (pages, plus one page's worth for each piece of a
+ * (request, kv head) page list), records where every partial state goes, and enqueues one
  * host-to-device copy of the tables (from `host_ws`, which must be pinned) into
  * `dev_ws` on `stream`.  Clears the device error word.
  *  - qo_indptr_h: host [batch+1]; NULL for decode (one row per request).
@@ -225,7 +226,7 @@ pkv_status pkv_plan_set_pipelined(pkv_plan* plan, int on);
 
 /*
  * Split-KV on or off for a decode plan (default on).  On, the plan step cuts
- * the (request, kv head) page lists into equal runs over the workers and merges
+ * the (request, kv head) page lists into runs of equal cost over the workers and merges
  * the partial states ("FlashInfer" guide, section 3 "FlashDecoding"; fdeinterviews
  * summary, "Load balancing that survives CUDA graphs").  Off, each page list goes
  * whole to one worker (one warp), longest first onto the least-loaded worker,

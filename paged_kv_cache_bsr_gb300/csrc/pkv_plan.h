@@ -31,6 +31,7 @@ struct PlanScratch {
   std::vector<DecodeSeg> dsegs;
   std::vector<int32_t> run_ptr;
   std::vector<int32_t> pk_indptr, pk_last;
+  std::vector<std::pair<int, int32_t>> cuts;
 };
 
 }  // namespace pkv

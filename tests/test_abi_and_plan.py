@@ -124,14 +124,14 @@ def check_decode_plan(h, b, num_sms=152):
             slots.add(slot)
     want = {(bb, kvh, p) for bb in range(b.batch) for kvh in range(hkv) for p in range(counts[bb])}
     assert set(covered) == want
-    # workers appear in non-decreasing order and the runs are equal chunks
+    # workers appear in non-decreasing order and no run holds more than ceil(T / 8) pages
     ws_ = work[:, 0].tolist()
     assert ws_ == sorted(ws_)
     total = sum(counts) * hkv
     assert info.total_cost == total
     if total:
-        run = max(-(-total // info.workers), 8)
-        assert info.max_cost <= run
+        # pages of one run have midpoints 8 apart inside a cost interval of length T
+        assert info.max_cost <= -(-decode_cost_target(b, info.workers) // 8)
         assert max(per_worker.values()) == info.max_cost
     assert info.num_slots == len(slots)
     # an empty request still gets exactly one entry per kv head (it writes o = 0)
@@ -388,35 +388,47 @@ def test_prefill_plan_is_the_longest_first_schedule(lib, seed, batch, C, causal,
     assert work == longest_first_prefill(b, C)
 
 
-def equal_runs_decode(b, W, tile_rows=16):
-    """The decode plan restated plainly: the (request, kv head) page lists concatenated in
-    order and cut into runs of ceil(total / W) pages, one run per worker; a
-    list that crosses a run boundary is split there, each piece a partial-state slot.  Run r
-    goes to warp r // C of CTA r % C (C = W // 8 CTAs of 8 warps), worker 8 * CTA + warp.
-    Returns the work rows [worker, request, kv head, first page, pages, last rows, slot, 0]
-    in worker order."""
-    P = b.page_size
+def decode_cost_target(b, W):
+    """The decode plan's cost per run T, in eighths of a page: a page costs 8 and each
+    piece of a (request, kv head) page list 8 more; the whole cost counting one piece per
+    list and one more per run boundary, over W runs (at least one piece and one page)."""
     lens = [int(b.kv_indptr[r + 1] - b.kv_indptr[r]) for r in range(b.batch)]
     total = sum(lens) * b.num_kv_heads
-    run = -(-total // W) if total else 1
-    active = -(-total // run) if total else (1 if b.batch else 0)
-    rows, x, slot = [], 0, 0
+    return max(16, -(-(8 * total + 8 * (b.batch * b.num_kv_heads + W - 1)) // W))
+
+
+def cost_runs_decode(b, W):
+    """The decode plan restated plainly, page by page: the (request, kv head) page lists in
+    order on a cost line, each page costing 8 and each piece of a list 8 before its first
+    page.  A page belongs to run min(midpoint // T, W - 1); a piece starts at a list's first
+    page and wherever a page (at the cost so far) falls in another run than the piece's.  A
+    list of several pieces has a partial-state slot per piece.  Run r goes to warp r // C of
+    CTA r % C (C = W // 8 CTAs of 8 warps), worker 8 * CTA + warp.  Returns the work rows
+    [worker, request, kv head, first page, pages, last rows, slot, 0] in worker order."""
+    P = b.page_size
+    lens = [int(b.kv_indptr[r + 1] - b.kv_indptr[r]) for r in range(b.batch)]
+    T = decode_cost_target(b, W)
+    rows, slot, X = [], 0, 0
     for r in range(b.batch):
         n = lens[r]
         last = int(b.kv_last_page_len[r])
         for h in range(b.num_kv_heads):
             if n == 0:
-                rows.append([min(x // run, active - 1), r, h, 0, 0, 0, -1, 0])
+                rows.append([min(X // T, W - 1), r, h, 0, 0, 0, -1, 0])
                 continue
-            w0, w1 = x // run, (x + n - 1) // run
-            if w0 == w1:
-                rows.append([w0, r, h, 0, n, last, -1, 0])
+            pieces = []  # [run, first page, pages]
+            for i in range(n):
+                if not pieces or min((X + 4) // T, W - 1) != pieces[-1][0]:
+                    X += 8  # the new piece's start
+                    pieces.append([min((X + 4) // T, W - 1), i, 0])
+                pieces[-1][2] += 1
+                X += 8
+            if len(pieces) == 1:
+                rows.append([pieces[0][0], r, h, 0, n, last, -1, 0])
             else:
-                for w in range(w0, w1 + 1):
-                    lo, hi = max(x, w * run) - x, min(x + n, (w + 1) * run) - x
-                    rows.append([w, r, h, lo, hi - lo, last if hi == n else P, slot, 0])
+                for w, lo, cnt in pieces:
+                    rows.append([w, r, h, lo, cnt, last if lo + cnt == n else P, slot, 0])
                     slot += 1
-            x += n
     C = W // 8
     for row in rows:
         row[0] = (row[0] % C) * 8 + row[0] // C
@@ -425,8 +437,8 @@ def equal_runs_decode(b, W, tile_rows=16):
 
 @pytest.mark.parametrize("seed,batch,workers,page", [(1001, 64, 1216, 16), (3, 9, 40, 16), (5, 7, 1216, 1),
                                                        (8, 3, 8, 64)])
-def test_decode_plan_is_the_equal_run_split(lib, seed, batch, workers, page):
-    """The decode plan's work rows equal the plainly restated equal-run split, worker by
+def test_decode_plan_is_the_equal_cost_split(lib, seed, batch, workers, page):
+    """The decode plan's work rows equal the plainly restated equal-cost split, worker by
     worker (8 workers per SM)."""
     b = W.llama3_decode(seed=seed, batch=batch, page_size=page)
     h, ws = host_plan(b, api.PLAN_DECODE, num_sms=workers // 8)
@@ -434,7 +446,7 @@ def test_decode_plan_is_the_equal_run_split(lib, seed, batch, workers, page):
     if fits_in_one_run(b, workers):
         check_whole_list_plan(h, b, workers)
     else:
-        assert api.plan_get_work(h).tolist() == equal_runs_decode(b, workers)
+        assert api.plan_get_work(h).tolist() == cost_runs_decode(b, workers)
 
 
 def fits_in_one_run(b, W, tile_rows=16):
@@ -460,7 +472,7 @@ def test_decode_plan_keeps_short_lists_whole_when_workers_allow(lib, kv_lens, sm
     if whole:
         check_whole_list_plan(h, b, sms * 8)
     else:
-        assert api.plan_get_work(h).tolist() == equal_runs_decode(b, sms * 8)
+        assert api.plan_get_work(h).tolist() == cost_runs_decode(b, sms * 8)
     api.plan_destroy(h)
 
 
@@ -782,7 +794,8 @@ def test_bench_mixed_batch_takes_the_measured_split(lib):
 @pytest.mark.parametrize("s", [1.1, 1.5])
 def test_decode_plan_balances_zipf_request_lengths(lib, s):
     """Request lengths from a Zipf law (the skew the pages' scheduler is built for):
-    every worker still streams at most ceil(total pages / workers) pages."""
+    every worker still streams at most ceil(T / 8) pages, T the equal cost per run (about
+    total pages / workers, plus a page for each piece of a list it holds)."""
     kv = W.zipf_lengths(128, s, 16, 131072, seed=11)
     assert max(kv) > 20 * sorted(kv)[len(kv) // 2]                 # heavy-tailed
     b = table_batch(kv)
@@ -790,7 +803,8 @@ def test_decode_plan_balances_zipf_request_lengths(lib, s):
     compute(h, ws, b)
     info, _ = check_decode_plan(h, b)
     total = sum((n + 15) // 16 for n in kv) * b.num_kv_heads
-    assert info.max_cost <= max(-(-total // info.workers), 8)
+    assert info.max_cost <= -(-decode_cost_target(b, info.workers) // 8)
+    assert info.total_cost == total
     api.plan_destroy(h)
 
 
