@@ -396,7 +396,9 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
   // its pages.  A page goes to the run r with r T <= its midpoint < (r + 1) T; a
   // piece ends where a list ends or its next page falls in the next run.  Every
   // list starts one piece and each of the W - 1 run boundaries at most one more,
-  // so with T below the whole cost fits in W runs.
+  // so with T below the whole cost fits in W runs.  T holds at least a piece
+  // start and a page, so a new piece's first page lands in the next run, never
+  // past it.
   const int64_t lists = static_cast<int64_t>(parts) * hkv;
   const int64_t T = std::max<int64_t>(kSegCost + kPageCost,
                                       ceil_div(total * kPageCost + kSegCost * (lists + W - 1), W));
@@ -428,7 +430,8 @@ pkv_status compute_decode(pkv_plan* pl, int batch, const int32_t* kv_indptr, con
         X += kSegCost;
         const int64_t r = std::min<int64_t>((X + kPageCost / 2) / T, W - 1);
         const int64_t room = (r + 1) * T - X - kPageCost / 2;  // > 0: this page's midpoint is in run r
-        const int32_t cnt = r == W - 1 ? n - lo : static_cast<int32_t>(std::min<int64_t>(n - lo, ceil_div(room, kPageCost)));
+        const int32_t cnt =
+            r == W - 1 ? n - lo : static_cast<int32_t>(std::min<int64_t>(n - lo, ceil_div(room, kPageCost)));
         cuts.push_back({static_cast<int>(r), lo});
         X += static_cast<int64_t>(cnt) * kPageCost;
         lo += cnt;
