@@ -529,64 +529,69 @@ template <int D, int G, typename T>
 __device__ __forceinline__ void decode_merge_pair(const DecodeArgs& a, int pair, int lane) {
   constexpr int PER = D / 32;  // dims per lane
   constexpr int U = 8;         // slots in flight per lane
-  {
-    const MergeItem it = a.merge[pair / G];
-    const int g = pair % G;
-    const float* lse_p = a.part_lse + static_cast<int64_t>(it.slot_begin) * G + g;
-    float mx = -INFINITY;
-    for (int i = lane; i < it.n_slots; i += 32) mx = fmaxf(mx, lse_p[static_cast<int64_t>(i) * G]);
-    mx = warp_max(mx);
-    float acc[PER];
+  const MergeItem it = a.merge[pair / G];
+  const int g = pair % G;
+  const int n = it.n_slots;
+  const float* lse_p = a.part_lse + static_cast<int64_t>(it.slot_begin) * G + g;
+  const float* o_p = a.part_o + (static_cast<int64_t>(it.slot_begin) * G + g) * D + lane * PER;
+  // Rows of slots i0 .. i0 + U - 1 (zeros past the last slot).
+  auto load_rows = [&](int i0, float (&vals)[U][PER]) {
 #pragma unroll
-    for (int v = 0; v < PER; ++v) acc[v] = 0.f;
-    float wsum = 0.f;
-    if (mx != -INFINITY) {
-      const float* o_p = a.part_o + (static_cast<int64_t>(it.slot_begin) * G + g) * D + lane * PER;
-      for (int i0 = 0; i0 < it.n_slots; i0 += 32) {
-        // lane j holds the weight of slot i0 + j
-        const float w_lane = (i0 + lane < it.n_slots)
-                                 ? fast_exp2((lse_p[static_cast<int64_t>(i0 + lane) * G] - mx) * kLog2e)
-                                 : 0.f;
-        const int cnt = min(32, it.n_slots - i0);
-        for (int j0 = 0; j0 < cnt; j0 += U) {
-          float vals[U][PER];
+    for (int u = 0; u < U; ++u) {
+      if (i0 + u < n) {
+        const float* src = o_p + static_cast<int64_t>(i0 + u) * G * D;
+        if constexpr (PER == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(src);
+          vals[u][0] = t.x; vals[u][1] = t.y; vals[u][2] = t.z; vals[u][3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2*>(src);
+          vals[u][0] = t.x; vals[u][1] = t.y;
+        }
+      } else {
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int i = i0 + j0 + u;
-            if (j0 + u < cnt) {
-              const float* src = o_p + static_cast<int64_t>(i) * G * D;
-              if constexpr (PER == 4) {
-                const float4 t = *reinterpret_cast<const float4*>(src);
-                vals[u][0] = t.x; vals[u][1] = t.y; vals[u][2] = t.z; vals[u][3] = t.w;
-              } else {
-                const float2 t = *reinterpret_cast<const float2*>(src);
-                vals[u][0] = t.x; vals[u][1] = t.y;
-              }
-            } else {
+        for (int v = 0; v < PER; ++v) vals[u][v] = 0.f;
+      }
+    }
+  };
+  // The first rows do not depend on the lse values: they load together with them,
+  // so the merge waits for two dependent loads (item, then lse and rows), not three.
+  float vals[U][PER];
+  load_rows(0, vals);
+  const float l0 = lane < n ? lse_p[static_cast<int64_t>(lane) * G] : -INFINITY;
+  float mx = l0;
+  for (int i = lane + 32; i < n; i += 32) mx = fmaxf(mx, lse_p[static_cast<int64_t>(i) * G]);
+  mx = warp_max(mx);
+  float acc[PER];
 #pragma unroll
-              for (int v = 0; v < PER; ++v) vals[u][v] = 0.f;
-            }
-          }
+  for (int v = 0; v < PER; ++v) acc[v] = 0.f;
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      // lane j holds the weight of slot i0 + j
+      const float l = i0 == 0 ? l0 : (i0 + lane < n ? lse_p[static_cast<int64_t>(i0 + lane) * G] : -INFINITY);
+      const float w_lane = i0 + lane < n ? fast_exp2((l - mx) * kLog2e) : 0.f;
+      const int cnt = min(32, n - i0);
+      for (int j0 = 0; j0 < cnt; j0 += U) {
+        if (i0 + j0 > 0) load_rows(i0 + j0, vals);
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const float w = __shfl_sync(kFull, w_lane, (j0 + u) & 31);
-            if (j0 + u < cnt) {
+        for (int u = 0; u < U; ++u) {
+          const float w = __shfl_sync(kFull, w_lane, (j0 + u) & 31);
+          if (j0 + u < cnt) {
 #pragma unroll
-              for (int v = 0; v < PER; ++v) acc[v] = fmaf(w, vals[u][v], acc[v]);
-              wsum += w;
-            }
+            for (int v = 0; v < PER; ++v) acc[v] = fmaf(w, vals[u][v], acc[v]);
+            wsum += w;
           }
         }
       }
     }
-    const int hq = it.kvh * G + g;
-    T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(it.row) * a.num_qo_heads + hq) * D;
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-    for (int v = 0; v < PER; ++v) orow[lane * PER + v] = from_float<T>(acc[v] * inv);
-    if (lane == 0 && a.lse)
-      a.lse[static_cast<int64_t>(it.row) * a.num_qo_heads + hq] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
   }
+  const int hq = it.kvh * G + g;
+  T* orow = static_cast<T*>(a.o) + (static_cast<int64_t>(it.row) * a.num_qo_heads + hq) * D;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int v = 0; v < PER; ++v) orow[lane * PER + v] = from_float<T>(acc[v] * inv);
+  if (lane == 0 && a.lse)
+    a.lse[static_cast<int64_t>(it.row) * a.num_qo_heads + hq] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 // Launch one decode instance (head_dim, group size and cap chosen at run time).
