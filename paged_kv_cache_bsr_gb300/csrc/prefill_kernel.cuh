@@ -781,17 +781,19 @@ __device__ __forceinline__ void prefill_merge_row(const PrefillArgs& a, int pair
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;
   if (mx != -INFINITY) {
+    // The row loads do not wait for the weights: a slot of weight 0 is dropped by
+    // a select after its load, not by a branch before it.
+#pragma unroll 4
     for (int i = 0; i < it.n_slots; ++i) {
       const int64_t row = static_cast<int64_t>(it.slot_begin + i) * kWR + r;
+      const float4 v = reinterpret_cast<const float4*>(a.part_o + row * kD)[lane];
       const float w = fast_exp2((a.part_lse[row] - mx) * kLog2e);
-      if (w > 0.f) {
-        const float4 v = reinterpret_cast<const float4*>(a.part_o + row * kD)[lane];
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-        acc[2] = fmaf(w, v.z, acc[2]);
-        acc[3] = fmaf(w, v.w, acc[3]);
-        wsum += w;
-      }
+      const bool use = w > 0.f;
+      acc[0] = use ? fmaf(w, v.x, acc[0]) : acc[0];
+      acc[1] = use ? fmaf(w, v.y, acc[1]) : acc[1];
+      acc[2] = use ? fmaf(w, v.z, acc[2]) : acc[2];
+      acc[3] = use ? fmaf(w, v.w, acc[3]) : acc[3];
+      wsum += use ? w : 0.f;
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
