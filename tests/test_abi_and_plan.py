@@ -904,3 +904,46 @@ def test_packed_prefill_refuses_limits_past_32_bit_rows(lib):
     assert e.value.status == -1
     h = api.plan_create_host(api.PLAN_PREFILL, params16, api.Limits(4, 1 << 20, 150_000_000 // 16), 152)
     api.plan_destroy(h)
+
+
+# --------------------------------------------------------------------------- launch ordering
+def _kernels(src):
+    """(name, body) of every __global__ function in a CUDA source text."""
+    out = []
+    for m in re.finditer(r"__global__\s+void\s+(?:__launch_bounds__\([^)]*\)\s*)?(\w+)\s*\(", src):
+        i = src.index("{", m.end())  # the body follows the parameter list
+        depth, j = 0, i
+        while True:
+            depth += {"{": 1, "}": -1}.get(src[j], 0)
+            if depth == 0:
+                break
+            j += 1
+        out.append((m.group(1), src[i:j + 1]))
+    return out
+
+
+def test_dependent_kernels_wait_before_any_return():
+    """Kernels launched as programmatic dependents are ordered only after the grid just
+    before them; the chain stays ordered after every earlier kernel only if each of them
+    waits (griddepcontrol.wait) before it can return.  Every kernel but the standalone
+    prefill kernel is launched that way, and that one keeps an ordinary launch."""
+    csrc = os.path.join(os.path.dirname(api.__file__), "csrc")
+    seen = set()
+    for f in sorted(os.listdir(csrc)):
+        if not f.endswith((".cu", ".cuh")):
+            continue
+        src = open(os.path.join(csrc, f)).read()
+        for name, body in _kernels(src):
+            seen.add(name)
+            if name == "prefill_kernel":
+                assert "griddepcontrol" not in body
+                continue
+            w = body.find("griddepcontrol.wait")
+            assert w >= 0, f"{f}: {name} never waits for the grid before it"
+            r = body.find("return")
+            assert r < 0 or r > w, f"{f}: {name} can return before griddepcontrol.wait"
+    assert {"decode_kernel", "prefill_kernel", "mixed_kernel", "pack_pages_kernel", "append_rope_kernel",
+            "decode_merge_kernel", "prefill_merge_kernel", "mixed_merge_kernel", "merge_state_kernel",
+            "merge_states_kernel"} <= seen
+    prefill_src = open(os.path.join(csrc, "prefill_kernel.cuh")).read()
+    assert "kern<<<grid, kThreads, smem, s>>>(a, tq, tkv)" in prefill_src
