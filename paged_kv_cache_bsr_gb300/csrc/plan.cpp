@@ -561,8 +561,8 @@ int64_t query_tile_blocks(const pkv_plan* pl, int batch, const int32_t* qo_indpt
 // with the ragged batch and the cascade unchanged).
 int64_t key_chunk(int64_t total, int C) { return std::max<int64_t>(ceil_div(total, std::max(C, 1)), 1); }
 
-// The busiest CTA's load (key blocks, plus one per item for its setup and
-// epilogue) when compute_prefill chunks the tiles for C CTAs and assigns them
+// The busiest CTA's load (key blocks, plus kItemOverhead per item for its setup
+// and epilogue) when compute_prefill chunks the tiles for C CTAs and assigns them
 // longest first.  `nb_tiles[k]` counts the tiles of k key blocks: an item's cost
 // depends on nothing else.  The costs are small integers and the least load of a
 // longest-first schedule never decreases, so the schedule runs on counts (`by_cost`
