@@ -947,3 +947,19 @@ def test_dependent_kernels_wait_before_any_return():
             "merge_states_kernel"} <= seen
     prefill_src = open(os.path.join(csrc, "prefill_kernel.cuh")).read()
     assert "kern<<<grid, kThreads, smem, s>>>(a, tq, tkv)" in prefill_src
+
+
+@pytest.mark.parametrize("s,sms", [(1.1, 152), (1.5, 152), (1.1, 5), (1.5, 1)])
+def test_decode_plan_is_the_equal_cost_split_on_zipf_lengths(lib, s, sms):
+    """Heavy-tailed request lengths on grids of 8 to 1216 workers: the plan's work rows equal
+    the page-by-page restatement of the equal-cost split exactly."""
+    kv = W.zipf_lengths(96, s, 16, 65536, seed=21)
+    b = table_batch(kv)
+    h, ws = host_plan(b, api.PLAN_DECODE, num_sms=sms)
+    compute(h, ws, b)
+    check_decode_plan(h, b, num_sms=sms)
+    if fits_in_one_run(b, sms * 8):
+        check_whole_list_plan(h, b, sms * 8)
+    else:
+        assert api.plan_get_work(h).tolist() == cost_runs_decode(b, sms * 8)
+    api.plan_destroy(h)
